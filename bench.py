@@ -1,0 +1,467 @@
+"""Benchmark of the sparse MLA forward on GB300 (one JSON line on stdout).
+
+Default workload: decode bf16 — 64 sequences x 1 query row, H=16,
+D_qk=D_v=512, paged 64-slot blocks, 131072-token contexts (8,388,608 slots,
+8.6 GB bf16 pool), top-k 2048 distinct uniform indices per row. A step is one
+sparse_mla_fwd call over the 64 rows (the whole path: index read, gather,
+QK, masked online softmax, PV, split partials and LSE merge; one kernel).
+
+Metric: gathered-KV GB/s = sum_t valid_t * D_qk * bytes_per_elem / step time
+(higher is better); query rows/s is reported beside it.
+
+Timing: W warm-up steps, then exactly K steps timed with CUDA events on the
+launching stream, replayed from a CUDA graph of R consecutive calls that
+rotate over R independent (q, indices) sets whose gathered bytes together
+exceed 4x the L2 (the pool stays resident; every call gathers more than L2).
+SM clocks are sampled with nvidia-smi during the timed region.
+
+--impl reference times the fp64 CPU oracle on the host cores instead: each
+step is one query row of the same workload (all heads), so K steps finish in
+minutes; its line carries "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np
+import torch
+
+from sparse_mla_attention_04_gb300 import inputs
+
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode_bf16", choices=sorted(inputs.CONFIGS))
+    ap.add_argument("--rotations", type=int, default=0, help="index/q sets (0 = enough for 4x L2)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--seed", type=int, default=0)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; timing reduction only)
+# ----------------------------------------------------------------------------
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def dist_init(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# measurement helpers
+# ----------------------------------------------------------------------------
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s)"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_mla_attention_04_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        if n.endswith((".cu", ".cuh", ".h")):
+            h.update(n.encode())
+            h.update(open(os.path.join(csrc, n), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else null)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        d = json.load(open(p))[workload]
+    except Exception:
+        return None
+    return float(d["bytes_per_launch"]) if d.get("kernel_hash") == kernel_source_hash() else None
+
+
+# ----------------------------------------------------------------------------
+# workload construction
+# ----------------------------------------------------------------------------
+
+def build_workload(name: str, seed: int, rotations: int, device, rank: int):
+    from sparse_mla_attention_04_gb300 import binding
+    w = inputs.CONFIGS[name](seed=seed)
+    src = inputs.make_kv_source(w, device=device)
+    if w.kv_fp8:
+        cache, kvs = binding.build_fp8_cache(src)
+    else:
+        cache, kvs = src, None
+    torch.cuda.synchronize()
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    sets = []
+    total = 0
+    r = 0
+    while True:
+        s = seed + 1 + r + 1000 * rank
+        idx = inputs.make_indices(w, seed=s)
+        q = inputs.make_q(w, seed=s, device=device)
+        gathered = inputs.valid_count(idx) * w.D_qk * w.kv_bytes_per_elem
+        sets.append(dict(q=q, idx_np=idx, idx=torch.from_numpy(idx).to(device), bytes=gathered))
+        total += gathered
+        r += 1
+        if rotations and r >= rotations:
+            break
+        if not rotations and total >= 4 * l2 and r >= 2:
+            break
+        if r >= 64:
+            break
+    return w, src, cache, kvs, sets, l2
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+
+def run_ours(args):
+    from sparse_mla_attention_04_gb300 import binding
+    rank, world, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist_init(world, "nccl")
+    w, src, cache, kvs, sets, l2 = build_workload(args.workload, args.seed, args.rotations, dev, rank)
+    R = len(sets)
+    dot = "fp8" if w.kv_fp8 else "auto"
+    stream = torch.cuda.Stream(device=dev)
+    T, H = w.T, w.H
+    out = torch.empty((T, H, w.D_v), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    splits = binding.smla_plan_num_splits(T, H, w.D_qk, w.topk, int(w.kv_fp8),
+                                          torch.cuda.get_device_properties(dev).multi_processor_count)
+    need = binding.sparse_mla_fwd_workspace_size(T, H, w.D_qk, w.D_v, w.topk, int(w.kv_fp8), splits)
+    ws = torch.zeros(max(need, 1), dtype=torch.uint8, device=dev)
+
+    def call(i):
+        s = sets[i % R]
+        binding.sparse_mla_fwd(s["q"], cache, s["idx"], w.scale, kv_scale=kvs, dot_precision=dot, D_v=w.D_v,
+                               out=out, lse=lse, workspace=ws, num_splits=splits, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            call(i)
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(R):
+                call(i)
+        graph.replay()
+        stream.synchronize()
+
+    K = args.steps
+    reps, rem = divmod(K, R)
+    bytes_per_step = [s["bytes"] for s in sets]
+    total_bytes = reps * sum(bytes_per_step) + sum(bytes_per_step[:rem])
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
+    time.sleep(0.3 if clocks else 0)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        for i in range(rem):
+            call(i)
+        end.record(stream)
+    end.synchronize()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    ms = start.elapsed_time(end)
+    ms_max = max_over_ranks(ms, world, dev)
+    ms_per_step = ms_max / K
+    rows = sum(int((s["idx_np"] != -1).any(axis=1).sum()) for s in sets) / R   # rows with work (all, here)
+    gbs = total_bytes * world / (ms_max * 1e-3) / 1e9
+    per_launch_bytes = total_bytes / K
+    achieved = per_launch_bytes / (ms / K * 1e-3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(w, cache, kvs, sets, dot, splits, dev, stream, K, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, src, sets[0])
+
+    if rank == 0:
+        peak, peak_src = measured_peaks()
+        line = {
+            "metric": "sparse MLA fwd gathered-KV GB/s (%s)" % w.name,
+            "value": round(gbs, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": K,
+            "warmup": max(args.warmup, 3),
+            "ms_per_step": round(ms_per_step, 6),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "fp8-e4m3 QK / fp16 PV" if w.kv_fp8 else "bf16",
+            "data": "synthetic (seeded N(0,1) bf16 q and KV, uniform distinct top-k over paged contexts)",
+            "config": {
+                "workload": w.name, "T": T, "H": H, "D_qk": w.D_qk, "D_v": w.D_v, "topk": w.topk,
+                "num_slots": w.num_slots, "kv_dtype": "e4m3" if w.kv_fp8 else "bf16",
+                "context_per_row": w.ctx, "splits": splits, "rotating_sets": R,
+                "gathered_bytes_per_step": per_launch_bytes,
+                "l2": "inputs larger than L2: each step gathers %.0f MB, %d rotating index sets (%.0f MB, L2 %.0f MB)"
+                      % (per_launch_bytes / 1e6, R, sum(bytes_per_step) / 1e6, l2 / 1e6),
+                "parallelism": "dp%d (independent rows per GPU, no collective)" % world,
+                "timing": "CUDA graph of %d calls replayed; CUDA events on the launching stream" % R,
+            },
+            "query_rows_per_s": round(rows * world / (ms_max * 1e-3 / K), 1),
+            "gpu_launches": K,
+            "roofline": {
+                "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(w.name),
+                "peak_source": peak_src,
+                "algorithmic_bytes_per_launch": per_launch_bytes,
+            },
+            "clocks": clk,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(w, cache, kvs, sets, dot, splits, dev, stream, K, world):
+    """Same metric through the public API with host buffers: every step copies
+    that step's q and indices from pinned host memory and reads out and lse
+    back into pinned host memory, inside the timed region."""
+    from sparse_mla_attention_04_gb300 import binding
+    R = len(sets)
+    hq = [s["q"].cpu().pin_memory() for s in sets]
+    hi = [s["idx"].cpu().pin_memory() for s in sets]
+    ho = torch.empty((w.T, w.H, w.D_v), dtype=torch.bfloat16).pin_memory()
+    hl = torch.empty((w.T, w.H), dtype=torch.float32).pin_memory()
+    dq = torch.empty_like(sets[0]["q"])
+    di = torch.empty_like(sets[0]["idx"])
+    out = torch.empty((w.T, w.H, w.D_v), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.T, w.H), dtype=torch.float32, device=dev)
+    need = binding.sparse_mla_fwd_workspace_size(w.T, w.H, w.D_qk, w.D_v, w.topk, int(w.kv_fp8), splits)
+    ws = torch.zeros(max(need, 1), dtype=torch.uint8, device=dev)
+    steps = max(R, min(K, 4000))
+
+    def step(i):
+        dq.copy_(hq[i % R], non_blocking=True)
+        di.copy_(hi[i % R], non_blocking=True)
+        binding.sparse_mla_fwd(dq, cache, di, w.scale, kv_scale=kvs, dot_precision=dot, D_v=w.D_v,
+                               out=out, lse=lse, workspace=ws, num_splits=splits, stream=stream)
+        ho.copy_(out, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            step(i)
+        stream.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(steps):
+            step(i)
+        b.record(stream)
+    b.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b), world, dev)
+    reps, rem = divmod(steps, R)
+    nbytes = reps * sum(s["bytes"] for s in sets) + sum(s["bytes"] for s in sets[:rem])
+    h2d = sets[0]["q"].numel() * 2 + sets[0]["idx"].numel() * 4
+    d2h = out.numel() * 2 + lse.numel() * 4
+    return {"value": round(nbytes * world / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "steps": steps,
+            "ms_per_step": round(ms / steps, 6), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ----------------------------------------------------------------------------
+# the oracle on the host cores (cpu_baseline leg and the reference arm)
+# ----------------------------------------------------------------------------
+
+def oracle_scale(src):
+    """The oracle's per-tensor fp8 scale of the whole bf16 source (chunked amax)."""
+    import oracle
+    amax = 0.0
+    for r0 in range(0, src.shape[0], 1 << 20):
+        amax = max(amax, oracle.amax_bf16(src[r0:r0 + (1 << 20)].cpu()))
+    return float(oracle.fp8_scale_from_amax(amax))
+
+
+def oracle_inputs(w, src, s, rows, kvs_val):
+    """Rows `rows` of a set, with the source rows their indices name gathered
+    from the device pool and renumbered densely (the oracle reads a host array;
+    an fp8 cache is encoded by the oracle itself from the bf16 source)."""
+    import oracle
+    idx = s["idx_np"][rows]
+    uniq = np.unique(idx[idx >= 0])
+    remap = np.where(idx >= 0, np.searchsorted(uniq, np.maximum(idx, 0)), -1).astype(np.int32)
+    kv_rows = src[torch.from_numpy(uniq).to(src.device)].cpu()
+    if w.kv_fp8:
+        kv_rows = oracle.fp8_quantize(kv_rows, kvs_val)
+    q = s["q"][torch.from_numpy(np.asarray(rows)).to(s["q"].device)].cpu()
+    nbytes = int((idx != -1).sum()) * w.D_qk * w.kv_bytes_per_elem
+    return q, kv_rows, remap, nbytes
+
+
+def time_oracle(w, q, kv_rows, remap, kvs_val):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.sparse_mla(q, kv_rows, remap, w.scale, kv_fp8=w.kv_fp8, kv_scale=kvs_val, D_v=w.D_v,
+                      q_mode=1 if w.kv_fp8 else 0)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, src, s, budget_s: float = 10.0):
+    import oracle
+    kvs_val = oracle_scale(src) if w.kv_fp8 else 1.0
+    rows = list(range(w.T))
+    q, kv_rows, remap, nbytes = oracle_inputs(w, src, s, rows, kvs_val)
+    done, el, reps = 0, 0.0, 0
+    while el < budget_s and reps < 50:
+        el += time_oracle(w, q, kv_rows, remap, kvs_val)
+        done += nbytes
+        reps += 1
+    return {"value": round(done / el / 1e9, 4), "unit": "GB/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": "%d pass(es) over all %d rows of one index set (%d heads, fp64 C + OpenMP), %.1f s"
+                      % (reps, w.T, w.H, el)}
+
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else None
+    if dev is None:
+        print(json.dumps({"impl": "reference", "unavailable": "no CUDA device to build the workload on"}))
+        return
+    torch.cuda.set_device(dev)
+    w, src, cache, kvs, sets, l2 = build_workload(args.workload, args.seed, max(args.rotations, 1), dev, 0)
+    kvs_val = oracle_scale(src) if w.kv_fp8 else 1.0
+    s = sets[0]
+    # one query row (all heads) per step
+    prepared = [oracle_inputs(w, src, s, [t], kvs_val) for t in range(w.T)]
+    for i in range(max(args.warmup, 3)):
+        p = prepared[i % w.T]
+        time_oracle(w, p[0], p[1], p[2], kvs_val)
+    K = args.steps
+    el, nbytes = 0.0, 0
+    for i in range(K):
+        p = prepared[i % w.T]
+        el += time_oracle(w, p[0], p[1], p[2], kvs_val)
+        nbytes += p[3]
+    value = nbytes / el / 1e9
+    line = {
+        "impl": "reference",
+        "metric": "sparse MLA fwd gathered-KV GB/s (%s)" % w.name,
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(el * 1e3 / K, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (same seeded workload as the GPU arm)",
+        "config": {"workload": w.name, "T": w.T, "H": w.H, "D_qk": w.D_qk, "topk": w.topk,
+                   "step": "one query row (all %d heads) of the workload" % w.H},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": "one query row per step, %d steps" % K},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

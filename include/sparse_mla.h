@@ -1,0 +1,193 @@
+/*
+ * sparse_mla.h — C ABI of libsparse_mla.so, a GB300 (sm_103a) sparse MLA
+ * attention forward and its companion fp8 cache writer.
+ *
+ * Sources (by page title and section):
+ *   [P1] "[ROCm][Perf][GLM-5.3-Flash] Enable AITER sparse MLA on gfx942,
+ *        including FP8 KV" (vLLM PR 60583): Overview, Claims, Details
+ *        ("FP8 KV on gfx942": q quantized per tile inside the kernel, fp8 dots;
+ *        the optional dot_precision argument; "Numerics").
+ *   [P3] "[ROCm][DSv4.1][Perf] Route gfx942 sparse MLA prefill to AITER
+ *        pa_prefill_sparse" (vLLM PR 60102): What changed (one KV pool, output
+ *        of q's dtype), Gating and the jin-amd A/B (split-K decode vs no split).
+ *   [P4] "[ROCm][MLA][Perf] Fuse decode QK-RoPE + Q-concat + KV-concat +
+ *        KV-cache write for sparse MLA" (vLLM PR 47757): Test plan (cache row =
+ *        concat(latent, rope); fp8 storage = x / scale, scaled_fp8_quant
+ *        convention), "Why positions is a real argument" (graph safety), and the
+ *        non-contiguous-input hazard.
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers marked "device" are CUDA device pointers on the current device.
+ *     The caller owns every buffer; the library never allocates, frees or
+ *     synchronizes, so every call may be captured into a CUDA graph.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *   - Arguments are checked on the host before anything is launched. A failed
+ *     check returns its status and writes nothing. SMLA_ERR_CUDA reports a
+ *     CUDA runtime error seen at launch.
+ *   - Tensors are dense and row-major (contiguous). Strided views are not
+ *     accepted: a strided input once produced silently wrong results [P4].
+ *   - bf16 is IEEE binary32's upper half; fp8 is OCP E4M3 ("e4m3fn": max 448,
+ *     S.1111.111 = NaN, no infinities).
+ */
+#ifndef SPARSE_MLA_H
+#define SPARSE_MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SMLA_API __attribute__((visibility("default")))
+#else
+#define SMLA_API
+#endif
+
+/* A cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st *smla_stream_t;
+
+typedef enum {
+    SMLA_OK = 0,
+    SMLA_ERR_NULL_POINTER = 1,        /* a required pointer is NULL                   */
+    SMLA_ERR_BAD_SHAPE = 2,           /* a size is negative or inconsistent            */
+    SMLA_ERR_BAD_DTYPE = 3,           /* unknown dtype / precision, or a bad pairing    */
+    SMLA_ERR_MISALIGNED = 4,          /* a pointer lacks the alignment stated below    */
+    SMLA_ERR_UNSUPPORTED = 5,         /* valid arguments this build has no kernel for  */
+    SMLA_ERR_WORKSPACE_TOO_SMALL = 6, /* workspace_bytes below the required size       */
+    SMLA_ERR_CUDA = 7                 /* CUDA runtime error (device query or launch)   */
+} smla_status;
+
+typedef enum {
+    SMLA_KV_BF16 = 0,
+    SMLA_KV_FP8_E4M3 = 1
+} smla_kv_dtype;
+
+/* Precision of the QK dot products [P1 Details: optional dot_precision; when
+ * omitted the precision follows q's dtype, which is bf16 here].
+ *   AUTO = BF16.
+ *   BF16: bf16 q . bf16 K (a bf16 cache).
+ *   FP8 : q quantized inside the kernel per (row, head) tile to E4M3 with
+ *         s_q = amax|q[t,h,:]| / 448 (1.0 if amax == 0), q8 = RNE_sat(q / s_q),
+ *         dotted with the E4M3 cache; requires an fp8 cache.
+ * The PV product always runs on 16-bit operands with fp32 accumulation. */
+typedef enum {
+    SMLA_DOT_AUTO = 0,
+    SMLA_DOT_BF16 = 1,
+    SMLA_DOT_FP8 = 2
+} smla_dot_precision;
+
+/* Human-readable name of a status. Never NULL. */
+SMLA_API const char *smla_status_string(int status);
+
+/* ABI version, (major << 16) | minor. */
+SMLA_API int smla_version(void);
+
+/* Number of splits of the top-k list ("split-K", [P3] jin-amd A/B: decode-sized
+ * calls need it) that sparse_mla_fwd uses when num_splits == 0, for a device
+ * with `sm_count` SMs. Host-only arithmetic; returns >= 1, or 0 for invalid
+ * arguments. */
+SMLA_API int smla_plan_num_splits(int T, int H, int D_qk, int topk, int kv_dtype,
+                                  int sm_count);
+
+/* Bytes of workspace sparse_mla_fwd needs with `num_splits` splits
+ * (num_splits == 0: the automatic plan for the current device, which queries
+ * the device). 0 means no workspace is needed. Returns (size_t)-1 on invalid
+ * arguments or a failed device query. */
+SMLA_API size_t sparse_mla_fwd_workspace_size(int T, int H, int D_qk, int D_v, int topk,
+                                              int kv_dtype, int num_splits);
+
+/*
+ * Sparse MLA attention forward (north star of the build; [P1] Overview and
+ * Details, [P3] per-call benchmark shapes, [P4] cache layout).
+ *
+ * For each query row t in [0, T) and head h in [0, H):
+ *   I      = { indices[t, i] : indices[t, i] != -1 }            (order free,
+ *            duplicates count; entries < -1 or >= num_slots are masked and
+ *            never dereferenced — smla_validate_indices reports them)
+ *   K(j)   = dequant(kv_cache[j, 0:D_qk]),  V(j) = dequant(kv_cache[j, 0:D_v])
+ *            (MLA: one latent row serves as key and value; for D_qk = 576 the
+ *            last 64 columns are the rope part, used by QK only)
+ *   s_i    = scale * q[t, h, :] . K(I_i)
+ *   out[t, h, :] = sum_i softmax(s)_i V(I_i)      (bf16, round to nearest even)
+ *   lse[t, h]    = ln sum_i exp(s_i)              (natural log; scale included)
+ *   An empty I gives out = 0 and lse = -inf.
+ *
+ * q            device, bf16 [T, H, D_qk], 16-byte aligned (q and out may be
+ *              NULL when T == 0).
+ * kv_cache     device, [num_slots, D_qk] of bf16 or E4M3 (kv_dtype): the paged
+ *              pool with its blocks flattened (slot = block * block_size +
+ *              offset), 16-byte aligned.
+ * kv_dtype     smla_kv_dtype.
+ * kv_scale     device pointer to one float (dequant = code * kv_scale);
+ *              required for SMLA_KV_FP8_E4M3, ignored (may be NULL) for bf16.
+ *              Read on the device, so a graph replays the current value.
+ * indices      device, int32 [T, topk], 4-byte aligned (may be NULL when topk == 0).
+ * T, H, D_qk, D_v, num_slots, topk
+ *              supported: H a multiple of 16, D_v = 512, D_qk in {512, 576}.
+ *              T = 0 is a no-op. topk = 0 gives empty rows.
+ * scale        softmax scale (e.g. 1/sqrt(D_qk)).
+ * dot_precision smla_dot_precision (FP8 needs an fp8 cache; bf16 dots over an
+ *              fp8 cache return SMLA_ERR_UNSUPPORTED in this version).
+ * out          device, bf16 [T, H, D_v], 16-byte aligned, written.
+ * lse          device, float [T, H], or NULL to skip.
+ * workspace    device, >= sparse_mla_fwd_workspace_size(...) bytes, 256-byte
+ *              aligned; may be NULL when that size is 0. Holds per-split
+ *              partial results and one counter per (row, 16-head group). It
+ *              must be zero-filled before its first use; every call returns
+ *              the counters to zero, so a buffer can be reused by later calls
+ *              on the same stream. Calls that overlap in time must not share
+ *              a workspace.
+ * num_splits   0 = automatic (smla_plan_num_splits for the current device);
+ *              otherwise the number of top-k splits to use (>= 1).
+ * stream       CUDA stream.
+ */
+SMLA_API smla_status sparse_mla_fwd(const void *q, const void *kv_cache, int kv_dtype,
+                                    const float *kv_scale, const int32_t *indices,
+                                    int T, int H, int D_qk, int D_v, int64_t num_slots,
+                                    int topk, float scale, int dot_precision,
+                                    void *out, float *lse,
+                                    void *workspace, size_t workspace_bytes,
+                                    int num_splits, smla_stream_t stream);
+
+/*
+ * Per-tensor fp8 scale of a bf16 tensor [P4 Test plan: scaled_fp8_quant with a
+ * per-tensor scale]: *scale_out = amax(|x|) / 448 in binary32, or 1.0 when
+ * amax == 0. NaN elements are ignored.
+ * x          device, bf16 [n], 16-byte aligned (may be NULL when n == 0).
+ * scale_out  device, one float, 4-byte aligned; used as the reduction cell
+ *            during the call.
+ */
+SMLA_API smla_status smla_compute_fp8_scale(const void *x, int64_t n, float *scale_out,
+                                            smla_stream_t stream);
+
+/*
+ * Quantizing cache write [P4 Summary and Test plan: concat_and_cache_mla into
+ * an fp8 cache]: for n in [0, N) with slot = slot_mapping[n] in [0, num_slots):
+ *   kv_cache[slot, d] = E4M3_RNE_satfinite(src[n, d] / *kv_scale)   (binary32
+ *   division), d in [0, D). slot == -1 skips the row, as does any slot outside
+ *   [0, num_slots) (a contract violation).
+ * src          device, bf16 [N, D], 16-byte aligned, D a multiple of 8.
+ * slot_mapping device, int64 [N].
+ * kv_scale     device, one float.
+ * kv_cache     device, uint8 [num_slots, D], 8-byte aligned.
+ */
+SMLA_API smla_status smla_fp8_cache_write(const void *src, const int64_t *slot_mapping,
+                                          int64_t N, int D, const float *kv_scale,
+                                          void *kv_cache, int64_t num_slots,
+                                          smla_stream_t stream);
+
+/*
+ * Counts the entries of indices [T, topk] that are neither -1 nor inside
+ * [0, num_slots) and stores the count in *bad_count (device int, overwritten).
+ */
+SMLA_API smla_status smla_validate_indices(const int32_t *indices, int T, int topk,
+                                           int64_t num_slots, int *bad_count,
+                                           smla_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSE_MLA_H */

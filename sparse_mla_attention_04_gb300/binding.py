@@ -1,0 +1,241 @@
+"""ctypes binding of libsparse_mla.so (include/sparse_mla.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library. Functions keep the C names. torch supplies device memory and the
+current stream; outputs and the workspace are allocated with torch when the
+caller passes none (the library itself never allocates).
+
+The library must exist: if it was not built, or fails to load, every call
+raises — there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsparse_mla.so")
+
+SMLA_OK = 0
+SMLA_ERR_NULL_POINTER = 1
+SMLA_ERR_BAD_SHAPE = 2
+SMLA_ERR_BAD_DTYPE = 3
+SMLA_ERR_MISALIGNED = 4
+SMLA_ERR_UNSUPPORTED = 5
+SMLA_ERR_WORKSPACE_TOO_SMALL = 6
+SMLA_ERR_CUDA = 7
+
+SMLA_KV_BF16 = 0
+SMLA_KV_FP8_E4M3 = 1
+SMLA_DOT_AUTO = 0
+SMLA_DOT_BF16 = 1
+SMLA_DOT_FP8 = 2
+_DOT = {"auto": SMLA_DOT_AUTO, "bf16": SMLA_DOT_BF16, "fp8": SMLA_DOT_FP8}
+
+# every function the header declares, with its ctypes signature
+_c = ctypes
+SIGNATURES = {
+    "smla_status_string": ([_c.c_int], _c.c_char_p),
+    "smla_version": ([], _c.c_int),
+    "smla_plan_num_splits": ([_c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int], _c.c_int),
+    "sparse_mla_fwd_workspace_size": ([_c.c_int] * 7, _c.c_size_t),
+    "sparse_mla_fwd": ([_c.c_void_p, _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_void_p,
+                        _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int64, _c.c_int,
+                        _c.c_float, _c.c_int, _c.c_void_p, _c.c_void_p,
+                        _c.c_void_p, _c.c_size_t, _c.c_int, _c.c_void_p], _c.c_int),
+    "smla_compute_fp8_scale": ([_c.c_void_p, _c.c_int64, _c.c_void_p, _c.c_void_p], _c.c_int),
+    "smla_fp8_cache_write": ([_c.c_void_p, _c.c_void_p, _c.c_int64, _c.c_int, _c.c_void_p,
+                              _c.c_void_p, _c.c_int64, _c.c_void_p], _c.c_int),
+    "smla_validate_indices": ([_c.c_void_p, _c.c_int, _c.c_int, _c.c_int64, _c.c_void_p,
+                               _c.c_void_p], _c.c_int),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SmlaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s" % (where, status_string(status)))
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it is missing: build it first)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError("libsparse_mla.so is not built (%s); run __graft_entry__.build()" % LIB_PATH)
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (args, res) in SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = L
+        return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().smla_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != SMLA_OK:
+        raise SmlaError(status, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(x: Optional[torch.Tensor]) -> Optional[int]:
+    return None if x is None else x.data_ptr()
+
+
+def _need(x: torch.Tensor, name: str, dtype, ndim: int):
+    if not isinstance(x, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if x.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, x.dtype))
+    if x.dim() != ndim:
+        raise ValueError("%s must have %d dims, got shape %s" % (name, ndim, tuple(x.shape)))
+    if not x.is_contiguous():
+        raise ValueError("%s must be contiguous (strided inputs are not accepted)" % name)
+    if not x.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+
+
+def smla_version() -> int:
+    return int(lib().smla_version())
+
+
+def smla_plan_num_splits(T: int, H: int, D_qk: int, topk: int, kv_dtype: int, sm_count: int) -> int:
+    return int(lib().smla_plan_num_splits(T, H, D_qk, topk, kv_dtype, sm_count))
+
+
+def sparse_mla_fwd_workspace_size(T: int, H: int, D_qk: int, D_v: int, topk: int, kv_dtype: int,
+                                  num_splits: int = 0) -> int:
+    n = lib().sparse_mla_fwd_workspace_size(T, H, D_qk, D_v, topk, kv_dtype, num_splits)
+    if n == ctypes.c_size_t(-1).value:
+        raise SmlaError(SMLA_ERR_BAD_SHAPE, "sparse_mla_fwd_workspace_size")
+    return int(n)
+
+
+# zeroed workspaces, one per (device, stream); the kernel leaves them zeroed
+_workspaces = {}
+
+
+def workspace_for(nbytes: int, device: torch.device, stream_handle: int) -> Optional[torch.Tensor]:
+    if nbytes == 0:
+        return None
+    key = (device.index, stream_handle)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def sparse_mla_fwd(q: torch.Tensor, kv_cache: torch.Tensor, indices: torch.Tensor, scale: float, *,
+                   kv_scale: Optional[torch.Tensor] = None, dot_precision: str = "auto",
+                   D_v: int = 512, out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                   return_lse: bool = True, workspace: Optional[torch.Tensor] = None,
+                   num_splits: int = 0, stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """out[T,H,D_v] (bf16), lse[T,H] (fp32) of the sparse MLA forward.
+
+    q bf16 [T,H,D_qk]; kv_cache [num_slots, D_qk] bf16 or torch.float8_e4m3fn/uint8
+    (E4M3 codes, then kv_scale: fp32 device scalar); indices int32 [T, topk].
+    """
+    _need(q, "q", torch.bfloat16, 3)
+    T, H, D_qk = q.shape
+    if kv_cache.dtype == torch.bfloat16:
+        kv_dtype = SMLA_KV_BF16
+    elif kv_cache.dtype in (torch.float8_e4m3fn, torch.uint8):
+        kv_dtype = SMLA_KV_FP8_E4M3
+    else:
+        raise TypeError("kv_cache must be bf16 or E4M3 (float8_e4m3fn / uint8), got %s" % kv_cache.dtype)
+    _need(kv_cache, "kv_cache", kv_cache.dtype, 2)
+    if kv_cache.shape[1] != D_qk:
+        raise ValueError("kv_cache row width %d != D_qk %d" % (kv_cache.shape[1], D_qk))
+    _need(indices, "indices", torch.int32, 2)
+    if indices.shape[0] != T:
+        raise ValueError("indices has %d rows, q has %d" % (indices.shape[0], T))
+    if kv_dtype == SMLA_KV_FP8_E4M3:
+        if kv_scale is None:
+            raise ValueError("an fp8 cache needs kv_scale (fp32 device scalar)")
+        _need(kv_scale.reshape(1), "kv_scale", torch.float32, 1)
+    if dot_precision not in _DOT:
+        raise ValueError("dot_precision must be one of %s" % sorted(_DOT))
+    topk = indices.shape[1]
+    if out is None:
+        out = torch.empty((T, H, D_v), dtype=torch.bfloat16, device=q.device)
+    _need(out, "out", torch.bfloat16, 3)
+    if lse is None and return_lse:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    sh = _stream(stream)
+    need = sparse_mla_fwd_workspace_size(T, H, D_qk, D_v, topk, kv_dtype, num_splits)
+    if workspace is None:
+        workspace = workspace_for(need, q.device, sh)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().sparse_mla_fwd(
+        _ptr(q), _ptr(kv_cache), kv_dtype, _ptr(kv_scale), _ptr(indices),
+        T, H, D_qk, D_v, kv_cache.shape[0], topk, float(scale), _DOT[dot_precision],
+        _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, int(num_splits), sh)
+    _check(st, "sparse_mla_fwd")
+    return out, lse
+
+
+def smla_compute_fp8_scale(x: torch.Tensor, scale_out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """fp32 device scalar amax(|x|)/448 of a bf16 tensor."""
+    if x.dtype != torch.bfloat16 or not x.is_contiguous() or not x.is_cuda:
+        raise ValueError("x must be a contiguous CUDA bf16 tensor")
+    if scale_out is None:
+        scale_out = torch.empty(1, dtype=torch.float32, device=x.device)
+    _check(lib().smla_compute_fp8_scale(_ptr(x), x.numel(), _ptr(scale_out), _stream(stream)),
+           "smla_compute_fp8_scale")
+    return scale_out
+
+
+def smla_fp8_cache_write(src: torch.Tensor, slot_mapping: torch.Tensor, kv_scale: torch.Tensor,
+                         kv_cache: torch.Tensor, stream=None) -> torch.Tensor:
+    """kv_cache[slot_mapping[n]] = E4M3(src[n] / kv_scale) (uint8 / float8_e4m3fn cache)."""
+    _need(src, "src", torch.bfloat16, 2)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    _need(kv_cache, "kv_cache", kv_cache.dtype, 2)
+    if kv_cache.element_size() != 1 or kv_cache.shape[1] != src.shape[1]:
+        raise ValueError("kv_cache must be 1-byte [num_slots, D]")
+    N, D = src.shape
+    _check(lib().smla_fp8_cache_write(_ptr(src), _ptr(slot_mapping), N, D, _ptr(kv_scale),
+                                      _ptr(kv_cache), kv_cache.shape[0], _stream(stream)),
+           "smla_fp8_cache_write")
+    return kv_cache
+
+
+def smla_validate_indices(indices: torch.Tensor, num_slots: int, bad_count: Optional[torch.Tensor] = None,
+                          stream=None) -> torch.Tensor:
+    """int32 device scalar: entries of indices that are neither -1 nor in [0, num_slots)."""
+    _need(indices, "indices", torch.int32, 2)
+    if bad_count is None:
+        bad_count = torch.empty(1, dtype=torch.int32, device=indices.device)
+    T, topk = indices.shape
+    _check(lib().smla_validate_indices(_ptr(indices), T, topk, int(num_slots), _ptr(bad_count), _stream(stream)),
+           "smla_validate_indices")
+    return bad_count
+
+
+def build_fp8_cache(kv_source: torch.Tensor, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Quantize a whole bf16 pool [num_slots, D] into a fresh E4M3 cache with its scale."""
+    scale = smla_compute_fp8_scale(kv_source, stream=stream)
+    cache = torch.empty(kv_source.shape, dtype=torch.uint8, device=kv_source.device)
+    slots = torch.arange(kv_source.shape[0], dtype=torch.int64, device=kv_source.device)
+    smla_fp8_cache_write(kv_source, slots, scale, cache, stream=stream)
+    return cache, scale

@@ -1,0 +1,276 @@
+// C ABI of libsparse_mla.so: argument checks on the host, the split plan, and
+// dispatch to the kernels. Declared and documented in include/sparse_mla.h.
+#include "../../include/sparse_mla.h"
+#include "smla_internal.h"
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+
+// SM count of the current device (cached per device).
+cudaError_t current_sm_count(int *out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= 0 && dev < kMaxDevices) {
+        const int cached = g_sm_count[dev].load(std::memory_order_relaxed);
+        if (cached > 0) {
+            *out = cached;
+            return cudaSuccess;
+        }
+    }
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= 0 && dev < kMaxDevices)
+        g_sm_count[dev].store(n, std::memory_order_relaxed);
+    *out = n;
+    return cudaSuccess;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Resident CTAs per SM of the warp-MMA kernel (shared memory bound).
+constexpr int kMmaCtasPerSm = 2;
+// A split keeps at least this many keys; at most this many splits.
+constexpr int kMinKeysPerSplit = 64;
+constexpr int kMaxSplits = 128;
+
+int plan_splits(int T, int H, int topk, int sm_count)
+{
+    if (T <= 0 || H <= 0 || topk <= 0 || sm_count <= 0)
+        return 1;
+    const int64_t units = (int64_t)T * (H / 16);
+    const int64_t slots = (int64_t)sm_count * kMmaCtasPerSm;
+    int64_t S = units >= slots ? 1 : slots / units;
+    const int64_t by_keys = topk / kMinKeysPerSplit;
+    if (S > by_keys)
+        S = by_keys;
+    if (S > kMaxSplits)
+        S = kMaxSplits;
+    return S < 1 ? 1 : (int)S;
+}
+
+int keys_per_split(int topk, int S)
+{
+    const int tile = smla::kMmaTileKeys;
+    const int per = (topk + S - 1) / S;
+    return ((per + tile - 1) / tile) * tile;
+}
+
+bool shape_supported(int H, int D_qk, int D_v)
+{
+    return H > 0 && H % 16 == 0 && D_v == 512 && (D_qk == 512 || D_qk == 576);
+}
+
+} // namespace
+
+namespace smla {
+
+WorkspaceLayout workspace_layout(int T, int H, int D_v, int S)
+{
+    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    WorkspaceLayout w{};
+    if (S <= 1)
+        return w;
+    w.part_o = 0;
+    w.part_lse = up(w.part_o + (size_t)T * S * H * D_v * sizeof(float));
+    w.tickets = up(w.part_lse + (size_t)T * S * H * sizeof(float));
+    w.total = up(w.tickets + (size_t)T * (H / 16) * sizeof(int));
+    return w;
+}
+
+} // namespace smla
+
+extern "C" {
+
+SMLA_API const char *smla_status_string(int status)
+{
+    switch (status) {
+    case SMLA_OK:
+        return "SMLA_OK";
+    case SMLA_ERR_NULL_POINTER:
+        return "SMLA_ERR_NULL_POINTER: a required pointer is NULL";
+    case SMLA_ERR_BAD_SHAPE:
+        return "SMLA_ERR_BAD_SHAPE: a size is negative or inconsistent";
+    case SMLA_ERR_BAD_DTYPE:
+        return "SMLA_ERR_BAD_DTYPE: unknown dtype or precision, or an invalid pairing";
+    case SMLA_ERR_MISALIGNED:
+        return "SMLA_ERR_MISALIGNED: a pointer lacks the required alignment";
+    case SMLA_ERR_UNSUPPORTED:
+        return "SMLA_ERR_UNSUPPORTED: no kernel for this shape / precision";
+    case SMLA_ERR_WORKSPACE_TOO_SMALL:
+        return "SMLA_ERR_WORKSPACE_TOO_SMALL: workspace below sparse_mla_fwd_workspace_size()";
+    case SMLA_ERR_CUDA:
+        return "SMLA_ERR_CUDA: CUDA runtime error";
+    default:
+        return "SMLA_ERR_UNKNOWN";
+    }
+}
+
+SMLA_API int smla_version(void) { return (1 << 16) | 0; }
+
+SMLA_API int smla_plan_num_splits(int T, int H, int D_qk, int topk, int kv_dtype, int sm_count)
+{
+    (void)D_qk;
+    (void)kv_dtype;
+    if (T < 0 || H <= 0 || H % 16 != 0 || topk < 0 || sm_count <= 0)
+        return 0;
+    return plan_splits(T, H, topk, sm_count);
+}
+
+SMLA_API size_t sparse_mla_fwd_workspace_size(int T, int H, int D_qk, int D_v, int topk, int kv_dtype,
+                                              int num_splits)
+{
+    if (T < 0 || topk < 0 || num_splits < 0 || !shape_supported(H, D_qk, D_v) ||
+        (kv_dtype != SMLA_KV_BF16 && kv_dtype != SMLA_KV_FP8_E4M3))
+        return (size_t)-1;
+    int S = num_splits;
+    if (S == 0) {
+        int sms = 0;
+        if (current_sm_count(&sms) != cudaSuccess)
+            return (size_t)-1;
+        S = plan_splits(T, H, topk, sms);
+    }
+    if (S > kMaxSplits)
+        return (size_t)-1;
+    return smla::workspace_layout(T, H, D_v, S).total;
+}
+
+SMLA_API smla_status sparse_mla_fwd(const void *q, const void *kv_cache, int kv_dtype, const float *kv_scale,
+                                    const int32_t *indices, int T, int H, int D_qk, int D_v, int64_t num_slots,
+                                    int topk, float scale, int dot_precision, void *out, float *lse,
+                                    void *workspace, size_t workspace_bytes, int num_splits,
+                                    smla_stream_t stream)
+{
+    // 1. pointers
+    if (kv_cache == nullptr || ((q == nullptr || out == nullptr) && T > 0) ||
+        (indices == nullptr && (int64_t)T * topk > 0))
+        return SMLA_ERR_NULL_POINTER;
+    if (kv_dtype == SMLA_KV_FP8_E4M3 && kv_scale == nullptr)
+        return SMLA_ERR_NULL_POINTER;
+    // 2. sizes
+    if (T < 0 || H <= 0 || D_qk <= 0 || D_v <= 0 || D_v > D_qk || num_slots < 0 || topk < 0 ||
+        num_splits < 0)
+        return SMLA_ERR_BAD_SHAPE;
+    // 3. dtypes and their pairing
+    if (kv_dtype != SMLA_KV_BF16 && kv_dtype != SMLA_KV_FP8_E4M3)
+        return SMLA_ERR_BAD_DTYPE;
+    if (dot_precision != SMLA_DOT_AUTO && dot_precision != SMLA_DOT_BF16 && dot_precision != SMLA_DOT_FP8)
+        return SMLA_ERR_BAD_DTYPE;
+    const bool fp8_dots = dot_precision == SMLA_DOT_FP8;
+    if (fp8_dots && kv_dtype != SMLA_KV_FP8_E4M3)
+        return SMLA_ERR_BAD_DTYPE;
+    // 4. what this build has kernels for
+    if (!shape_supported(H, D_qk, D_v))
+        return SMLA_ERR_UNSUPPORTED;
+    if (kv_dtype == SMLA_KV_FP8_E4M3 && !fp8_dots)
+        return SMLA_ERR_UNSUPPORTED; // bf16 dots over an fp8 cache: not built yet
+    if (num_splits > kMaxSplits)
+        return SMLA_ERR_UNSUPPORTED;
+    // 5. alignment
+    if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(indices, 4) ||
+        (lse != nullptr && !aligned(lse, 4)) || (kv_scale != nullptr && !aligned(kv_scale, 4)))
+        return SMLA_ERR_MISALIGNED;
+    if (T == 0)
+        return SMLA_OK;
+    // 6. split plan and workspace
+    int S = num_splits;
+    if (S == 0) {
+        int sms = 0;
+        if (current_sm_count(&sms) != cudaSuccess)
+            return SMLA_ERR_CUDA;
+        S = plan_splits(T, H, topk, sms);
+    }
+    const smla::WorkspaceLayout wl = smla::workspace_layout(T, H, D_v, S);
+    if (wl.total > 0) {
+        if (workspace == nullptr)
+            return SMLA_ERR_NULL_POINTER;
+        if (workspace_bytes < wl.total)
+            return SMLA_ERR_WORKSPACE_TOO_SMALL;
+        if (!aligned(workspace, 256))
+            return SMLA_ERR_MISALIGNED;
+    }
+
+    smla::FwdArgs a{};
+    a.q = q;
+    a.kv = kv_cache;
+    a.kv_scale = kv_scale;
+    a.indices = indices;
+    a.out = out;
+    a.lse = lse;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    a.part_o = wl.total ? reinterpret_cast<float *>(ws + wl.part_o) : nullptr;
+    a.part_lse = wl.total ? reinterpret_cast<float *>(ws + wl.part_lse) : nullptr;
+    a.tickets = wl.total ? reinterpret_cast<int *>(ws + wl.tickets) : nullptr;
+    a.num_slots = num_slots;
+    a.T = T;
+    a.H = H;
+    a.D_qk = D_qk;
+    a.D_v = D_v;
+    a.topk = topk;
+    a.S = S;
+    a.keys_per_split = topk > 0 ? keys_per_split(topk, S) : smla::kMmaTileKeys;
+    a.scale = scale;
+    a.kv_fp8 = kv_dtype == SMLA_KV_FP8_E4M3;
+    const cudaError_t e = smla::launch_fwd_mma(a, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+}
+
+SMLA_API smla_status smla_compute_fp8_scale(const void *x, int64_t n, float *scale_out, smla_stream_t stream)
+{
+    if ((x == nullptr && n > 0) || scale_out == nullptr)
+        return SMLA_ERR_NULL_POINTER;
+    if (n < 0)
+        return SMLA_ERR_BAD_SHAPE;
+    if (!aligned(x, 16) || !aligned(scale_out, 4))
+        return SMLA_ERR_MISALIGNED;
+    int sms = 0;
+    if (current_sm_count(&sms) != cudaSuccess)
+        return SMLA_ERR_CUDA;
+    const cudaError_t e = smla::launch_fp8_scale(x, n, scale_out, sms, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+}
+
+SMLA_API smla_status smla_fp8_cache_write(const void *src, const int64_t *slot_mapping, int64_t N, int D,
+                                          const float *kv_scale, void *kv_cache, int64_t num_slots,
+                                          smla_stream_t stream)
+{
+    if (src == nullptr || slot_mapping == nullptr || kv_scale == nullptr || kv_cache == nullptr)
+        return SMLA_ERR_NULL_POINTER;
+    if (N < 0 || D <= 0 || D % 8 != 0 || num_slots < 0)
+        return SMLA_ERR_BAD_SHAPE;
+    if (!aligned(src, 16) || !aligned(kv_cache, 8) || !aligned(slot_mapping, 8) || !aligned(kv_scale, 4))
+        return SMLA_ERR_MISALIGNED;
+    const cudaError_t e = smla::launch_fp8_cache_write(src, slot_mapping, N, D, kv_scale, kv_cache, num_slots,
+                                                       reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+}
+
+SMLA_API smla_status smla_validate_indices(const int32_t *indices, int T, int topk, int64_t num_slots,
+                                           int *bad_count, smla_stream_t stream)
+{
+    if ((indices == nullptr && (int64_t)T * topk > 0) || bad_count == nullptr)
+        return SMLA_ERR_NULL_POINTER;
+    if (T < 0 || topk < 0 || num_slots < 0)
+        return SMLA_ERR_BAD_SHAPE;
+    if (!aligned(indices, 4) || !aligned(bad_count, 4))
+        return SMLA_ERR_MISALIGNED;
+    int sms = 0;
+    if (current_sm_count(&sms) != cudaSuccess)
+        return SMLA_ERR_CUDA;
+    const cudaError_t e = smla::launch_validate_indices(indices, (int64_t)T * topk, num_slots, bad_count, sms,
+                                                        reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+}
+
+} // extern "C"

@@ -1,0 +1,49 @@
+// Internal host-side interface between the C ABI layer (smla_api.cu) and the
+// kernel translation units. Not installed; not part of the ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace smla {
+
+// Everything a forward launch needs, already validated by the ABI layer.
+struct FwdArgs {
+    const void *q;          // bf16 [T, H, D_qk]
+    const void *kv;         // [num_slots, D_qk] bf16 or E4M3
+    const float *kv_scale;  // device scalar (fp8) or nullptr
+    const int32_t *indices; // [T, topk]
+    void *out;              // bf16 [T, H, D_v]
+    float *lse;             // [T, H] or nullptr
+    float *part_o;          // [T, S, H, D_v]   (S > 1)
+    float *part_lse;        // [T, S, H]        (S > 1)
+    int *tickets;           // [T, H / 16]      (S > 1)
+    int64_t num_slots;
+    int T, H, D_qk, D_v, topk;
+    int S;                  // splits of the top-k list
+    int keys_per_split;     // multiple of the key tile
+    float scale;
+    bool kv_fp8;            // E4M3 cache with fp8 QK dots
+};
+
+// Key tile of the warp-MMA kernel (keys per pipeline stage).
+constexpr int kMmaTileKeys = 32;
+
+// Workspace layout for S > 1 (byte offsets, each 256-byte aligned).
+struct WorkspaceLayout {
+    size_t part_o, part_lse, tickets, total;
+};
+WorkspaceLayout workspace_layout(int T, int H, int D_v, int S);
+
+cudaError_t launch_fwd_mma(const FwdArgs &a, cudaStream_t stream);
+
+cudaError_t launch_fp8_scale(const void *x, int64_t n, float *scale_out, int sm_count,
+                             cudaStream_t stream);
+cudaError_t launch_fp8_cache_write(const void *src, const int64_t *slot_mapping, int64_t N, int D,
+                                   const float *kv_scale, void *cache, int64_t num_slots,
+                                   cudaStream_t stream);
+cudaError_t launch_validate_indices(const int32_t *indices, int64_t n, int64_t num_slots,
+                                    int *bad_count, int sm_count, cudaStream_t stream);
+
+} // namespace smla

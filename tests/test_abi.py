@@ -1,0 +1,118 @@
+"""The C-ABI library loads, exports every declared symbol, and rejects bad
+arguments on the host before touching the GPU (CPU only: no compute call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from sparse_mla_attention_04_gb300 import build, binding
+    build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "sparse_mla.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return set(re.findall(r"SMLA_API\s+[\w\s\*]+?\b(\w+)\s*\(", src))
+
+
+def test_every_declared_symbol_is_exported(L):
+    from sparse_mla_attention_04_gb300 import binding
+    names = declared_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(L, n), n
+    assert names == set(binding.SIGNATURES)
+
+
+def test_status_strings(L):
+    from sparse_mla_attention_04_gb300 import binding
+    for s in range(8):
+        assert binding.status_string(s).startswith("SMLA_")
+    assert binding.status_string(99) == "SMLA_ERR_UNKNOWN"
+    assert binding.smla_version() >> 16 == 1
+
+
+def test_split_plan(L):
+    from sparse_mla_attention_04_gb300 import binding as b
+    assert b.smla_plan_num_splits(64, 16, 512, 2048, 0, 152) == 4     # decode: 256 CTAs
+    assert b.smla_plan_num_splits(4, 16, 512, 128, 0, 152) == 2       # capped by keys per split
+    assert b.smla_plan_num_splits(8192, 16, 512, 2048, 0, 152) == 1   # prefill: no split
+    assert b.smla_plan_num_splits(128, 128, 576, 2048, 1, 152) == 1
+    assert b.smla_plan_num_splits(1, 16, 512, 100000, 0, 152) == 128  # capped
+    assert b.smla_plan_num_splits(4, 15, 512, 128, 0, 152) == 0       # invalid H
+
+
+def test_workspace_size(L):
+    from sparse_mla_attention_04_gb300 import binding as b
+    assert b.sparse_mla_fwd_workspace_size(64, 16, 512, 512, 2048, 0, 1) == 0
+    n = b.sparse_mla_fwd_workspace_size(64, 16, 512, 512, 2048, 0, 4)
+    up = lambda x: (x + 255) // 256 * 256
+    po = 64 * 4 * 16 * 512 * 4
+    pl = up(po) + 64 * 4 * 16 * 4
+    assert n == up(up(pl) + 64 * 1 * 4)
+    with pytest.raises(b.SmlaError):
+        b.sparse_mla_fwd_workspace_size(64, 12, 512, 512, 2048, 0, 4)
+
+
+def _call(L, q=0x1000, kv=0x2000, kvd=0, kvs=None, idx=0x3000, T=2, H=16, Dqk=512, Dv=512,
+          slots=100, topk=8, scale=0.1, dot=0, out=0x4000, lse=None, ws=None, wsb=0, splits=1):
+    return L.sparse_mla_fwd(q, kv, kvd, kvs, idx, T, H, Dqk, Dv, slots, topk, scale, dot, out, lse,
+                            ws, wsb, splits, None)
+
+
+def test_argument_checks_return_before_any_launch(L):
+    """Every case fails a host check; the fake pointers are never dereferenced."""
+    from sparse_mla_attention_04_gb300 import binding as b
+    assert _call(L, q=None) == b.SMLA_ERR_NULL_POINTER
+    assert _call(L, out=None) == b.SMLA_ERR_NULL_POINTER
+    assert _call(L, kvd=1, dot=2, kvs=None) == b.SMLA_ERR_NULL_POINTER
+    assert _call(L, T=-1) == b.SMLA_ERR_BAD_SHAPE
+    assert _call(L, topk=-3) == b.SMLA_ERR_BAD_SHAPE
+    assert _call(L, Dv=600) == b.SMLA_ERR_BAD_SHAPE
+    assert _call(L, splits=-1) == b.SMLA_ERR_BAD_SHAPE
+    assert _call(L, kvd=7) == b.SMLA_ERR_BAD_DTYPE
+    assert _call(L, dot=9) == b.SMLA_ERR_BAD_DTYPE
+    assert _call(L, kvd=0, dot=2) == b.SMLA_ERR_BAD_DTYPE            # fp8 dots need an fp8 cache
+    assert _call(L, H=8) == b.SMLA_ERR_UNSUPPORTED
+    assert _call(L, Dqk=256, Dv=256) == b.SMLA_ERR_UNSUPPORTED
+    assert _call(L, kvd=1, kvs=0x5000, dot=0) == b.SMLA_ERR_UNSUPPORTED
+    assert _call(L, splits=129) == b.SMLA_ERR_UNSUPPORTED
+    assert _call(L, q=0x1002) == b.SMLA_ERR_MISALIGNED
+    assert _call(L, out=0x4008) == b.SMLA_ERR_MISALIGNED
+    assert _call(L, idx=0x3002) == b.SMLA_ERR_MISALIGNED
+    assert _call(L, splits=4, ws=None) == b.SMLA_ERR_NULL_POINTER
+    assert _call(L, splits=4, ws=0x8000, wsb=100) == b.SMLA_ERR_WORKSPACE_TOO_SMALL
+    need = b.sparse_mla_fwd_workspace_size(2, 16, 512, 512, 8, 0, 4)
+    assert _call(L, splits=4, ws=0x8010, wsb=need) == b.SMLA_ERR_MISALIGNED
+    assert _call(L, T=0) == b.SMLA_OK                                   # no-op
+
+
+def test_companion_argument_checks(L):
+    from sparse_mla_attention_04_gb300 import binding as b
+    assert L.smla_compute_fp8_scale(None, 10, 0x100, None) == b.SMLA_ERR_NULL_POINTER
+    assert L.smla_compute_fp8_scale(0x1000, -1, 0x100, None) == b.SMLA_ERR_BAD_SHAPE
+    assert L.smla_compute_fp8_scale(0x1008, 10, 0x100, None) == b.SMLA_ERR_MISALIGNED
+    assert L.smla_fp8_cache_write(0x1000, 0x2000, 4, 12, 0x3000, 0x4000, 10, None) == b.SMLA_ERR_BAD_SHAPE
+    assert L.smla_fp8_cache_write(0x1000, None, 4, 16, 0x3000, 0x4000, 10, None) == b.SMLA_ERR_NULL_POINTER
+    assert L.smla_fp8_cache_write(0x1004, 0x2000, 4, 16, 0x3000, 0x4000, 10, None) == b.SMLA_ERR_MISALIGNED
+    assert L.smla_validate_indices(None, 2, 3, 10, 0x100, None) == b.SMLA_ERR_NULL_POINTER
+    assert L.smla_validate_indices(0x1000, -2, 3, 10, 0x100, None) == b.SMLA_ERR_BAD_SHAPE
+
+
+def test_binding_rejects_strided_and_wrong_dtypes():
+    import torch
+    from sparse_mla_attention_04_gb300 import binding as b
+    q = torch.zeros((2, 16, 512), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        b._need(q.transpose(0, 1), "q", torch.bfloat16, 3)
+    with pytest.raises(TypeError):
+        b._need(q.float(), "q", torch.bfloat16, 3)
+    with pytest.raises(ValueError):
+        b._need(q, "q", torch.bfloat16, 3)   # not a CUDA tensor

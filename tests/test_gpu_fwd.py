@@ -1,0 +1,201 @@
+"""Parity of the CUDA sparse MLA forward with the fp64 oracle (GPU).
+
+Sizes span several key tiles and splits with ragged tails while the oracle
+finishes in seconds; the edge cases cover empty and ragged inputs, the
+degenerate cases of the method and index handling (bit-exact)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parity
+from parity import DEV, TOL_BF16, compare
+from sparse_mla_attention_04_gb300 import binding, inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def test_tiny_config():
+    res, _, _ = parity.case(inputs.tiny(seed=0))
+    print(res)
+
+
+@pytest.mark.parametrize("splits", [0, 1, 2, 3, 4, 8])
+def test_decode_bf16_small(splits):
+    w = inputs.decode(n_seqs=8, ctx=8192, topk=2048, name="decode_bf16_small")
+    parity.case(w, num_splits=splits)
+
+
+def test_split_counts_agree():
+    w = inputs.decode(n_seqs=4, ctx=8192, topk=1000, name="decode_ragged")
+    outs = [parity.case(w, num_splits=s)[1] for s in (1, 2, 5, 7)]
+    for o in outs[1:]:
+        rel = np.linalg.norm(o - outs[0]) / np.linalg.norm(outs[0])
+        assert rel < 2e-3, rel
+
+
+@pytest.mark.parametrize("splits", [0, 1, 4])
+def test_decode_fp8_small(splits):
+    w = inputs.decode(n_seqs=8, ctx=8192, topk=2048, fp8=True, short_rows=2, name="decode_fp8_small")
+    res, _, _ = parity.case(w, num_splits=splits)
+    print(res)
+
+
+def test_prefill_small():
+    w = inputs.prefill(T=384, topk=128, name="prefill_small")
+    parity.case(w)
+
+
+def test_wide_head_small():
+    w = inputs.wide(T=4, ctx=4096, topk=2048, name="wide_small")
+    res, _, _ = parity.case(w)
+    print(res)
+
+
+def test_wide_head_bf16_cache():
+    w = inputs.wide(T=3, ctx=2048, topk=700, name="wide_bf16")
+    w.kv_fp8 = False
+    parity.case(w, num_splits=2)
+
+
+@pytest.mark.parametrize("topk", [1, 31, 32, 33, 63, 64, 65, 127, 129])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_topk_edges(topk, fp8):
+    w = inputs.Workload("edge", 3, 16, 512, 512, 1000, topk, fp8, 1 / math.sqrt(512), "uniform", seed=topk)
+    for s in (1, 2):
+        if s <= max(1, topk // 32):
+            parity.case(w, num_splits=s)
+
+
+def test_masks_anywhere_and_empty_rows():
+    w = inputs.Workload("masks", 5, 32, 512, 512, 3000, 200, False, 0.05, "uniform", seed=3)
+    idx = inputs.make_indices(w)
+    rng = np.random.default_rng(7)
+    idx[0, rng.choice(200, 150, replace=False)] = -1      # scattered
+    idx[1, :] = -1                                         # empty row
+    idx[2, :199] = -1                                      # one index, at the end
+    idx[3, ::2] = -1
+    for s in (1, 3, 7):
+        res, out, lse = parity.case(w, idx=idx, num_splits=s)
+        assert (out[1] == 0).all() and np.isneginf(lse[1]).all()
+
+
+def test_single_index_is_bit_exact():
+    w = inputs.Workload("single", 3, 16, 512, 512, 500, 64, False, 0.3, "uniform", seed=4)
+    idx = np.full((3, 64), -1, dtype=np.int32)
+    idx[0, 5] = 17
+    idx[1, 63] = 499
+    idx[2, 0] = 0
+    q = inputs.make_q(w)
+    kv = inputs.make_kv_source(w)
+    for s in (1, 2):
+        out, lse = binding.sparse_mla_fwd(q.to(DEV), kv.to(DEV), torch.from_numpy(idx).to(DEV), w.scale,
+                                          num_splits=s)
+        out = out.cpu()
+        for t, j in ((0, 17), (1, 499), (2, 0)):
+            assert torch.equal(out[t], kv[j].unsqueeze(0).expand(16, 512)), (s, t)
+
+
+def test_scale_zero_gives_mean():
+    w = inputs.Workload("scale0", 2, 16, 512, 512, 800, 96, False, 0.0, "uniform", seed=5)
+    parity.case(w, num_splits=2)
+
+
+def test_duplicate_indices_count():
+    w = inputs.Workload("dups", 2, 16, 512, 512, 600, 128, False, 1 / math.sqrt(512), "uniform", seed=6)
+    idx = inputs.make_indices(w)
+    idx[0, 64:] = idx[0, :64]          # every slot twice
+    idx[1, 1:40] = idx[1, 0]           # one slot 40 times
+    parity.case(w, idx=idx, num_splits=2)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_nan_poison_in_unreferenced_slots(fp8):
+    """Slots no index names (including 0 and num_slots-1) hold NaN; the output
+    must be finite and bit-identical to the run without poison."""
+    w = inputs.Workload("poison", 4, 16, 512, 512, 2048, 256, fp8, 1 / math.sqrt(512), "uniform", seed=8)
+    rng = np.random.default_rng(8)
+    idx = np.stack([1 + rng.choice(w.num_slots - 2, 256, replace=False) for _ in range(4)]).astype(np.int32)
+    idx[2, 100:] = -1
+    q = inputs.make_q(w).to(DEV)
+    kv_src = inputs.make_kv_source(w).to(DEV)
+    cache, kvs = parity.gpu_cache(kv_src, fp8)
+    used = np.zeros(w.num_slots, bool)
+    used[idx[idx >= 0]] = True
+    unused = torch.from_numpy(np.nonzero(~used)[0]).to(DEV)
+    assert used[0] == False and used[-1] == False
+    ti = torch.from_numpy(idx).to(DEV)
+    dot = "fp8" if fp8 else "auto"
+    for s in (1, 3):
+        o1, l1 = binding.sparse_mla_fwd(q, cache, ti, w.scale, kv_scale=kvs, dot_precision=dot, num_splits=s)
+        o1, l1 = o1.clone(), l1.clone()
+        poisoned = cache.clone()
+        if fp8:
+            poisoned[unused] = 0x7F
+        else:
+            poisoned[unused] = float("nan")
+        o2, l2 = binding.sparse_mla_fwd(q, poisoned, ti, w.scale, kv_scale=kvs, dot_precision=dot, num_splits=s)
+        torch.cuda.synchronize()
+        assert torch.isfinite(o2.float()).all()
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_out_of_range_indices_are_masked_and_reported():
+    w = inputs.Workload("oob", 3, 16, 512, 512, 1000, 64, False, 0.1, "uniform", seed=9)
+    idx = inputs.make_indices(w)
+    bad = idx.copy()
+    bad[0, 3] = 1000
+    bad[0, 9] = -2
+    bad[1, 0] = 2 ** 31 - 1
+    bad[2, 63] = -(2 ** 31)
+    clean = bad.copy()
+    clean[(clean < -1) | (clean >= 1000)] = -1
+    q = inputs.make_q(w).to(DEV)
+    kv = inputs.make_kv_source(w).to(DEV)
+    o1, l1 = binding.sparse_mla_fwd(q, kv, torch.from_numpy(bad).to(DEV), w.scale, num_splits=2)
+    o2, l2 = binding.sparse_mla_fwd(q, kv, torch.from_numpy(clean).to(DEV), w.scale, num_splits=2)
+    n_bad = binding.smla_validate_indices(torch.from_numpy(bad).to(DEV), 1000)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert int(n_bad.item()) == 4
+    assert int(binding.smla_validate_indices(torch.from_numpy(clean).to(DEV), 1000).item()) == 0
+
+
+def test_lse_optional_and_t_zero():
+    w = inputs.tiny()
+    q = inputs.make_q(w).to(DEV)
+    kv = inputs.make_kv_source(w).to(DEV)
+    idx = torch.from_numpy(inputs.make_indices(w)).to(DEV)
+    o1, _ = binding.sparse_mla_fwd(q, kv, idx, w.scale)
+    o2, l2 = binding.sparse_mla_fwd(q, kv, idx, w.scale, return_lse=False)
+    assert l2 is None and torch.equal(o1, o2)
+    e, el = binding.sparse_mla_fwd(q[:0], kv, idx[:0], w.scale)
+    assert e.shape == (0, 16, 512)
+
+
+def test_topk_zero_gives_empty_rows():
+    w = inputs.tiny()
+    q = inputs.make_q(w).to(DEV)
+    kv = inputs.make_kv_source(w).to(DEV)
+    idx = torch.empty((4, 0), dtype=torch.int32, device=DEV)
+    out, lse = binding.sparse_mla_fwd(q, kv, idx, w.scale)
+    torch.cuda.synchronize()
+    assert (out == 0).all() and torch.isneginf(lse).all()
+
+
+def test_workspace_errors_on_device():
+    w = inputs.tiny()
+    q = inputs.make_q(w).to(DEV)
+    kv = inputs.make_kv_source(w).to(DEV)
+    idx = torch.from_numpy(inputs.make_indices(w)).to(DEV)
+    small = torch.zeros(64, dtype=torch.uint8, device=DEV)
+    with pytest.raises(binding.SmlaError) as ei:
+        binding.sparse_mla_fwd(q, kv, idx, w.scale, num_splits=2, workspace=small)
+    assert ei.value.status == binding.SMLA_ERR_WORKSPACE_TOO_SMALL
+    # a misaligned q (odd bf16 offset) is refused before launch
+    qq = torch.empty(q.numel() + 8, dtype=torch.bfloat16, device=DEV)[1:1 + q.numel()].view(q.shape)
+    st = binding.lib().sparse_mla_fwd(qq.data_ptr(), kv.data_ptr(), 0, None, idx.data_ptr(), 4, 16, 512, 512,
+                                      4096, 128, 0.1, 0, q.data_ptr(), None, None, 0, 1, None)
+    assert st == binding.SMLA_ERR_MISALIGNED
