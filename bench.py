@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--ctx", type=int, default=0,
+                    help="override the per-row context (pool size) of a decode workload, for profiling")
     return ap.parse_args()
 
 
@@ -167,9 +169,12 @@ def ncu_traffic(workload: str):
 # workload construction
 # ----------------------------------------------------------------------------
 
-def build_workload(name: str, seed: int, rotations: int, device, rank: int):
+def build_workload(name: str, seed: int, rotations: int, device, rank: int, ctx: int = 0):
     from sparse_mla_attention_04_gb300 import binding
     w = inputs.CONFIGS[name](seed=seed)
+    if ctx and w.kind in ("decode", "wide"):
+        w.ctx = ctx
+        w.num_slots = w.T * ctx
     src = inputs.make_kv_source(w, device=device)
     if w.kv_fp8:
         cache, kvs = binding.build_fp8_cache(src)
@@ -207,7 +212,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     dist_init(world, "nccl")
-    w, src, cache, kvs, sets, l2 = build_workload(args.workload, args.seed, args.rotations, dev, rank)
+    w, src, cache, kvs, sets, l2 = build_workload(args.workload, args.seed, args.rotations, dev, rank, args.ctx)
     R = len(sets)
     dot = "fp8" if w.kv_fp8 else "auto"
     stream = torch.cuda.Stream(device=dev)

@@ -133,14 +133,18 @@ SMLA_API size_t sparse_mla_fwd_workspace_size(int T, int H, int D_qk, int D_v, i
  * out          device, bf16 [T, H, D_v], 16-byte aligned, written.
  * lse          device, float [T, H], or NULL to skip.
  * workspace    device, >= sparse_mla_fwd_workspace_size(...) bytes, 256-byte
- *              aligned; may be NULL when that size is 0. Holds per-split
- *              partial results and one counter per (row, 16-head group). It
- *              must be zero-filled before its first use; every call returns
- *              the counters to zero, so a buffer can be reused by later calls
- *              on the same stream. Calls that overlap in time must not share
- *              a workspace.
+ *              aligned; may be NULL when that size is 0, which is the case for
+ *              up to 8 splits (the splits of a row then form one thread-block
+ *              cluster and merge through distributed shared memory). With more
+ *              splits it holds the partial results and, in a fixed region at
+ *              its start, one merge counter per (row, 16-head group). It must
+ *              be zero-filled before its first use; every call returns its
+ *              counters to zero and never writes partials into that region, so
+ *              one buffer serves later calls of any shape on the same stream.
+ *              Calls that overlap in time must not share a workspace.
  * num_splits   0 = automatic (smla_plan_num_splits for the current device);
- *              otherwise the number of top-k splits to use (>= 1).
+ *              otherwise the number of top-k splits to use, 1..128. More than 8
+ *              splits need T * H / 16 <= 4096 (else SMLA_ERR_UNSUPPORTED).
  * stream       CUDA stream.
  */
 SMLA_API smla_status sparse_mla_fwd(const void *q, const void *kv_cache, int kv_dtype,

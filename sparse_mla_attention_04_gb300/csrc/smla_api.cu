@@ -41,9 +41,11 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 // Resident CTAs per SM of the warp-MMA kernel (shared memory bound).
 constexpr int kMmaCtasPerSm = 2;
-// A split keeps at least this many keys; at most this many splits.
+// A split keeps at least this many keys.
 constexpr int kMinKeysPerSplit = 64;
-constexpr int kMaxSplits = 128;
+using smla::kClusterMaxSplits;
+using smla::kMaxSplits;
+using smla::kTicketSlots;
 
 int plan_splits(int T, int H, int topk, int sm_count)
 {
@@ -80,12 +82,12 @@ WorkspaceLayout workspace_layout(int T, int H, int D_v, int S)
 {
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
     WorkspaceLayout w{};
-    if (S <= 1)
+    if (S <= kClusterMaxSplits)
         return w;
-    w.part_o = 0;
-    w.part_lse = up(w.part_o + (size_t)T * S * H * D_v * sizeof(float));
-    w.tickets = up(w.part_lse + (size_t)T * S * H * sizeof(float));
-    w.total = up(w.tickets + (size_t)T * (H / 16) * sizeof(int));
+    w.tickets = 0;
+    w.part_lse = up((size_t)kTicketSlots * sizeof(int));
+    w.part_o = up(w.part_lse + (size_t)T * S * H * sizeof(float));
+    w.total = up(w.part_o + (size_t)T * S * H * D_v * sizeof(float));
     return w;
 }
 
@@ -141,7 +143,7 @@ SMLA_API size_t sparse_mla_fwd_workspace_size(int T, int H, int D_qk, int D_v, i
             return (size_t)-1;
         S = plan_splits(T, H, topk, sms);
     }
-    if (S > kMaxSplits)
+    if (S > kMaxSplits || (S > kClusterMaxSplits && (int64_t)T * (H / 16) > kTicketSlots))
         return (size_t)-1;
     return smla::workspace_layout(T, H, D_v, S).total;
 }
@@ -191,6 +193,8 @@ SMLA_API smla_status sparse_mla_fwd(const void *q, const void *kv_cache, int kv_
             return SMLA_ERR_CUDA;
         S = plan_splits(T, H, topk, sms);
     }
+    if (S > kClusterMaxSplits && (int64_t)T * (H / 16) > kTicketSlots)
+        return SMLA_ERR_UNSUPPORTED;
     const smla::WorkspaceLayout wl = smla::workspace_layout(T, H, D_v, S);
     if (wl.total > 0) {
         if (workspace == nullptr)

@@ -4,10 +4,12 @@
 // streams the split's key rows through a multi-stage shared-memory ring with
 // 16-byte cp.async gathers (zero-filled for masked entries, which are never
 // dereferenced), computes S = q K^T and O += P V with mma.sync, and keeps an
-// online softmax in registers. A row's splits meet in a last-arriving-CTA
-// merge: every split writes (o_j, lse_j) to the workspace and takes a ticket;
-// the CTA that draws the last ticket combines the partials with LSE weights
-// and writes out / lse. Nothing spins: the ticket is a single atomic.
+// online softmax in registers. A row's splits (at most 8) form one
+// thread-block cluster: each split stages its normalised partial (o_j, lse_j)
+// in shared memory, and after a cluster barrier every split merges a slice of
+// the output from all partials through distributed shared memory with LSE
+// weights. With more splits (very small T) the partials go to the workspace
+// and the split that draws the last ticket (one atomic, no spinning) merges.
 //
 // Method sources (page titles and sections):
 //   "Enable AITER sparse MLA on gfx942, including FP8 KV" — Overview, Details
@@ -32,12 +34,16 @@
 #include "smla_device.cuh"
 #include "smla_internal.h"
 
+#include <cooperative_groups.h>
+
 #include <atomic>
 #include <cfloat>
 #include <cmath>
 
 namespace smla {
 namespace {
+
+namespace cg = cooperative_groups;
 
 constexpr int kWarps = 4;
 constexpr int kThreads = 128;
@@ -449,7 +455,55 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_fwd_mma_kernel(const F
         return;
     }
 
-    // ---- split partial: (o_j, lse_j) to the workspace, then take a ticket ----
+    if (a.S <= kClusterMaxSplits) {
+        // ---- the row's S splits form one cluster: merge through DSMEM ----
+        cg::cluster_group cluster = cg::this_cluster();
+        const int rank = (int)cluster.block_rank(); // == s
+        cluster.sync(); // every split's staged o and lse are visible cluster-wide
+        float *wts = reinterpret_cast<float *>(smem + C::OFF_RED); // [S][16]
+        if (tid < kHeads) {
+            float mx = -INFINITY;
+            for (int j = 0; j < a.S; ++j)
+                mx = fmaxf(mx, *cluster.map_shared_rank(lse_s + tid, j));
+            float tot = 0.f;
+            for (int j = 0; j < a.S; ++j) {
+                const float lj = *cluster.map_shared_rank(lse_s + tid, j);
+                const float e = (mx == -INFINITY) ? 0.f : expf(lj - mx);
+                wts[j * kHeads + tid] = e;
+                tot += e;
+            }
+            const float inv = tot > 0.f ? 1.0f / tot : 0.f;
+            for (int j = 0; j < a.S; ++j)
+                wts[j * kHeads + tid] *= inv;
+            if (rank == 0 && a.lse != nullptr)
+                a.lse[(int64_t)t * a.H + hbase + tid] = (mx == -INFINITY) ? -INFINITY : mx + logf(tot);
+        }
+        __syncthreads();
+        // this CTA writes a contiguous share of the 16 x 512 tile
+        constexpr int E4 = kHeads * kDv / 4;
+        const int chunk = (E4 + a.S - 1) / a.S;
+        const int e_end = min(E4, (rank + 1) * chunk);
+        for (int e = rank * chunk + tid; e < e_end; e += kThreads) {
+            const int h = e / (kDv / 4);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < a.S; ++j) {
+                const float w = wts[j * kHeads + h];
+                const float4 x = *cluster.map_shared_rank(reinterpret_cast<const float4 *>(ost) + e, j);
+                acc.x += w * x.x;
+                acc.y += w * x.y;
+                acc.z += w * x.z;
+                acc.w += w * x.w;
+            }
+            uint2 u;
+            u.x = pack_bf16x2(acc.x, acc.y);
+            u.y = pack_bf16x2(acc.z, acc.w);
+            *reinterpret_cast<uint2 *>(out + (int64_t)e * 4) = u;
+        }
+        cluster.sync(); // keep this CTA's staging alive until every peer has read it
+        return;
+    }
+
+    // ---- many splits: (o_j, lse_j) to the workspace, then take a ticket ----
     float *po = a.part_o + (((int64_t)t * a.S + s) * a.H + hbase) * kDv;
     for (int e = tid; e < kHeads * kDv / 4; e += kThreads)
         __stcg(reinterpret_cast<float4 *>(po) + e, reinterpret_cast<const float4 *>(ost)[e]);
@@ -533,6 +587,22 @@ cudaError_t launch_one(const FwdArgs &a, cudaStream_t stream)
     const int64_t blocks = (int64_t)a.T * (a.H / kHeads) * a.S;
     if (blocks == 0)
         return cudaSuccess;
+    if (a.S > 1 && a.S <= kClusterMaxSplits) {
+        // the S splits of a (row, head group) are consecutive blocks: one cluster
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)blocks);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = C::SMEM;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)a.S;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, kern, a);
+    }
     kern<<<dim3((unsigned)blocks), dim3(kThreads), C::SMEM, stream>>>(a);
     return cudaGetLastError();
 }

@@ -16,9 +16,9 @@ struct FwdArgs {
     const int32_t *indices; // [T, topk]
     void *out;              // bf16 [T, H, D_v]
     float *lse;             // [T, H] or nullptr
-    float *part_o;          // [T, S, H, D_v]   (S > 1)
-    float *part_lse;        // [T, S, H]        (S > 1)
-    int *tickets;           // [T, H / 16]      (S > 1)
+    float *part_o;          // [T, S, H, D_v]   (S > kClusterMaxSplits)
+    float *part_lse;        // [T, S, H]        (S > kClusterMaxSplits)
+    int *tickets;           // [T, H / 16]      (S > kClusterMaxSplits)
     int64_t num_slots;
     int T, H, D_qk, D_v, topk;
     int S;                  // splits of the top-k list
@@ -30,9 +30,21 @@ struct FwdArgs {
 // Key tile of the warp-MMA kernel (keys per pipeline stage).
 constexpr int kMmaTileKeys = 32;
 
-// Workspace layout for S > 1 (byte offsets, each 256-byte aligned).
+// Up to this many splits of a row's top-k list run as one thread-block
+// cluster and merge their partial results through distributed shared memory
+// (no workspace). More splits (very small T) merge through the workspace.
+constexpr int kClusterMaxSplits = 8;
+constexpr int kMaxSplits = 128;
+
+// The workspace opens with a fixed-size region of merge counters, so the
+// counters of any call land in memory that is zero between calls: each call
+// returns the counters it used to zero, and partial results never overlap
+// the region, whatever the shapes of earlier calls.
+constexpr int kTicketSlots = 4096;
+
+// Workspace layout for S > kClusterMaxSplits (byte offsets, 256-byte aligned).
 struct WorkspaceLayout {
-    size_t part_o, part_lse, tickets, total;
+    size_t tickets, part_lse, part_o, total;
 };
 WorkspaceLayout workspace_layout(int T, int H, int D_v, int S);
 

@@ -51,14 +51,18 @@ def test_split_plan(L):
 
 def test_workspace_size(L):
     from sparse_mla_attention_04_gb300 import binding as b
-    assert b.sparse_mla_fwd_workspace_size(64, 16, 512, 512, 2048, 0, 1) == 0
-    n = b.sparse_mla_fwd_workspace_size(64, 16, 512, 512, 2048, 0, 4)
+    # up to 8 splits merge inside a thread-block cluster: no workspace
+    for S in (1, 2, 4, 8):
+        assert b.sparse_mla_fwd_workspace_size(64, 16, 512, 512, 2048, 0, S) == 0
     up = lambda x: (x + 255) // 256 * 256
-    po = 64 * 4 * 16 * 512 * 4
-    pl = up(po) + 64 * 4 * 16 * 4
-    assert n == up(up(pl) + 64 * 1 * 4)
+    tickets = 4096 * 4
+    for T, S in ((64, 16), (3, 9)):
+        n = b.sparse_mla_fwd_workspace_size(T, 16, 512, 512, 2048, 0, S)
+        assert n == up(up(tickets + T * S * 16 * 4) + T * S * 16 * 512 * 4)
     with pytest.raises(b.SmlaError):
-        b.sparse_mla_fwd_workspace_size(64, 12, 512, 512, 2048, 0, 4)
+        b.sparse_mla_fwd_workspace_size(64, 12, 512, 512, 2048, 0, 16)
+    with pytest.raises(b.SmlaError):                       # more (row, group) pairs than counters
+        b.sparse_mla_fwd_workspace_size(8192, 16, 512, 512, 2048, 0, 16)
 
 
 def _call(L, q=0x1000, kv=0x2000, kvd=0, kvs=None, idx=0x3000, T=2, H=16, Dqk=512, Dv=512,
@@ -87,10 +91,11 @@ def test_argument_checks_return_before_any_launch(L):
     assert _call(L, q=0x1002) == b.SMLA_ERR_MISALIGNED
     assert _call(L, out=0x4008) == b.SMLA_ERR_MISALIGNED
     assert _call(L, idx=0x3002) == b.SMLA_ERR_MISALIGNED
-    assert _call(L, splits=4, ws=None) == b.SMLA_ERR_NULL_POINTER
-    assert _call(L, splits=4, ws=0x8000, wsb=100) == b.SMLA_ERR_WORKSPACE_TOO_SMALL
-    need = b.sparse_mla_fwd_workspace_size(2, 16, 512, 512, 8, 0, 4)
-    assert _call(L, splits=4, ws=0x8010, wsb=need) == b.SMLA_ERR_MISALIGNED
+    assert _call(L, splits=16, ws=None) == b.SMLA_ERR_NULL_POINTER
+    assert _call(L, splits=16, ws=0x8000, wsb=100) == b.SMLA_ERR_WORKSPACE_TOO_SMALL
+    need = b.sparse_mla_fwd_workspace_size(2, 16, 512, 512, 8, 0, 16)
+    assert _call(L, splits=16, ws=0x8010, wsb=need) == b.SMLA_ERR_MISALIGNED
+    assert _call(L, T=5000, splits=16, ws=0x8000, wsb=1 << 40) == b.SMLA_ERR_UNSUPPORTED
     assert _call(L, T=0) == b.SMLA_OK                                   # no-op
 
 

@@ -22,7 +22,7 @@ def test_tiny_config():
     print(res)
 
 
-@pytest.mark.parametrize("splits", [0, 1, 2, 3, 4, 8])
+@pytest.mark.parametrize("splits", [0, 1, 2, 3, 4, 8, 9, 16, 32])
 def test_decode_bf16_small(splits):
     w = inputs.decode(n_seqs=8, ctx=8192, topk=2048, name="decode_bf16_small")
     parity.case(w, num_splits=splits)
@@ -30,13 +30,15 @@ def test_decode_bf16_small(splits):
 
 def test_split_counts_agree():
     w = inputs.decode(n_seqs=4, ctx=8192, topk=1000, name="decode_ragged")
-    outs = [parity.case(w, num_splits=s)[1] for s in (1, 2, 5, 7)]
+    outs = [parity.case(w, num_splits=s)[1] for s in (1, 2, 5, 6, 7, 11)]
     for o in outs[1:]:
+        # each split count rounds P to bf16 against its own running max, so
+        # runs differ by the bf16 tolerance, not by fp32 noise
         rel = np.linalg.norm(o - outs[0]) / np.linalg.norm(outs[0])
-        assert rel < 2e-3, rel
+        assert rel < 5e-3, rel
 
 
-@pytest.mark.parametrize("splits", [0, 1, 4])
+@pytest.mark.parametrize("splits", [0, 1, 4, 12])
 def test_decode_fp8_small(splits):
     w = inputs.decode(n_seqs=8, ctx=8192, topk=2048, fp8=True, short_rows=2, name="decode_fp8_small")
     res, _, _ = parity.case(w, num_splits=splits)
@@ -192,10 +194,28 @@ def test_workspace_errors_on_device():
     idx = torch.from_numpy(inputs.make_indices(w)).to(DEV)
     small = torch.zeros(64, dtype=torch.uint8, device=DEV)
     with pytest.raises(binding.SmlaError) as ei:
-        binding.sparse_mla_fwd(q, kv, idx, w.scale, num_splits=2, workspace=small)
+        binding.sparse_mla_fwd(q, kv, idx, w.scale, num_splits=16, workspace=small)
     assert ei.value.status == binding.SMLA_ERR_WORKSPACE_TOO_SMALL
     # a misaligned q (odd bf16 offset) is refused before launch
     qq = torch.empty(q.numel() + 8, dtype=torch.bfloat16, device=DEV)[1:1 + q.numel()].view(q.shape)
     st = binding.lib().sparse_mla_fwd(qq.data_ptr(), kv.data_ptr(), 0, None, idx.data_ptr(), 4, 16, 512, 512,
                                       4096, 128, 0.1, 0, q.data_ptr(), None, None, 0, 1, None)
     assert st == binding.SMLA_ERR_MISALIGNED
+
+
+def test_workspace_reuse_across_shapes():
+    """One workspace buffer serves calls of different shapes and split counts
+    (the merge counters live in a fixed region that every call leaves zero)."""
+    ws = torch.zeros(64 << 20, dtype=torch.uint8, device=DEV)
+    shapes = [(2, 16, 900, 16), (5, 32, 700, 9), (1, 16, 2048, 32), (3, 16, 512, 12), (2, 16, 900, 16)]
+    for i, (T, H, topk, S) in enumerate(shapes):
+        w = inputs.Workload("reuse%d" % i, T, H, 512, 512, 4000, topk, False, 0.05, "uniform", seed=20 + i)
+        q = inputs.make_q(w)
+        kv = inputs.make_kv_source(w)
+        idx = inputs.make_indices(w)
+        out, lse = binding.sparse_mla_fwd(q.to(DEV), kv.to(DEV), torch.from_numpy(idx).to(DEV), w.scale,
+                                          num_splits=S, workspace=ws)
+        torch.cuda.synchronize()
+        ref_o, ref_l, _ = oracle.sparse_mla(q, kv, idx, w.scale)
+        compare(out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
+                ref_o, ref_l, TOL_BF16, w.name)
