@@ -84,6 +84,10 @@ SMLA_API const char *smla_status_string(int status);
 /* ABI version, (major << 16) | minor. */
 SMLA_API int smla_version(void);
 
+/* Text of the last CUDA runtime error behind an SMLA_ERR_CUDA returned to the
+ * calling thread ("no CUDA error" if there was none). Never NULL. */
+SMLA_API const char *smla_last_error_string(void);
+
 /* Number of splits of the top-k list ("split-K", [P3] jin-amd A/B: decode-sized
  * calls need it) that sparse_mla_fwd uses when num_splits == 0, for a device
  * with `sm_count` SMs. Host-only arithmetic; returns >= 1, or 0 for invalid
@@ -142,6 +146,11 @@ SMLA_API size_t sparse_mla_fwd_workspace_size(int T, int H, int D_qk, int D_v, i
  *              counters to zero and never writes partials into that region, so
  *              one buffer serves later calls of any shape on the same stream.
  *              Calls that overlap in time must not share a workspace.
+ * Kernels: 16 heads with a bf16 cache (D_qk = D_v = 512) run on the tcgen05
+ *              tensor cores with accumulators in tensor memory; every other
+ *              supported shape runs on a warp-MMA (mma.sync) kernel. Setting
+ *              SMLA_KERNEL=mma in the environment routes every call to the
+ *              warp-MMA kernel (a comparison and test switch).
  * num_splits   0 = automatic (smla_plan_num_splits for the current device);
  *              otherwise the number of top-k splits to use, 1..128. More than 8
  *              splits need T * H / 16 <= 4096 (else SMLA_ERR_UNSUPPORTED).
@@ -154,6 +163,16 @@ SMLA_API smla_status sparse_mla_fwd(const void *q, const void *kv_cache, int kv_
                                     void *out, float *lse,
                                     void *workspace, size_t workspace_bytes,
                                     int num_splits, smla_stream_t stream);
+
+/*
+ * Error word of the device-side waits (0 = none). The tcgen05 kernels wait on
+ * the tensor core and on their own warps with a time limit (about 2 s); a wait
+ * that gives up sets a bit here (1 = an awaited barrier never completed),
+ * abandons the call's arithmetic, frees its tensor memory and returns, leaving
+ * the context usable. Synchronous (copies the word from the device).
+ * reset != 0 clears it.
+ */
+SMLA_API smla_status smla_device_error(int *code, int reset);
 
 /*
  * Per-tensor fp8 scale of a bf16 tensor [P4 Test plan: scaled_fp8_quant with a

@@ -52,6 +52,8 @@ SIGNATURES = {
                               _c.c_void_p, _c.c_int64, _c.c_void_p], _c.c_int),
     "smla_validate_indices": ([_c.c_void_p, _c.c_int, _c.c_int, _c.c_int64, _c.c_void_p,
                                _c.c_void_p], _c.c_int),
+    "smla_device_error": ([_c.c_void_p, _c.c_int], _c.c_int),
+    "smla_last_error_string": ([], _c.c_char_p),
 }
 
 _lock = threading.Lock()
@@ -61,7 +63,10 @@ _lib = None
 class SmlaError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__("%s: %s" % (where, status_string(status)))
+        msg = "%s: %s" % (where, status_string(status))
+        if status == SMLA_ERR_CUDA:
+            msg += " (%s)" % lib().smla_last_error_string().decode()
+        super().__init__(msg)
 
 
 def lib() -> ctypes.CDLL:
@@ -110,6 +115,13 @@ def _need(x: torch.Tensor, name: str, dtype, ndim: int):
         raise ValueError("%s must be contiguous (strided inputs are not accepted)" % name)
     if not x.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % name)
+
+
+def smla_device_error(reset: bool = False) -> int:
+    """Error word of the device-side bounded waits (0 = none); synchronous."""
+    v = ctypes.c_int(0)
+    _check(lib().smla_device_error(ctypes.byref(v), int(reset)), "smla_device_error")
+    return int(v.value)
 
 
 def smla_version() -> int:

@@ -7,8 +7,21 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 
 namespace {
+
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
+// Record a CUDA error for smla_last_error_string and map it to a status.
+smla_status cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess)
+        return SMLA_OK;
+    t_last_cuda_error = e;
+    return SMLA_ERR_CUDA;
+}
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];
@@ -39,20 +52,39 @@ cudaError_t current_sm_count(int *out)
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-// Resident CTAs per SM of the warp-MMA kernel (shared memory bound).
-constexpr int kMmaCtasPerSm = 2;
+// Which kernel serves a call.
+enum class Path { Mma, Umma16 };
+
+// SMLA_KERNEL=mma in the environment routes every shape to the warp-MMA
+// kernel (a comparison and test switch).
+bool force_mma()
+{
+    const char *v = getenv("SMLA_KERNEL");
+    return v != nullptr && strcmp(v, "mma") == 0;
+}
+
+Path choose_path(int H, int D_qk, int D_v, bool kv_fp8)
+{
+    if (H == 16 && D_qk == 512 && D_v == 512 && !kv_fp8 && !force_mma())
+        return Path::Umma16;
+    return Path::Mma;
+}
+
+int ctas_per_sm(Path p) { return p == Path::Umma16 ? 1 : 2; }
+int tile_keys(Path p) { return p == Path::Umma16 ? smla::kUmma16TileKeys : smla::kMmaTileKeys; }
+
 // A split keeps at least this many keys.
 constexpr int kMinKeysPerSplit = 64;
 using smla::kClusterMaxSplits;
 using smla::kMaxSplits;
 using smla::kTicketSlots;
 
-int plan_splits(int T, int H, int topk, int sm_count)
+int plan_splits(int T, int H, int topk, int sm_count, Path path)
 {
     if (T <= 0 || H <= 0 || topk <= 0 || sm_count <= 0)
         return 1;
     const int64_t units = (int64_t)T * (H / 16);
-    const int64_t slots = (int64_t)sm_count * kMmaCtasPerSm;
+    const int64_t slots = (int64_t)sm_count * ctas_per_sm(path);
     int64_t S = units >= slots ? 1 : slots / units;
     const int64_t by_keys = topk / kMinKeysPerSplit;
     if (S > by_keys)
@@ -62,9 +94,8 @@ int plan_splits(int T, int H, int topk, int sm_count)
     return S < 1 ? 1 : (int)S;
 }
 
-int keys_per_split(int topk, int S)
+int keys_per_split(int topk, int S, int tile)
 {
-    const int tile = smla::kMmaTileKeys;
     const int per = (topk + S - 1) / S;
     return ((per + tile - 1) / tile) * tile;
 }
@@ -121,13 +152,18 @@ SMLA_API const char *smla_status_string(int status)
 
 SMLA_API int smla_version(void) { return (1 << 16) | 0; }
 
+SMLA_API const char *smla_last_error_string(void)
+{
+    return t_last_cuda_error == cudaSuccess ? "no CUDA error" : cudaGetErrorString(t_last_cuda_error);
+}
+
 SMLA_API int smla_plan_num_splits(int T, int H, int D_qk, int topk, int kv_dtype, int sm_count)
 {
     (void)D_qk;
     (void)kv_dtype;
     if (T < 0 || H <= 0 || H % 16 != 0 || topk < 0 || sm_count <= 0)
         return 0;
-    return plan_splits(T, H, topk, sm_count);
+    return plan_splits(T, H, topk, sm_count, choose_path(H, D_qk, 512, kv_dtype == SMLA_KV_FP8_E4M3));
 }
 
 SMLA_API size_t sparse_mla_fwd_workspace_size(int T, int H, int D_qk, int D_v, int topk, int kv_dtype,
@@ -141,7 +177,7 @@ SMLA_API size_t sparse_mla_fwd_workspace_size(int T, int H, int D_qk, int D_v, i
         int sms = 0;
         if (current_sm_count(&sms) != cudaSuccess)
             return (size_t)-1;
-        S = plan_splits(T, H, topk, sms);
+        S = plan_splits(T, H, topk, sms, choose_path(H, D_qk, D_v, kv_dtype == SMLA_KV_FP8_E4M3));
     }
     if (S > kMaxSplits || (S > kClusterMaxSplits && (int64_t)T * (H / 16) > kTicketSlots))
         return (size_t)-1;
@@ -186,12 +222,13 @@ SMLA_API smla_status sparse_mla_fwd(const void *q, const void *kv_cache, int kv_
     if (T == 0)
         return SMLA_OK;
     // 6. split plan and workspace
+    const Path path = choose_path(H, D_qk, D_v, kv_dtype == SMLA_KV_FP8_E4M3);
     int S = num_splits;
     if (S == 0) {
         int sms = 0;
-        if (current_sm_count(&sms) != cudaSuccess)
-            return SMLA_ERR_CUDA;
-        S = plan_splits(T, H, topk, sms);
+        if (const cudaError_t e = current_sm_count(&sms); e != cudaSuccess)
+            return cuda_status(e);
+        S = plan_splits(T, H, topk, sms, path);
     }
     if (S > kClusterMaxSplits && (int64_t)T * (H / 16) > kTicketSlots)
         return SMLA_ERR_UNSUPPORTED;
@@ -223,11 +260,18 @@ SMLA_API smla_status sparse_mla_fwd(const void *q, const void *kv_cache, int kv_
     a.D_v = D_v;
     a.topk = topk;
     a.S = S;
-    a.keys_per_split = topk > 0 ? keys_per_split(topk, S) : smla::kMmaTileKeys;
+    a.keys_per_split = topk > 0 ? keys_per_split(topk, S, tile_keys(path)) : tile_keys(path);
     a.scale = scale;
     a.kv_fp8 = kv_dtype == SMLA_KV_FP8_E4M3;
-    const cudaError_t e = smla::launch_fwd_mma(a, reinterpret_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return cuda_status(path == Path::Umma16 ? smla::launch_fwd_umma16(a, st) : smla::launch_fwd_mma(a, st));
+}
+
+SMLA_API smla_status smla_device_error(int *code, int reset)
+{
+    if (code == nullptr)
+        return SMLA_ERR_NULL_POINTER;
+    return cuda_status(smla::read_umma_error(code, reset != 0));
 }
 
 SMLA_API smla_status smla_compute_fp8_scale(const void *x, int64_t n, float *scale_out, smla_stream_t stream)
@@ -239,10 +283,9 @@ SMLA_API smla_status smla_compute_fp8_scale(const void *x, int64_t n, float *sca
     if (!aligned(x, 16) || !aligned(scale_out, 4))
         return SMLA_ERR_MISALIGNED;
     int sms = 0;
-    if (current_sm_count(&sms) != cudaSuccess)
-        return SMLA_ERR_CUDA;
-    const cudaError_t e = smla::launch_fp8_scale(x, n, scale_out, sms, reinterpret_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+    if (const cudaError_t e = current_sm_count(&sms); e != cudaSuccess)
+        return cuda_status(e);
+    return cuda_status(smla::launch_fp8_scale(x, n, scale_out, sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 SMLA_API smla_status smla_fp8_cache_write(const void *src, const int64_t *slot_mapping, int64_t N, int D,
@@ -255,9 +298,8 @@ SMLA_API smla_status smla_fp8_cache_write(const void *src, const int64_t *slot_m
         return SMLA_ERR_BAD_SHAPE;
     if (!aligned(src, 16) || !aligned(kv_cache, 8) || !aligned(slot_mapping, 8) || !aligned(kv_scale, 4))
         return SMLA_ERR_MISALIGNED;
-    const cudaError_t e = smla::launch_fp8_cache_write(src, slot_mapping, N, D, kv_scale, kv_cache, num_slots,
-                                                       reinterpret_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+    return cuda_status(smla::launch_fp8_cache_write(src, slot_mapping, N, D, kv_scale, kv_cache, num_slots,
+                                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
 SMLA_API smla_status smla_validate_indices(const int32_t *indices, int T, int topk, int64_t num_slots,
@@ -270,11 +312,10 @@ SMLA_API smla_status smla_validate_indices(const int32_t *indices, int T, int to
     if (!aligned(indices, 4) || !aligned(bad_count, 4))
         return SMLA_ERR_MISALIGNED;
     int sms = 0;
-    if (current_sm_count(&sms) != cudaSuccess)
-        return SMLA_ERR_CUDA;
-    const cudaError_t e = smla::launch_validate_indices(indices, (int64_t)T * topk, num_slots, bad_count, sms,
-                                                        reinterpret_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+    if (const cudaError_t e = current_sm_count(&sms); e != cudaSuccess)
+        return cuda_status(e);
+    return cuda_status(smla::launch_validate_indices(indices, (int64_t)T * topk, num_slots, bad_count, sms,
+                                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
 } // extern "C"

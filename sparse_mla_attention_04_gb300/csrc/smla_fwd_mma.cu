@@ -32,9 +32,8 @@
 //       and V = code * 2^-8 formed exactly from the code bits in registers
 //       (the 2^8 and kv_scale fold into the epilogue).
 #include "smla_device.cuh"
+#include "smla_epilogue.cuh"
 #include "smla_internal.h"
-
-#include <cooperative_groups.h>
 
 #include <atomic>
 #include <cfloat>
@@ -42,8 +41,6 @@
 
 namespace smla {
 namespace {
-
-namespace cg = cooperative_groups;
 
 constexpr int kWarps = 4;
 constexpr int kThreads = 128;
@@ -436,133 +433,7 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_fwd_mma_kernel(const F
     }
     __syncthreads();
 
-    const int hbase = hg * kHeads;
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out) + ((int64_t)t * a.H + hbase) * kDv;
-    if (a.S == 1) {
-        for (int e = tid; e < kHeads * kDv / 8; e += kThreads) {
-            const int h = e / (kDv / 8), d = (e % (kDv / 8)) * 8;
-            const float4 x = *reinterpret_cast<const float4 *>(ost + h * kDv + d);
-            const float4 y = *reinterpret_cast<const float4 *>(ost + h * kDv + d + 4);
-            uint4 u;
-            u.x = pack_bf16x2(x.x, x.y);
-            u.y = pack_bf16x2(x.z, x.w);
-            u.z = pack_bf16x2(y.x, y.y);
-            u.w = pack_bf16x2(y.z, y.w);
-            *reinterpret_cast<uint4 *>(out + (int64_t)h * kDv + d) = u;
-        }
-        if (a.lse != nullptr && tid < kHeads)
-            a.lse[(int64_t)t * a.H + hbase + tid] = lse_s[tid];
-        return;
-    }
-
-    if (a.S <= kClusterMaxSplits) {
-        // ---- the row's S splits form one cluster: merge through DSMEM ----
-        cg::cluster_group cluster = cg::this_cluster();
-        const int rank = (int)cluster.block_rank(); // == s
-        cluster.sync(); // every split's staged o and lse are visible cluster-wide
-        float *wts = reinterpret_cast<float *>(smem + C::OFF_RED); // [S][16]
-        if (tid < kHeads) {
-            float mx = -INFINITY;
-            for (int j = 0; j < a.S; ++j)
-                mx = fmaxf(mx, *cluster.map_shared_rank(lse_s + tid, j));
-            float tot = 0.f;
-            for (int j = 0; j < a.S; ++j) {
-                const float lj = *cluster.map_shared_rank(lse_s + tid, j);
-                const float e = (mx == -INFINITY) ? 0.f : expf(lj - mx);
-                wts[j * kHeads + tid] = e;
-                tot += e;
-            }
-            const float inv = tot > 0.f ? 1.0f / tot : 0.f;
-            for (int j = 0; j < a.S; ++j)
-                wts[j * kHeads + tid] *= inv;
-            if (rank == 0 && a.lse != nullptr)
-                a.lse[(int64_t)t * a.H + hbase + tid] = (mx == -INFINITY) ? -INFINITY : mx + logf(tot);
-        }
-        __syncthreads();
-        // this CTA writes a contiguous share of the 16 x 512 tile
-        constexpr int E4 = kHeads * kDv / 4;
-        const int chunk = (E4 + a.S - 1) / a.S;
-        const int e_end = min(E4, (rank + 1) * chunk);
-        for (int e = rank * chunk + tid; e < e_end; e += kThreads) {
-            const int h = e / (kDv / 4);
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int j = 0; j < a.S; ++j) {
-                const float w = wts[j * kHeads + h];
-                const float4 x = *cluster.map_shared_rank(reinterpret_cast<const float4 *>(ost) + e, j);
-                acc.x += w * x.x;
-                acc.y += w * x.y;
-                acc.z += w * x.z;
-                acc.w += w * x.w;
-            }
-            uint2 u;
-            u.x = pack_bf16x2(acc.x, acc.y);
-            u.y = pack_bf16x2(acc.z, acc.w);
-            *reinterpret_cast<uint2 *>(out + (int64_t)e * 4) = u;
-        }
-        cluster.sync(); // keep this CTA's staging alive until every peer has read it
-        return;
-    }
-
-    // ---- many splits: (o_j, lse_j) to the workspace, then take a ticket ----
-    float *po = a.part_o + (((int64_t)t * a.S + s) * a.H + hbase) * kDv;
-    for (int e = tid; e < kHeads * kDv / 4; e += kThreads)
-        __stcg(reinterpret_cast<float4 *>(po) + e, reinterpret_cast<const float4 *>(ost)[e]);
-    if (tid < kHeads)
-        __stcg(a.part_lse + ((int64_t)t * a.S + s) * a.H + hbase + tid, lse_s[tid]);
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        int *tk = a.tickets + (int64_t)t * G + hg;
-        const int ticket = atomicAdd(tk, 1);
-        const int last = (ticket == a.S - 1);
-        if (last)
-            *tk = 0; // every split of this row has arrived: reset for the next call
-        *flag_s = last;
-    }
-    __syncthreads();
-    if (!*flag_s)
-        return;
-    __threadfence();
-
-    // ---- last CTA of the row: LSE merge of the S partials ----
-    float *wts = reinterpret_cast<float *>(smem + C::OFF_RED); // [S][16]
-    if (tid < kHeads) {
-        float mx = -INFINITY;
-        for (int j = 0; j < a.S; ++j)
-            mx = fmaxf(mx, __ldcg(a.part_lse + ((int64_t)t * a.S + j) * a.H + hbase + tid));
-        float tot = 0.f;
-        for (int j = 0; j < a.S; ++j) {
-            const float lj = __ldcg(a.part_lse + ((int64_t)t * a.S + j) * a.H + hbase + tid);
-            const float e = (mx == -INFINITY) ? 0.f : expf(lj - mx);
-            wts[j * kHeads + tid] = e;
-            tot += e;
-        }
-        const float inv = tot > 0.f ? 1.0f / tot : 0.f;
-        for (int j = 0; j < a.S; ++j)
-            wts[j * kHeads + tid] *= inv;
-        if (a.lse != nullptr)
-            a.lse[(int64_t)t * a.H + hbase + tid] = (mx == -INFINITY) ? -INFINITY : mx + logf(tot);
-    }
-    __syncthreads();
-    for (int e = tid; e < kHeads * kDv / 4; e += kThreads) {
-        const int h = e / (kDv / 4);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < a.S; ++j) {
-            const float w = wts[j * kHeads + h];
-            const float4 x = (j == s) ? reinterpret_cast<const float4 *>(ost)[e]
-                                      : __ldcg(reinterpret_cast<const float4 *>(
-                                                   a.part_o + (((int64_t)t * a.S + j) * a.H + hbase) * kDv) +
-                                               e);
-            acc.x += w * x.x;
-            acc.y += w * x.y;
-            acc.z += w * x.z;
-            acc.w += w * x.w;
-        }
-        uint2 u;
-        u.x = pack_bf16x2(acc.x, acc.y);
-        u.y = pack_bf16x2(acc.z, acc.w);
-        *reinterpret_cast<uint2 *>(out + (int64_t)e * 4) = u;
-    }
+    finish_tile<kThreads>(a, ost, lse_s, reinterpret_cast<float *>(smem + C::OFF_RED), flag_s, t, hg, s, tid);
 }
 
 template <bool FP8, int DQK>

@@ -29,6 +29,8 @@ struct FwdArgs {
 
 // Key tile of the warp-MMA kernel (keys per pipeline stage).
 constexpr int kMmaTileKeys = 32;
+// Key tile of the tcgen05 16-head kernel (the M of its QK MMA).
+constexpr int kUmma16TileKeys = 64;
 
 // Up to this many splits of a row's top-k list run as one thread-block
 // cluster and merge their partial results through distributed shared memory
@@ -49,6 +51,9 @@ struct WorkspaceLayout {
 WorkspaceLayout workspace_layout(int T, int H, int D_v, int S);
 
 cudaError_t launch_fwd_mma(const FwdArgs &a, cudaStream_t stream);
+cudaError_t launch_fwd_umma16(const FwdArgs &a, cudaStream_t stream);
+// First error code recorded by a bounded device-side wait that gave up (0 = none).
+cudaError_t read_umma_error(int *out, bool reset);
 
 cudaError_t launch_fp8_scale(const void *x, int64_t n, float *scale_out, int sm_count,
                              cudaStream_t stream);

@@ -16,19 +16,33 @@ from sparse_mla_attention_04_gb300 import binding, inputs
 
 pytestmark = pytest.mark.gpu
 
+# both kernels that serve 16 heads with a bf16 cache: the tcgen05 one (default)
+# and the warp-MMA one (SMLA_KERNEL=mma)
+KERNELS = ["tcgen05", "mma"]
 
-def test_tiny_config():
+
+@pytest.fixture(params=KERNELS)
+def kernel(request, monkeypatch):
+    if request.param == "mma":
+        monkeypatch.setenv("SMLA_KERNEL", "mma")
+    else:
+        monkeypatch.delenv("SMLA_KERNEL", raising=False)
+    yield request.param
+    assert binding.smla_device_error() == 0
+
+
+def test_tiny_config(kernel):
     res, _, _ = parity.case(inputs.tiny(seed=0))
     print(res)
 
 
 @pytest.mark.parametrize("splits", [0, 1, 2, 3, 4, 8, 9, 16, 32])
-def test_decode_bf16_small(splits):
+def test_decode_bf16_small(splits, kernel):
     w = inputs.decode(n_seqs=8, ctx=8192, topk=2048, name="decode_bf16_small")
     parity.case(w, num_splits=splits)
 
 
-def test_split_counts_agree():
+def test_split_counts_agree(kernel):
     w = inputs.decode(n_seqs=4, ctx=8192, topk=1000, name="decode_ragged")
     outs = [parity.case(w, num_splits=s)[1] for s in (1, 2, 5, 6, 7, 11)]
     for o in outs[1:]:
@@ -45,7 +59,7 @@ def test_decode_fp8_small(splits):
     print(res)
 
 
-def test_prefill_small():
+def test_prefill_small(kernel):
     w = inputs.prefill(T=384, topk=128, name="prefill_small")
     parity.case(w)
 
@@ -64,14 +78,14 @@ def test_wide_head_bf16_cache():
 
 @pytest.mark.parametrize("topk", [1, 31, 32, 33, 63, 64, 65, 127, 129])
 @pytest.mark.parametrize("fp8", [False, True])
-def test_topk_edges(topk, fp8):
+def test_topk_edges(topk, fp8, kernel):
     w = inputs.Workload("edge", 3, 16, 512, 512, 1000, topk, fp8, 1 / math.sqrt(512), "uniform", seed=topk)
     for s in (1, 2):
         if s <= max(1, topk // 32):
             parity.case(w, num_splits=s)
 
 
-def test_masks_anywhere_and_empty_rows():
+def test_masks_anywhere_and_empty_rows(kernel):
     w = inputs.Workload("masks", 5, 32, 512, 512, 3000, 200, False, 0.05, "uniform", seed=3)
     idx = inputs.make_indices(w)
     rng = np.random.default_rng(7)
@@ -84,7 +98,7 @@ def test_masks_anywhere_and_empty_rows():
         assert (out[1] == 0).all() and np.isneginf(lse[1]).all()
 
 
-def test_single_index_is_bit_exact():
+def test_single_index_is_bit_exact(kernel):
     w = inputs.Workload("single", 3, 16, 512, 512, 500, 64, False, 0.3, "uniform", seed=4)
     idx = np.full((3, 64), -1, dtype=np.int32)
     idx[0, 5] = 17
@@ -100,12 +114,12 @@ def test_single_index_is_bit_exact():
             assert torch.equal(out[t], kv[j].unsqueeze(0).expand(16, 512)), (s, t)
 
 
-def test_scale_zero_gives_mean():
+def test_scale_zero_gives_mean(kernel):
     w = inputs.Workload("scale0", 2, 16, 512, 512, 800, 96, False, 0.0, "uniform", seed=5)
     parity.case(w, num_splits=2)
 
 
-def test_duplicate_indices_count():
+def test_duplicate_indices_count(kernel):
     w = inputs.Workload("dups", 2, 16, 512, 512, 600, 128, False, 1 / math.sqrt(512), "uniform", seed=6)
     idx = inputs.make_indices(w)
     idx[0, 64:] = idx[0, :64]          # every slot twice
@@ -114,7 +128,7 @@ def test_duplicate_indices_count():
 
 
 @pytest.mark.parametrize("fp8", [False, True])
-def test_nan_poison_in_unreferenced_slots(fp8):
+def test_nan_poison_in_unreferenced_slots(fp8, kernel):
     """Slots no index names (including 0 and num_slots-1) hold NaN; the output
     must be finite and bit-identical to the run without poison."""
     w = inputs.Workload("poison", 4, 16, 512, 512, 2048, 256, fp8, 1 / math.sqrt(512), "uniform", seed=8)
@@ -144,7 +158,7 @@ def test_nan_poison_in_unreferenced_slots(fp8):
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-def test_out_of_range_indices_are_masked_and_reported():
+def test_out_of_range_indices_are_masked_and_reported(kernel):
     w = inputs.Workload("oob", 3, 16, 512, 512, 1000, 64, False, 0.1, "uniform", seed=9)
     idx = inputs.make_indices(w)
     bad = idx.copy()
@@ -177,7 +191,7 @@ def test_lse_optional_and_t_zero():
     assert e.shape == (0, 16, 512)
 
 
-def test_topk_zero_gives_empty_rows():
+def test_topk_zero_gives_empty_rows(kernel):
     w = inputs.tiny()
     q = inputs.make_q(w).to(DEV)
     kv = inputs.make_kv_source(w).to(DEV)
@@ -203,7 +217,7 @@ def test_workspace_errors_on_device():
     assert st == binding.SMLA_ERR_MISALIGNED
 
 
-def test_workspace_reuse_across_shapes():
+def test_workspace_reuse_across_shapes(kernel):
     """One workspace buffer serves calls of different shapes and split counts
     (the merge counters live in a fixed region that every call leaves zero)."""
     ws = torch.zeros(64 << 20, dtype=torch.uint8, device=DEV)
@@ -219,3 +233,18 @@ def test_workspace_reuse_across_shapes():
         ref_o, ref_l, _ = oracle.sparse_mla(q, kv, idx, w.scale)
         compare(out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
                 ref_o, ref_l, TOL_BF16, w.name)
+
+
+def test_large_logits_take_the_rescale_path(kernel):
+    """Logits whose running max climbs by far more than 2^8 from tile to tile
+    force the rescale path (the tcgen05 kernel then rescales O in tensor
+    memory): q is scaled up and row 0 lists its keys in ascending order of
+    head 0's logit. V is left as drawn, so |out| stays small."""
+    w = inputs.Workload("rescale", 3, 16, 512, 512, 3000, 640, False, 0.35, "uniform", seed=31)
+    q = (inputs.make_q(w).float() * 4).to(torch.bfloat16)
+    kv = inputs.make_kv_source(w)
+    idx = inputs.make_indices(w)
+    logits0 = kv[idx[0]].float() @ q[0, 0].float()
+    idx[0] = idx[0][np.argsort(logits0.numpy())]
+    for S in (1, 2, 3):
+        parity.case(w, idx=idx, kv_src=kv, q=q, num_splits=S)
