@@ -165,6 +165,38 @@ SMLA_API smla_status sparse_mla_fwd(const void *q, const void *kv_cache, int kv_
                                     int num_splits, smla_stream_t stream);
 
 /*
+ * Maximum workspace bytes sparse_mla_fwd_no_alloc can serve from its static
+ * device array (8 MiB): every GPU that loads the library holds this much.
+ */
+#define SMLA_NO_ALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+
+/*
+ * sparse_mla_fwd without a caller-provided workspace (the pages have no
+ * counterpart; it exists for callers of this library that cannot allocate
+ * device memory: a serving engine that reserved nearly all of HBM for its
+ * KV-cache pool up front, or a host framework that only lets a plug-in use
+ * the buffers it hands over).
+ *
+ * Arguments and results are those of sparse_mla_fwd; q, kv_cache, indices,
+ * out and lse remain the caller's. When the split plan needs a workspace
+ * (more than 8 splits of a row), the library uses a static device array of
+ * SMLA_NO_ALLOC_SCRATCH_BYTES instead, and returns
+ * SMLA_ERR_WORKSPACE_TOO_SMALL (nothing launched) when the call would need
+ * more. Nothing is allocated or freed. The first call on a device, made with
+ * that device current, looks the array's device address up once
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Each call clears the array's merge counters on `stream` before launching.
+ * All calls share the one array: calls that can run at the same time on the
+ * GPU (unordered streams) race on it and must not overlap.
+ */
+SMLA_API smla_status sparse_mla_fwd_no_alloc(const void *q, const void *kv_cache, int kv_dtype,
+                                             const float *kv_scale, const int32_t *indices,
+                                             int T, int H, int D_qk, int D_v, int64_t num_slots,
+                                             int topk, float scale, int dot_precision,
+                                             void *out, float *lse, int num_splits,
+                                             smla_stream_t stream);
+
+/*
  * Error word of the device-side waits (0 = none). The tcgen05 kernels wait on
  * the tensor core and on their own warps with a time limit (about 2 s); a wait
  * that gives up sets a bit here (1 = an awaited barrier never completed),

@@ -54,6 +54,10 @@ SIGNATURES = {
                                _c.c_void_p], _c.c_int),
     "smla_device_error": ([_c.c_void_p, _c.c_int], _c.c_int),
     "smla_last_error_string": ([], _c.c_char_p),
+    "sparse_mla_fwd_no_alloc": ([_c.c_void_p, _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_void_p,
+                                 _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int64, _c.c_int,
+                                 _c.c_float, _c.c_int, _c.c_void_p, _c.c_void_p, _c.c_int,
+                                 _c.c_void_p], _c.c_int),
 }
 
 _lock = threading.Lock()
