@@ -1,5 +1,5 @@
 // Sparse MLA forward for 16 heads on the 5th-generation tensor cores
-// (tcgen05 + tensor memory), sm_103a.
+// (tcgen05 + tensor memory) with TMA row gathers, sm_103a.
 //
 // One CTA = (query row t, split s of its top-k list). With only 16 heads per
 // row the contraction is computed transposed, keys on the MMA's M axis:
@@ -9,14 +9,22 @@
 // columns). One shared-memory tile of gathered rows serves as the K-major A
 // operand of QK and, read MN-major, as V^T of PV.
 //
+// The tile is gathered by the TMA engine: a 2-D tensor map over the cache
+// ([num_slots rows x 512] bf16, boxes of 64 columns x 1 row, 128-byte
+// swizzle) and tile::gather4 copies, each moving a 64-column slice of 4
+// named rows. A 64-key tile is 16 key quads x 8 column blocks = 128 copies,
+// one per producer thread, landing as 8 blocks of [64 keys x 128 B] in
+// exactly the swizzled layout the MMA reads. Masked (-1) and out-of-range
+// indices are passed as row -1, which the TMA fills with zeros without
+// reading memory. A tile's copies are issued from four warps: the TMA engine
+// accepts copies from several warps in parallel, and one warp alone cannot
+// issue random 1 KB rows fast enough to keep up with HBM.
+//
 // Warp roles, handing tiles over through mbarriers:
-//   producers (warps 5..): gather the split's key rows, 64 per tile, with
-//     16-byte global loads into registers and store them into a 3-stage
-//     shared-memory ring in the tensor core's core-matrix layout (masked or
-//     out-of-range indices are never read; their rows are zeros), then arrive
-//     on the stage's "full" barrier. Loads through registers keep many more
-//     bytes in flight per SM than cp.async for scattered 1 KB rows. A stage is
-//     refilled once the PV that read it has completed ("empty").
+//   producers (warps 5-8): q into shared memory once; then per tile one
+//     gather4 per thread into a 3-stage ring, completing the stage's "full"
+//     barrier by transaction bytes. A stage is refilled once the PV that read
+//     it has completed ("empty").
 //   MMA issuer (warp 4, one thread): QK(i) as soon as tile i has landed, then
 //     PV(i-1) as soon as the softmax has written P(i-1); commits signal the
 //     softmax (S full), the producers (stage empty), the P buffers and O.
@@ -24,10 +32,12 @@
 //     logits from TMEM, masks, and exponentiates against a running reference
 //     max; the max is recomputed over the tile (and O^T rescaled in TMEM) only
 //     when some logit exceeds the reference by more than 2^8, so the common
-//     tile needs no cross-thread reduction; writes one row of P^T.
+//     tile needs no cross-thread reduction beyond one flag exchange; writes
+//     one row of P^T.
 // Every barrier completes once per use of the resource it guards, so no
 // waiter can fall two phases behind; every wait gives up after about 2 s
-// (the call then records an error and finishes without further waiting).
+// (the call then records an error, stops issuing, waits with a bound for the
+// copies and MMAs already issued, and finishes).
 //
 // Method sources (page titles and sections):
 //   "Enable AITER sparse MLA on gfx942, including FP8 KV" — Overview, Details.
@@ -38,8 +48,13 @@
 #include "smla_internal.h"
 #include "smla_umma.cuh"
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <atomic>
+#include <climits>
 #include <cmath>
+#include <mutex>
 
 namespace smla {
 
@@ -47,17 +62,12 @@ __device__ int g_umma_error = 0; // set when a bounded wait gives up
 
 namespace {
 
-#ifndef SMLA_UMMA16_PRODUCER_WARPS
-#define SMLA_UMMA16_PRODUCER_WARPS 8
-#endif
 constexpr int kSoftmaxWarps = 4;
 constexpr int kMmaWarp = 4;
 constexpr int kProducerWarp0 = 5;
-constexpr int kProducerThreads = 32 * SMLA_UMMA16_PRODUCER_WARPS;
-constexpr int kThreads = (kProducerWarp0 * 32) + kProducerThreads;
-constexpr int kGroupSets = kProducerThreads / 128;   // producer sets, one per column of key groups
-constexpr int kGroupsPerThread = 8 / kGroupSets;     // 8-key groups each producer moves per tile
-static_assert(kProducerThreads % 128 == 0 && 8 % kGroupSets == 0, "producer mapping");
+constexpr int kProducerWarps = 4;
+constexpr int kProducerThreads = 32 * kProducerWarps; // one gather4 per thread per tile
+constexpr int kThreads = 32 * (kProducerWarp0 + kProducerWarps);
 constexpr int kKeys = kUmma16TileKeys; // keys per tile (M of QK)
 constexpr int kHeads = 16;
 constexpr int kDv = 512;
@@ -67,39 +77,45 @@ constexpr float kRescaleThreshold = 8.0f; // log2 units: p <= 2^8 between rescal
 
 struct U16 {
     static constexpr int ROW = 1024;              // bytes per cache row (bf16, D = 512)
-    static constexpr int CPR = ROW / 16;          // core-matrix columns per row (64)
-    static constexpr int KGRP = CPR * 128;        // one 8-key group (8 KB)
-    static constexpr int TILE = 8 * KGRP;         // 64 keys (64 KB)
+    static constexpr int BLK = kKeys * 128;       // one 64-column block of a tile (8 KB)
+    static constexpr int TILE = 8 * BLK;          // 64 keys x 512 columns (64 KB)
     static constexpr int STAGES = 3;
     static constexpr int OFF_Q = STAGES * TILE;   // q [16 x 512] bf16 in core matrices (16 KB)
+    static constexpr int QGRP = 64 * 128;         // q: 8 heads x 512 columns
     static constexpr int OFF_P = OFF_Q + 16 * ROW;// P^T [64 keys x 16 heads] bf16, 2 buffers x 2 KB
     static constexpr int OFF_EX = OFF_P + 2 * 2048; // [2][4] exceed flags
-    static constexpr int OFF_WMAX = OFF_EX + 32;
+    static constexpr int OFF_GO = OFF_EX + 32;    // [2] producer issue decisions
+    static constexpr int OFF_WMAX = OFF_GO + 8;
     static constexpr int OFF_LRED = OFF_WMAX + 4 * 16 * 4;
     static constexpr int OFF_LSE = OFF_LRED + 4 * 16 * 4;
     static constexpr int OFF_ALPHA = OFF_LSE + 16 * 4;
     static constexpr int OFF_MISC = OFF_ALPHA + 16 * 4; // flag, tmem address, abort
-    static constexpr int OFF_MBAR = OFF_MISC + 16;
-    // full[3], empty[3], s_full[2], p_full[2], p_empty[2], o_done
-    static constexpr int NBAR = 13;
+    static constexpr int OFF_MBAR = (OFF_MISC + 16 + 7) & ~7;
+    // full[3], empty[3], s_full[2], p_full[2], p_empty[2], o_done, q_full, drain
+    static constexpr int NBAR = 15;
     static constexpr int SMEM = OFF_MBAR + NBAR * 8;
+    static constexpr int SMEM_ALLOC = SMEM + 1024; // the base is aligned up to 1 KB in the kernel
     static_assert(STAGES * TILE >= kHeads * kDv * 4, "epilogue staging fits in the ring");
     static_assert(16 * ROW >= 128 * kHeads * 4, "merge weights fit in the q area");
-    static_assert(OFF_MBAR % 8 == 0, "mbarrier alignment");
+    static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
-// QK: A = KV tile (K-major), B = q (K-major), M = 64 keys, N = 16 heads, bf16
+// QK: A = KV tile (K-major, 128-byte swizzle), B = q (K-major), M = 64 keys, N = 16 heads, bf16
 constexpr uint32_t kIdescQK = umma::idesc(64, 16, 1, 1, 0, 0);
 // PV: A = V^T (MN-major over the same tile), B = P^T (MN-major), M = 128 dims, N = 16
 constexpr uint32_t kIdescPV = umma::idesc(128, 16, 1, 1, 1, 1);
 
-__global__ void __launch_bounds__(kThreads, 1) sparse_mla_fwd_umma16_kernel(const FwdArgs a)
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_mla_fwd_umma16_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap kv_map)
 {
     using C = U16;
-    extern __shared__ __align__(1024) uint8_t smem[];
-    const uint32_t sbase = smem_u32(smem);
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_base = smem_u32(smem_raw);
+    const uint32_t sbase = (raw_base + 1023u) & ~1023u; // swizzle atoms need 1 KB alignment
+    uint8_t *smem = smem_raw + (sbase - raw_base);
     const uint32_t ring = sbase, q_s = sbase + C::OFF_Q, p_s = sbase + C::OFF_P;
     int *ex_s = reinterpret_cast<int *>(smem + C::OFF_EX);
+    volatile int *go_s = reinterpret_cast<volatile int *>(smem + C::OFF_GO);
     float *wmax_s = reinterpret_cast<float *>(smem + C::OFF_WMAX);
     float *lred_s = reinterpret_cast<float *>(smem + C::OFF_LRED);
     float *lse_s = reinterpret_cast<float *>(smem + C::OFF_LSE);
@@ -114,6 +130,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_fwd_umma16_kernel(cons
     auto p_full = [&](int b) { return bar0 + 8 * (8 + b); };
     auto p_empty = [&](int b) { return bar0 + 8 * (10 + b); };
     const uint32_t o_done = bar0 + 8 * 12;
+    const uint32_t q_full = bar0 + 8 * 13;
+    const uint32_t drain = bar0 + 8 * 14;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int s = blockIdx.x % a.S;
@@ -125,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_fwd_umma16_kernel(cons
 
     if (tid == 0) {
         for (int st = 0; st < C::STAGES; ++st) {
-            umma::mbar_init(full(st), kProducerThreads);
+            umma::mbar_init(full(st), 1);
             umma::mbar_init(empty(st), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -134,6 +152,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_fwd_umma16_kernel(cons
             umma::mbar_init(p_empty(b), 1);
         }
         umma::mbar_init(o_done, 1);
+        umma::mbar_init(q_full, kProducerThreads);
+        umma::mbar_init(drain, 1);
         umma::mbar_init_fence();
         *abort_s = 0;
     }
@@ -152,79 +172,85 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_fwd_umma16_kernel(cons
             *(volatile int *)abort_s = 1;
         }
     };
+    // a wait that runs even after an abort (for work already issued), still bounded
+    auto wait_issued = [&](uint32_t mbar, uint32_t parity) {
+        if (!umma::mbar_wait(mbar, parity))
+            atomicOr(&g_umma_error, 2);
+    };
 
     if (warp >= kProducerWarp0) {
         // ======================= producers =======================
-        const int ptid = tid - kProducerWarp0 * 32;
-        const uint8_t *__restrict__ kv = static_cast<const uint8_t *>(a.kv);
+        const int pt = tid - kProducerWarp0 * 32;
         const __nv_bfloat16 *__restrict__ qg =
             static_cast<const __nv_bfloat16 *>(a.q) + (int64_t)t * kHeads * 512;
-        // q [16 x 512] -> core matrices (8 heads x 16 B): LBO 128 (K), SBO 8 KB
-        // (heads); published with tile 0
-        for (int e = ptid; e < kHeads * C::CPR; e += kProducerThreads) {
-            const int h = e / C::CPR, c = e % C::CPR;
-            cp_async_16(q_s + (h >> 3) * C::KGRP + c * 128 + (h & 7) * 16, qg + h * 512 + c * 8, 16);
+        // q [16 x 512] -> core matrices (8 heads x 16 B): LBO 128 (K), SBO 8 KB (heads)
+        for (int e = pt; e < kHeads * 64; e += kProducerThreads) {
+            const int h = e >> 6, c = e & 63;
+            cp_async_16(q_s + (h >> 3) * C::QGRP + c * 128 + (h & 7) * 16, qg + h * 512 + c * 8, 16);
         }
         cp_async_commit();
         cp_async_wait<0>();
-        // The thread moves chunks 16*c4 + kc (c4 = 0..3) of key 8*g + kr for its
-        // key groups g; each warp-wide store fills four whole core matrices.
-        const int kr = ptid & 7, kc = (ptid >> 3) & 15, gs = ptid >> 7;
-        int raw[kGroupsPerThread];
-        auto fetch = [&](int tile) {
+        umma::fence_async_smem();
+        umma::mbar_arrive(q_full);
+
+        // this thread's copy: key quad qd (keys 4qd..4qd+3), column block cb
+        const int qd = pt >> 3, cb = pt & 7;
+        auto fetch = [&](int tile, int (&r)[4]) {
 #pragma unroll
-            for (int u = 0; u < kGroupsPerThread; ++u) {
-                const int p = kb + tile * kKeys + 8 * (gs * kGroupsPerThread + u) + kr;
-                raw[u] = (tile < ntiles && p < ke) ? __ldg(row_idx + p) : -1;
+            for (int u = 0; u < 4; ++u) {
+                const int p = kb + tile * kKeys + 4 * qd + u;
+                const int x = (tile < ntiles && p < ke) ? __ldg(row_idx + p) : -1;
+                r[u] = (x >= 0 && (int64_t)x < a.num_slots) ? x : -1;
             }
         };
-        fetch(0);
+        int r[4];
+        fetch(0, r);
+        int issued = 0;
         for (int j = 0; j < ntiles; ++j) {
             const int st = j % C::STAGES;
-            uint4 v[kGroupsPerThread * 4];
-#pragma unroll
-            for (int u = 0; u < kGroupsPerThread; ++u) {
-                const int r = raw[u];
-                const bool ok = r >= 0 && (int64_t)r < a.num_slots;
-                const uint4 *src = reinterpret_cast<const uint4 *>(kv + (int64_t)(ok ? r : 0) * C::ROW) + kc;
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4)
-                    v[4 * u + c4] = ok ? __ldcs(src + 16 * c4) : make_uint4(0u, 0u, 0u, 0u);
+            if (pt == 0) {
+                if (j >= C::STAGES)
+                    wait_bar(empty(st), (uint32_t)((j / C::STAGES - 1) & 1));
+                const int go = !*(volatile int *)abort_s;
+                if (go)
+                    umma::mbar_arrive_expect_tx(full(st), C::TILE);
+                go_s[j & 1] = go;
             }
-            fetch(j + 1);
-            if (j >= C::STAGES)
-                wait_bar(empty(st), (uint32_t)((j / C::STAGES - 1) & 1));
-            const uint32_t base = ring + st * C::TILE;
-#pragma unroll
-            for (int u = 0; u < kGroupsPerThread; ++u) {
-                const uint32_t dst = base + (gs * kGroupsPerThread + u) * C::KGRP + kc * 128 + kr * 16;
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    const uint4 x = v[4 * u + c4];
-                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(dst + c4 * 16 * 128), "r"(x.x),
-                                 "r"(x.y), "r"(x.z), "r"(x.w)
-                                 : "memory");
-                }
-            }
-            umma::fence_async_smem();
-            umma::mbar_arrive(full(st));
+            // all or none of a tile's copies are issued, so a stage's barrier
+            // always completes once its copies are in flight
+            umma::named_bar(2, kProducerThreads);
+            if (!go_s[j & 1])
+                break;
+            umma::tma_gather4(ring + st * C::TILE + cb * C::BLK + qd * 512, &kv_map, 64 * cb, r[0], r[1], r[2],
+                              r[3], full(st));
+            issued = j + 1;
+            fetch(j + 1, r);
+        }
+        // every copy issued has landed before the CTA can finish (also after an abort)
+        if (pt == 0) {
+            for (int j = max(0, issued - C::STAGES); j < issued; ++j)
+                wait_issued(full(j % C::STAGES), (uint32_t)((j / C::STAGES) & 1));
         }
     } else if (warp == kMmaWarp) {
         // ======================= MMA issuer =======================
         if (lane == 0) {
-            const uint64_t qdesc = umma::desc(q_s, 128, C::KGRP);
+            wait_bar(q_full, 0);
+            const uint64_t qdesc = umma::desc(q_s, 128, C::QGRP);
             auto issue_pv = [&](int i) {
                 const int b = i & 1, st = i % C::STAGES;
                 wait_bar(p_full(b), (uint32_t)((i >> 1) & 1));
+                if (*(volatile int *)abort_s)
+                    return;
                 umma::fence_after_sync();
-                const uint64_t ad = umma::desc(ring + st * C::TILE, C::KGRP, 128);
+                // V^T: MN-major, 64-column atoms 8 KB apart (LBO), 8-key atoms 1 KB apart (SBO)
+                const uint64_t ad = umma::desc_sw128(ring + st * C::TILE, C::BLK, 1024);
                 const uint64_t bd = umma::desc(p_s + b * 2048, 256, 128);
 #pragma unroll
                 for (int blk = 0; blk < 4; ++blk)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma::mma_f16(tmem + 16 * blk, ad + (uint64_t)(blk * 128 + kk * 1024), bd + (uint64_t)(kk * 32),
-                                      kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+                        umma::mma_f16(tmem + 16 * blk, ad + (uint64_t)((blk * 2 * C::BLK + kk * 2048) >> 4),
+                                      bd + (uint64_t)(kk * 32), kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
                 umma::commit(empty(st));
                 umma::commit(p_empty(b));
                 umma::commit(o_done);
@@ -232,19 +258,25 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_fwd_umma16_kernel(cons
             for (int i = 0; i < ntiles; ++i) {
                 const int b = i & 1, st = i % C::STAGES;
                 wait_bar(full(st), (uint32_t)((i / C::STAGES) & 1));
-                umma::fence_async_smem();
+                if (*(volatile int *)abort_s)
+                    break;
                 umma::fence_after_sync();
-                const uint64_t ad = umma::desc(ring + st * C::TILE, 128, C::KGRP);
+                // KV tile: K-major, 8-key atoms 1 KB apart; k-step ks reads column
+                // block ks/4, starting 32 B * (ks%4) into its 128-byte rows
+                const uint64_t ad = umma::desc_sw128(ring + st * C::TILE, 16, 1024);
 #pragma unroll 8
                 for (int ks = 0; ks < 32; ++ks)
-                    umma::mma_f16(tmem + 64 + 16 * b, ad + (uint64_t)(ks * 16), qdesc + (uint64_t)(ks * 16), kIdescQK,
-                                  ks > 0);
+                    umma::mma_f16(tmem + 64 + 16 * b, ad + (uint64_t)(((ks >> 2) * C::BLK + (ks & 3) * 32) >> 4),
+                                  qdesc + (uint64_t)(ks * 16), kIdescQK, ks > 0);
                 umma::commit(s_full(b));
                 if (i >= 1)
                     issue_pv(i - 1);
             }
             if (ntiles > 0)
                 issue_pv(ntiles - 1);
+            // every MMA issued has completed before TMEM is released
+            umma::commit(drain);
+            wait_issued(drain, 0);
         }
         __syncwarp();
     } else {
@@ -390,6 +422,21 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_fwd_umma16_kernel(cons
                           flag_s, t, 0, s, tid);
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
 } // namespace
 
 cudaError_t launch_fwd_umma16(const FwdArgs &a, cudaStream_t stream)
@@ -402,7 +449,7 @@ cudaError_t launch_fwd_umma16(const FwdArgs &a, cudaStream_t stream)
         return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(attr_done.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, U16::SMEM);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, U16::SMEM_ALLOC);
         if (e != cudaSuccess)
             return e;
         attr_done.fetch_or(bit, std::memory_order_release);
@@ -410,11 +457,29 @@ cudaError_t launch_fwd_umma16(const FwdArgs &a, cudaStream_t stream)
     const int64_t blocks = (int64_t)a.T * a.S;
     if (blocks == 0)
         return cudaSuccess;
+
+    // The cache as a 2-D tensor [rows x 512] bf16 (row pitch 1 KB), read in
+    // boxes of 64 columns x 1 row with the 128-byte swizzle. Rows beyond the
+    // int32 index range are unreachable, so the row count is clamped there.
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (encode == nullptr)
+        return cudaErrorNotSupported;
+    CUtensorMap kv_map;
+    const int64_t rows = a.num_slots < 1 ? 1 : (a.num_slots > INT_MAX ? (int64_t)INT_MAX : a.num_slots);
+    cuuint64_t gdim[2] = {(cuuint64_t)kDv, (cuuint64_t)rows};
+    cuuint64_t gstride[1] = {(cuuint64_t)U16::ROW};
+    cuuint32_t box[2] = {64, 1};
+    cuuint32_t estride[2] = {1, 1};
+    if (encode(&kv_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.kv), gdim, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+
     if (a.S > 1 && a.S <= kClusterMaxSplits) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)blocks);
         cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = U16::SMEM;
+        cfg.dynamicSmemBytes = U16::SMEM_ALLOC;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -423,9 +488,9 @@ cudaError_t launch_fwd_umma16(const FwdArgs &a, cudaStream_t stream)
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, kern, a);
+        return cudaLaunchKernelEx(&cfg, kern, a, kv_map);
     }
-    kern<<<dim3((unsigned)blocks), dim3(kThreads), U16::SMEM, stream>>>(a);
+    kern<<<dim3((unsigned)blocks), dim3(kThreads), U16::SMEM_ALLOC, stream>>>(a, kv_map);
     return cudaGetLastError();
 }
 

@@ -24,6 +24,18 @@ __device__ __forceinline__ uint64_t desc(uint32_t saddr, uint32_t lbo, uint32_t 
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
 }
 
+// Shared-memory matrix descriptor for the 128-byte swizzled layout (the
+// layout a TMA copy with CU_TENSOR_MAP_SWIZZLE_128B writes): rows of 128 B in
+// atoms of 8 rows (1 KB), the 16-byte chunk index XORed with the row index in
+// the atom; the atom base must be 1024-byte aligned. K-major: SBO = distance
+// between 8-row atoms, LBO unused, a K step inside the 128-byte row moves the
+// start address. MN-major: LBO = distance between atoms along M/N (the next
+// 64 bf16 elements), SBO = distance between atoms along K (the next 8 rows).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    return desc(saddr, lbo, sbo) | (2ull << 61);
+}
+
 // Instruction descriptor: fp32 accumulate; fmt 0/1 = f16/bf16 (kind::f16) or
 // 0 = e4m3 (kind::f8f6f4); major 0 = K-major, 1 = MN-major.
 __host__ __device__ constexpr uint32_t idesc(int M, int N, int afmt, int bfmt, int amaj, int bmaj)
@@ -96,6 +108,24 @@ __device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count)
 }
 
 __device__ __forceinline__ void mbar_init_fence() { asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory"); }
+
+// Arrive once and add `bytes` to the transaction count of the current phase.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mbar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(mbar), "r"(bytes) : "memory");
+}
+
+// TMA row gather: rows r0..r3, columns [x, x + box width) of a 2-D tensor map
+// into shared memory at dst (4 rows of the box, in the map's swizzle), bytes
+// counted on mbar. Rows outside the tensor are filled with zeros.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int x, int r0, int r1, int r2, int r3,
+                                            uint32_t mbar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];\n" ::"r"(dst),
+                 "l"(tmap), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(mbar)
+                 : "memory");
+}
 
 __device__ __forceinline__ void mbar_arrive(uint32_t mbar)
 {
