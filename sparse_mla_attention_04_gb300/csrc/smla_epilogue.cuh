@@ -49,42 +49,69 @@ __device__ __forceinline__ void finish_tile(const FwdArgs &a, float *ost, const 
         const int rank = (int)cluster.block_rank(); // == s
         cluster.sync(); // every split's staged o and lse are visible cluster-wide
         if (tid < kHeads) {
+            // every split's lse in one round of remote loads
+            float lj[kClusterMaxSplits];
+#pragma unroll
+            for (int j = 0; j < kClusterMaxSplits; ++j)
+                lj[j] = j < a.S ? *cluster.map_shared_rank(lse_s + tid, j) : -INFINITY;
             float mx = -INFINITY;
-            for (int j = 0; j < a.S; ++j)
-                mx = fmaxf(mx, *cluster.map_shared_rank(lse_s + tid, j));
+#pragma unroll
+            for (int j = 0; j < kClusterMaxSplits; ++j)
+                mx = fmaxf(mx, lj[j]);
             float tot = 0.f;
-            for (int j = 0; j < a.S; ++j) {
-                const float lj = *cluster.map_shared_rank(lse_s + tid, j);
-                const float e = (mx == -INFINITY) ? 0.f : expf(lj - mx);
-                wts[j * kHeads + tid] = e;
-                tot += e;
+#pragma unroll
+            for (int j = 0; j < kClusterMaxSplits; ++j) {
+                lj[j] = (mx == -INFINITY || j >= a.S) ? 0.f : expf(lj[j] - mx);
+                tot += lj[j];
             }
             const float inv = tot > 0.f ? 1.0f / tot : 0.f;
-            for (int j = 0; j < a.S; ++j)
-                wts[j * kHeads + tid] *= inv;
+#pragma unroll
+            for (int j = 0; j < kClusterMaxSplits; ++j)
+                if (j < a.S)
+                    wts[j * kHeads + tid] = lj[j] * inv;
             if (rank == 0 && a.lse != nullptr)
                 a.lse[(int64_t)t * a.H + hbase + tid] = (mx == -INFINITY) ? -INFINITY : mx + logf(tot);
         }
         __syncthreads();
-        // this CTA writes a contiguous share of the 16 x 512 tile
+        // this CTA writes a contiguous share of the 16 x 512 tile; each thread
+        // takes kU float4 elements and issues their remote loads together
         constexpr int E4 = kHeads * kDv / 4;
+        constexpr int kU = 4;
         const int chunk = (E4 + a.S - 1) / a.S;
-        const int e_end = min(E4, (rank + 1) * chunk);
-        for (int e = rank * chunk + tid; e < e_end; e += kThreads) {
-            const int h = e / (kDv / 4);
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int e_beg = rank * chunk, e_end = min(E4, (rank + 1) * chunk);
+        for (int e0 = e_beg + tid; e0 < e_end; e0 += kU * kThreads) {
+            float4 acc[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u)
+                acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int j = 0; j < a.S; ++j) {
-                const float w = wts[j * kHeads + h];
-                const float4 x = *cluster.map_shared_rank(reinterpret_cast<const float4 *>(ost) + e, j);
-                acc.x += w * x.x;
-                acc.y += w * x.y;
-                acc.z += w * x.z;
-                acc.w += w * x.w;
+                const float4 *src = cluster.map_shared_rank(reinterpret_cast<const float4 *>(ost), j);
+                float4 x[kU];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int e = e0 + u * kThreads;
+                    x[u] = e < e_end ? src[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int e = e0 + u * kThreads;
+                    const float w = wts[j * kHeads + min(e, E4 - 1) / (kDv / 4)];
+                    acc[u].x += w * x[u].x;
+                    acc[u].y += w * x[u].y;
+                    acc[u].z += w * x[u].z;
+                    acc[u].w += w * x[u].w;
+                }
             }
-            uint2 u;
-            u.x = pack_bf16x2(acc.x, acc.y);
-            u.y = pack_bf16x2(acc.z, acc.w);
-            *reinterpret_cast<uint2 *>(out + (int64_t)e * 4) = u;
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int e = e0 + u * kThreads;
+                if (e < e_end) {
+                    uint2 v;
+                    v.x = pack_bf16x2(acc[u].x, acc[u].y);
+                    v.y = pack_bf16x2(acc[u].z, acc[u].w);
+                    *reinterpret_cast<uint2 *>(out + (int64_t)e * 4) = v;
+                }
+            }
         }
         cluster.sync(); // keep this CTA's staging alive until every peer has read it
         return;

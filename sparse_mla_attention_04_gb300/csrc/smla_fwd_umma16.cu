@@ -5,7 +5,8 @@
 // row the contraction is computed transposed, keys on the MMA's M axis:
 //   S^T [64 keys x 16 heads] = KV_tile [64 x 512] . q^T          (QK, M=64, N=16)
 //   O^T [512 dims x 16 heads] += V^T [512 x 64 keys] . P^T       (PV, 4 x M=128, N=16)
-// Both accumulators live in tensor memory (S^T double-buffered, O^T in 64
+// Both accumulators live in tensor memory (O^T in 64 columns; S^T double-
+// buffered, each buffer as two partial sums over halves of the 512
 // columns). One shared-memory tile of gathered rows serves as the K-major A
 // operand of QK and, read MN-major, as V^T of PV.
 //
@@ -25,12 +26,16 @@
 //     gather4 per thread into a 3-stage ring, completing the stage's "full"
 //     barrier by transaction bytes. A stage is refilled once the PV that read
 //     it has completed ("empty").
-//   MMA issuer (warp 4, one thread): QK(i) as soon as tile i has landed, then
-//     PV(i-1) as soon as the softmax has written P(i-1); commits signal the
+//   MMA issuers (one thread each in three warps): two issue the halves of
+//     QK(i) as soon as tile i has landed (and the softmax is done with the S
+//     buffer), one issues PV(i) as soon as the softmax has written P(i). A
+//     single thread issues small MMAs at about one per 26 ns; two threads
+//     issue in parallel, so splitting the 48 MMAs of a tile across three
+//     issuers shortens the time each stage is held. Commits signal the
 //     softmax (S full), the producers (stage empty), the P buffers and O.
 //   softmax (warps 0-3, one key per thread of lanes 0-15): reads the key's 16
-//     logits from TMEM, masks, and exponentiates against a running reference
-//     max; the max is recomputed over the tile (and O^T rescaled in TMEM) only
+//     logits (two partial sums) from TMEM, masks, and exponentiates against a
+//     running reference max; the max is recomputed over the tile (and O^T rescaled in TMEM) only
 //     when some logit exceeds the reference by more than 2^8, so the common
 //     tile needs no cross-thread reduction beyond one flag exchange; writes
 //     one row of P^T.
@@ -63,17 +68,21 @@ __device__ int g_umma_error = 0; // set when a bounded wait gives up
 namespace {
 
 constexpr int kSoftmaxWarps = 4;
-constexpr int kMmaWarp = 4;
+constexpr int kMmaWarp = 4;       // QK, first half of the columns
 constexpr int kProducerWarp0 = 5;
 constexpr int kProducerWarps = 4;
 constexpr int kProducerThreads = 32 * kProducerWarps; // one gather4 per thread per tile
-constexpr int kThreads = 32 * (kProducerWarp0 + kProducerWarps);
+constexpr int kMmaWarp2 = kProducerWarp0 + kProducerWarps; // QK second half; PV in the next warp
+constexpr int kThreads = 32 * (kMmaWarp2 + 2);
+// tensor memory columns: O^T 0..63, S^T partial p of buffer b at kSCol + 32 p + 16 b
+constexpr int kSCol = 64;
 constexpr int kKeys = kUmma16TileKeys; // keys per tile (M of QK)
 constexpr int kHeads = 16;
 constexpr int kDv = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f; // log2 units: p <= 2^8 between rescales
+constexpr int kIdxAhead = 4;              // tiles of index look-ahead
 
 struct U16 {
     static constexpr int ROW = 1024;              // bytes per cache row (bf16, D = 512)
@@ -91,8 +100,9 @@ struct U16 {
     static constexpr int OFF_ALPHA = OFF_LSE + 16 * 4;
     static constexpr int OFF_MISC = OFF_ALPHA + 16 * 4; // flag, tmem address, abort
     static constexpr int OFF_MBAR = (OFF_MISC + 16 + 7) & ~7;
-    // full[3], empty[3], s_full[2], p_full[2], p_empty[2], o_done, q_full, drain
-    static constexpr int NBAR = 15;
+    // full[3], empty[3], s_full[2] (two commits), p_full[2], p_empty[2], q_full,
+    // drain (three commits)
+    static constexpr int NBAR = 14;
     static constexpr int SMEM = OFF_MBAR + NBAR * 8;
     static constexpr int SMEM_ALLOC = SMEM + 1024; // the base is aligned up to 1 KB in the kernel
     static_assert(STAGES * TILE >= kHeads * kDv * 4, "epilogue staging fits in the ring");
@@ -129,9 +139,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto s_full = [&](int b) { return bar0 + 8 * (6 + b); };
     auto p_full = [&](int b) { return bar0 + 8 * (8 + b); };
     auto p_empty = [&](int b) { return bar0 + 8 * (10 + b); };
-    const uint32_t o_done = bar0 + 8 * 12;
-    const uint32_t q_full = bar0 + 8 * 13;
-    const uint32_t drain = bar0 + 8 * 14;
+    const uint32_t q_full = bar0 + 8 * 12;
+    const uint32_t drain = bar0 + 8 * 13;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int s = blockIdx.x % a.S;
@@ -147,13 +156,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma::mbar_init(empty(st), 1);
         }
         for (int b = 0; b < 2; ++b) {
-            umma::mbar_init(s_full(b), 1);
+            umma::mbar_init(s_full(b), 2);
             umma::mbar_init(p_full(b), kSoftmaxWarps * 32);
             umma::mbar_init(p_empty(b), 1);
         }
-        umma::mbar_init(o_done, 1);
         umma::mbar_init(q_full, kProducerThreads);
-        umma::mbar_init(drain, 1);
+        umma::mbar_init(drain, 3);
         umma::mbar_init_fence();
         *abort_s = 0;
     }
@@ -178,35 +186,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             atomicOr(&g_umma_error, 2);
     };
 
-    if (warp >= kProducerWarp0) {
+    if (warp >= kProducerWarp0 && warp < kProducerWarp0 + kProducerWarps) {
         // ======================= producers =======================
         const int pt = tid - kProducerWarp0 * 32;
         const __nv_bfloat16 *__restrict__ qg =
             static_cast<const __nv_bfloat16 *>(a.q) + (int64_t)t * kHeads * 512;
-        // q [16 x 512] -> core matrices (8 heads x 16 B): LBO 128 (K), SBO 8 KB (heads)
+        // this thread's copy: key quad qd (keys 4qd..4qd+3), column block cb
+        const int qd = pt >> 3, cb = pt & 7;
+        // raw indices only: checking them here would wait for the loads
+        auto fetch = [&](int tile, int (&r)[4]) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int p = kb + tile * kKeys + 4 * qd + u;
+                r[u] = (tile < ntiles && p < ke) ? __ldg(row_idx + p) : -1;
+            }
+        };
+        auto row = [&](int x) { return (x >= 0 && (int64_t)x < a.num_slots) ? x : -1; };
+        // Indices are loaded kIdxAhead tiles before their copies are issued
+        // (a load from HBM under full load takes longer than a tile), in
+        // register slots fixed at compile time by unrolling over the slots.
+        int r0[4], r1[4], r2[4], r3[4];
+        static_assert(kIdxAhead == 4, "one register slot per tile of look-ahead");
+        fetch(0, r0);
+        fetch(1, r1);
+        fetch(2, r2);
+        fetch(3, r3);
+        // q [16 x 512] -> core matrices (8 heads x 16 B): LBO 128 (K), SBO 8 KB (heads);
+        // published once the first tile's copies are in flight, so both latencies overlap
         for (int e = pt; e < kHeads * 64; e += kProducerThreads) {
             const int h = e >> 6, c = e & 63;
             cp_async_16(q_s + (h >> 3) * C::QGRP + c * 128 + (h & 7) * 16, qg + h * 512 + c * 8, 16);
         }
         cp_async_commit();
-        cp_async_wait<0>();
-        umma::fence_async_smem();
-        umma::mbar_arrive(q_full);
-
-        // this thread's copy: key quad qd (keys 4qd..4qd+3), column block cb
-        const int qd = pt >> 3, cb = pt & 7;
-        auto fetch = [&](int tile, int (&r)[4]) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int p = kb + tile * kKeys + 4 * qd + u;
-                const int x = (tile < ntiles && p < ke) ? __ldg(row_idx + p) : -1;
-                r[u] = (x >= 0 && (int64_t)x < a.num_slots) ? x : -1;
-            }
+        bool q_pending = true;
+        auto publish_q = [&] {
+            cp_async_wait<0>();
+            umma::fence_async_smem();
+            umma::mbar_arrive(q_full);
+            q_pending = false;
         };
-        int r[4];
-        fetch(0, r);
         int issued = 0;
-        for (int j = 0; j < ntiles; ++j) {
+        bool stop = false;
+        auto step = [&](int j, int(&r)[4]) {
+            if (stop || j >= ntiles) {
+                stop = true;
+                return;
+            }
             const int st = j % C::STAGES;
             if (pt == 0) {
                 if (j >= C::STAGES)
@@ -219,61 +244,79 @@ __global__ void __launch_bounds__(kThreads, 1)
             // all or none of a tile's copies are issued, so a stage's barrier
             // always completes once its copies are in flight
             umma::named_bar(2, kProducerThreads);
-            if (!go_s[j & 1])
-                break;
-            umma::tma_gather4(ring + st * C::TILE + cb * C::BLK + qd * 512, &kv_map, 64 * cb, r[0], r[1], r[2],
-                              r[3], full(st));
+            if (!go_s[j & 1]) {
+                stop = true;
+                return;
+            }
+            umma::tma_gather4(ring + st * C::TILE + cb * C::BLK + qd * 512, &kv_map, 64 * cb, row(r[0]), row(r[1]),
+                              row(r[2]), row(r[3]), full(st));
             issued = j + 1;
-            fetch(j + 1, r);
+            fetch(j + kIdxAhead, r);
+            if (q_pending)
+                publish_q();
+        };
+        for (int j0 = 0; !stop; j0 += kIdxAhead) {
+            step(j0, r0);
+            step(j0 + 1, r1);
+            step(j0 + 2, r2);
+            step(j0 + 3, r3);
         }
+        if (q_pending)
+            publish_q();
         // every copy issued has landed before the CTA can finish (also after an abort)
         if (pt == 0) {
             for (int j = max(0, issued - C::STAGES); j < issued; ++j)
                 wait_issued(full(j % C::STAGES), (uint32_t)((j / C::STAGES) & 1));
         }
-    } else if (warp == kMmaWarp) {
-        // ======================= MMA issuer =======================
+    } else if (warp == kMmaWarp || warp >= kMmaWarp2) {
+        // ======================= MMA issuers =======================
         if (lane == 0) {
-            wait_bar(q_full, 0);
-            const uint64_t qdesc = umma::desc(q_s, 128, C::QGRP);
-            auto issue_pv = [&](int i) {
-                const int b = i & 1, st = i % C::STAGES;
-                wait_bar(p_full(b), (uint32_t)((i >> 1) & 1));
-                if (*(volatile int *)abort_s)
-                    return;
-                umma::fence_after_sync();
-                // V^T: MN-major, 64-column atoms 8 KB apart (LBO), 8-key atoms 1 KB apart (SBO)
-                const uint64_t ad = umma::desc_sw128(ring + st * C::TILE, C::BLK, 1024);
-                const uint64_t bd = umma::desc(p_s + b * 2048, 256, 128);
+            const int role = warp == kMmaWarp ? 0 : 1 + warp - kMmaWarp2; // 0, 1: QK halves; 2: PV
+            if (role < 2) {
+                wait_bar(q_full, 0);
+                const uint64_t qdesc = umma::desc(q_s, 128, C::QGRP);
+                const int ks0 = 16 * role;
+                for (int i = 0; i < ntiles; ++i) {
+                    const int b = i & 1, st = i % C::STAGES;
+                    wait_bar(full(st), (uint32_t)((i / C::STAGES) & 1));
+                    if (i >= 2) // the softmax has read S buffer b for tile i-2
+                        wait_bar(p_full(b), (uint32_t)(((i - 2) >> 1) & 1));
+                    if (*(volatile int *)abort_s)
+                        break;
+                    umma::fence_after_sync();
+                    // KV tile: K-major, 8-key atoms 1 KB apart; k-step ks reads column
+                    // block ks/4, starting 32 B * (ks%4) into its 128-byte rows
+                    const uint64_t ad = umma::desc_sw128(ring + st * C::TILE, 16, 1024);
 #pragma unroll
-                for (int blk = 0; blk < 4; ++blk)
+                    for (int ks = ks0; ks < ks0 + 16; ++ks)
+                        umma::mma_f16(tmem + kSCol + 32 * role + 16 * b,
+                                      ad + (uint64_t)(((ks >> 2) * C::BLK + (ks & 3) * 32) >> 4),
+                                      qdesc + (uint64_t)(ks * 16), kIdescQK, ks > ks0);
+                    umma::commit(s_full(b));
+                }
+            } else {
+                for (int i = 0; i < ntiles; ++i) {
+                    const int b = i & 1, st = i % C::STAGES;
+                    wait_bar(p_full(b), (uint32_t)((i >> 1) & 1));
+                    if (*(volatile int *)abort_s)
+                        break;
+                    umma::fence_after_sync();
+                    // V^T: MN-major, 64-column atoms 8 KB apart (LBO), 8-key atoms 1 KB apart (SBO)
+                    const uint64_t ad = umma::desc_sw128(ring + st * C::TILE, C::BLK, 1024);
+                    const uint64_t bd = umma::desc(p_s + b * 2048, 256, 128);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        umma::mma_f16(tmem + 16 * blk, ad + (uint64_t)((blk * 2 * C::BLK + kk * 2048) >> 4),
-                                      bd + (uint64_t)(kk * 32), kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
-                umma::commit(empty(st));
-                umma::commit(p_empty(b));
-                umma::commit(o_done);
-            };
-            for (int i = 0; i < ntiles; ++i) {
-                const int b = i & 1, st = i % C::STAGES;
-                wait_bar(full(st), (uint32_t)((i / C::STAGES) & 1));
-                if (*(volatile int *)abort_s)
-                    break;
-                umma::fence_after_sync();
-                // KV tile: K-major, 8-key atoms 1 KB apart; k-step ks reads column
-                // block ks/4, starting 32 B * (ks%4) into its 128-byte rows
-                const uint64_t ad = umma::desc_sw128(ring + st * C::TILE, 16, 1024);
-#pragma unroll 8
-                for (int ks = 0; ks < 32; ++ks)
-                    umma::mma_f16(tmem + 64 + 16 * b, ad + (uint64_t)(((ks >> 2) * C::BLK + (ks & 3) * 32) >> 4),
-                                  qdesc + (uint64_t)(ks * 16), kIdescQK, ks > 0);
-                umma::commit(s_full(b));
-                if (i >= 1)
-                    issue_pv(i - 1);
+                    for (int blk = 0; blk < 4; ++blk)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            umma::mma_f16(tmem + 16 * blk, ad + (uint64_t)((blk * 2 * C::BLK + kk * 2048) >> 4),
+                                          bd + (uint64_t)(kk * 32), kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+                    // PV(i) follows the softmax's read of S(i), so QK(i) is complete too.
+                    // p_empty(b) also tells the softmax that O^T holds PV(0..i): PVs
+                    // are issued by this one thread and complete in order.
+                    umma::commit(empty(st));
+                    umma::commit(p_empty(b));
+                }
             }
-            if (ntiles > 0)
-                issue_pv(ntiles - 1);
             // every MMA issued has completed before TMEM is released
             umma::commit(drain);
             wait_issued(drain, 0);
@@ -294,20 +337,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int p = kb + tile * kKeys + key;
             return (lane < 16 && tile < ntiles && p < ke) ? __ldg(row_idx + p) : -1;
         };
-        int my_idx = load_idx(0);
-        for (int i = 0; i < ntiles; ++i) {
+        // the key's index, loaded kIdxAhead tiles ahead in fixed register slots
+        int x0 = load_idx(0), x1 = load_idx(1), x2 = load_idx(2), x3 = load_idx(3);
+        auto step = [&](int i, int &my_idx) {
+            if (i >= ntiles)
+                return;
             const int b = i & 1;
             const bool kvalid = my_idx >= 0 && (int64_t)my_idx < a.num_slots;
-            my_idx = load_idx(i + 1);
+            my_idx = load_idx(i + kIdxAhead);
             wait_bar(s_full(b), (uint32_t)((i >> 1) & 1));
             umma::fence_after_sync();
-            float sv[16];
-            umma::ld16(tmem + 64 + 16 * b + tm_lane, reinterpret_cast<uint32_t(&)[16]>(sv));
+            float sv[16], s2[16];
+            umma::ld16(tmem + kSCol + 16 * b + tm_lane, reinterpret_cast<uint32_t(&)[16]>(sv));
+            umma::ld16(tmem + kSCol + 32 + 16 * b + tm_lane, reinterpret_cast<uint32_t(&)[16]>(s2));
             umma::wait_ld();
             bool exceed = false;
 #pragma unroll
             for (int h = 0; h < 16; ++h) {
-                sv[h] = kvalid ? sv[h] * fac : -INFINITY;
+                sv[h] = kvalid ? (sv[h] + s2[h]) * fac : -INFINITY;
                 exceed |= sv[h] > m_ref[h] + kRescaleThreshold;
             }
             exceed = __any_sync(0xffffffffu, exceed);
@@ -338,8 +385,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 umma::named_bar(1, kSoftmaxWarps * 32);
                 if (i >= 1) {
-                    // O^T holds PV(0..i-1): let PV(i-1) finish, then rescale each head (column)
-                    wait_bar(o_done, (uint32_t)((i - 1) & 1));
+                    // O^T holds PV(0..i-1): let PV(i-1) finish (its P buffer's barrier; this
+                    // thread already waited there for PV(i-3), so the phase cannot alias),
+                    // then rescale each head (column)
+                    wait_bar(p_empty((i - 1) & 1), (uint32_t)(((i - 1) >> 1) & 1));
                     umma::fence_after_sync();
 #pragma unroll
                     for (int blk = 0; blk < 4; ++blk) {
@@ -374,10 +423,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma::fence_async_smem();
             umma::fence_before_sync();
             umma::mbar_arrive(p_full(b));
+        };
+        for (int i0 = 0; i0 < ntiles; i0 += kIdxAhead) {
+            step(i0, x0);
+            step(i0 + 1, x1);
+            step(i0 + 2, x2);
+            step(i0 + 3, x3);
         }
         // ---- epilogue part 1: l per head, normalised O^T -> staging [16][512] fp32 ----
-        if (ntiles > 0)
-            wait_bar(o_done, (uint32_t)((ntiles - 1) & 1)); // the last PV (and every MMA) is done
+        if (ntiles > 0) // the last PV is done (and with it every earlier PV)
+            wait_bar(p_empty((ntiles - 1) & 1), (uint32_t)(((ntiles - 1) >> 1) & 1));
         umma::fence_after_sync();
 #pragma unroll
         for (int h = 0; h < 16; ++h) {
@@ -391,26 +446,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 lred_s[warp * 16 + h] = l_part[h];
         }
         umma::named_bar(1, kSoftmaxWarps * 32);
+        if (tid < 16) { // thread h finishes head h (all heads at once)
+            float mh = m_ref[0];
 #pragma unroll
-        for (int h = 0; h < 16; ++h) {
-            if (tid == h) {
-                const float l = lred_s[h] + lred_s[16 + h] + lred_s[32 + h] + lred_s[48 + h];
-                lse_s[h] = l > 0.f ? (m_ref[h] + log2f(l)) * kLn2 : -INFINITY;
-                alpha_s[h] = l > 0.f ? 1.0f / l : 0.f; // reused: 1 / l per head
-            }
+            for (int h = 1; h < 16; ++h)
+                mh = tid == h ? m_ref[h] : mh;
+            const float l = lred_s[tid] + lred_s[16 + tid] + lred_s[32 + tid] + lred_s[48 + tid];
+            lse_s[tid] = l > 0.f ? (mh + log2f(l)) * kLn2 : -INFINITY;
+            alpha_s[tid] = l > 0.f ? 1.0f / l : 0.f; // reused: 1 / l per head
         }
         umma::named_bar(1, kSoftmaxWarps * 32);
         float *ost = reinterpret_cast<float *>(smem);
+        uint32_t o[4][16];
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk)
+            umma::ld16(tmem + 16 * blk + tm_lane, o[blk]);
+        umma::wait_ld();
 #pragma unroll
         for (int blk = 0; blk < 4; ++blk) {
-            uint32_t o[16];
-            umma::ld16(tmem + 16 * blk + tm_lane, o);
-            umma::wait_ld();
             const int d = blk * 128 + warp * 32 + lane;
 #pragma unroll
             for (int h = 0; h < 16; ++h) {
                 const float iv = alpha_s[h];
-                ost[h * kDv + d] = iv > 0.f ? __uint_as_float(o[h]) * iv : 0.f;
+                ost[h * kDv + d] = iv > 0.f ? __uint_as_float(o[blk][h]) * iv : 0.f;
             }
         }
         umma::fence_before_sync();
