@@ -63,9 +63,12 @@ bool force_mma()
     return v != nullptr && strcmp(v, "mma") == 0;
 }
 
+// 16 heads with D_qk = D_v = 512 (bf16 cache, or E4M3 cache with fp8 dots):
+// the tcgen05 kernel; every other shape: the warp-MMA kernel.
 Path choose_path(int H, int D_qk, int D_v, bool kv_fp8)
 {
-    if (H == 16 && D_qk == 512 && D_v == 512 && !kv_fp8 && !force_mma())
+    (void)kv_fp8;
+    if (H == 16 && D_qk == 512 && D_v == 512 && !force_mma())
         return Path::Umma16;
     return Path::Mma;
 }

@@ -1,5 +1,6 @@
 // Sparse MLA forward for 16 heads on the 5th-generation tensor cores
-// (tcgen05 + tensor memory) with TMA row gathers, sm_103a.
+// (tcgen05 + tensor memory) with TMA row gathers, sm_103a. Two variants: a
+// bf16 cache, and an E4M3 cache with a per-tensor scale and fp8 QK dots.
 //
 // One CTA = (query row t, split s of its top-k list). With only 16 heads per
 // row the contraction is computed transposed, keys on the MMA's M axis:
@@ -7,45 +8,57 @@
 //   O^T [512 dims x 16 heads] += V^T [512 x 64 keys] . P^T       (PV, 4 x M=128, N=16)
 // Both accumulators live in tensor memory (O^T in 64 columns; S^T double-
 // buffered, each buffer as two partial sums over halves of the 512
-// columns). One shared-memory tile of gathered rows serves as the K-major A
-// operand of QK and, read MN-major, as V^T of PV.
+// columns).
 //
 // The tile is gathered by the TMA engine: a 2-D tensor map over the cache
-// ([num_slots rows x 512] bf16, boxes of 64 columns x 1 row, 128-byte
-// swizzle) and tile::gather4 copies, each moving a 64-column slice of 4
-// named rows. A 64-key tile is 16 key quads x 8 column blocks = 128 copies,
-// one per producer thread, landing as 8 blocks of [64 keys x 128 B] in
-// exactly the swizzled layout the MMA reads. Masked (-1) and out-of-range
-// indices are passed as row -1, which the TMA fills with zeros without
-// reading memory. A tile's copies are issued from four warps: the TMA engine
-// accepts copies from several warps in parallel, and one warp alone cannot
-// issue random 1 KB rows fast enough to keep up with HBM.
+// ([num_slots rows x 512] elements, boxes of 128 bytes x 1 row, 128-byte
+// swizzle) and tile::gather4 copies, each moving a 128-byte column block of
+// 4 named rows. A 64-key tile is 16 key quads x (8 bf16 | 4 E4M3) column
+// blocks, landing as blocks of [64 keys x 128 B] in exactly the swizzled
+// layout the MMA reads. Masked (-1) and out-of-range indices are passed as
+// row -1, which the TMA fills with zeros without reading memory. A tile's
+// copies are issued from four warps: the TMA engine accepts copies from
+// several warps in parallel, and one warp alone cannot issue random rows
+// fast enough to keep up with HBM.
+//
+// bf16 cache: the tile is the K-major A operand of QK and, read MN-major,
+// V^T of PV.
+// E4M3 cache: q is quantized in the kernel per (row, head), s_q =
+// amax|q[t,h,:]| / 448 (1 if zero), q8 = RNE_satfinite(q / s_q); QK runs in
+// E4M3 (kind::f8f6f4) on the gathered tile and the logits are scaled by
+// scale * s_q * kv_scale. PV needs 16-bit operands of one type, so four
+// converter warps rewrite each tile's values as binary16 holding code * 2^-8
+// (exact: the code's bits shifted into a binary16) into a separate swizzled
+// tile, and P is kept in fp16; the 2^8 and kv_scale are applied with 1/l.
 //
 // Warp roles, handing tiles over through mbarriers:
-//   producers (warps 5-8): q into shared memory once; then per tile one
-//     gather4 per thread into a 3-stage ring, completing the stage's "full"
-//     barrier by transaction bytes. A stage is refilled once the PV that read
-//     it has completed ("empty").
-//   MMA issuers (one thread each in three warps): two issue the halves of
-//     QK(i) as soon as tile i has landed (and the softmax is done with the S
-//     buffer), one issues PV(i) as soon as the softmax has written P(i). A
+//   producers (warps 5-8): q into shared memory once (quantized for E4M3);
+//     then per tile one gather4 per thread into the stage ring, completing
+//     the stage's "full" barrier by transaction bytes. A stage is refilled
+//     once everything that reads it is done ("empty").
+//   MMA issuers (one thread each in warps 4, 9, 10): two issue the halves
+//     of QK(i) as soon as tile i has landed (and the softmax is done with the
+//     S buffer), one issues PV(i) as soon as the softmax has written P(i). A
 //     single thread issues small MMAs at about one per 26 ns; two threads
-//     issue in parallel, so splitting the 48 MMAs of a tile across three
-//     issuers shortens the time each stage is held. Commits signal the
-//     softmax (S full), the producers (stage empty), the P buffers and O.
+//     issue in parallel, so splitting a tile's MMAs across three issuers
+//     shortens the time each stage is held. Commits signal the softmax (S
+//     full), the producers (stage empty) and the P buffers.
+//   converters (E4M3 only, warps 11-14): tile i -> the binary16 value tile,
+//     once PV(i-1) is done with it.
 //   softmax (warps 0-3, one key per thread of lanes 0-15): reads the key's 16
 //     logits (two partial sums) from TMEM, masks, and exponentiates against a
-//     running reference max; the max is recomputed over the tile (and O^T rescaled in TMEM) only
-//     when some logit exceeds the reference by more than 2^8, so the common
-//     tile needs no cross-thread reduction beyond one flag exchange; writes
-//     one row of P^T.
+//     running reference max; the max is recomputed over the tile (and O^T
+//     rescaled in TMEM) only when some logit exceeds the reference by more
+//     than 2^8, so the common tile needs no cross-thread reduction beyond one
+//     flag exchange; writes one row of P^T.
 // Every barrier completes once per use of the resource it guards, so no
 // waiter can fall two phases behind; every wait gives up after about 2 s
 // (the call then records an error, stops issuing, waits with a bound for the
 // copies and MMAs already issued, and finishes).
 //
 // Method sources (page titles and sections):
-//   "Enable AITER sparse MLA on gfx942, including FP8 KV" — Overview, Details.
+//   "Enable AITER sparse MLA on gfx942, including FP8 KV" — Overview, Details
+//     ("FP8 KV on gfx942": the kernel quantizes q per tile, dots in fp8).
 //   "Route gfx942 sparse MLA prefill to AITER pa_prefill_sparse" — jin-amd
 //     A/B: split-K for decode-sized calls.
 #include "smla_device.cuh"
@@ -71,28 +84,41 @@ constexpr int kSoftmaxWarps = 4;
 constexpr int kMmaWarp = 4;       // QK, first half of the columns
 constexpr int kProducerWarp0 = 5;
 constexpr int kProducerWarps = 4;
-constexpr int kProducerThreads = 32 * kProducerWarps; // one gather4 per thread per tile
+constexpr int kProducerThreads = 32 * kProducerWarps;
 constexpr int kMmaWarp2 = kProducerWarp0 + kProducerWarps; // QK second half; PV in the next warp
-constexpr int kThreads = 32 * (kMmaWarp2 + 2);
+constexpr int kConverterWarp0 = kMmaWarp2 + 2;             // E4M3 only
+constexpr int kConverterThreads = 128;
 // tensor memory columns: O^T 0..63, S^T partial p of buffer b at kSCol + 32 p + 16 b
 constexpr int kSCol = 64;
 constexpr int kKeys = kUmma16TileKeys; // keys per tile (M of QK)
 constexpr int kHeads = 16;
-constexpr int kDv = 512;
+constexpr int kD = 512;                // D_qk = D_v
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f; // log2 units: p <= 2^8 between rescales
 constexpr int kIdxAhead = 4;              // tiles of index look-ahead
 
-struct U16 {
-    static constexpr int ROW = 1024;              // bytes per cache row (bf16, D = 512)
-    static constexpr int BLK = kKeys * 128;       // one 64-column block of a tile (8 KB)
-    static constexpr int TILE = 8 * BLK;          // 64 keys x 512 columns (64 KB)
-    static constexpr int STAGES = 3;
-    static constexpr int OFF_Q = STAGES * TILE;   // q [16 x 512] bf16 in core matrices (16 KB)
-    static constexpr int QGRP = 64 * 128;         // q: 8 heads x 512 columns
-    static constexpr int OFF_P = OFF_Q + 16 * ROW;// P^T [64 keys x 16 heads] bf16, 2 buffers x 2 KB
-    static constexpr int OFF_EX = OFF_P + 2 * 2048; // [2][4] exceed flags
+template <bool FP8>
+struct Cfg {
+    static constexpr int EB = FP8 ? 1 : 2;        // bytes per cache element
+    static constexpr int ROW = kD * EB;           // bytes per cache row
+    static constexpr int NCB = ROW / 128;         // 128-byte column blocks per row (8 | 4)
+    static constexpr int BOXW = 128 / EB;         // elements per gather box
+    static constexpr int BLK = kKeys * 128;       // one column block of a tile (8 KB)
+    static constexpr int TILE = NCB * BLK;        // 64 keys (64 KB | 32 KB)
+    static constexpr int COPIES = 16 * NCB;       // gather4 copies per tile (128 | 64)
+    static constexpr int STAGES = FP8 ? 4 : 3;
+    static constexpr int KSTEP = FP8 ? 32 : 16;   // reduction depth of one QK MMA
+    static constexpr int QK_MMAS = kD / KSTEP;    // per tile (32 | 16)
+    static constexpr int QK_ISSUERS = FP8 ? 1 : 2; // threads issuing QK (S partial sums)
+    static constexpr int V16 = 8 * BLK;           // binary16 value tile (E4M3 only), 64 KB
+    static constexpr int OFF_V16 = STAGES * TILE;
+    static constexpr int OFF_Q = OFF_V16 + (FP8 ? V16 : 0); // q [16 x 512] in core matrices
+    static constexpr int QGRP = 8 * ROW;          // q: 8 heads x 512 elements
+    static constexpr int OFF_P = OFF_Q + 2 * QGRP;// P^T [64 keys x 16 heads] 16-bit, 2 buffers x 2 KB
+    static constexpr int OFF_SQ = OFF_P + 2 * 2048; // [16] per-head q scales (E4M3)
+    static constexpr int OFF_FAC = OFF_SQ + 16 * 4; // [16] per-head logit factors (E4M3)
+    static constexpr int OFF_EX = OFF_FAC + 16 * 4; // [2][4] exceed flags
     static constexpr int OFF_GO = OFF_EX + 32;    // [2] producer issue decisions
     static constexpr int OFF_WMAX = OFF_GO + 8;
     static constexpr int OFF_LRED = OFF_WMAX + 4 * 16 * 4;
@@ -100,30 +126,53 @@ struct U16 {
     static constexpr int OFF_ALPHA = OFF_LSE + 16 * 4;
     static constexpr int OFF_MISC = OFF_ALPHA + 16 * 4; // flag, tmem address, abort
     static constexpr int OFF_MBAR = (OFF_MISC + 16 + 7) & ~7;
-    // full[3], empty[3], s_full[2] (two commits), p_full[2], p_empty[2], q_full,
-    // drain (three commits)
-    static constexpr int NBAR = 14;
+    // full[S], empty[S], s_full[2] (a commit per QK issuer), p_full[2], p_empty[2],
+    // q_full, drain (a commit per MMA issuer), v_full (E4M3)
+    static constexpr int NBAR = 2 * STAGES + 9;
     static constexpr int SMEM = OFF_MBAR + NBAR * 8;
     static constexpr int SMEM_ALLOC = SMEM + 1024; // the base is aligned up to 1 KB in the kernel
-    static_assert(STAGES * TILE >= kHeads * kDv * 4, "epilogue staging fits in the ring");
-    static_assert(16 * ROW >= 128 * kHeads * 4, "merge weights fit in the q area");
+    static constexpr int THREADS = 32 * (FP8 ? kConverterWarp0 + 4 : kConverterWarp0);
+    // E4M3: 15 warps share the register file, so at most 128 registers a thread
+    static constexpr int BOUND_THREADS = FP8 ? 512 : THREADS;
+    // stage "empty" arrivals: the PV commit (bf16), or the QK commits and every
+    // converter thread (E4M3: PV reads the binary16 tile, not the stage)
+    static constexpr int EMPTY_COUNT = FP8 ? QK_ISSUERS + kConverterThreads : 1;
+    static_assert(STAGES * TILE >= kHeads * kD * 4, "epilogue staging fits in the ring");
+    static_assert(2 * QGRP >= 128 * kHeads * 4, "merge weights fit in the q area");
+    static_assert(COPIES <= kProducerThreads, "one copy per producer thread at most");
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
-// QK: A = KV tile (K-major, 128-byte swizzle), B = q (K-major), M = 64 keys, N = 16 heads, bf16
-constexpr uint32_t kIdescQK = umma::idesc(64, 16, 1, 1, 0, 0);
-// PV: A = V^T (MN-major over the same tile), B = P^T (MN-major), M = 128 dims, N = 16
-constexpr uint32_t kIdescPV = umma::idesc(128, 16, 1, 1, 1, 1);
+// QK: A = KV tile (K-major, 128-byte swizzle), B = q (K-major), M = 64 keys, N = 16 heads
+constexpr uint32_t kIdescQKbf16 = umma::idesc(64, 16, 1, 1, 0, 0);
+constexpr uint32_t kIdescQKe4m3 = umma::idesc(64, 16, 0, 0, 0, 0);
+// PV: A = V^T (MN-major), B = P^T (MN-major), M = 128 dims, N = 16; bf16 or fp16
+constexpr uint32_t kIdescPVbf16 = umma::idesc(128, 16, 1, 1, 1, 1);
+constexpr uint32_t kIdescPVf16 = umma::idesc(128, 16, 0, 0, 1, 1);
 
-__global__ void __launch_bounds__(kThreads, 1)
+// Bytes B and B+1 of w (E4M3 codes) as an f16x2 holding each code's value
+// times 2^-8 (low half from byte B); see e4m3x2_to_f16x2_scaled.
+template <int B>
+__device__ __forceinline__ uint32_t e4m3pair_to_f16x2_scaled(uint32_t w)
+{
+    constexpr uint32_t sel = 4u | (B << 4) | (4u << 8) | ((B + 1) << 12);
+    const uint32_t y = __byte_perm(w, 0u, sel); // code B at bits 15:8, code B+1 at 31:24
+    return (y & 0x80008000u) | ((y >> 1) & 0x3F803F80u);
+}
+
+template <bool FP8>
+__global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
     sparse_mla_fwd_umma16_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap kv_map)
 {
-    using C = U16;
+    using C = Cfg<FP8>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t sbase = (raw_base + 1023u) & ~1023u; // swizzle atoms need 1 KB alignment
     uint8_t *smem = smem_raw + (sbase - raw_base);
     const uint32_t ring = sbase, q_s = sbase + C::OFF_Q, p_s = sbase + C::OFF_P;
+    const uint32_t v16_s = sbase + C::OFF_V16;
+    float *sq_s = reinterpret_cast<float *>(smem + C::OFF_SQ);
+    float *fac_s = reinterpret_cast<float *>(smem + C::OFF_FAC);
     int *ex_s = reinterpret_cast<int *>(smem + C::OFF_EX);
     volatile int *go_s = reinterpret_cast<volatile int *>(smem + C::OFF_GO);
     float *wmax_s = reinterpret_cast<float *>(smem + C::OFF_WMAX);
@@ -134,13 +183,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC + 4);
     int *abort_s = reinterpret_cast<int *>(smem + C::OFF_MISC + 8);
     const uint32_t bar0 = sbase + C::OFF_MBAR;
+    constexpr int S_ = C::STAGES;
     auto full = [&](int st) { return bar0 + 8 * st; };
-    auto empty = [&](int st) { return bar0 + 8 * (3 + st); };
-    auto s_full = [&](int b) { return bar0 + 8 * (6 + b); };
-    auto p_full = [&](int b) { return bar0 + 8 * (8 + b); };
-    auto p_empty = [&](int b) { return bar0 + 8 * (10 + b); };
-    const uint32_t q_full = bar0 + 8 * 12;
-    const uint32_t drain = bar0 + 8 * 13;
+    auto empty = [&](int st) { return bar0 + 8 * (S_ + st); };
+    auto s_full = [&](int b) { return bar0 + 8 * (2 * S_ + b); };
+    auto p_full = [&](int b) { return bar0 + 8 * (2 * S_ + 2 + b); };
+    auto p_empty = [&](int b) { return bar0 + 8 * (2 * S_ + 4 + b); };
+    const uint32_t q_full = bar0 + 8 * (2 * S_ + 6);
+    const uint32_t drain = bar0 + 8 * (2 * S_ + 7);
+    const uint32_t v_full = bar0 + 8 * (2 * S_ + 8);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int s = blockIdx.x % a.S;
@@ -151,17 +202,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t *__restrict__ row_idx = a.indices + (int64_t)t * a.topk;
 
     if (tid == 0) {
-        for (int st = 0; st < C::STAGES; ++st) {
+        for (int st = 0; st < S_; ++st) {
             umma::mbar_init(full(st), 1);
-            umma::mbar_init(empty(st), 1);
+            umma::mbar_init(empty(st), C::EMPTY_COUNT);
         }
         for (int b = 0; b < 2; ++b) {
-            umma::mbar_init(s_full(b), 2);
+            umma::mbar_init(s_full(b), C::QK_ISSUERS);
             umma::mbar_init(p_full(b), kSoftmaxWarps * 32);
             umma::mbar_init(p_empty(b), 1);
         }
         umma::mbar_init(q_full, kProducerThreads);
-        umma::mbar_init(drain, 3);
+        umma::mbar_init(drain, C::QK_ISSUERS + 1);
+        umma::mbar_init(v_full, kConverterThreads);
         umma::mbar_init_fence();
         *abort_s = 0;
     }
@@ -190,15 +242,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ======================= producers =======================
         const int pt = tid - kProducerWarp0 * 32;
         const __nv_bfloat16 *__restrict__ qg =
-            static_cast<const __nv_bfloat16 *>(a.q) + (int64_t)t * kHeads * 512;
-        // this thread's copy: key quad qd (keys 4qd..4qd+3), column block cb
-        const int qd = pt >> 3, cb = pt & 7;
+            static_cast<const __nv_bfloat16 *>(a.q) + (int64_t)t * kHeads * kD;
+        // this thread's copy (bf16: all 128 threads; E4M3: lanes 0-15 of each
+        // warp): key quad qd (keys 4qd..4qd+3), column block cb
+        const int cid = FP8 ? (pt >> 5) * 16 + (pt & 15) : pt;
+        const bool copier = FP8 ? (pt & 31) < 16 : true;
+        const int qd = cid / C::NCB, cb = cid % C::NCB;
         // raw indices only: checking them here would wait for the loads
         auto fetch = [&](int tile, int (&r)[4]) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int p = kb + tile * kKeys + 4 * qd + u;
-                r[u] = (tile < ntiles && p < ke) ? __ldg(row_idx + p) : -1;
+                r[u] = (copier && tile < ntiles && p < ke) ? __ldg(row_idx + p) : -1;
             }
         };
         auto row = [&](int x) { return (x >= 0 && (int64_t)x < a.num_slots) ? x : -1; };
@@ -211,16 +266,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         fetch(1, r1);
         fetch(2, r2);
         fetch(3, r3);
-        // q [16 x 512] -> core matrices (8 heads x 16 B): LBO 128 (K), SBO 8 KB (heads);
+        // q [16 x 512] -> core matrices (8 heads x 16 B): LBO 128 (K), SBO = 8 heads;
         // published once the first tile's copies are in flight, so both latencies overlap
-        for (int e = pt; e < kHeads * 64; e += kProducerThreads) {
-            const int h = e >> 6, c = e & 63;
-            cp_async_16(q_s + (h >> 3) * C::QGRP + c * 128 + (h & 7) * 16, qg + h * 512 + c * 8, 16);
+        if constexpr (!FP8) {
+            for (int e = pt; e < kHeads * 64; e += kProducerThreads) {
+                const int h = e >> 6, c = e & 63;
+                cp_async_16(q_s + (h >> 3) * C::QGRP + c * 128 + (h & 7) * 16, qg + h * kD + c * 8, 16);
+            }
+            cp_async_commit();
         }
-        cp_async_commit();
         bool q_pending = true;
         auto publish_q = [&] {
-            cp_async_wait<0>();
+            if constexpr (!FP8) {
+                cp_async_wait<0>();
+            } else {
+                // thread pt quantizes 64 elements of head pt/8 (loaded here, after the
+                // first tile's copies are in flight, so no registers are held before)
+                const int h = pt >> 3;
+                uint4 qraw[8];
+                const uint4 *src = reinterpret_cast<const uint4 *>(qg + h * kD + (pt & 7) * 64);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    qraw[u] = __ldg(src + u);
+                float m = 0.f;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&qraw[u]);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __bfloat1622float2(b2[e]);
+                        m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+                    }
+                }
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) // the 8 threads of a head are adjacent lanes
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                const float sq = (m == 0.f) ? 1.0f : __fdiv_rn(m, 448.0f);
+                if ((pt & 7) == 0)
+                    sq_s[h] = sq;
+                // 64 codes = 4 core-matrix rows of 16 B
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&qraw[2 * cc + v / 2]);
+                        const float2 f0 = __bfloat1622float2(b2[2 * (v & 1)]);
+                        const float2 f1 = __bfloat1622float2(b2[2 * (v & 1) + 1]);
+                        w[v] = quant4_e4m3(f0.x, f0.y, f1.x, f1.y, sq);
+                    }
+                    const int c = (pt & 7) * 4 + cc; // 16-byte column of the head's row
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(q_s + (h >> 3) * C::QGRP + c * 128 +
+                                                                                 (h & 7) * 16),
+                                 "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                                 : "memory");
+                }
+            }
             umma::fence_async_smem();
             umma::mbar_arrive(q_full);
             q_pending = false;
@@ -232,10 +333,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 stop = true;
                 return;
             }
-            const int st = j % C::STAGES;
+            const int st = j % S_;
             if (pt == 0) {
-                if (j >= C::STAGES)
-                    wait_bar(empty(st), (uint32_t)((j / C::STAGES - 1) & 1));
+                if (j >= S_)
+                    wait_bar(empty(st), (uint32_t)((j / S_ - 1) & 1));
                 const int go = !*(volatile int *)abort_s;
                 if (go)
                     umma::mbar_arrive_expect_tx(full(st), C::TILE);
@@ -248,8 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 stop = true;
                 return;
             }
-            umma::tma_gather4(ring + st * C::TILE + cb * C::BLK + qd * 512, &kv_map, 64 * cb, row(r[0]), row(r[1]),
-                              row(r[2]), row(r[3]), full(st));
+            if (copier)
+                umma::tma_gather4(ring + st * C::TILE + cb * C::BLK + qd * 512, &kv_map, C::BOXW * cb, row(r[0]),
+                                  row(r[1]), row(r[2]), row(r[3]), full(st));
             issued = j + 1;
             fetch(j + kIdxAhead, r);
             if (q_pending)
@@ -265,20 +367,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             publish_q();
         // every copy issued has landed before the CTA can finish (also after an abort)
         if (pt == 0) {
-            for (int j = max(0, issued - C::STAGES); j < issued; ++j)
-                wait_issued(full(j % C::STAGES), (uint32_t)((j / C::STAGES) & 1));
+            for (int j = max(0, issued - S_); j < issued; ++j)
+                wait_issued(full(j % S_), (uint32_t)((j / S_) & 1));
         }
-    } else if (warp == kMmaWarp || warp >= kMmaWarp2) {
+    } else if (warp == kMmaWarp || warp == kMmaWarp2 || warp == kMmaWarp2 + 1) {
         // ======================= MMA issuers =======================
         if (lane == 0) {
-            const int role = warp == kMmaWarp ? 0 : 1 + warp - kMmaWarp2; // 0, 1: QK halves; 2: PV
-            if (role < 2) {
+            const int role = warp == kMmaWarp ? 0 : 1 + warp - kMmaWarp2; // 0, 1: QK parts; 2: PV
+            if (role < C::QK_ISSUERS) {
                 wait_bar(q_full, 0);
                 const uint64_t qdesc = umma::desc(q_s, 128, C::QGRP);
-                const int ks0 = 16 * role;
+                constexpr int kHalf = C::QK_MMAS / C::QK_ISSUERS;
+                const int ks0 = kHalf * role;
                 for (int i = 0; i < ntiles; ++i) {
-                    const int b = i & 1, st = i % C::STAGES;
-                    wait_bar(full(st), (uint32_t)((i / C::STAGES) & 1));
+                    const int b = i & 1, st = i % S_;
+                    wait_bar(full(st), (uint32_t)((i / S_) & 1));
                     if (i >= 2) // the softmax has read S buffer b for tile i-2
                         wait_bar(p_full(b), (uint32_t)(((i - 2) >> 1) & 1));
                     if (*(volatile int *)abort_s)
@@ -288,45 +391,103 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // block ks/4, starting 32 B * (ks%4) into its 128-byte rows
                     const uint64_t ad = umma::desc_sw128(ring + st * C::TILE, 16, 1024);
 #pragma unroll
-                    for (int ks = ks0; ks < ks0 + 16; ++ks)
-                        umma::mma_f16(tmem + kSCol + 32 * role + 16 * b,
-                                      ad + (uint64_t)(((ks >> 2) * C::BLK + (ks & 3) * 32) >> 4),
-                                      qdesc + (uint64_t)(ks * 16), kIdescQK, ks > ks0);
+                    for (int ks = ks0; ks < ks0 + kHalf; ++ks) {
+                        const uint64_t ak = ad + (uint64_t)(((ks >> 2) * C::BLK + (ks & 3) * 32) >> 4);
+                        const uint64_t bk = qdesc + (uint64_t)(ks * 16); // 2 core matrices of q per k-step
+                        if constexpr (FP8)
+                            umma::mma_f8(tmem + kSCol + 32 * role + 16 * b, ak, bk, kIdescQKe4m3, ks > ks0);
+                        else
+                            umma::mma_f16(tmem + kSCol + 32 * role + 16 * b, ak, bk, kIdescQKbf16, ks > ks0);
+                    }
                     umma::commit(s_full(b));
+                    if constexpr (FP8)
+                        umma::commit(empty(st)); // this half of QK(i) no longer reads the stage
                 }
-            } else {
+            } else if (role == 2) {
                 for (int i = 0; i < ntiles; ++i) {
-                    const int b = i & 1, st = i % C::STAGES;
+                    const int b = i & 1, st = i % S_;
                     wait_bar(p_full(b), (uint32_t)((i >> 1) & 1));
+                    if constexpr (FP8)
+                        wait_bar(v_full, (uint32_t)(i & 1));
                     if (*(volatile int *)abort_s)
                         break;
                     umma::fence_after_sync();
                     // V^T: MN-major, 64-column atoms 8 KB apart (LBO), 8-key atoms 1 KB apart (SBO)
-                    const uint64_t ad = umma::desc_sw128(ring + st * C::TILE, C::BLK, 1024);
+                    const uint64_t ad = umma::desc_sw128(FP8 ? v16_s : ring + st * C::TILE, C::BLK, 1024);
                     const uint64_t bd = umma::desc(p_s + b * 2048, 256, 128);
+                    constexpr uint32_t idesc = FP8 ? kIdescPVf16 : kIdescPVbf16;
 #pragma unroll
                     for (int blk = 0; blk < 4; ++blk)
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
                             umma::mma_f16(tmem + 16 * blk, ad + (uint64_t)((blk * 2 * C::BLK + kk * 2048) >> 4),
-                                          bd + (uint64_t)(kk * 32), kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+                                          bd + (uint64_t)(kk * 32), idesc, (i > 0 || kk > 0) ? 1u : 0u);
                     // PV(i) follows the softmax's read of S(i), so QK(i) is complete too.
-                    // p_empty(b) also tells the softmax that O^T holds PV(0..i): PVs
-                    // are issued by this one thread and complete in order.
-                    umma::commit(empty(st));
+                    // p_empty(b) also tells the softmax (and the converters) that O^T holds
+                    // PV(0..i): PVs are issued by this one thread and complete in order.
+                    if constexpr (!FP8)
+                        umma::commit(empty(st));
                     umma::commit(p_empty(b));
                 }
             }
             // every MMA issued has completed before TMEM is released
-            umma::commit(drain);
-            wait_issued(drain, 0);
+            if (role < C::QK_ISSUERS || role == 2) {
+                umma::commit(drain);
+                wait_issued(drain, 0);
+            }
         }
         __syncwarp();
+    } else if (warp >= kConverterWarp0) {
+        // ======================= converters (E4M3) =======================
+        if constexpr (FP8) {
+            const int ct = tid - kConverterWarp0 * 32;
+            for (int i = 0; i < ntiles; ++i) {
+                const int st = i % S_;
+                wait_bar(full(st), (uint32_t)((i / S_) & 1));
+                if (i >= 1) // PV(i-1) is done with the binary16 tile
+                    wait_bar(p_empty((i - 1) & 1), (uint32_t)(((i - 1) >> 1) & 1));
+                const uint32_t src0 = ring + st * C::TILE;
+                // 2048 16-byte chunks (64 keys x 4 blocks x 8): 16 codes each,
+                // which become two 16-byte chunks of binary16
+#pragma unroll 4
+                for (int j = 0; j < 16; ++j) {
+                    const int k = ct + kConverterThreads * j;
+                    const int r = k >> 5, cb8 = (k >> 3) & 3, c = k & 7;
+                    uint32_t w0, w1, w2, w3;
+                    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
+                                 : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                                 : "r"(src0 + cb8 * C::BLK + r * 128 + ((c ^ (r & 7)) << 4)));
+                    const int cb16 = 2 * cb8 + (c >> 2), c16 = (c & 3) * 2;
+                    const uint32_t dst = v16_s + cb16 * C::BLK + r * 128;
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(dst + ((c16 ^ (r & 7)) << 4)),
+                                 "r"(e4m3pair_to_f16x2_scaled<0>(w0)), "r"(e4m3pair_to_f16x2_scaled<2>(w0)),
+                                 "r"(e4m3pair_to_f16x2_scaled<0>(w1)), "r"(e4m3pair_to_f16x2_scaled<2>(w1))
+                                 : "memory");
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(dst + (((c16 + 1) ^ (r & 7)) << 4)),
+                                 "r"(e4m3pair_to_f16x2_scaled<0>(w2)), "r"(e4m3pair_to_f16x2_scaled<2>(w2)),
+                                 "r"(e4m3pair_to_f16x2_scaled<0>(w3)), "r"(e4m3pair_to_f16x2_scaled<2>(w3))
+                                 : "memory");
+                }
+                umma::fence_async_smem();
+                umma::mbar_arrive(v_full);
+                umma::mbar_arrive(empty(st)); // done reading the stage
+            }
+        }
     } else {
         // ======================= softmax =======================
         const uint32_t tm_lane = (uint32_t)(warp * 32) << 16;
-        const float fac = a.scale * kLog2e;
         const int key = warp * 16 + lane; // meaningful for lane < 16
+        // log2-domain logit factor: per head for E4M3 (in shared memory), one for bf16
+        float ovs = 1.0f; // output factor besides 1/l
+        if constexpr (FP8) {
+            const float kvs = *a.kv_scale;
+            ovs = 256.0f * kvs;
+            wait_bar(q_full, 0); // the per-head q scales
+            if (tid < 16)
+                fac_s[tid] = a.scale * kLog2e * sq_s[tid] * kvs;
+            umma::named_bar(1, kSoftmaxWarps * 32);
+        }
+        auto fac = [&](int h) { return FP8 ? fac_s[h] : a.scale * kLog2e; };
         float m_ref[16], l_part[16];
 #pragma unroll
         for (int h = 0; h < 16; ++h) {
@@ -347,14 +508,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             my_idx = load_idx(i + kIdxAhead);
             wait_bar(s_full(b), (uint32_t)((i >> 1) & 1));
             umma::fence_after_sync();
-            float sv[16], s2[16];
+            float sv[16];
             umma::ld16(tmem + kSCol + 16 * b + tm_lane, reinterpret_cast<uint32_t(&)[16]>(sv));
-            umma::ld16(tmem + kSCol + 32 + 16 * b + tm_lane, reinterpret_cast<uint32_t(&)[16]>(s2));
-            umma::wait_ld();
+            if constexpr (C::QK_ISSUERS == 2) {
+                float s2[16];
+                umma::ld16(tmem + kSCol + 32 + 16 * b + tm_lane, reinterpret_cast<uint32_t(&)[16]>(s2));
+                umma::wait_ld();
+#pragma unroll
+                for (int h = 0; h < 16; ++h)
+                    sv[h] += s2[h];
+            } else {
+                umma::wait_ld();
+            }
             bool exceed = false;
 #pragma unroll
             for (int h = 0; h < 16; ++h) {
-                sv[h] = kvalid ? (sv[h] + s2[h]) * fac : -INFINITY;
+                sv[h] = kvalid ? sv[h] * fac(h) : -INFINITY;
                 exceed |= sv[h] > m_ref[h] + kRescaleThreshold;
             }
             exceed = __any_sync(0xffffffffu, exceed);
@@ -412,13 +581,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (i >= 2)
                 wait_bar(p_empty(b), (uint32_t)(((i - 2) >> 1) & 1)); // PV(i-2) is done with this P buffer
             if (lane < 16) {
+                auto pk = [&](float x, float y) { return FP8 ? pack_f16x2(x, y) : pack_bf16x2(x, y); };
                 const uint32_t prow = p_s + b * 2048 + (key >> 3) * 256 + (key & 7) * 16;
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow), "r"(pack_bf16x2(sv[0], sv[1])),
-                             "r"(pack_bf16x2(sv[2], sv[3])), "r"(pack_bf16x2(sv[4], sv[5])),
-                             "r"(pack_bf16x2(sv[6], sv[7])));
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow + 128),
-                             "r"(pack_bf16x2(sv[8], sv[9])), "r"(pack_bf16x2(sv[10], sv[11])),
-                             "r"(pack_bf16x2(sv[12], sv[13])), "r"(pack_bf16x2(sv[14], sv[15])));
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow), "r"(pk(sv[0], sv[1])),
+                             "r"(pk(sv[2], sv[3])), "r"(pk(sv[4], sv[5])), "r"(pk(sv[6], sv[7])));
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow + 128), "r"(pk(sv[8], sv[9])),
+                             "r"(pk(sv[10], sv[11])), "r"(pk(sv[12], sv[13])), "r"(pk(sv[14], sv[15])));
             }
             umma::fence_async_smem();
             umma::fence_before_sync();
@@ -453,22 +621,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mh = tid == h ? m_ref[h] : mh;
             const float l = lred_s[tid] + lred_s[16 + tid] + lred_s[32 + tid] + lred_s[48 + tid];
             lse_s[tid] = l > 0.f ? (mh + log2f(l)) * kLn2 : -INFINITY;
-            alpha_s[tid] = l > 0.f ? 1.0f / l : 0.f; // reused: 1 / l per head
+            alpha_s[tid] = l > 0.f ? ovs / l : 0.f; // reused: output factor per head
         }
         umma::named_bar(1, kSoftmaxWarps * 32);
         float *ost = reinterpret_cast<float *>(smem);
-        uint32_t o[4][16];
 #pragma unroll
-        for (int blk = 0; blk < 4; ++blk)
-            umma::ld16(tmem + 16 * blk + tm_lane, o[blk]);
-        umma::wait_ld();
+        for (int half = 0; half < 2; ++half) {
+            uint32_t o[2][16];
 #pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
-            const int d = blk * 128 + warp * 32 + lane;
+            for (int u = 0; u < 2; ++u)
+                umma::ld16(tmem + 16 * (2 * half + u) + tm_lane, o[u]);
+            umma::wait_ld();
 #pragma unroll
-            for (int h = 0; h < 16; ++h) {
-                const float iv = alpha_s[h];
-                ost[h * kDv + d] = iv > 0.f ? __uint_as_float(o[blk][h]) * iv : 0.f;
+            for (int u = 0; u < 2; ++u) {
+                const int d = (2 * half + u) * 128 + warp * 32 + lane;
+#pragma unroll
+                for (int h = 0; h < 16; ++h) {
+                    const float iv = alpha_s[h];
+                    ost[h * kD + d] = iv > 0.f ? __uint_as_float(o[u][h]) * iv : 0.f;
+                }
             }
         }
         umma::fence_before_sync();
@@ -476,8 +647,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 0)
         umma::dealloc(tmem, 128);
-    finish_tile<kThreads>(a, reinterpret_cast<float *>(smem), lse_s, reinterpret_cast<float *>(smem + C::OFF_Q),
-                          flag_s, t, 0, s, tid);
+    finish_tile<C::THREADS>(a, reinterpret_cast<float *>(smem), lse_s, reinterpret_cast<float *>(smem + C::OFF_Q),
+                            flag_s, t, 0, s, tid);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
@@ -495,11 +666,11 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
     return fn;
 }
 
-} // namespace
-
-cudaError_t launch_fwd_umma16(const FwdArgs &a, cudaStream_t stream)
+template <bool FP8>
+cudaError_t launch(const FwdArgs &a, cudaStream_t stream)
 {
-    auto kern = sparse_mla_fwd_umma16_kernel;
+    using C = Cfg<FP8>;
+    auto kern = sparse_mla_fwd_umma16_kernel<FP8>;
     static std::atomic<uint64_t> attr_done{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -507,7 +678,7 @@ cudaError_t launch_fwd_umma16(const FwdArgs &a, cudaStream_t stream)
         return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(attr_done.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, U16::SMEM_ALLOC);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
         if (e != cudaSuccess)
             return e;
         attr_done.fetch_or(bit, std::memory_order_release);
@@ -516,28 +687,29 @@ cudaError_t launch_fwd_umma16(const FwdArgs &a, cudaStream_t stream)
     if (blocks == 0)
         return cudaSuccess;
 
-    // The cache as a 2-D tensor [rows x 512] bf16 (row pitch 1 KB), read in
-    // boxes of 64 columns x 1 row with the 128-byte swizzle. Rows beyond the
-    // int32 index range are unreachable, so the row count is clamped there.
+    // The cache as a 2-D tensor [rows x 512] (row pitch 1 KB bf16 | 512 B E4M3),
+    // read in boxes of 128 bytes x 1 row with the 128-byte swizzle. Rows beyond
+    // the int32 index range are unreachable, so the row count is clamped there.
     const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (encode == nullptr)
         return cudaErrorNotSupported;
     CUtensorMap kv_map;
     const int64_t rows = a.num_slots < 1 ? 1 : (a.num_slots > INT_MAX ? (int64_t)INT_MAX : a.num_slots);
-    cuuint64_t gdim[2] = {(cuuint64_t)kDv, (cuuint64_t)rows};
-    cuuint64_t gstride[1] = {(cuuint64_t)U16::ROW};
-    cuuint32_t box[2] = {64, 1};
+    cuuint64_t gdim[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+    cuuint64_t gstride[1] = {(cuuint64_t)C::ROW};
+    cuuint32_t box[2] = {(cuuint32_t)C::BOXW, 1};
     cuuint32_t estride[2] = {1, 1};
-    if (encode(&kv_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.kv), gdim, gstride, box, estride,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    if (encode(&kv_map, FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+               const_cast<void *>(a.kv), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
 
     if (a.S > 1 && a.S <= kClusterMaxSplits) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)blocks);
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = U16::SMEM_ALLOC;
+        cfg.blockDim = dim3(C::THREADS);
+        cfg.dynamicSmemBytes = C::SMEM_ALLOC;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -548,8 +720,15 @@ cudaError_t launch_fwd_umma16(const FwdArgs &a, cudaStream_t stream)
         cfg.numAttrs = 1;
         return cudaLaunchKernelEx(&cfg, kern, a, kv_map);
     }
-    kern<<<dim3((unsigned)blocks), dim3(kThreads), U16::SMEM_ALLOC, stream>>>(a, kv_map);
+    kern<<<dim3((unsigned)blocks), dim3(C::THREADS), C::SMEM_ALLOC, stream>>>(a, kv_map);
     return cudaGetLastError();
+}
+
+} // namespace
+
+cudaError_t launch_fwd_umma16(const FwdArgs &a, cudaStream_t stream)
+{
+    return a.kv_fp8 ? launch<true>(a, stream) : launch<false>(a, stream);
 }
 
 cudaError_t read_umma_error(int *out, bool reset)

@@ -42,7 +42,7 @@ def test_status_strings(L):
 def test_split_plan(L):
     from sparse_mla_attention_04_gb300 import binding as b
     assert b.smla_plan_num_splits(64, 16, 512, 2048, 0, 152) == 2     # decode bf16, tcgen05 kernel: 1 CTA/SM
-    assert b.smla_plan_num_splits(64, 16, 512, 2048, 1, 152) == 4     # decode fp8, warp-MMA kernel: 2 CTAs/SM
+    assert b.smla_plan_num_splits(64, 16, 512, 2048, 1, 152) == 2     # decode fp8, tcgen05 kernel: 1 CTA/SM
     assert b.smla_plan_num_splits(4, 16, 512, 128, 0, 152) == 2       # capped by keys per split
     assert b.smla_plan_num_splits(8192, 16, 512, 2048, 0, 152) == 1   # prefill: no split
     assert b.smla_plan_num_splits(128, 128, 576, 2048, 1, 152) == 1
