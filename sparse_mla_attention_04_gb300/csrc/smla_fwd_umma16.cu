@@ -27,9 +27,11 @@
 // amax|q[t,h,:]| / 448 (1 if zero), q8 = RNE_satfinite(q / s_q); QK runs in
 // E4M3 (kind::f8f6f4) on the gathered tile and the logits are scaled by
 // scale * s_q * kv_scale. PV needs 16-bit operands of one type, so four
-// converter warps rewrite each tile's values as binary16 holding code * 2^-8
-// (exact: the code's bits shifted into a binary16) into a separate swizzled
-// tile, and P is kept in fp16; the 2^8 and kv_scale are applied with 1/l.
+// converter warps turn each tile's values into binary16 (exact) and write
+// V^T straight into tensor memory (double-buffered), where PV reads its A
+// operand; P is kept in fp16 and kv_scale is applied with 1/l. Keeping V^T
+// out of shared memory matters: a binary16 copy there costs 128 KB of
+// shared-memory traffic per 32 KB tile, more than the rest of the tile.
 //
 // Warp roles, handing tiles over through mbarriers:
 //   producers (warps 5-8): q into shared memory once (quantized for E4M3);
@@ -43,8 +45,11 @@
 //     issue in parallel, so splitting a tile's MMAs across three issuers
 //     shortens the time each stage is held. Commits signal the softmax (S
 //     full), the producers (stage empty) and the P buffers.
-//   converters (E4M3 only, warps 11-14): tile i -> the binary16 value tile,
-//     once PV(i-1) is done with it.
+//   converters (E4M3 only, warps 11-14, one per quarter of the TMEM lanes):
+//     tile i -> V^T in tensor memory buffer i%2 once PV(i-2) has read it;
+//     lane d of M-block b holds dim 128b + d, two keys per column. Each
+//     thread loads 4-byte words (4 dims of one key), transposes 4x4 bytes
+//     within its lane quad by two shuffles, converts, and stores 32 columns.
 //   softmax (warps 0-3, one key per thread of lanes 0-15): reads the key's 16
 //     logits (two partial sums) from TMEM, masks, and exponentiates against a
 //     running reference max; the max is recomputed over the tile (and O^T
@@ -107,13 +112,13 @@ struct Cfg {
     static constexpr int BLK = kKeys * 128;       // one column block of a tile (8 KB)
     static constexpr int TILE = NCB * BLK;        // 64 keys (64 KB | 32 KB)
     static constexpr int COPIES = 16 * NCB;       // gather4 copies per tile (128 | 64)
-    static constexpr int STAGES = FP8 ? 4 : 3;
+    static constexpr int STAGES = FP8 ? 5 : 3;
     static constexpr int KSTEP = FP8 ? 32 : 16;   // reduction depth of one QK MMA
     static constexpr int QK_MMAS = kD / KSTEP;    // per tile (32 | 16)
     static constexpr int QK_ISSUERS = FP8 ? 1 : 2; // threads issuing QK (S partial sums)
-    static constexpr int V16 = 8 * BLK;           // binary16 value tile (E4M3 only), 64 KB
-    static constexpr int OFF_V16 = STAGES * TILE;
-    static constexpr int OFF_Q = OFF_V16 + (FP8 ? V16 : 0); // q [16 x 512] in core matrices
+    static constexpr int PV_ISSUERS = FP8 ? 2 : 1; // threads issuing PV (halves of the 512 dims)
+    static constexpr int OFF_QSTG = STAGES * TILE; // E4M3: bf16 q staged for the quantizer (16 KB)
+    static constexpr int OFF_Q = OFF_QSTG + (FP8 ? kHeads * kD * 2 : 0); // q [16 x 512] in core matrices
     static constexpr int QGRP = 8 * ROW;          // q: 8 heads x 512 elements
     static constexpr int OFF_P = OFF_Q + 2 * QGRP;// P^T [64 keys x 16 heads] 16-bit, 2 buffers x 2 KB
     static constexpr int OFF_SQ = OFF_P + 2 * 2048; // [16] per-head q scales (E4M3)
@@ -126,16 +131,21 @@ struct Cfg {
     static constexpr int OFF_ALPHA = OFF_LSE + 16 * 4;
     static constexpr int OFF_MISC = OFF_ALPHA + 16 * 4; // flag, tmem address, abort
     static constexpr int OFF_MBAR = (OFF_MISC + 16 + 7) & ~7;
-    // full[S], empty[S], s_full[2] (a commit per QK issuer), p_full[2], p_empty[2],
-    // q_full, drain (a commit per MMA issuer), v_full (E4M3)
-    static constexpr int NBAR = 2 * STAGES + 9;
+    // full[S], empty[S], s_full[2] (a commit per QK issuer), p_full[2], p_empty[2] (a
+    // commit per PV issuer), q_full, drain (a commit per MMA issuer), v_full[2] (E4M3:
+    // V^T buffer written)
+    static constexpr int NBAR = 2 * STAGES + 10;
+    // tensor memory: O^T 0..63, S^T 64..127; E4M3: V^T buffers at 256 + 128 v
+    static constexpr int TMEM_COLS = FP8 ? 512 : 128;
+    static constexpr int VCOL = 256;
+    static_assert(!FP8 || VCOL + 2 * 128 <= TMEM_COLS, "two V^T buffers fit in tensor memory");
     static constexpr int SMEM = OFF_MBAR + NBAR * 8;
     static constexpr int SMEM_ALLOC = SMEM + 1024; // the base is aligned up to 1 KB in the kernel
     static constexpr int THREADS = 32 * (FP8 ? kConverterWarp0 + 4 : kConverterWarp0);
     // E4M3: 15 warps share the register file, so at most 128 registers a thread
     static constexpr int BOUND_THREADS = FP8 ? 512 : THREADS;
     // stage "empty" arrivals: the PV commit (bf16), or the QK commits and every
-    // converter thread (E4M3: PV reads the binary16 tile, not the stage)
+    // converter thread (E4M3: PV reads V^T from tensor memory, not the stage)
     static constexpr int EMPTY_COUNT = FP8 ? QK_ISSUERS + kConverterThreads : 1;
     static_assert(STAGES * TILE >= kHeads * kD * 4, "epilogue staging fits in the ring");
     static_assert(2 * QGRP >= 128 * kHeads * 4, "merge weights fit in the q area");
@@ -148,16 +158,18 @@ constexpr uint32_t kIdescQKbf16 = umma::idesc(64, 16, 1, 1, 0, 0);
 constexpr uint32_t kIdescQKe4m3 = umma::idesc(64, 16, 0, 0, 0, 0);
 // PV: A = V^T (MN-major), B = P^T (MN-major), M = 128 dims, N = 16; bf16 or fp16
 constexpr uint32_t kIdescPVbf16 = umma::idesc(128, 16, 1, 1, 1, 1);
-constexpr uint32_t kIdescPVf16 = umma::idesc(128, 16, 0, 0, 1, 1);
+// E4M3: A = V^T in tensor memory (binary16), B = P^T fp16 (MN-major)
+constexpr uint32_t kIdescPVf16ts = umma::idesc(128, 16, 0, 0, 0, 1);
 
-// Bytes B and B+1 of w (E4M3 codes) as an f16x2 holding each code's value
-// times 2^-8 (low half from byte B); see e4m3x2_to_f16x2_scaled.
-template <int B>
-__device__ __forceinline__ uint32_t e4m3pair_to_f16x2_scaled(uint32_t w)
+// Four E4M3 codes (lowest byte first) as two f16x2 words holding their
+// values exactly (every E4M3 value, subnormals included, is a normal
+// binary16), by the hardware conversion.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t &hi)
 {
-    constexpr uint32_t sel = 4u | (B << 4) | (4u << 8) | ((B + 1) << 12);
-    const uint32_t y = __byte_perm(w, 0u, sel); // code B at bits 15:8, code B+1 at 31:24
-    return (y & 0x80008000u) | ((y >> 1) & 0x3F803F80u);
+    asm("{\n.reg .b16 a, b;\nmov.b32 {a, b}, %2;\n"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\ncvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
 }
 
 template <bool FP8>
@@ -170,7 +182,6 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
     const uint32_t sbase = (raw_base + 1023u) & ~1023u; // swizzle atoms need 1 KB alignment
     uint8_t *smem = smem_raw + (sbase - raw_base);
     const uint32_t ring = sbase, q_s = sbase + C::OFF_Q, p_s = sbase + C::OFF_P;
-    const uint32_t v16_s = sbase + C::OFF_V16;
     float *sq_s = reinterpret_cast<float *>(smem + C::OFF_SQ);
     float *fac_s = reinterpret_cast<float *>(smem + C::OFF_FAC);
     int *ex_s = reinterpret_cast<int *>(smem + C::OFF_EX);
@@ -191,7 +202,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
     auto p_empty = [&](int b) { return bar0 + 8 * (2 * S_ + 4 + b); };
     const uint32_t q_full = bar0 + 8 * (2 * S_ + 6);
     const uint32_t drain = bar0 + 8 * (2 * S_ + 7);
-    const uint32_t v_full = bar0 + 8 * (2 * S_ + 8);
+    auto v_full = [&](int vb) { return bar0 + 8 * (2 * S_ + 8 + vb); };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int s = blockIdx.x % a.S;
@@ -209,16 +220,17 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
         for (int b = 0; b < 2; ++b) {
             umma::mbar_init(s_full(b), C::QK_ISSUERS);
             umma::mbar_init(p_full(b), kSoftmaxWarps * 32);
-            umma::mbar_init(p_empty(b), 1);
+            umma::mbar_init(p_empty(b), C::PV_ISSUERS);
         }
         umma::mbar_init(q_full, kProducerThreads);
-        umma::mbar_init(drain, C::QK_ISSUERS + 1);
-        umma::mbar_init(v_full, kConverterThreads);
+        umma::mbar_init(drain, C::QK_ISSUERS + C::PV_ISSUERS);
+        for (int vb = 0; vb < 2; ++vb)
+            umma::mbar_init(v_full(vb), kConverterThreads);
         umma::mbar_init_fence();
         *abort_s = 0;
     }
     if (warp == 0)
-        umma::alloc(smem_u32(tmem_slot), 128);
+        umma::alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
@@ -273,21 +285,26 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
                 const int h = e >> 6, c = e & 63;
                 cp_async_16(q_s + (h >> 3) * C::QGRP + c * 128 + (h & 7) * 16, qg + h * kD + c * 8, 16);
             }
-            cp_async_commit();
+        } else {
+            // bf16 q staged row-major: this thread's 64 elements of head pt/8,
+            // the ones it quantizes
+            const int h = pt >> 3, e0 = h * kD + (pt & 7) * 64;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                cp_async_16(sbase + C::OFF_QSTG + (e0 + 8 * u) * 2, qg + e0 + 8 * u, 16);
         }
+        cp_async_commit();
         bool q_pending = true;
         auto publish_q = [&] {
-            if constexpr (!FP8) {
-                cp_async_wait<0>();
-            } else {
-                // thread pt quantizes 64 elements of head pt/8 (loaded here, after the
-                // first tile's copies are in flight, so no registers are held before)
+            cp_async_wait<0>();
+            if constexpr (FP8) {
+                // thread pt quantizes the 64 elements of head pt/8 it staged
                 const int h = pt >> 3;
                 uint4 qraw[8];
-                const uint4 *src = reinterpret_cast<const uint4 *>(qg + h * kD + (pt & 7) * 64);
+                const uint4 *src = reinterpret_cast<const uint4 *>(smem + C::OFF_QSTG + (h * kD + (pt & 7) * 64) * 2);
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
-                    qraw[u] = __ldg(src + u);
+                    qraw[u] = src[u];
                 float m = 0.f;
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
@@ -373,7 +390,10 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
     } else if (warp == kMmaWarp || warp == kMmaWarp2 || warp == kMmaWarp2 + 1) {
         // ======================= MMA issuers =======================
         if (lane == 0) {
-            const int role = warp == kMmaWarp ? 0 : 1 + warp - kMmaWarp2; // 0, 1: QK parts; 2: PV
+            // role 0: QK part 0; role 1: QK part 1 (bf16) or PV dims 256..511 (E4M3);
+            // role 2: PV (bf16) or PV dims 0..255 (E4M3)
+            const int role = warp == kMmaWarp ? 0 : 1 + warp - kMmaWarp2;
+            const bool is_pv = role == 2 || (role == 1 && C::PV_ISSUERS == 2);
             if (role < C::QK_ISSUERS) {
                 wait_bar(q_full, 0);
                 const uint64_t qdesc = umma::desc(q_s, 128, C::QGRP);
@@ -403,35 +423,45 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
                     if constexpr (FP8)
                         umma::commit(empty(st)); // this half of QK(i) no longer reads the stage
                 }
-            } else if (role == 2) {
+            } else if (is_pv) {
+                const int blk0 = C::PV_ISSUERS == 2 && role == 1 ? 2 : 0;
+                const int blk1 = C::PV_ISSUERS == 2 && role == 2 ? 2 : 4;
                 for (int i = 0; i < ntiles; ++i) {
                     const int b = i & 1, st = i % S_;
                     wait_bar(p_full(b), (uint32_t)((i >> 1) & 1));
-                    if constexpr (FP8)
-                        wait_bar(v_full, (uint32_t)(i & 1));
+                    if constexpr (FP8) // V^T buffer b holds tile i
+                        wait_bar(v_full(b), (uint32_t)((i >> 1) & 1));
                     if (*(volatile int *)abort_s)
                         break;
                     umma::fence_after_sync();
-                    // V^T: MN-major, 64-column atoms 8 KB apart (LBO), 8-key atoms 1 KB apart (SBO)
-                    const uint64_t ad = umma::desc_sw128(FP8 ? v16_s : ring + st * C::TILE, C::BLK, 1024);
                     const uint64_t bd = umma::desc(p_s + b * 2048, 256, 128);
-                    constexpr uint32_t idesc = FP8 ? kIdescPVf16 : kIdescPVbf16;
+                    if constexpr (FP8) {
+                        // V^T in tensor memory: M-block blk at +32 blk, 16 keys = 8 columns
+                        const uint32_t va = tmem + C::VCOL + 128 * b;
+                        for (int blk = blk0; blk < blk1; ++blk)
 #pragma unroll
-                    for (int blk = 0; blk < 4; ++blk)
+                            for (int kk = 0; kk < 4; ++kk)
+                                umma::mma_f16_ts(tmem + 16 * blk, va + 32 * blk + 8 * kk, bd + (uint64_t)(kk * 32),
+                                                 kIdescPVf16ts, (i > 0 || kk > 0) ? 1u : 0u);
+                    } else {
+                        // V^T: MN-major, 64-column atoms 8 KB apart (LBO), 8-key atoms 1 KB apart (SBO)
+                        const uint64_t ad = umma::desc_sw128(ring + st * C::TILE, C::BLK, 1024);
+                        for (int blk = blk0; blk < blk1; ++blk)
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            umma::mma_f16(tmem + 16 * blk, ad + (uint64_t)((blk * 2 * C::BLK + kk * 2048) >> 4),
-                                          bd + (uint64_t)(kk * 32), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+                            for (int kk = 0; kk < 4; ++kk)
+                                umma::mma_f16(tmem + 16 * blk, ad + (uint64_t)((blk * 2 * C::BLK + kk * 2048) >> 4),
+                                              bd + (uint64_t)(kk * 32), kIdescPVbf16, (i > 0 || kk > 0) ? 1u : 0u);
+                    }
                     // PV(i) follows the softmax's read of S(i), so QK(i) is complete too.
                     // p_empty(b) also tells the softmax (and the converters) that O^T holds
-                    // PV(0..i): PVs are issued by this one thread and complete in order.
+                    // PV(0..i): each issuer's commit covers all its earlier MMAs.
                     if constexpr (!FP8)
                         umma::commit(empty(st));
-                    umma::commit(p_empty(b));
+                    umma::commit(p_empty(b)); // E4M3: also frees V^T buffer b
                 }
             }
             // every MMA issued has completed before TMEM is released
-            if (role < C::QK_ISSUERS || role == 2) {
+            if (role < C::QK_ISSUERS || is_pv) {
                 umma::commit(drain);
                 wait_issued(drain, 0);
             }
@@ -440,36 +470,35 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
     } else if (warp >= kConverterWarp0) {
         // ======================= converters (E4M3) =======================
         if constexpr (FP8) {
-            const int ct = tid - kConverterWarp0 * 32;
+            // lane quad (g, ii): member ii loads 4 dims (4g..4g+3 of this warp's 32)
+            // of key 4kq+ii; after the transpose it holds dim 4g+ii of keys 4kq..4kq+3
+            const int q4 = warp & 3, g = lane >> 2, ii = lane & 3;
+            const uint32_t selA = ii < 2 ? 0x5410u : 0x3276u; // keep / take 16-bit halves (xor 2)
+            const uint32_t selB = ii & 1 ? 0x3715u : 0x6240u; // interleave bytes (xor 1)
+            const uint32_t tlane = (uint32_t)(32 * q4) << 16;
             for (int i = 0; i < ntiles; ++i) {
-                const int st = i % S_;
+                const int st = i % S_, vb = i & 1;
                 wait_bar(full(st), (uint32_t)((i / S_) & 1));
-                if (i >= 1) // PV(i-1) is done with the binary16 tile
-                    wait_bar(p_empty((i - 1) & 1), (uint32_t)(((i - 1) >> 1) & 1));
+                if (i >= 2) // PV(i-2) has read V^T buffer vb
+                    wait_bar(p_empty(vb), (uint32_t)(((i - 2) >> 1) & 1));
                 const uint32_t src0 = ring + st * C::TILE;
-                // 2048 16-byte chunks (64 keys x 4 blocks x 8): 16 codes each,
-                // which become two 16-byte chunks of binary16
-#pragma unroll 4
-                for (int j = 0; j < 16; ++j) {
-                    const int k = ct + kConverterThreads * j;
-                    const int r = k >> 5, cb8 = (k >> 3) & 3, c = k & 7;
-                    uint32_t w0, w1, w2, w3;
-                    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
-                                 : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                                 : "r"(src0 + cb8 * C::BLK + r * 128 + ((c ^ (r & 7)) << 4)));
-                    const int cb16 = 2 * cb8 + (c >> 2), c16 = (c & 3) * 2;
-                    const uint32_t dst = v16_s + cb16 * C::BLK + r * 128;
-                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(dst + ((c16 ^ (r & 7)) << 4)),
-                                 "r"(e4m3pair_to_f16x2_scaled<0>(w0)), "r"(e4m3pair_to_f16x2_scaled<2>(w0)),
-                                 "r"(e4m3pair_to_f16x2_scaled<0>(w1)), "r"(e4m3pair_to_f16x2_scaled<2>(w1))
-                                 : "memory");
-                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(dst + (((c16 + 1) ^ (r & 7)) << 4)),
-                                 "r"(e4m3pair_to_f16x2_scaled<0>(w2)), "r"(e4m3pair_to_f16x2_scaled<2>(w2)),
-                                 "r"(e4m3pair_to_f16x2_scaled<0>(w3)), "r"(e4m3pair_to_f16x2_scaled<2>(w3))
-                                 : "memory");
+#pragma unroll 1
+                for (int mb = 0; mb < 4; ++mb) {
+                    uint32_t col[32];
+#pragma unroll
+                    for (int kq = 0; kq < 16; ++kq) {
+                        const int key = 4 * kq + ii;
+                        const uint32_t w = lds32(src0 + mb * C::BLK + key * 128 +
+                                                 (((2 * q4 + (g >> 2)) ^ (key & 7)) << 4) + (g & 3) * 4);
+                        const uint32_t x = __byte_perm(w, __shfl_xor_sync(0xffffffffu, w, 2), selA);
+                        const uint32_t y = __byte_perm(x, __shfl_xor_sync(0xffffffffu, x, 1), selB);
+                        e4m3x4_to_f16x4(y, col[2 * kq], col[2 * kq + 1]);
+                    }
+                    umma::st32(tmem + tlane + C::VCOL + 128 * vb + 32 * mb, col);
                 }
-                umma::fence_async_smem();
-                umma::mbar_arrive(v_full);
+                umma::wait_st();
+                umma::fence_before_sync();
+                umma::mbar_arrive(v_full(vb));
                 umma::mbar_arrive(empty(st)); // done reading the stage
             }
         }
@@ -481,7 +510,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
         float ovs = 1.0f; // output factor besides 1/l
         if constexpr (FP8) {
             const float kvs = *a.kv_scale;
-            ovs = 256.0f * kvs;
+            ovs = kvs;
             wait_bar(q_full, 0); // the per-head q scales
             if (tid < 16)
                 fac_s[tid] = a.scale * kLog2e * sq_s[tid] * kvs;
@@ -646,7 +675,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
     }
     __syncthreads();
     if (warp == 0)
-        umma::dealloc(tmem, 128);
+        umma::dealloc(tmem, C::TMEM_COLS);
     finish_tile<C::THREADS>(a, reinterpret_cast<float *>(smem), lse_s, reinterpret_cast<float *>(smem + C::OFF_Q),
                             flag_s, t, 0, s, tid);
 }
