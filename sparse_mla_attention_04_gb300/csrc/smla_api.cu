@@ -53,7 +53,7 @@ cudaError_t current_sm_count(int *out)
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // Which kernel serves a call.
-enum class Path { Mma, Umma16 };
+enum class Path { Mma, Umma16, Wide };
 
 // SMLA_KERNEL=mma in the environment routes every shape to the warp-MMA
 // kernel (a comparison and test switch).
@@ -64,16 +64,21 @@ bool force_mma()
 }
 
 // 16 heads with D_qk = D_v = 512 (bf16 cache, or E4M3 cache with fp8 dots):
-// the tcgen05 kernel; every other shape: the warp-MMA kernel.
+// the tcgen05 16-head kernel; a multiple of 128 heads with D_qk = 576,
+// D_v = 512 and an E4M3 cache: the tcgen05 128-head kernel (no split of the
+// top-k list); every other shape: the warp-MMA kernel.
 Path choose_path(int H, int D_qk, int D_v, bool kv_fp8)
 {
-    (void)kv_fp8;
-    if (H == 16 && D_qk == 512 && D_v == 512 && !force_mma())
+    if (force_mma())
+        return Path::Mma;
+    if (H == 16 && D_qk == 512 && D_v == 512)
         return Path::Umma16;
+    if (H % 128 == 0 && D_qk == 576 && D_v == 512 && kv_fp8)
+        return Path::Wide;
     return Path::Mma;
 }
 
-int ctas_per_sm(Path p) { return p == Path::Umma16 ? 1 : 2; }
+int ctas_per_sm(Path p) { return p == Path::Mma ? 2 : 1; }
 int tile_keys(Path p) { return p == Path::Umma16 ? smla::kUmma16TileKeys : smla::kMmaTileKeys; }
 
 // A split keeps at least this many keys.
@@ -84,7 +89,7 @@ using smla::kTicketSlots;
 
 int plan_splits(int T, int H, int topk, int sm_count, Path path)
 {
-    if (T <= 0 || H <= 0 || topk <= 0 || sm_count <= 0)
+    if (T <= 0 || H <= 0 || topk <= 0 || sm_count <= 0 || path == Path::Wide)
         return 1;
     const int64_t units = (int64_t)T * (H / 16);
     const int64_t slots = (int64_t)sm_count * ctas_per_sm(path);
@@ -225,7 +230,9 @@ SMLA_API smla_status sparse_mla_fwd(const void *q, const void *kv_cache, int kv_
     if (T == 0)
         return SMLA_OK;
     // 6. split plan and workspace
-    const Path path = choose_path(H, D_qk, D_v, kv_dtype == SMLA_KV_FP8_E4M3);
+    Path path = choose_path(H, D_qk, D_v, kv_dtype == SMLA_KV_FP8_E4M3);
+    if (path == Path::Wide && num_splits > 1)
+        path = Path::Mma; // the 128-head kernel does not split the top-k list
     int S = num_splits;
     if (S == 0) {
         int sms = 0;
@@ -267,14 +274,27 @@ SMLA_API smla_status sparse_mla_fwd(const void *q, const void *kv_cache, int kv_
     a.scale = scale;
     a.kv_fp8 = kv_dtype == SMLA_KV_FP8_E4M3;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    return cuda_status(path == Path::Umma16 ? smla::launch_fwd_umma16(a, st) : smla::launch_fwd_mma(a, st));
+    switch (path) {
+    case Path::Umma16:
+        return cuda_status(smla::launch_fwd_umma16(a, st));
+    case Path::Wide:
+        return cuda_status(smla::launch_fwd_wide(a, st));
+    default:
+        return cuda_status(smla::launch_fwd_mma(a, st));
+    }
 }
 
 SMLA_API smla_status smla_device_error(int *code, int reset)
 {
     if (code == nullptr)
         return SMLA_ERR_NULL_POINTER;
-    return cuda_status(smla::read_umma_error(code, reset != 0));
+    int c16 = 0, cw = 0;
+    if (const cudaError_t e = smla::read_umma_error(&c16, reset != 0); e != cudaSuccess)
+        return cuda_status(e);
+    if (const cudaError_t e = smla::read_wide_error(&cw, reset != 0); e != cudaSuccess)
+        return cuda_status(e);
+    *code = c16 | cw;
+    return SMLA_OK;
 }
 
 SMLA_API smla_status smla_compute_fp8_scale(const void *x, int64_t n, float *scale_out, smla_stream_t stream)

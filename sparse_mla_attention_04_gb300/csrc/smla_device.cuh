@@ -115,6 +115,17 @@ __device__ __forceinline__ uint32_t quant4_e4m3(float x0, float x1, float x2, fl
     return (a & 0xFFFFu) | (b << 16);
 }
 
+// Four E4M3 codes (lowest byte first) as two f16x2 words holding their
+// values exactly (every E4M3 value, subnormals included, is a normal
+// binary16), by the hardware conversion.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t &hi)
+{
+    asm("{\n.reg .b16 a, b;\nmov.b32 {a, b}, %2;\n"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\ncvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
 __device__ __forceinline__ float warp_max(float v)
 {
 #pragma unroll

@@ -161,17 +161,6 @@ constexpr uint32_t kIdescPVbf16 = umma::idesc(128, 16, 1, 1, 1, 1);
 // E4M3: A = V^T in tensor memory (binary16), B = P^T fp16 (MN-major)
 constexpr uint32_t kIdescPVf16ts = umma::idesc(128, 16, 0, 0, 0, 1);
 
-// Four E4M3 codes (lowest byte first) as two f16x2 words holding their
-// values exactly (every E4M3 value, subnormals included, is a normal
-// binary16), by the hardware conversion.
-__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t &hi)
-{
-    asm("{\n.reg .b16 a, b;\nmov.b32 {a, b}, %2;\n"
-        "cvt.rn.f16x2.e4m3x2 %0, a;\ncvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
-        : "=r"(lo), "=r"(hi)
-        : "r"(w));
-}
-
 template <bool FP8>
 __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
     sparse_mla_fwd_umma16_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap kv_map)
@@ -680,20 +669,6 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
                             flag_s, t, 0, s, tid);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
 
 template <bool FP8>
 cudaError_t launch(const FwdArgs &a, cudaStream_t stream)
@@ -754,6 +729,21 @@ cudaError_t launch(const FwdArgs &a, cudaStream_t stream)
 }
 
 } // namespace
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
 
 cudaError_t launch_fwd_umma16(const FwdArgs &a, cudaStream_t stream)
 {

@@ -1,0 +1,539 @@
+// Sparse MLA forward for 128 heads with an E4M3 cache (D_qk = 576: 512
+// latent + 64 rope columns, D_v = 512) on the 5th-generation tensor cores
+// (tcgen05 + tensor memory) with TMA row gathers, sm_103a.
+//
+// With 128 heads the contraction runs head-major, heads on the MMA's M axis:
+//   S [128 heads x 64 keys] = q8 [128 x 576] . K_tile^T         (QK, E4M3, 18 MMAs)
+//   O [128 heads x 256 dims] += P [128 x 64] . V_tile[:, half]  (PV, fp16, 4 MMAs)
+// The fp32 output for 128 heads x 512 dims alone would fill an SM's tensor
+// memory (256 KB), so each query row runs as two CTAs, each owning one half
+// of the value dims; both compute the full QK and softmax (identical
+// inputs, identical P).
+//
+// Warp roles, handing tiles over through mbarriers (every wait bounded):
+//   producers (warps 5-8): quantize q per head (s_q = amax|q[t,h,:]| / 448,
+//     1 if zero; q8 = RNE_satfinite(q / s_q)) into shared memory, K-major
+//     with the 128-byte swizzle (5 blocks of [128 heads x 128 B]); then per
+//     64-key tile 80 TMA tile::gather4 copies (16 key quads x 5 column
+//     blocks of 128 B; the last block reaches past column 576 and is zero
+//     filled) into a 2-stage ring. Masked and out-of-range indices are
+//     passed as row -1 (zero fill, no memory read).
+//   QK issuer (warp 4): S(i) into tensor memory (double-buffered) once tile i
+//     has landed and the softmax has read S(i-2).
+//   softmax (warps 0-3, thread = head, whole S row in the thread): masks,
+//     scales by scale * s_q[h] * kv_scale, exponentiates base 2 against a
+//     running reference max that moves (rescaling the head's O row in
+//     tensor memory) only when a logit exceeds it by more than 2^8; writes
+//     P as fp16 pairs into tensor memory (double-buffered), the A operand
+//     of PV.
+//   converters (warps 10-13): the tile's half of the value columns, E4M3 ->
+//     binary16 (exact), into a shared-memory tile MN-major with the 128-byte
+//     swizzle (double-buffered), the B operand of PV.
+//   PV issuer (warp 9): O += P(i) . V16(i) once both are written.
+//
+// Method sources (page titles and sections):
+//   "Enable AITER sparse MLA on gfx942, including FP8 KV" — Overview, Details
+//     ("FP8 KV on gfx942": the kernel quantizes q per tile, dots in fp8).
+//   "[ROCm][MLA][Perf] Fuse decode QK-RoPE + Q-concat + KV-concat + KV-cache
+//     write for sparse MLA" — Summary (the cache row is the latent part
+//     followed by the rope part, written as fp8).
+#include "smla_device.cuh"
+#include "smla_internal.h"
+#include "smla_umma.cuh"
+
+#include <atomic>
+#include <climits>
+#include <cmath>
+
+namespace smla {
+
+__device__ int g_wide_error = 0; // set when a bounded wait gives up
+
+namespace {
+
+constexpr int kHeads = 128;    // heads per CTA (M of both MMAs)
+constexpr int kDqk = 576;
+constexpr int kDv = 512;
+constexpr int kDvHalf = 256;   // value dims per CTA
+constexpr int kKeys = 64;      // keys per tile (N of QK)
+constexpr int kQkSteps = kDqk / 32;   // 18 E4M3 k-steps of 32
+constexpr int kCB = 5;                // 128-byte column blocks per row (the last half used)
+constexpr int kStages = 2;
+constexpr int kCopies = 16 * kCB;     // gather4 copies per tile
+constexpr int kIdxAhead = 4;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;
+
+// warps 0-3: softmax
+constexpr int kQkWarp = 4;
+constexpr int kProducerWarp0 = 5;     // warps 5-8
+constexpr int kPvWarp = 9;
+constexpr int kConverterWarp0 = 10;   // warps 10-13
+constexpr int kThreads = 14 * 32;
+constexpr int kProducerThreads = 128;
+constexpr int kConverterThreads = 128;
+
+// shared memory (bytes from a 1 KB-aligned base)
+constexpr int kQBlk = kHeads * 128;           // one column block of q8 (16 KB)
+constexpr int kOffQ8 = 0;                     // 5 blocks
+constexpr int kKBlk = kKeys * 128;            // one column block of a tile (8 KB)
+constexpr int kTile = kCB * kKBlk;            // 40 KB
+constexpr int kOffRing = kOffQ8 + kCB * kQBlk;
+constexpr int kV16 = 4 * kKBlk;               // [64 keys x 256 dims] binary16, 4 blocks of 64 dims
+constexpr int kOffV16 = kOffRing + kStages * kTile;
+constexpr int kOffSq = kOffV16 + 2 * kV16;    // [128] per-head q scales
+constexpr int kOffMisc = kOffSq + kHeads * 4; // tmem address, abort, go[2]
+constexpr int kOffMbar = kOffMisc + 32;
+// full[2], empty[2], s_full[2], p_full[2], p_empty[2], v_full[2], v_empty[2], q_full, drain
+constexpr int kNBar = 16;
+constexpr int kSmem = kOffMbar + kNBar * 8;
+constexpr int kSmemAlloc = kSmem + 1024;
+static_assert(kSmemAlloc <= 227 * 1024, "shared memory budget");
+
+// tensor memory columns: O 0..255, S(b) 256 + 64 b, P(b) 384 + 32 b
+constexpr int kTmemCols = 512;
+constexpr int kSCol = 256;
+constexpr int kPCol = 384;
+
+// QK: A = q8 (K-major), B = K tile (K-major), M = 128 heads, N = 64 keys, E4M3
+constexpr uint32_t kIdescQK = umma::idesc(128, 64, 0, 0, 0, 0);
+// PV: A = P in tensor memory (fp16), B = V16 (MN-major), M = 128 heads, N = 256 dims
+constexpr uint32_t kIdescPV = umma::idesc(128, 256, 0, 0, 0, 1);
+
+// byte offset of (row, byte) in a [rows x 128 B] block with the 128-byte swizzle
+__device__ __forceinline__ uint32_t sw128(int row, int byte)
+{
+    return (uint32_t)(row * 128 + ((((byte >> 4) ^ (row & 7)) << 4) | (byte & 15)));
+}
+
+__global__ void __launch_bounds__(512, 1)
+    sparse_mla_fwd_wide_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap kv_map)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_base = smem_u32(smem_raw);
+    const uint32_t sbase = (raw_base + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (sbase - raw_base);
+    const uint32_t q8_s = sbase + kOffQ8, ring = sbase + kOffRing, v16_s = sbase + kOffV16;
+    float *sq_s = reinterpret_cast<float *>(smem + kOffSq);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
+    int *abort_s = reinterpret_cast<int *>(smem + kOffMisc + 4);
+    volatile int *go_s = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
+    const uint32_t bar0 = sbase + kOffMbar;
+    auto full = [&](int st) { return bar0 + 8 * st; };
+    auto empty = [&](int st) { return bar0 + 8 * (2 + st); };
+    auto s_full = [&](int b) { return bar0 + 8 * (4 + b); };
+    auto p_full = [&](int b) { return bar0 + 8 * (6 + b); };
+    auto p_empty = [&](int b) { return bar0 + 8 * (8 + b); };
+    auto v_full = [&](int b) { return bar0 + 8 * (10 + b); };
+    auto v_empty = [&](int b) { return bar0 + 8 * (12 + b); };
+    const uint32_t q_full = bar0 + 8 * 14;
+    const uint32_t drain = bar0 + 8 * 15;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = a.H / kHeads;
+    const int half = blockIdx.x & 1;
+    const int hg = (blockIdx.x >> 1) % G;
+    const int t = (blockIdx.x >> 1) / G;
+    const int ntiles = (a.topk + kKeys - 1) / kKeys;
+    const int32_t *__restrict__ row_idx = a.indices + (int64_t)t * a.topk;
+
+    if (tid == 0) {
+        for (int st = 0; st < kStages; ++st) {
+            umma::mbar_init(full(st), 1);
+            umma::mbar_init(empty(st), 1 + kConverterThreads); // QK commit + converters
+        }
+        for (int b = 0; b < 2; ++b) {
+            umma::mbar_init(s_full(b), 1);
+            umma::mbar_init(p_full(b), 128);
+            umma::mbar_init(p_empty(b), 1);
+            umma::mbar_init(v_full(b), kConverterThreads);
+            umma::mbar_init(v_empty(b), 1);
+        }
+        umma::mbar_init(q_full, kProducerThreads);
+        umma::mbar_init(drain, 2);
+        umma::mbar_init_fence();
+        *abort_s = 0;
+    }
+    if (warp == kQkWarp)
+        umma::alloc(smem_u32(tmem_slot), kTmemCols);
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    auto wait_bar = [&](uint32_t mbar, uint32_t parity) {
+        if (*(volatile int *)abort_s)
+            return;
+        if (!umma::mbar_wait(mbar, parity)) {
+            atomicOr(&g_wide_error, 1);
+            *(volatile int *)abort_s = 1;
+        }
+    };
+    auto wait_issued = [&](uint32_t mbar, uint32_t parity) {
+        if (!umma::mbar_wait(mbar, parity))
+            atomicOr(&g_wide_error, 2);
+    };
+
+    if (warp >= kProducerWarp0 && warp < kProducerWarp0 + 4) {
+        // ======================= producers =======================
+        const int pt = tid - kProducerWarp0 * 32;
+        // copy cid (20 per warp): key quad qd, column block cb
+        const bool copier = (pt & 31) < kCopies / 4;
+        const int cid = (pt >> 5) * (kCopies / 4) + (pt & 31);
+        const int qd = cid / kCB, cb = cid % kCB;
+        auto fetch = [&](int tile, int (&r)[4]) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int p = tile * kKeys + 4 * qd + u;
+                r[u] = (copier && tile < ntiles && p < a.topk) ? __ldg(row_idx + p) : -1;
+            }
+        };
+        auto row = [&](int x) { return (x >= 0 && (int64_t)x < a.num_slots) ? x : -1; };
+        int r0[4], r1[4], r2[4], r3[4];
+        static_assert(kIdxAhead == 4, "one register slot per tile of look-ahead");
+        fetch(0, r0);
+        fetch(1, r1);
+        fetch(2, r2);
+        fetch(3, r3);
+        bool q_pending = true;
+        // thread pt quantizes head pt: amax over its 576 elements, then 36
+        // chunks of 16 codes into the swizzled K-major q8 blocks
+        auto publish_q = [&] {
+            const __nv_bfloat16 *qh =
+                static_cast<const __nv_bfloat16 *>(a.q) + ((int64_t)t * a.H + hg * kHeads + pt) * kDqk;
+            const uint4 *src = reinterpret_cast<const uint4 *>(qh);
+            float m = 0.f;
+            for (int c = 0; c < kDqk / 8; ++c) {
+                const uint4 u = __ldg(src + c);
+                const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __bfloat1622float2(b2[e]);
+                    m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+                }
+            }
+            const float sq = (m == 0.f) ? 1.0f : __fdiv_rn(m, 448.0f);
+            sq_s[pt] = sq;
+            for (int c = 0; c < kDqk / 16; ++c) {
+                const uint4 u0 = __ldg(src + 2 * c), u1 = __ldg(src + 2 * c + 1);
+                const __nv_bfloat162 *b0 = reinterpret_cast<const __nv_bfloat162 *>(&u0);
+                const __nv_bfloat162 *b1 = reinterpret_cast<const __nv_bfloat162 *>(&u1);
+                uint32_t w[4];
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const __nv_bfloat162 *bb = v < 2 ? b0 : b1;
+                    const float2 f0 = __bfloat1622float2(bb[2 * (v & 1)]);
+                    const float2 f1 = __bfloat1622float2(bb[2 * (v & 1) + 1]);
+                    w[v] = quant4_e4m3(f0.x, f0.y, f1.x, f1.y, sq);
+                }
+                const int d = 16 * c; // column of the chunk
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(q8_s + (d >> 7) * kQBlk +
+                                                                             sw128(pt, d & 127)),
+                             "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                             : "memory");
+            }
+            // the unused half of the last block stays zero for the MMA
+            for (int d = kDqk; d < kCB * 128; d += 16)
+                asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};\n" ::"r"(q8_s + (d >> 7) * kQBlk +
+                                                                            sw128(pt, d & 127)),
+                             "r"(0u)
+                             : "memory");
+            umma::fence_async_smem();
+            umma::mbar_arrive(q_full);
+            q_pending = false;
+        };
+        int issued = 0;
+        bool stop = false;
+        auto step = [&](int j, int(&r)[4]) {
+            if (stop || j >= ntiles) {
+                stop = true;
+                return;
+            }
+            const int st = j % kStages;
+            if (pt == 0) {
+                if (j >= kStages)
+                    wait_bar(empty(st), (uint32_t)((j / kStages - 1) & 1));
+                const int go = !*(volatile int *)abort_s;
+                if (go)
+                    umma::mbar_arrive_expect_tx(full(st), kTile);
+                go_s[j & 1] = go;
+            }
+            umma::named_bar(2, kProducerThreads);
+            if (!go_s[j & 1]) {
+                stop = true;
+                return;
+            }
+            if (copier)
+                umma::tma_gather4(ring + st * kTile + cb * kKBlk + qd * 512, &kv_map, 128 * cb, row(r[0]),
+                                  row(r[1]), row(r[2]), row(r[3]), full(st));
+            issued = j + 1;
+            fetch(j + kIdxAhead, r);
+            if (q_pending && j + 1 >= kStages)
+                publish_q();
+        };
+        for (int j0 = 0; !stop; j0 += kIdxAhead) {
+            step(j0, r0);
+            step(j0 + 1, r1);
+            step(j0 + 2, r2);
+            step(j0 + 3, r3);
+        }
+        if (q_pending)
+            publish_q();
+        if (pt == 0) {
+            for (int j = max(0, issued - kStages); j < issued; ++j)
+                wait_issued(full(j % kStages), (uint32_t)((j / kStages) & 1));
+        }
+    } else if (warp == kQkWarp) {
+        // ======================= QK issuer =======================
+        if (lane == 0) {
+            wait_bar(q_full, 0);
+            for (int i = 0; i < ntiles; ++i) {
+                const int b = i & 1, st = i % kStages;
+                wait_bar(full(st), (uint32_t)((i / kStages) & 1));
+                if (i >= 2) // the softmax has read S(i-2)
+                    wait_bar(p_full(b), (uint32_t)(((i - 2) >> 1) & 1));
+                if (*(volatile int *)abort_s)
+                    break;
+                umma::fence_after_sync();
+                const uint64_t ad = umma::desc_sw128(q8_s, 16, 1024);
+                const uint64_t bd = umma::desc_sw128(ring + st * kTile, 16, 1024);
+#pragma unroll
+                for (int ks = 0; ks < kQkSteps; ++ks)
+                    umma::mma_f8(tmem + kSCol + 64 * b, ad + (uint64_t)(((ks >> 2) * kQBlk + (ks & 3) * 32) >> 4),
+                                 bd + (uint64_t)(((ks >> 2) * kKBlk + (ks & 3) * 32) >> 4), kIdescQK, ks > 0);
+                umma::commit(s_full(b));
+                umma::commit(empty(st));
+            }
+            umma::commit(drain);
+            wait_issued(drain, 0);
+        }
+        __syncwarp();
+    } else if (warp == kPvWarp) {
+        // ======================= PV issuer =======================
+        if (lane == 0) {
+            for (int i = 0; i < ntiles; ++i) {
+                const int b = i & 1;
+                wait_bar(p_full(b), (uint32_t)((i >> 1) & 1));
+                wait_bar(v_full(b), (uint32_t)((i >> 1) & 1));
+                if (*(volatile int *)abort_s)
+                    break;
+                umma::fence_after_sync();
+                // V16(b): MN-major, 64-dim atoms 8 KB apart (LBO), 8-key atoms 1 KB apart (SBO)
+                const uint64_t bd = umma::desc_sw128(v16_s + b * kV16, kKBlk, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    umma::mma_f16_ts(tmem, tmem + kPCol + 32 * b + 8 * kk, bd + (uint64_t)((kk * 2048) >> 4),
+                                     kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+                umma::commit(p_empty(b)); // P(b) read; with it O holds PV(0..i)
+                umma::commit(v_empty(b));
+            }
+            umma::commit(drain);
+            wait_issued(drain, 0);
+        }
+        __syncwarp();
+    } else if (warp >= kConverterWarp0) {
+        // ======================= converters =======================
+        const int ct = tid - kConverterWarp0 * 32;
+        for (int i = 0; i < ntiles; ++i) {
+            const int st = i % kStages, b = i & 1;
+            wait_bar(full(st), (uint32_t)((i / kStages) & 1));
+            if (i >= 2) // PV(i-2) has read V16(b)
+                wait_bar(v_empty(b), (uint32_t)(((i - 2) >> 1) & 1));
+            const uint32_t src0 = ring + st * kTile, dst0 = v16_s + b * kV16;
+            // 1024 16-byte chunks (64 keys x 2 blocks x 8) of this CTA's 256 dims
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int k = ct + kConverterThreads * j;
+                const int r = k >> 4, lb = (k >> 3) & 1, c = k & 7; // key, local block, chunk
+                uint32_t w0, w1, w2, w3;
+                asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
+                             : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                             : "r"(src0 + (2 * half + lb) * kKBlk + r * 128 + ((c ^ (r & 7)) << 4)));
+                const int cb16 = 2 * lb + (c >> 2), c16 = (c & 3) * 2;
+                const uint32_t dst = dst0 + cb16 * kKBlk + r * 128;
+                uint32_t h[8];
+                e4m3x4_to_f16x4(w0, h[0], h[1]);
+                e4m3x4_to_f16x4(w1, h[2], h[3]);
+                e4m3x4_to_f16x4(w2, h[4], h[5]);
+                e4m3x4_to_f16x4(w3, h[6], h[7]);
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(dst + ((c16 ^ (r & 7)) << 4)), "r"(h[0]),
+                             "r"(h[1]), "r"(h[2]), "r"(h[3])
+                             : "memory");
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(dst + (((c16 + 1) ^ (r & 7)) << 4)),
+                             "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
+                             : "memory");
+            }
+            umma::fence_async_smem();
+            umma::mbar_arrive(v_full(b));
+            umma::mbar_arrive(empty(st));
+        }
+    } else {
+        // ======================= softmax (thread = head) =======================
+        const int h = tid; // 0..127
+        const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+        const float kvs = *a.kv_scale;
+        wait_bar(q_full, 0);
+        const float fac = a.scale * kLog2e * sq_s[h] * kvs;
+        float m_ref = -INFINITY, l = 0.f;
+        // validity of the tile's 64 keys (the same for every head): lane j
+        // checks keys j and j + 32, a ballot gathers the mask
+        auto load_idx = [&](int tile, int off) {
+            const int p = tile * kKeys + off + lane;
+            return (tile < ntiles && p < a.topk) ? __ldg(row_idx + p) : -1;
+        };
+        int xa0 = load_idx(0, 0), xb0 = load_idx(0, 32), xa1 = load_idx(1, 0), xb1 = load_idx(1, 32);
+        int xa2 = load_idx(2, 0), xb2 = load_idx(2, 32), xa3 = load_idx(3, 0), xb3 = load_idx(3, 32);
+        auto ok = [&](int x) { return x >= 0 && (int64_t)x < a.num_slots; };
+        auto step = [&](int i, int &xa, int &xb) {
+            if (i >= ntiles)
+                return;
+            const int b = i & 1;
+            const uint32_t m_lo = __ballot_sync(0xffffffffu, ok(xa));
+            const uint32_t m_hi = __ballot_sync(0xffffffffu, ok(xb));
+            xa = load_idx(i + kIdxAhead, 0);
+            xb = load_idx(i + kIdxAhead, 32);
+            wait_bar(s_full(b), (uint32_t)((i >> 1) & 1));
+            umma::fence_after_sync();
+            float sv[64];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                umma::ld16(tl + kSCol + 64 * b + 16 * c, reinterpret_cast<uint32_t(&)[16]>(sv[16 * c]));
+            umma::wait_ld();
+            float mt = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                const bool v = ((j < 32 ? m_lo >> j : m_hi >> (j - 32)) & 1u) != 0;
+                sv[j] = v ? sv[j] * fac : -INFINITY;
+                mt = fmaxf(mt, sv[j]);
+            }
+            // move the reference max (warp-wide decision: TMEM access is warp-collective)
+            const bool exceed = mt > m_ref + kRescaleThreshold;
+            if (__any_sync(0xffffffffu, exceed)) {
+                const float mn = exceed ? mt : m_ref;
+                const float al = (m_ref == -INFINITY || !exceed) ? (exceed ? 0.f : 1.f) : exp2f(m_ref - mn);
+                m_ref = mn;
+                l *= al;
+                if (i >= 1) {
+                    // O holds PV(0..i-1): let PV(i-1) finish, then rescale this head's row
+                    wait_bar(p_empty((i - 1) & 1), (uint32_t)(((i - 1) >> 1) & 1));
+                    umma::fence_after_sync();
+#pragma unroll 1
+                    for (int c = 0; c < kDvHalf; c += 16) {
+                        uint32_t o[16];
+                        umma::ld16(tl + c, o);
+                        umma::wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            o[e] = __float_as_uint(__uint_as_float(o[e]) * al);
+                        umma::st16(tl + c, o);
+                    }
+                    umma::wait_st();
+                }
+            }
+            const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
+            uint32_t pw[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float p0 = exp2f(sv[2 * c] - mu), p1 = exp2f(sv[2 * c + 1] - mu);
+                l += p0 + p1;
+                pw[c] = pack_f16x2(p0, p1);
+            }
+            if (i >= 2) // PV(i-2) has read P(b)
+                wait_bar(p_empty(b), (uint32_t)(((i - 2) >> 1) & 1));
+            umma::st32(tl + kPCol + 32 * b, pw);
+            umma::wait_st();
+            umma::fence_before_sync();
+            umma::mbar_arrive(p_full(b));
+        };
+        for (int i0 = 0; i0 < ntiles; i0 += kIdxAhead) {
+            step(i0, xa0, xb0);
+            step(i0 + 1, xa1, xb1);
+            step(i0 + 2, xa2, xb2);
+            step(i0 + 3, xa3, xb3);
+        }
+        // ---- epilogue: this head's 256 output dims and its lse ----
+        if (ntiles > 0) // the last PV (and every earlier one) is done
+            wait_bar(p_empty((ntiles - 1) & 1), (uint32_t)(((ntiles - 1) >> 1) & 1));
+        umma::fence_after_sync();
+        const float ov = l > 0.f ? kvs / l : 0.f;
+        __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) +
+                              ((int64_t)t * a.H + hg * kHeads + h) * kDv + half * kDvHalf;
+#pragma unroll 1
+        for (int c = 0; c < kDvHalf; c += 16) {
+            uint32_t o[16];
+            umma::ld16(tl + c, o);
+            umma::wait_ld();
+            uint4 u0, u1;
+            auto val = [&](int e) { return l > 0.f ? __uint_as_float(o[e]) * ov : 0.f; };
+            u0.x = pack_bf16x2(val(0), val(1));
+            u0.y = pack_bf16x2(val(2), val(3));
+            u0.z = pack_bf16x2(val(4), val(5));
+            u0.w = pack_bf16x2(val(6), val(7));
+            u1.x = pack_bf16x2(val(8), val(9));
+            u1.y = pack_bf16x2(val(10), val(11));
+            u1.z = pack_bf16x2(val(12), val(13));
+            u1.w = pack_bf16x2(val(14), val(15));
+            reinterpret_cast<uint4 *>(orow + c)[0] = u0;
+            reinterpret_cast<uint4 *>(orow + c)[1] = u1;
+        }
+        if (half == 0 && a.lse != nullptr)
+            a.lse[(int64_t)t * a.H + hg * kHeads + h] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+        umma::fence_before_sync();
+    }
+    __syncthreads();
+    if (warp == kQkWarp)
+        umma::dealloc(tmem, kTmemCols);
+}
+
+} // namespace
+
+cudaError_t launch_fwd_wide(const FwdArgs &a, cudaStream_t stream)
+{
+    auto kern = sparse_mla_fwd_wide_kernel;
+    static std::atomic<uint64_t> attr_done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+        if (e != cudaSuccess)
+            return e;
+        attr_done.fetch_or(bit, std::memory_order_release);
+    }
+    const int64_t blocks = (int64_t)a.T * (a.H / kHeads) * 2;
+    if (blocks == 0)
+        return cudaSuccess;
+    // The cache as a 2-D tensor [rows x 576] bytes, read in boxes of 128 bytes
+    // x 1 row with the 128-byte swizzle (the fifth box of a row reaches past
+    // column 576 and is zero filled).
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (encode == nullptr)
+        return cudaErrorNotSupported;
+    CUtensorMap kv_map;
+    const int64_t rows = a.num_slots < 1 ? 1 : (a.num_slots > INT_MAX ? (int64_t)INT_MAX : a.num_slots);
+    cuuint64_t gdim[2] = {(cuuint64_t)kDqk, (cuuint64_t)rows};
+    cuuint64_t gstride[1] = {(cuuint64_t)kDqk};
+    cuuint32_t box[2] = {128, 1};
+    cuuint32_t estride[2] = {1, 1};
+    if (encode(&kv_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(a.kv), gdim, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    kern<<<dim3((unsigned)blocks), dim3(kThreads), kSmemAlloc, stream>>>(a, kv_map);
+    return cudaGetLastError();
+}
+
+cudaError_t read_wide_error(int *out, bool reset)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_wide_error, sizeof(int));
+    if (e == cudaSuccess && reset) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(g_wide_error, &zero, sizeof(int));
+    }
+    return e;
+}
+
+} // namespace smla

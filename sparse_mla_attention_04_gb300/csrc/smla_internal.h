@@ -4,6 +4,8 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 namespace smla {
@@ -51,9 +53,13 @@ struct WorkspaceLayout {
 WorkspaceLayout workspace_layout(int T, int H, int D_v, int S);
 
 cudaError_t launch_fwd_mma(const FwdArgs &a, cudaStream_t stream);
+cudaError_t launch_fwd_wide(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_fwd_umma16(const FwdArgs &a, cudaStream_t stream);
+// cuTensorMapEncodeTiled from the driver (resolved once; nullptr if unavailable).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 // First error code recorded by a bounded device-side wait that gave up (0 = none).
 cudaError_t read_umma_error(int *out, bool reset);
+cudaError_t read_wide_error(int *out, bool reset);
 
 cudaError_t launch_fp8_scale(const void *x, int64_t n, float *scale_out, int sm_count,
                              cudaStream_t stream);

@@ -75,8 +75,15 @@ def compare(out, lse, ref_o, ref_l, tol, what=""):
     return dict(rel=rel, max_abs=mab, lse_abs=lab)
 
 
-def case(w: inputs.Workload, *, num_splits=0, idx=None, kv_src=None, q=None, check_mirror=True):
-    """Run workload `w` (small enough for the whole-pool oracle) on both sides."""
+def case(w: inputs.Workload, *, num_splits=0, idx=None, kv_src=None, q=None, check_mirror=True,
+         check_plain=True):
+    """Run workload `w` (small enough for the whole-pool oracle) on both sides.
+
+    For an E4M3 cache the plain comparison (oracle with unquantized q, the
+    fp8 tolerance) measures the method's error and the mirrored one (oracle
+    quantizing q the same way, the bf16-level tolerance) the kernel's
+    arithmetic; `check_plain=False` keeps only the latter, for inputs built
+    to stress the kernel rather than to look like a workload."""
     q = inputs.make_q(w) if q is None else q
     kv_src = inputs.make_kv_source(w) if kv_src is None else kv_src
     idx = inputs.make_indices(w) if idx is None else idx
@@ -85,7 +92,9 @@ def case(w: inputs.Workload, *, num_splits=0, idx=None, kv_src=None, q=None, che
                        fp8=w.kv_fp8, num_splits=num_splits, D_v=w.D_v)
     ocache, oscale = oracle_cache(kv_src, w.kv_fp8)
     ref_o, ref_l, _ = oracle.sparse_mla(q, ocache, idx, w.scale, kv_fp8=w.kv_fp8, kv_scale=oscale, D_v=w.D_v)
-    res = compare(out, lse, ref_o, ref_l, TOL_FP8 if w.kv_fp8 else TOL_BF16, w.name)
+    res = {}
+    if check_plain or not w.kv_fp8:
+        res = compare(out, lse, ref_o, ref_l, TOL_FP8 if w.kv_fp8 else TOL_BF16, w.name)
     if w.kv_fp8 and check_mirror:
         mo, ml, _ = oracle.sparse_mla(q, ocache, idx, w.scale, kv_fp8=True, kv_scale=oscale, D_v=w.D_v, q_mode=1)
         res["mirror"] = compare(out, lse, mo, ml, TOL_FP8_MIRROR, w.name + " (q quantized)")

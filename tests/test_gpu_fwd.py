@@ -70,6 +70,56 @@ def test_wide_head_small():
     print(res)
 
 
+# --- 128-head kernel (E4M3 cache, D_qk = 576): ragged top-k, masks, the
+# rescale path, several head groups, and the fallback for explicit splits ---
+
+@pytest.mark.parametrize("topk", [1, 63, 65, 700])
+def test_wide_head_ragged_topk(topk):
+    w = inputs.Workload("wide_ragged", 3, 128, 576, 512, 3000, topk, True, 1 / math.sqrt(576), "uniform",
+                        seed=topk)
+    parity.case(w)
+    assert binding.smla_device_error() == 0
+
+
+def test_wide_head_masks_and_empty_rows():
+    w = inputs.Workload("wide_masks", 4, 128, 576, 512, 3000, 300, True, 1 / math.sqrt(576), "uniform", seed=9)
+    idx = inputs.make_indices(w)
+    rng = np.random.default_rng(11)
+    idx[0, rng.choice(300, 200, replace=False)] = -1   # scattered
+    idx[1, :] = -1                                      # empty row
+    idx[2, :299] = -1                                   # one index, at the end
+    res, out, lse = parity.case(w, idx=idx)
+    assert (out[1] == 0).all() and np.isneginf(lse[1]).all()
+
+
+def test_wide_head_rescale_path():
+    """Row 0 lists its keys in ascending order of head 0's logit with q
+    scaled up, so the running max of most heads climbs by more than 2^8
+    several times and the kernel rescales O rows in tensor memory. Scaled-up
+    logits amplify the fp8 rounding of q itself, so only the mirrored
+    comparison (the oracle quantizes q the same way) applies."""
+    w = inputs.Workload("wide_rescale", 2, 128, 576, 512, 3000, 640, True, 1 / math.sqrt(576), "uniform", seed=13)
+    q = (inputs.make_q(w).float() * 3).to(torch.bfloat16)
+    kv = inputs.make_kv_source(w)
+    idx = inputs.make_indices(w)
+    logits0 = kv[idx[0]].float() @ q[0, 0].float()
+    idx[0] = idx[0][np.argsort(logits0.numpy())]
+    res, _, _ = parity.case(w, idx=idx, kv_src=kv, q=q, check_plain=False)
+    assert "mirror" in res
+
+
+def test_wide_head_two_head_groups():
+    w = inputs.Workload("wide_h256", 2, 256, 576, 512, 3000, 300, True, 1 / math.sqrt(576), "uniform", seed=5)
+    parity.case(w)
+
+
+def test_wide_head_explicit_splits():
+    """An explicit split count goes to the warp-MMA kernel (the 128-head
+    kernel does not split the top-k list); results agree within tolerance."""
+    w = inputs.Workload("wide_split", 2, 128, 576, 512, 3000, 700, True, 1 / math.sqrt(576), "uniform", seed=17)
+    parity.case(w, num_splits=3)
+
+
 def test_wide_head_bf16_cache():
     w = inputs.wide(T=3, ctx=2048, topk=700, name="wide_bf16")
     w.kv_fp8 = False
