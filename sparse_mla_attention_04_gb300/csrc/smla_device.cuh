@@ -126,6 +126,15 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t &lo, uint32
         : "r"(w));
 }
 
+// 2^x by the hardware approximation (relative error about 2^-22, far below
+// the 16-bit rounding the softmax weights get next); -inf gives 0.
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ float warp_max(float v)
 {
 #pragma unroll

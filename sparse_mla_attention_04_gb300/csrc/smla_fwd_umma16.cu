@@ -54,8 +54,10 @@
 //     logits (two partial sums) from TMEM, masks, and exponentiates against a
 //     running reference max; the max is recomputed over the tile (and O^T
 //     rescaled in TMEM) only when some logit exceeds the reference by more
-//     than 2^8, so the common tile needs no cross-thread reduction beyond one
-//     flag exchange; writes one row of P^T.
+//     than 2^8, and the reference then moves to 2^8 above the tile max (p
+//     stays <= 1; O/l does not depend on the reference), so the common tile
+//     needs no cross-thread reduction beyond one flag exchange; writes one
+//     row of P^T.
 // Every barrier completes once per use of the resource it guards, so no
 // waiter can fall two phases behind; every wait gives up after about 2 s
 // (the call then records an error, stops issuing, waits with a bound for the
@@ -100,7 +102,8 @@ constexpr int kHeads = 16;
 constexpr int kD = 512;                // D_qk = D_v
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f; // log2 units: p <= 2^8 between rescales
+constexpr float kRescaleThreshold = 8.0f; // log2 units a logit may exceed the reference by
+constexpr float kHeadroom = 8.0f;         // a moved reference sits this far above the tile max
 constexpr int kIdxAhead = 4;              // tiles of index look-ahead
 
 template <bool FP8>
@@ -563,7 +566,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
 #pragma unroll
                 for (int h = 0; h < 16; ++h) {
                     const float tmx = fmaxf(fmaxf(wmax_s[h], wmax_s[16 + h]), fmaxf(wmax_s[32 + h], wmax_s[48 + h]));
-                    const float mn = fmaxf(m_ref[h], tmx);
+                    const float mn = fmaxf(m_ref[h], tmx + kHeadroom);
                     const float al = (m_ref[h] == -INFINITY) ? 0.f : exp2f(m_ref[h] - mn);
                     m_ref[h] = mn;
                     l_part[h] *= al;
@@ -593,7 +596,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
 #pragma unroll
             for (int h = 0; h < 16; ++h) {
                 const float mu = (m_ref[h] == -INFINITY) ? 0.f : m_ref[h];
-                sv[h] = exp2f(sv[h] - mu);
+                sv[h] = ex2_approx(sv[h] - mu);
                 l_part[h] += sv[h];
             }
             if (i >= 2)

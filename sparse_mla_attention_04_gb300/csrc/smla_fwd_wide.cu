@@ -11,10 +11,12 @@
 // inputs, identical P).
 //
 // Warp roles, handing tiles over through mbarriers (every wait bounded):
-//   producers (warps 5-8): quantize q per head (s_q = amax|q[t,h,:]| / 448,
-//     1 if zero; q8 = RNE_satfinite(q / s_q)) into shared memory, K-major
-//     with the 128-byte swizzle (5 blocks of [128 heads x 128 B]); then per
-//     64-key tile 80 TMA tile::gather4 copies (16 key quads x 5 column
+//   all threads, first: quantize q per head (s_q = amax|q[t,h,:]| / 448, 1
+//     if zero; q8 = RNE_satfinite(q / s_q)) into shared memory, K-major with
+//     the 128-byte swizzle (5 blocks of [128 heads x 128 B]); every thread
+//     takes ~11 chunks of 16 elements and issues all its loads at once, the
+//     per-head amax meeting in shared memory.
+//   producers (warps 5-8): per 64-key tile 80 TMA tile::gather4 copies (16 key quads x 5 column
 //     blocks of 128 B; the last block reaches past column 576 and is zero
 //     filled) into a 2-stage ring. Masked and out-of-range indices are
 //     passed as row -1 (zero fill, no memory read).
@@ -23,7 +25,8 @@
 //   softmax (warps 0-3, thread = head, whole S row in the thread): masks,
 //     scales by scale * s_q[h] * kv_scale, exponentiates base 2 against a
 //     running reference max that moves (rescaling the head's O row in
-//     tensor memory) only when a logit exceeds it by more than 2^8; writes
+//     tensor memory) only when a logit exceeds it by more than 2^8, and then
+//     to 2^8 above the tile max, so later tiles rarely move it again; writes
 //     P as fp16 pairs into tensor memory (double-buffered), the A operand
 //     of PV.
 //   converters (warps 10-13): the tile's half of the value columns, E4M3 ->
@@ -63,7 +66,8 @@ constexpr int kCopies = 16 * kCB;     // gather4 copies per tile
 constexpr int kIdxAhead = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;
+constexpr float kRescaleThreshold = 8.0f; // log2 units a logit may exceed the reference by
+constexpr float kHeadroom = 8.0f;         // a moved reference sits this far above the tile max
 
 // warps 0-3: softmax
 constexpr int kQkWarp = 4;
@@ -83,7 +87,8 @@ constexpr int kOffRing = kOffQ8 + kCB * kQBlk;
 constexpr int kV16 = 4 * kKBlk;               // [64 keys x 256 dims] binary16, 4 blocks of 64 dims
 constexpr int kOffV16 = kOffRing + kStages * kTile;
 constexpr int kOffSq = kOffV16 + 2 * kV16;    // [128] per-head q scales
-constexpr int kOffMisc = kOffSq + kHeads * 4; // tmem address, abort, go[2]
+constexpr int kOffAmax = kOffSq + kHeads * 4; // [128] per-head amax (float bits)
+constexpr int kOffMisc = kOffAmax + kHeads * 4; // tmem address, abort, go[2]
 constexpr int kOffMbar = kOffMisc + 32;
 // full[2], empty[2], s_full[2], p_full[2], p_empty[2], v_full[2], v_empty[2], q_full, drain
 constexpr int kNBar = 16;
@@ -116,6 +121,7 @@ __global__ void __launch_bounds__(512, 1)
     uint8_t *smem = smem_raw + (sbase - raw_base);
     const uint32_t q8_s = sbase + kOffQ8, ring = sbase + kOffRing, v16_s = sbase + kOffV16;
     float *sq_s = reinterpret_cast<float *>(smem + kOffSq);
+    int *amax_s = reinterpret_cast<int *>(smem + kOffAmax);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     int *abort_s = reinterpret_cast<int *>(smem + kOffMisc + 4);
     volatile int *go_s = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
@@ -150,7 +156,7 @@ __global__ void __launch_bounds__(512, 1)
             umma::mbar_init(v_full(b), kConverterThreads);
             umma::mbar_init(v_empty(b), 1);
         }
-        umma::mbar_init(q_full, kProducerThreads);
+        umma::mbar_init(q_full, 1);
         umma::mbar_init(drain, 2);
         umma::mbar_init_fence();
         *abort_s = 0;
@@ -161,6 +167,85 @@ __global__ void __launch_bounds__(512, 1)
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+
+    // ---- q -> q8 (all threads): 128 heads x 36 chunks of 16 elements ----
+    // two passes over q (amax, then quantize; the second hits L2), each in two
+    // batches of at most kPer chunks a thread with all loads issued at once
+    {
+        constexpr int kChunks = kHeads * (kDqk / 16);
+        constexpr int kPer = (kChunks + 2 * kThreads - 1) / (2 * kThreads);
+        const uint4 *qsrc = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.q) +
+                                                           ((int64_t)t * a.H + hg * kHeads) * kDqk);
+        if (tid < kHeads)
+            amax_s[tid] = 0;
+        __syncthreads();
+        auto batch = [&](int first, bool quantize) {
+            uint4 qv[kPer][2];
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const int c = first + tid + kThreads * u;
+                if (c < kChunks) {
+                    qv[u][0] = __ldg(qsrc + 2 * c);
+                    qv[u][1] = __ldg(qsrc + 2 * c + 1);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const int c = first + tid + kThreads * u;
+                if (c >= kChunks)
+                    continue;
+                const int h = c / (kDqk / 16), d = 16 * (c % (kDqk / 16));
+                if (!quantize) {
+                    float m = 0.f;
+#pragma unroll
+                    for (int v = 0; v < 2; ++v) {
+                        const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&qv[u][v]);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = __bfloat1622float2(b2[e]);
+                            m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+                        }
+                    }
+                    atomicMax(amax_s + h, __float_as_int(m)); // m >= 0: int order = float order
+                } else {
+                    const float sq = sq_s[h];
+                    uint32_t w[4];
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&qv[u][v >> 1]);
+                        const float2 f0 = __bfloat1622float2(b2[2 * (v & 1)]);
+                        const float2 f1 = __bfloat1622float2(b2[2 * (v & 1) + 1]);
+                        w[v] = quant4_e4m3(f0.x, f0.y, f1.x, f1.y, sq);
+                    }
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(q8_s + (d >> 7) * kQBlk +
+                                                                                 sw128(h, d & 127)),
+                                 "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                                 : "memory");
+                }
+            }
+        };
+        batch(0, false);
+        batch(kPer * kThreads, false);
+        __syncthreads();
+        if (tid < kHeads) {
+            const float m = __int_as_float(amax_s[tid]);
+            sq_s[tid] = (m == 0.f) ? 1.0f : __fdiv_rn(m, 448.0f);
+        }
+        __syncthreads();
+        batch(0, true);
+        batch(kPer * kThreads, true);
+        // the unused half of the last block stays zero for the MMA
+        for (int c = tid; c < kHeads * 4; c += kThreads) {
+            const int h = c >> 2, d = kDqk + 16 * (c & 3);
+            asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};\n" ::"r"(q8_s + (d >> 7) * kQBlk + sw128(h, d & 127)),
+                         "r"(0u)
+                         : "memory");
+        }
+        umma::fence_async_smem();
+        __syncthreads();
+        if (tid == 0)
+            umma::mbar_arrive(q_full); // q8 and the scales are in place (one arrival)
+    }
 
     auto wait_bar = [&](uint32_t mbar, uint32_t parity) {
         if (*(volatile int *)abort_s)
@@ -196,53 +281,6 @@ __global__ void __launch_bounds__(512, 1)
         fetch(1, r1);
         fetch(2, r2);
         fetch(3, r3);
-        bool q_pending = true;
-        // thread pt quantizes head pt: amax over its 576 elements, then 36
-        // chunks of 16 codes into the swizzled K-major q8 blocks
-        auto publish_q = [&] {
-            const __nv_bfloat16 *qh =
-                static_cast<const __nv_bfloat16 *>(a.q) + ((int64_t)t * a.H + hg * kHeads + pt) * kDqk;
-            const uint4 *src = reinterpret_cast<const uint4 *>(qh);
-            float m = 0.f;
-            for (int c = 0; c < kDqk / 8; ++c) {
-                const uint4 u = __ldg(src + c);
-                const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&u);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = __bfloat1622float2(b2[e]);
-                    m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
-                }
-            }
-            const float sq = (m == 0.f) ? 1.0f : __fdiv_rn(m, 448.0f);
-            sq_s[pt] = sq;
-            for (int c = 0; c < kDqk / 16; ++c) {
-                const uint4 u0 = __ldg(src + 2 * c), u1 = __ldg(src + 2 * c + 1);
-                const __nv_bfloat162 *b0 = reinterpret_cast<const __nv_bfloat162 *>(&u0);
-                const __nv_bfloat162 *b1 = reinterpret_cast<const __nv_bfloat162 *>(&u1);
-                uint32_t w[4];
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const __nv_bfloat162 *bb = v < 2 ? b0 : b1;
-                    const float2 f0 = __bfloat1622float2(bb[2 * (v & 1)]);
-                    const float2 f1 = __bfloat1622float2(bb[2 * (v & 1) + 1]);
-                    w[v] = quant4_e4m3(f0.x, f0.y, f1.x, f1.y, sq);
-                }
-                const int d = 16 * c; // column of the chunk
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(q8_s + (d >> 7) * kQBlk +
-                                                                             sw128(pt, d & 127)),
-                             "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
-                             : "memory");
-            }
-            // the unused half of the last block stays zero for the MMA
-            for (int d = kDqk; d < kCB * 128; d += 16)
-                asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};\n" ::"r"(q8_s + (d >> 7) * kQBlk +
-                                                                            sw128(pt, d & 127)),
-                             "r"(0u)
-                             : "memory");
-            umma::fence_async_smem();
-            umma::mbar_arrive(q_full);
-            q_pending = false;
-        };
         int issued = 0;
         bool stop = false;
         auto step = [&](int j, int(&r)[4]) {
@@ -269,8 +307,6 @@ __global__ void __launch_bounds__(512, 1)
                                   row(r[1]), row(r[2]), row(r[3]), full(st));
             issued = j + 1;
             fetch(j + kIdxAhead, r);
-            if (q_pending && j + 1 >= kStages)
-                publish_q();
         };
         for (int j0 = 0; !stop; j0 += kIdxAhead) {
             step(j0, r0);
@@ -278,8 +314,6 @@ __global__ void __launch_bounds__(512, 1)
             step(j0 + 2, r2);
             step(j0 + 3, r3);
         }
-        if (q_pending)
-            publish_q();
         if (pt == 0) {
             for (int j = max(0, issued - kStages); j < issued; ++j)
                 wait_issued(full(j % kStages), (uint32_t)((j / kStages) & 1));
@@ -410,7 +444,7 @@ __global__ void __launch_bounds__(512, 1)
             // move the reference max (warp-wide decision: TMEM access is warp-collective)
             const bool exceed = mt > m_ref + kRescaleThreshold;
             if (__any_sync(0xffffffffu, exceed)) {
-                const float mn = exceed ? mt : m_ref;
+                const float mn = exceed ? mt + kHeadroom : m_ref;
                 const float al = (m_ref == -INFINITY || !exceed) ? (exceed ? 0.f : 1.f) : exp2f(m_ref - mn);
                 m_ref = mn;
                 l *= al;
@@ -435,7 +469,7 @@ __global__ void __launch_bounds__(512, 1)
             uint32_t pw[32];
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
-                const float p0 = exp2f(sv[2 * c] - mu), p1 = exp2f(sv[2 * c + 1] - mu);
+                const float p0 = ex2_approx(sv[2 * c] - mu), p1 = ex2_approx(sv[2 * c + 1] - mu);
                 l += p0 + p1;
                 pw[c] = pack_f16x2(p0, p1);
             }
