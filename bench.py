@@ -98,6 +98,46 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s)"
 
 
+FALLBACK_BF16_TFLOPS = 1900.0
+FP8_OVER_BF16 = 2.0   # nominal dense E4M3 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
+
+
+def measured_bf16_tflops():
+    """Burst bf16 tensor peak (a kernel timed on its own)."""
+    try:
+        d = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        return float(d["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops)"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback (1.9 PFLOP/s bf16)"
+
+
+def roofline(w, per_launch_bytes, valid_per_launch, sec_per_launch, traffic):
+    """The bound of one launch: HBM (gathered bytes / copy bandwidth) or the
+    tensor cores (QK at 2*H*D_qk and PV at 2*H*D_v FLOP per valid index, QK
+    at the E4M3 rate for an fp8 cache, PV at the bf16 rate), whichever takes
+    longer; achieved and peak in that bound's unit."""
+    hbm, hbm_src = measured_peaks()
+    bf16, bf16_src = measured_bf16_tflops()
+    qk_flop = 2.0 * w.H * w.D_qk * valid_per_launch
+    pv_flop = 2.0 * w.H * w.D_v * valid_per_launch
+    qk_peak = bf16 * (FP8_OVER_BF16 if w.kv_fp8 else 1.0)
+    t_tensor = qk_flop / (qk_peak * 1e12) + pv_flop / (bf16 * 1e12)
+    t_hbm = per_launch_bytes / (hbm * 1e9)
+    if t_tensor > t_hbm:
+        flop = qk_flop + pv_flop
+        peak = flop / t_tensor / 1e12   # the mix's peak: fp8 QK share at 2x
+        achieved = flop / sec_per_launch / 1e12
+        return {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_source": bf16_src + (" x %.0f for the E4M3 QK share" % FP8_OVER_BF16 if w.kv_fp8 else ""),
+                "algorithmic_flop_per_launch": flop, "algorithmic_bytes_per_launch": per_launch_bytes,
+                "hbm_frac": round(per_launch_bytes / sec_per_launch / 1e9 / hbm, 4)}
+    achieved = per_launch_bytes / sec_per_launch / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved / hbm, 4), "traffic": traffic, "peak_source": hbm_src,
+            "algorithmic_bytes_per_launch": per_launch_bytes}
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons during the timed region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -267,7 +307,8 @@ def run_ours(args):
     rows = sum(int((s["idx_np"] != -1).any(axis=1).sum()) for s in sets) / R   # rows with work (all, here)
     gbs = total_bytes * world / (ms_max * 1e-3) / 1e9
     per_launch_bytes = total_bytes / K
-    achieved = per_launch_bytes / (ms / K * 1e-3) / 1e9
+    valid_per_step = [int((s["idx_np"] != -1).sum()) for s in sets]
+    valid_per_launch = (reps * sum(valid_per_step) + sum(valid_per_step[:rem])) / K
 
     e2e = None
     if not args.no_e2e:
@@ -278,7 +319,6 @@ def run_ours(args):
         cpu = cpu_baseline(w, src, sets[0])
 
     if rank == 0:
-        peak, peak_src = measured_peaks()
         line = {
             "metric": "sparse MLA fwd gathered-KV GB/s (%s)" % w.name,
             "value": round(gbs, 2),
@@ -304,12 +344,7 @@ def run_ours(args):
             },
             "query_rows_per_s": round(rows * world / (ms_max * 1e-3 / K), 1),
             "gpu_launches": K,
-            "roofline": {
-                "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(w.name),
-                "peak_source": peak_src,
-                "algorithmic_bytes_per_launch": per_launch_bytes,
-            },
+            "roofline": roofline(w, per_launch_bytes, valid_per_launch, ms / K * 1e-3, ncu_traffic(w.name)),
             "clocks": clk,
             "e2e": e2e,
             "cpu_baseline": cpu,
