@@ -145,12 +145,20 @@ SMLA_API size_t sparse_mla_fwd_workspace_size(int T, int H, int D_qk, int D_v, i
  *              be zero-filled before its first use; every call returns its
  *              counters to zero and never writes partials into that region, so
  *              one buffer serves later calls of any shape on the same stream.
+ *              The 128-head E4M3 kernel (below) also needs a workspace, after
+ *              that region: q quantized per (row, head), T*H*D_qk bytes, and
+ *              its T*H scales.
  *              Calls that overlap in time must not share a workspace.
- * Kernels: 16 heads with a bf16 cache (D_qk = D_v = 512) run on the tcgen05
- *              tensor cores with accumulators in tensor memory; every other
- *              supported shape runs on a warp-MMA (mma.sync) kernel. Setting
- *              SMLA_KERNEL=mma in the environment routes every call to the
- *              warp-MMA kernel (a comparison and test switch).
+ * Kernels: 16 heads with D_qk = D_v = 512 (bf16 cache, or E4M3 with fp8
+ *              dots) run on a tcgen05 kernel (keys on the MMA's M axis,
+ *              accumulators in tensor memory, TMA row gathers); H a multiple of
+ *              128 with D_qk = 576, D_v = 512 and an E4M3 cache runs, when the
+ *              call does not ask for more than one split, on a tcgen05 kernel
+ *              with heads on M (two CTAs per row, each owning half of the
+ *              value dims; a first pass quantizes q into the workspace); every
+ *              other supported shape runs on a warp-MMA (mma.sync) kernel.
+ *              Setting SMLA_KERNEL=mma in the environment routes every call to
+ *              the warp-MMA kernel (a comparison and test switch).
  * num_splits   0 = automatic (smla_plan_num_splits for the current device);
  *              otherwise the number of top-k splits to use, 1..128. More than 8
  *              splits need T * H / 16 <= 4096 (else SMLA_ERR_UNSUPPORTED).

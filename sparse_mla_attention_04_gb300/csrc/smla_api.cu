@@ -117,10 +117,17 @@ bool shape_supported(int H, int D_qk, int D_v)
 
 namespace smla {
 
-WorkspaceLayout workspace_layout(int T, int H, int D_v, int S)
+WorkspaceLayout workspace_layout(int T, int H, int D_qk, int D_v, int S, bool wide)
 {
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
     WorkspaceLayout w{};
+    if (wide) {
+        // after the merge-counter region, which must stay zero between calls
+        w.q8 = up((size_t)kTicketSlots * sizeof(int));
+        w.q_scale = up(w.q8 + (size_t)T * H * D_qk);
+        w.total = up(w.q_scale + (size_t)T * H * sizeof(float));
+        return w;
+    }
     if (S <= kClusterMaxSplits)
         return w;
     w.tickets = 0;
@@ -189,7 +196,8 @@ SMLA_API size_t sparse_mla_fwd_workspace_size(int T, int H, int D_qk, int D_v, i
     }
     if (S > kMaxSplits || (S > kClusterMaxSplits && (int64_t)T * (H / 16) > kTicketSlots))
         return (size_t)-1;
-    return smla::workspace_layout(T, H, D_v, S).total;
+    const bool wide = choose_path(H, D_qk, D_v, kv_dtype == SMLA_KV_FP8_E4M3) == Path::Wide && S == 1;
+    return smla::workspace_layout(T, H, D_qk, D_v, S, wide).total;
 }
 
 SMLA_API smla_status sparse_mla_fwd(const void *q, const void *kv_cache, int kv_dtype, const float *kv_scale,
@@ -242,7 +250,7 @@ SMLA_API smla_status sparse_mla_fwd(const void *q, const void *kv_cache, int kv_
     }
     if (S > kClusterMaxSplits && (int64_t)T * (H / 16) > kTicketSlots)
         return SMLA_ERR_UNSUPPORTED;
-    const smla::WorkspaceLayout wl = smla::workspace_layout(T, H, D_v, S);
+    const smla::WorkspaceLayout wl = smla::workspace_layout(T, H, D_qk, D_v, S, path == Path::Wide);
     if (wl.total > 0) {
         if (workspace == nullptr)
             return SMLA_ERR_NULL_POINTER;
@@ -263,6 +271,8 @@ SMLA_API smla_status sparse_mla_fwd(const void *q, const void *kv_cache, int kv_
     a.part_o = wl.total ? reinterpret_cast<float *>(ws + wl.part_o) : nullptr;
     a.part_lse = wl.total ? reinterpret_cast<float *>(ws + wl.part_lse) : nullptr;
     a.tickets = wl.total ? reinterpret_cast<int *>(ws + wl.tickets) : nullptr;
+    a.q8 = path == Path::Wide ? ws + wl.q8 : nullptr;
+    a.q_scale = path == Path::Wide ? reinterpret_cast<float *>(ws + wl.q_scale) : nullptr;
     a.num_slots = num_slots;
     a.T = T;
     a.H = H;

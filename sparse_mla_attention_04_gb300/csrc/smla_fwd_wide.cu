@@ -11,11 +11,12 @@
 // inputs, identical P).
 //
 // Warp roles, handing tiles over through mbarriers (every wait bounded):
-//   all threads, first: quantize q per head (s_q = amax|q[t,h,:]| / 448, 1
-//     if zero; q8 = RNE_satfinite(q / s_q)) into shared memory, K-major with
-//     the 128-byte swizzle (5 blocks of [128 heads x 128 B]); every thread
-//     takes ~11 chunks of 16 elements and issues all its loads at once, the
-//     per-head amax meeting in shared memory.
+// q is quantized per (row, head) by a separate pass over all rows (one warp
+// per head: s_q = amax|q[t,h,:]| / 448, 1 if zero; q8 = RNE_satfinite(q /
+// s_q)) into the workspace, so each CTA pair does not repeat it; the CTA
+// copies its 128 heads of q8 with five TMA tile loads (boxes of 128 B x 128
+// rows, 128-byte swizzle; the fifth box reaches past column 576 and comes
+// back zero filled, the unused half of the last block).
 //   producers (warps 5-8): per 64-key tile 80 TMA tile::gather4 copies (16 key quads x 5 column
 //     blocks of 128 B; the last block reaches past column 576 and is zero
 //     filled) into a 2-stage ring. Masked and out-of-range indices are
@@ -86,9 +87,7 @@ constexpr int kTile = kCB * kKBlk;            // 40 KB
 constexpr int kOffRing = kOffQ8 + kCB * kQBlk;
 constexpr int kV16 = 4 * kKBlk;               // [64 keys x 256 dims] binary16, 4 blocks of 64 dims
 constexpr int kOffV16 = kOffRing + kStages * kTile;
-constexpr int kOffSq = kOffV16 + 2 * kV16;    // [128] per-head q scales
-constexpr int kOffAmax = kOffSq + kHeads * 4; // [128] per-head amax (float bits)
-constexpr int kOffMisc = kOffAmax + kHeads * 4; // tmem address, abort, go[2]
+constexpr int kOffMisc = kOffV16 + 2 * kV16; // tmem address, abort, go[2]
 constexpr int kOffMbar = kOffMisc + 32;
 // full[2], empty[2], s_full[2], p_full[2], p_empty[2], v_full[2], v_empty[2], q_full, drain
 constexpr int kNBar = 16;
@@ -106,22 +105,59 @@ constexpr uint32_t kIdescQK = umma::idesc(128, 64, 0, 0, 0, 0);
 // PV: A = P in tensor memory (fp16), B = V16 (MN-major), M = 128 heads, N = 256 dims
 constexpr uint32_t kIdescPV = umma::idesc(128, 256, 0, 0, 0, 1);
 
-// byte offset of (row, byte) in a [rows x 128 B] block with the 128-byte swizzle
-__device__ __forceinline__ uint32_t sw128(int row, int byte)
+// q [rows x 576] bf16 -> q8 [rows x 576] E4M3 and scale[rows]; one warp per row
+// (lanes 0-23 hold 24 elements each).
+__global__ void __launch_bounds__(128) quantize_q_e4m3_kernel(const __nv_bfloat16 *__restrict__ q, int64_t rows,
+                                                             uint8_t *__restrict__ q8, float *__restrict__ scale)
 {
-    return (uint32_t)(row * 128 + ((((byte >> 4) ^ (row & 7)) << 4) | (byte & 15)));
+    const int64_t r = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= rows)
+        return;
+    const uint4 *src = reinterpret_cast<const uint4 *>(q + r * kDqk);
+    uint4 v[3];
+    float m = 0.f;
+    if (lane < 24) {
+#pragma unroll
+        for (int u = 0; u < 3; ++u)
+            v[u] = __ldg(src + 3 * lane + u);
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {
+            const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&v[u]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(b2[e]);
+                m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+        }
+    }
+    m = warp_max(m);
+    const float s = (m == 0.f) ? 1.0f : __fdiv_rn(m, 448.0f);
+    if (lane == 0)
+        scale[r] = s;
+    if (lane < 24) {
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {
+            const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&v[u]);
+            const float2 f0 = __bfloat1622float2(b2[0]), f1 = __bfloat1622float2(b2[1]);
+            const float2 f2 = __bfloat1622float2(b2[2]), f3 = __bfloat1622float2(b2[3]);
+            uint2 o;
+            o.x = quant4_e4m3(f0.x, f0.y, f1.x, f1.y, s);
+            o.y = quant4_e4m3(f2.x, f2.y, f3.x, f3.y, s);
+            *reinterpret_cast<uint2 *>(q8 + r * kDqk + (3 * lane + u) * 8) = o;
+        }
+    }
 }
 
 __global__ void __launch_bounds__(512, 1)
-    sparse_mla_fwd_wide_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap kv_map)
+    sparse_mla_fwd_wide_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap kv_map,
+                               const __grid_constant__ CUtensorMap q8_map)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t sbase = (raw_base + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (sbase - raw_base);
     const uint32_t q8_s = sbase + kOffQ8, ring = sbase + kOffRing, v16_s = sbase + kOffV16;
-    float *sq_s = reinterpret_cast<float *>(smem + kOffSq);
-    int *amax_s = reinterpret_cast<int *>(smem + kOffAmax);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     int *abort_s = reinterpret_cast<int *>(smem + kOffMisc + 4);
     volatile int *go_s = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
@@ -168,83 +204,12 @@ __global__ void __launch_bounds__(512, 1)
     umma::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    // ---- q -> q8 (all threads): 128 heads x 36 chunks of 16 elements ----
-    // two passes over q (amax, then quantize; the second hits L2), each in two
-    // batches of at most kPer chunks a thread with all loads issued at once
-    {
-        constexpr int kChunks = kHeads * (kDqk / 16);
-        constexpr int kPer = (kChunks + 2 * kThreads - 1) / (2 * kThreads);
-        const uint4 *qsrc = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.q) +
-                                                           ((int64_t)t * a.H + hg * kHeads) * kDqk);
-        if (tid < kHeads)
-            amax_s[tid] = 0;
-        __syncthreads();
-        auto batch = [&](int first, bool quantize) {
-            uint4 qv[kPer][2];
-#pragma unroll
-            for (int u = 0; u < kPer; ++u) {
-                const int c = first + tid + kThreads * u;
-                if (c < kChunks) {
-                    qv[u][0] = __ldg(qsrc + 2 * c);
-                    qv[u][1] = __ldg(qsrc + 2 * c + 1);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < kPer; ++u) {
-                const int c = first + tid + kThreads * u;
-                if (c >= kChunks)
-                    continue;
-                const int h = c / (kDqk / 16), d = 16 * (c % (kDqk / 16));
-                if (!quantize) {
-                    float m = 0.f;
-#pragma unroll
-                    for (int v = 0; v < 2; ++v) {
-                        const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&qv[u][v]);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 f = __bfloat1622float2(b2[e]);
-                            m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
-                        }
-                    }
-                    atomicMax(amax_s + h, __float_as_int(m)); // m >= 0: int order = float order
-                } else {
-                    const float sq = sq_s[h];
-                    uint32_t w[4];
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&qv[u][v >> 1]);
-                        const float2 f0 = __bfloat1622float2(b2[2 * (v & 1)]);
-                        const float2 f1 = __bfloat1622float2(b2[2 * (v & 1) + 1]);
-                        w[v] = quant4_e4m3(f0.x, f0.y, f1.x, f1.y, sq);
-                    }
-                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(q8_s + (d >> 7) * kQBlk +
-                                                                                 sw128(h, d & 127)),
-                                 "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
-                                 : "memory");
-                }
-            }
-        };
-        batch(0, false);
-        batch(kPer * kThreads, false);
-        __syncthreads();
-        if (tid < kHeads) {
-            const float m = __int_as_float(amax_s[tid]);
-            sq_s[tid] = (m == 0.f) ? 1.0f : __fdiv_rn(m, 448.0f);
-        }
-        __syncthreads();
-        batch(0, true);
-        batch(kPer * kThreads, true);
-        // the unused half of the last block stays zero for the MMA
-        for (int c = tid; c < kHeads * 4; c += kThreads) {
-            const int h = c >> 2, d = kDqk + 16 * (c & 3);
-            asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};\n" ::"r"(q8_s + (d >> 7) * kQBlk + sw128(h, d & 127)),
-                         "r"(0u)
-                         : "memory");
-        }
-        umma::fence_async_smem();
-        __syncthreads();
-        if (tid == 0)
-            umma::mbar_arrive(q_full); // q8 and the scales are in place (one arrival)
+    // ---- q8 of this CTA's 128 heads: five TMA tile loads ----
+    if (tid == 0) {
+        umma::mbar_arrive_expect_tx(q_full, kCB * kQBlk);
+        const int qrow = t * a.H + hg * kHeads;
+        for (int cb = 0; cb < kCB; ++cb)
+            umma::tma_load_2d(q8_s + cb * kQBlk, &q8_map, 128 * cb, qrow, q_full);
     }
 
     auto wait_bar = [&](uint32_t mbar, uint32_t parity) {
@@ -315,6 +280,7 @@ __global__ void __launch_bounds__(512, 1)
             step(j0 + 3, r3);
         }
         if (pt == 0) {
+            wait_issued(q_full, 0); // the q8 copies have landed (also after an abort)
             for (int j = max(0, issued - kStages); j < issued; ++j)
                 wait_issued(full(j % kStages), (uint32_t)((j / kStages) & 1));
         }
@@ -407,8 +373,7 @@ __global__ void __launch_bounds__(512, 1)
         const int h = tid; // 0..127
         const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
         const float kvs = *a.kv_scale;
-        wait_bar(q_full, 0);
-        const float fac = a.scale * kLog2e * sq_s[h] * kvs;
+        const float fac = a.scale * kLog2e * a.q_scale[(int64_t)t * a.H + hg * kHeads + h] * kvs;
         float m_ref = -INFINITY, l = 0.f;
         // validity of the tile's 64 keys (the same for every head): lane j
         // checks keys j and j + 32, a ballot gathers the mask
@@ -556,7 +521,20 @@ cudaError_t launch_fwd_wide(const FwdArgs &a, cudaStream_t stream)
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    kern<<<dim3((unsigned)blocks), dim3(kThreads), kSmemAlloc, stream>>>(a, kv_map);
+    // q8 as a 2-D tensor [T*H rows x 576] bytes, copied in boxes of 128 B x 128
+    // rows with the 128-byte swizzle
+    CUtensorMap q8_map;
+    cuuint64_t qdim[2] = {(cuuint64_t)kDqk, (cuuint64_t)a.T * a.H};
+    cuuint64_t qstride[1] = {(cuuint64_t)kDqk};
+    cuuint32_t qbox[2] = {128, (cuuint32_t)kHeads};
+    if (encode(&q8_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.q8, qdim, qstride, qbox, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    const int64_t qrows = (int64_t)a.T * a.H;
+    quantize_q_e4m3_kernel<<<dim3((unsigned)((qrows + 3) / 4)), dim3(128), 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(a.q), qrows, a.q8, a.q_scale);
+    kern<<<dim3((unsigned)blocks), dim3(kThreads), kSmemAlloc, stream>>>(a, kv_map, q8_map);
     return cudaGetLastError();
 }
 

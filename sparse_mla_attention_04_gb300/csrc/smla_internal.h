@@ -21,6 +21,8 @@ struct FwdArgs {
     float *part_o;          // [T, S, H, D_v]   (S > kClusterMaxSplits)
     float *part_lse;        // [T, S, H]        (S > kClusterMaxSplits)
     int *tickets;           // [T, H / 16]      (S > kClusterMaxSplits)
+    uint8_t *q8;            // [T, H, D_qk] E4M3 q codes (128-head kernel)
+    float *q_scale;         // [T, H] their per-(row, head) scales (128-head kernel)
     int64_t num_slots;
     int T, H, D_qk, D_v, topk;
     int S;                  // splits of the top-k list
@@ -46,11 +48,14 @@ constexpr int kMaxSplits = 128;
 // the region, whatever the shapes of earlier calls.
 constexpr int kTicketSlots = 4096;
 
-// Workspace layout for S > kClusterMaxSplits (byte offsets, 256-byte aligned).
+// Workspace layout (byte offsets, 256-byte aligned): merge counters and
+// split partials for S > kClusterMaxSplits, or, for the 128-head kernel, the
+// quantized q and its scales (after the counter region, which every layout
+// leaves zero).
 struct WorkspaceLayout {
-    size_t tickets, part_lse, part_o, total;
+    size_t tickets, part_lse, part_o, q8, q_scale, total;
 };
-WorkspaceLayout workspace_layout(int T, int H, int D_v, int S);
+WorkspaceLayout workspace_layout(int T, int H, int D_qk, int D_v, int S, bool wide);
 
 cudaError_t launch_fwd_mma(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_fwd_wide(const FwdArgs &a, cudaStream_t stream);

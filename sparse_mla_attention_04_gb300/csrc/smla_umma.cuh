@@ -150,6 +150,17 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int 
                  : "memory");
 }
 
+// TMA tile load of the box at (x, y) of a 2-D tensor map into shared memory at
+// dst (in the map's swizzle), bytes counted on mbar; out-of-range parts of the
+// box are filled with zeros.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int x, int y, uint32_t mbar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst),
+                 "l"(tmap), "r"(x), "r"(y), "r"(mbar)
+                 : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t mbar)
 {
     asm volatile("{\n.reg .b64 st;\nmbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(mbar) : "memory");

@@ -120,6 +120,32 @@ def test_wide_head_explicit_splits():
     parity.case(w, num_splits=3)
 
 
+def test_wide_head_then_many_splits_share_a_workspace():
+    """The 128-head kernel's quantized q lives in the workspace after the
+    merge counters: a 16-split call that follows on the same buffer still
+    finds its counters at zero."""
+    ww = inputs.Workload("wide_ws", 2, 128, 576, 512, 3000, 300, True, 1 / math.sqrt(576), "uniform", seed=21)
+    wd = inputs.decode(n_seqs=4, ctx=8192, topk=2048, name="decode_after_wide")
+    need = max(binding.sparse_mla_fwd_workspace_size(ww.T, ww.H, ww.D_qk, ww.D_v, ww.topk, 1, 0),
+               binding.sparse_mla_fwd_workspace_size(wd.T, wd.H, wd.D_qk, wd.D_v, wd.topk, 0, 16))
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    for w, kw in ((ww, {}), (wd, {"num_splits": 16}), (ww, {}), (wd, {"num_splits": 16})):
+        q = inputs.make_q(w)
+        src = inputs.make_kv_source(w)
+        idx = inputs.make_indices(w)
+        cache, kvs = parity.gpu_cache(src.to(DEV), w.kv_fp8)
+        out, lse = binding.sparse_mla_fwd(q.to(DEV), cache, torch.from_numpy(idx).to(DEV), w.scale, kv_scale=kvs,
+                                          dot_precision="fp8" if w.kv_fp8 else "auto", workspace=ws, **kw)
+        torch.cuda.synchronize()
+        ocache, oscale = parity.oracle_cache(src, w.kv_fp8)
+        qm = 1 if w.kv_fp8 else 0
+        ro, rl, _ = oracle.sparse_mla(q, ocache, idx, w.scale, kv_fp8=w.kv_fp8, kv_scale=oscale, q_mode=qm)
+        tol = parity.TOL_FP8_MIRROR if w.kv_fp8 else TOL_BF16
+        compare(out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), ro, rl, tol,
+                w.name)
+    assert binding.smla_device_error() == 0
+
+
 def test_wide_head_bf16_cache():
     w = inputs.wide(T=3, ctx=2048, topk=700, name="wide_bf16")
     w.kv_fp8 = False
