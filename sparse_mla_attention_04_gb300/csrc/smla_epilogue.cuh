@@ -85,7 +85,9 @@ __device__ __forceinline__ void finish_tile(const FwdArgs &a, float *ost, const 
             for (int u = 0; u < kU; ++u)
                 acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int j = 0; j < a.S; ++j) {
-                const float4 *src = cluster.map_shared_rank(reinterpret_cast<const float4 *>(ost), j);
+                // this CTA's own partial from its shared memory, the others' through DSMEM
+                const float4 *src = j == rank ? reinterpret_cast<const float4 *>(ost)
+                                              : cluster.map_shared_rank(reinterpret_cast<const float4 *>(ost), j);
                 float4 x[kU];
 #pragma unroll
                 for (int u = 0; u < kU; ++u) {

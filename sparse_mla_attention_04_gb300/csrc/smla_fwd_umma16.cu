@@ -227,6 +227,12 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    // the prologue above touches no global memory: from here on the previous
+    // kernel in the stream (which may produce this call's inputs, or still
+    // read this call's outputs) must be complete; the next one may start its
+    // own prologue on free SMs meanwhile
+    umma::grid_launch_dependents();
+    umma::grid_wait();
 
     auto wait_bar = [&](uint32_t mbar, uint32_t parity) {
         if (*(volatile int *)abort_s)
@@ -712,23 +718,27 @@ cudaError_t launch(const FwdArgs &a, cudaStream_t stream)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
 
+    // programmatic dependent launch (the kernel waits for its predecessor in
+    // grid_wait after a prologue that reads no global memory), and the row's
+    // splits as one cluster when they merge through distributed shared memory
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (a.S > 1 && a.S <= kClusterMaxSplits) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)blocks);
-        cfg.blockDim = dim3(C::THREADS);
-        cfg.dynamicSmemBytes = C::SMEM_ALLOC;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)a.S;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, kern, a, kv_map);
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)a.S;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     }
-    kern<<<dim3((unsigned)blocks), dim3(C::THREADS), C::SMEM_ALLOC, stream>>>(a, kv_map);
-    return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, kern, a, kv_map);
 }
 
 } // namespace

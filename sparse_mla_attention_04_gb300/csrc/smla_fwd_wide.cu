@@ -203,6 +203,12 @@ __global__ void __launch_bounds__(512, 1)
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    // the prologue above touches no global memory: from here on the previous
+    // kernel in the stream (which may produce this call's inputs, or still
+    // read this call's outputs) must be complete; the next one may start its
+    // own prologue on free SMs meanwhile
+    umma::grid_launch_dependents();
+    umma::grid_wait();
 
     // ---- q8 of this CTA's 128 heads: five TMA tile loads ----
     if (tid == 0) {
@@ -534,8 +540,22 @@ cudaError_t launch_fwd_wide(const FwdArgs &a, cudaStream_t stream)
     const int64_t qrows = (int64_t)a.T * a.H;
     quantize_q_e4m3_kernel<<<dim3((unsigned)((qrows + 3) / 4)), dim3(128), 0, stream>>>(
         static_cast<const __nv_bfloat16 *>(a.q), qrows, a.q8, a.q_scale);
-    kern<<<dim3((unsigned)blocks), dim3(kThreads), kSmemAlloc, stream>>>(a, kv_map, q8_map);
-    return cudaGetLastError();
+    // programmatic dependent launch: the kernel's prologue overlaps the q pass's
+    // tail; it waits for it in grid_wait before reading q8
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t qe = cudaGetLastError();
+    if (qe != cudaSuccess)
+        return qe;
+    return cudaLaunchKernelEx(&cfg, kern, a, kv_map, q8_map);
 }
 
 cudaError_t read_wide_error(int *out, bool reset)

@@ -197,6 +197,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity)
     }
 }
 
+// Programmatic dependent launch: allow the next kernel in the stream to be
+// scheduled now (it still waits in its own grid_wait), and wait until the
+// previous kernel has completed and its memory operations are visible.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
 // Named barrier over `count` threads (ids 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_bar(int id, int count)
 {
