@@ -124,7 +124,8 @@ WorkspaceLayout workspace_layout(int T, int H, int D_qk, int D_v, int S, bool wi
     if (wide) {
         // after the merge-counter region, which must stay zero between calls
         w.q8 = up((size_t)kTicketSlots * sizeof(int));
-        w.q_scale = up(w.q8 + (size_t)T * H * D_qk);
+        w.q8_rope = up(w.q8 + (size_t)T * H * 512);
+        w.q_scale = up(w.q8_rope + (size_t)T * H * (D_qk - 512));
         w.total = up(w.q_scale + (size_t)T * H * sizeof(float));
         return w;
     }
@@ -272,6 +273,7 @@ SMLA_API smla_status sparse_mla_fwd(const void *q, const void *kv_cache, int kv_
     a.part_lse = wl.total ? reinterpret_cast<float *>(ws + wl.part_lse) : nullptr;
     a.tickets = wl.total ? reinterpret_cast<int *>(ws + wl.tickets) : nullptr;
     a.q8 = path == Path::Wide ? ws + wl.q8 : nullptr;
+    a.q8_rope = path == Path::Wide ? ws + wl.q8_rope : nullptr;
     a.q_scale = path == Path::Wide ? reinterpret_cast<float *>(ws + wl.q_scale) : nullptr;
     a.num_slots = num_slots;
     a.T = T;

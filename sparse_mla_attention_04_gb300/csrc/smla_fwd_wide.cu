@@ -2,38 +2,44 @@
 // latent + 64 rope columns, D_v = 512) on the 5th-generation tensor cores
 // (tcgen05 + tensor memory) with TMA row gathers, sm_103a.
 //
-// With 128 heads the contraction runs head-major, heads on the MMA's M axis:
-//   S [128 heads x 64 keys] = q8 [128 x 576] . K_tile^T         (QK, E4M3, 18 MMAs)
-//   O [128 heads x 256 dims] += P [128 x 64] . V_tile[:, half]  (PV, fp16, 4 MMAs)
+// With 128 heads QK runs head-major and PV dims-major:
+//   S   [128 heads x 64 keys]  = q8 [128 x 576] . K_tile^T          (E4M3, 18 MMAs, M=128 N=64)
+//   O^T [256 dims x 128 heads] += V^T[half] [256 x 64] . P^T        (fp16, 8 MMAs, 2 x M=128 N=128)
 // The fp32 output for 128 heads x 512 dims alone would fill an SM's tensor
 // memory (256 KB), so each query row runs as two CTAs, each owning one half
-// of the value dims; both compute the full QK and softmax (identical
-// inputs, identical P).
+// of the value dims; both compute the full QK and softmax (identical inputs,
+// identical P).
 //
-// Warp roles, handing tiles over through mbarriers (every wait bounded):
+// Tensor memory (512 columns): O^T in 0..255 (two M-blocks of 128 dims x 128
+// heads), S in 256 + 64 b (double-buffered), V^T in 384 + 64 b (binary16,
+// two keys per column, double-buffered; the A operand of PV). Shared memory:
+// q8 (4 swizzled blocks of [128 heads x 128 B] for the latent part plus an
+// 8 KB core-matrix block for the rope part), a 3-stage ring of 40 KB tiles,
+// and P^T (fp16, [128 heads x 64 keys] K-major, double-buffered; the B
+// operand of PV).
+//
 // q is quantized per (row, head) by a separate pass over all rows (one warp
 // per head: s_q = amax|q[t,h,:]| / 448, 1 if zero; q8 = RNE_satfinite(q /
-// s_q)) into the workspace, so each CTA pair does not repeat it; the CTA
-// copies its 128 heads of q8 with five TMA tile loads (boxes of 128 B x 128
-// rows, 128-byte swizzle; the fifth box reaches past column 576 and comes
-// back zero filled, the unused half of the last block).
-//   producers (warps 5-8): per 64-key tile 80 TMA tile::gather4 copies (16 key quads x 5 column
-//     blocks of 128 B; the last block reaches past column 576 and is zero
-//     filled) into a 2-stage ring. Masked and out-of-range indices are
+// s_q)) into the workspace, the rope part already in core-matrix order; the
+// CTA copies its 128 heads with four TMA tile loads and one bulk copy.
+//
+// Warp roles, handing tiles over through mbarriers (every wait bounded):
+//   producers (warps 5-8): per 64-key tile 80 TMA tile::gather4 copies (16
+//     key quads x 5 column blocks of 128 B; the last block reaches past
+//     column 576 and is zero filled). Masked and out-of-range indices are
 //     passed as row -1 (zero fill, no memory read).
-//   QK issuer (warp 4): S(i) into tensor memory (double-buffered) once tile i
-//     has landed and the softmax has read S(i-2).
+//   QK issuer (warp 4): S(i) once tile i has landed and the softmax has read
+//     S(i-2).
 //   softmax (warps 0-3, thread = head, whole S row in the thread): masks,
 //     scales by scale * s_q[h] * kv_scale, exponentiates base 2 against a
-//     running reference max that moves (rescaling the head's O row in
-//     tensor memory) only when a logit exceeds it by more than 2^8, and then
-//     to 2^8 above the tile max, so later tiles rarely move it again; writes
-//     P as fp16 pairs into tensor memory (double-buffered), the A operand
-//     of PV.
-//   converters (warps 10-13): the tile's half of the value columns, E4M3 ->
-//     binary16 (exact), into a shared-memory tile MN-major with the 128-byte
-//     swizzle (double-buffered), the B operand of PV.
-//   PV issuer (warp 9): O += P(i) . V16(i) once both are written.
+//     running reference max that moves (all heads agree per tile, then the
+//     O^T columns are rescaled in tensor memory) only when a logit exceeds
+//     it by more than 2^8, and then to 2^8 above the tile max; writes its
+//     row of P^T (fp16).
+//   converters (warps 10-13, one per quarter of the TMEM lanes): the tile's
+//     half of the value columns, E4M3 -> binary16 (exact), as V^T into
+//     tensor memory (4x4 byte transposes within lane quads).
+//   PV issuer (warp 9): O^T += V^T(i) . P^T(i) once both are written.
 //
 // Method sources (page titles and sections):
 //   "Enable AITER sparse MLA on gfx942, including FP8 KV" — Overview, Details
@@ -55,14 +61,14 @@ __device__ int g_wide_error = 0; // set when a bounded wait gives up
 
 namespace {
 
-constexpr int kHeads = 128;    // heads per CTA (M of both MMAs)
+constexpr int kHeads = 128;    // heads per CTA (M of QK, N of PV)
 constexpr int kDqk = 576;
 constexpr int kDv = 512;
 constexpr int kDvHalf = 256;   // value dims per CTA
 constexpr int kKeys = 64;      // keys per tile (N of QK)
 constexpr int kQkSteps = kDqk / 32;   // 18 E4M3 k-steps of 32
-constexpr int kCB = 5;                // 128-byte column blocks per row (the last half used)
-constexpr int kStages = 2;
+constexpr int kCB = 5;                // 128-byte column blocks per cache row (the last half used)
+constexpr int kStages = 3;
 constexpr int kCopies = 16 * kCB;     // gather4 copies per tile
 constexpr int kIdxAhead = 4;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -80,35 +86,44 @@ constexpr int kProducerThreads = 128;
 constexpr int kConverterThreads = 128;
 
 // shared memory (bytes from a 1 KB-aligned base)
-constexpr int kQBlk = kHeads * 128;           // one column block of q8 (16 KB)
-constexpr int kOffQ8 = 0;                     // 5 blocks
+constexpr int kQBlk = kHeads * 128;           // one swizzled column block of q8 (16 KB)
+constexpr int kOffQ8 = 0;                     // 4 blocks: columns 0..511
+constexpr int kQRope = kHeads * 64;           // rope part in core matrices (8 KB)
+constexpr int kOffQRope = kOffQ8 + 4 * kQBlk;
 constexpr int kKBlk = kKeys * 128;            // one column block of a tile (8 KB)
 constexpr int kTile = kCB * kKBlk;            // 40 KB
-constexpr int kOffRing = kOffQ8 + kCB * kQBlk;
-constexpr int kV16 = 4 * kKBlk;               // [64 keys x 256 dims] binary16, 4 blocks of 64 dims
-constexpr int kOffV16 = kOffRing + kStages * kTile;
-constexpr int kOffMisc = kOffV16 + 2 * kV16; // tmem address, abort, go[2]
+constexpr int kOffRing = kOffQRope + kQRope;
+constexpr int kPT = kHeads * 128;             // P^T: 128 heads x 64 keys fp16 (16 KB)
+constexpr int kOffPT = kOffRing + kStages * kTile;
+constexpr int kOffAlpha = kOffPT + 2 * kPT;   // [128] per-head factors (rescale, then 1/l)
+constexpr int kOffEx = kOffAlpha + kHeads * 4;// [2][4] exceed flags
+constexpr int kOffMisc = kOffEx + 32;         // tmem address, abort, go[2]
 constexpr int kOffMbar = kOffMisc + 32;
-// full[2], empty[2], s_full[2], p_full[2], p_empty[2], v_full[2], v_empty[2], q_full, drain
+// full[3], empty[3], s_full[2], p_full[2], p_empty[2], v_full[2], q_full, drain
 constexpr int kNBar = 16;
 constexpr int kSmem = kOffMbar + kNBar * 8;
 constexpr int kSmemAlloc = kSmem + 1024;
+static_assert(kOffRing % 1024 == 0 && kOffPT % 1024 == 0, "swizzle atoms need 1 KB alignment");
 static_assert(kSmemAlloc <= 227 * 1024, "shared memory budget");
 
-// tensor memory columns: O 0..255, S(b) 256 + 64 b, P(b) 384 + 32 b
+// tensor memory columns
 constexpr int kTmemCols = 512;
 constexpr int kSCol = 256;
-constexpr int kPCol = 384;
+constexpr int kVCol = 384;
 
 // QK: A = q8 (K-major), B = K tile (K-major), M = 128 heads, N = 64 keys, E4M3
 constexpr uint32_t kIdescQK = umma::idesc(128, 64, 0, 0, 0, 0);
-// PV: A = P in tensor memory (fp16), B = V16 (MN-major), M = 128 heads, N = 256 dims
-constexpr uint32_t kIdescPV = umma::idesc(128, 256, 0, 0, 0, 1);
+// PV: A = V^T in tensor memory (fp16), B = P^T (K-major), M = 128 dims, N = 128 heads
+constexpr uint32_t kIdescPV = umma::idesc(128, 128, 0, 0, 0, 0);
 
-// q [rows x 576] bf16 -> q8 [rows x 576] E4M3 and scale[rows]; one warp per row
-// (lanes 0-23 hold 24 elements each).
-__global__ void __launch_bounds__(128) quantize_q_e4m3_kernel(const __nv_bfloat16 *__restrict__ q, int64_t rows,
-                                                             uint8_t *__restrict__ q8, float *__restrict__ scale)
+// q [rows x 576] bf16 (rows = T * H) -> E4M3 codes: columns 0..511 to q8
+// [rows x 512], columns 512..575 to q8_rope in the core-matrix order the QK
+// reads (per (row t, group of 128 heads) an 8 KB block: 8-head groups of 4
+// chunks of 8 heads x 16 B), and the per-row scale. One warp per row; lanes
+// 0-23 hold 24 elements each.
+__global__ void __launch_bounds__(128) quantize_q_e4m3_kernel(const __nv_bfloat16 *__restrict__ q, int64_t rows, int H,
+                                                             uint8_t *__restrict__ q8, uint8_t *__restrict__ q8_rope,
+                                                             float *__restrict__ scale)
 {
     const int64_t r = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -136,6 +151,9 @@ __global__ void __launch_bounds__(128) quantize_q_e4m3_kernel(const __nv_bfloat1
     if (lane == 0)
         scale[r] = s;
     if (lane < 24) {
+        const int64_t t = r / H;
+        const int h = (int)(r % H), hg = h / kHeads, hl = h % kHeads;
+        uint8_t *rope = q8_rope + (t * (H / kHeads) + hg) * kQRope;
 #pragma unroll
         for (int u = 0; u < 3; ++u) {
             const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&v[u]);
@@ -144,7 +162,13 @@ __global__ void __launch_bounds__(128) quantize_q_e4m3_kernel(const __nv_bfloat1
             uint2 o;
             o.x = quant4_e4m3(f0.x, f0.y, f1.x, f1.y, s);
             o.y = quant4_e4m3(f2.x, f2.y, f3.x, f3.y, s);
-            *reinterpret_cast<uint2 *>(q8 + r * kDqk + (3 * lane + u) * 8) = o;
+            const int e0 = 24 * lane + 8 * u; // first column of these 8 codes
+            if (e0 < 512) {
+                *reinterpret_cast<uint2 *>(q8 + r * 512 + e0) = o;
+            } else {
+                const int d = e0 - 512;
+                *reinterpret_cast<uint2 *>(rope + ((hl >> 3) * 4 + (d >> 4)) * 128 + (hl & 7) * 16 + (d & 15)) = o;
+            }
         }
     }
 }
@@ -157,18 +181,20 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t sbase = (raw_base + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (sbase - raw_base);
-    const uint32_t q8_s = sbase + kOffQ8, ring = sbase + kOffRing, v16_s = sbase + kOffV16;
+    const uint32_t q8_s = sbase + kOffQ8, qrope_s = sbase + kOffQRope, ring = sbase + kOffRing,
+                   pt_s = sbase + kOffPT;
+    float *alpha_s = reinterpret_cast<float *>(smem + kOffAlpha);
+    int *ex_s = reinterpret_cast<int *>(smem + kOffEx);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     int *abort_s = reinterpret_cast<int *>(smem + kOffMisc + 4);
     volatile int *go_s = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
     const uint32_t bar0 = sbase + kOffMbar;
     auto full = [&](int st) { return bar0 + 8 * st; };
-    auto empty = [&](int st) { return bar0 + 8 * (2 + st); };
-    auto s_full = [&](int b) { return bar0 + 8 * (4 + b); };
-    auto p_full = [&](int b) { return bar0 + 8 * (6 + b); };
-    auto p_empty = [&](int b) { return bar0 + 8 * (8 + b); };
-    auto v_full = [&](int b) { return bar0 + 8 * (10 + b); };
-    auto v_empty = [&](int b) { return bar0 + 8 * (12 + b); };
+    auto empty = [&](int st) { return bar0 + 8 * (3 + st); };
+    auto s_full = [&](int b) { return bar0 + 8 * (6 + b); };
+    auto p_full = [&](int b) { return bar0 + 8 * (8 + b); };
+    auto p_empty = [&](int b) { return bar0 + 8 * (10 + b); };
+    auto v_full = [&](int b) { return bar0 + 8 * (12 + b); };
     const uint32_t q_full = bar0 + 8 * 14;
     const uint32_t drain = bar0 + 8 * 15;
 
@@ -188,9 +214,8 @@ __global__ void __launch_bounds__(512, 1)
         for (int b = 0; b < 2; ++b) {
             umma::mbar_init(s_full(b), 1);
             umma::mbar_init(p_full(b), 128);
-            umma::mbar_init(p_empty(b), 1);
+            umma::mbar_init(p_empty(b), 1); // PV(i) done: P^T(b) and V^T(b) free, O^T holds PV(0..i)
             umma::mbar_init(v_full(b), kConverterThreads);
-            umma::mbar_init(v_empty(b), 1);
         }
         umma::mbar_init(q_full, 1);
         umma::mbar_init(drain, 2);
@@ -210,12 +235,13 @@ __global__ void __launch_bounds__(512, 1)
     umma::grid_launch_dependents();
     umma::grid_wait();
 
-    // ---- q8 of this CTA's 128 heads: five TMA tile loads ----
+    // ---- q8 of this CTA's 128 heads: four TMA tile loads and one bulk copy ----
     if (tid == 0) {
-        umma::mbar_arrive_expect_tx(q_full, kCB * kQBlk);
+        umma::mbar_arrive_expect_tx(q_full, 4 * kQBlk + kQRope);
         const int qrow = t * a.H + hg * kHeads;
-        for (int cb = 0; cb < kCB; ++cb)
+        for (int cb = 0; cb < 4; ++cb)
             umma::tma_load_2d(q8_s + cb * kQBlk, &q8_map, 128 * cb, qrow, q_full);
+        umma::bulk_copy_g2s(qrope_s, a.q8_rope + ((int64_t)t * G + hg) * kQRope, kQRope, q_full);
     }
 
     auto wait_bar = [&](uint32_t mbar, uint32_t parity) {
@@ -303,11 +329,15 @@ __global__ void __launch_bounds__(512, 1)
                     break;
                 umma::fence_after_sync();
                 const uint64_t ad = umma::desc_sw128(q8_s, 16, 1024);
+                const uint64_t rd = umma::desc(qrope_s, 128, 512); // core matrices: K 128 B, M 512 B apart
                 const uint64_t bd = umma::desc_sw128(ring + st * kTile, 16, 1024);
 #pragma unroll
-                for (int ks = 0; ks < kQkSteps; ++ks)
-                    umma::mma_f8(tmem + kSCol + 64 * b, ad + (uint64_t)(((ks >> 2) * kQBlk + (ks & 3) * 32) >> 4),
+                for (int ks = 0; ks < kQkSteps; ++ks) {
+                    const uint64_t ak = ks < 16 ? ad + (uint64_t)(((ks >> 2) * kQBlk + (ks & 3) * 32) >> 4)
+                                                : rd + (uint64_t)(((ks - 16) * 256) >> 4);
+                    umma::mma_f8(tmem + kSCol + 64 * b, ak,
                                  bd + (uint64_t)(((ks >> 2) * kKBlk + (ks & 3) * 32) >> 4), kIdescQK, ks > 0);
+                }
                 umma::commit(s_full(b));
                 umma::commit(empty(st));
             }
@@ -325,14 +355,15 @@ __global__ void __launch_bounds__(512, 1)
                 if (*(volatile int *)abort_s)
                     break;
                 umma::fence_after_sync();
-                // V16(b): MN-major, 64-dim atoms 8 KB apart (LBO), 8-key atoms 1 KB apart (SBO)
-                const uint64_t bd = umma::desc_sw128(v16_s + b * kV16, kKBlk, 1024);
+                // P^T(b): K-major, 8-head atoms 1 KB apart; k-step kk starts 32 B into the rows
+                const uint64_t bd = umma::desc_sw128(pt_s + b * kPT, 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    umma::mma_f16_ts(tmem, tmem + kPCol + 32 * b + 8 * kk, bd + (uint64_t)((kk * 2048) >> 4),
-                                     kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
-                umma::commit(p_empty(b)); // P(b) read; with it O holds PV(0..i)
-                umma::commit(v_empty(b));
+                for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma::mma_f16_ts(tmem + 128 * mb, tmem + kVCol + 64 * b + 32 * mb + 8 * kk,
+                                         bd + (uint64_t)((kk * 32) >> 4), kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+                umma::commit(p_empty(b));
             }
             umma::commit(drain);
             wait_issued(drain, 0);
@@ -340,38 +371,35 @@ __global__ void __launch_bounds__(512, 1)
         __syncwarp();
     } else if (warp >= kConverterWarp0) {
         // ======================= converters =======================
-        const int ct = tid - kConverterWarp0 * 32;
+        // lane quad (g, ii): member ii loads 4 dims (4g..4g+3 of this warp's 32)
+        // of key 4kq+ii; after the transpose it holds dim 4g+ii of keys 4kq..4kq+3
+        const int q4 = warp & 3, g = lane >> 2, ii = lane & 3;
+        const uint32_t selA = ii < 2 ? 0x5410u : 0x3276u; // keep / take 16-bit halves (xor 2)
+        const uint32_t selB = ii & 1 ? 0x3715u : 0x6240u; // interleave bytes (xor 1)
+        const uint32_t tlane = (uint32_t)(32 * q4) << 16;
         for (int i = 0; i < ntiles; ++i) {
-            const int st = i % kStages, b = i & 1;
+            const int st = i % kStages, vb = i & 1;
             wait_bar(full(st), (uint32_t)((i / kStages) & 1));
-            if (i >= 2) // PV(i-2) has read V16(b)
-                wait_bar(v_empty(b), (uint32_t)(((i - 2) >> 1) & 1));
-            const uint32_t src0 = ring + st * kTile, dst0 = v16_s + b * kV16;
-            // 1024 16-byte chunks (64 keys x 2 blocks x 8) of this CTA's 256 dims
+            if (i >= 2) // PV(i-2) has read V^T buffer vb
+                wait_bar(p_empty(vb), (uint32_t)(((i - 2) >> 1) & 1));
+            const uint32_t src0 = ring + st * kTile;
+#pragma unroll 1
+            for (int mb = 0; mb < 2; ++mb) {
+                const uint32_t blk = src0 + (2 * half + mb) * kKBlk; // E4M3 block: dims 256 half + 128 mb + ...
+                uint32_t col[32];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int k = ct + kConverterThreads * j;
-                const int r = k >> 4, lb = (k >> 3) & 1, c = k & 7; // key, local block, chunk
-                uint32_t w0, w1, w2, w3;
-                asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
-                             : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                             : "r"(src0 + (2 * half + lb) * kKBlk + r * 128 + ((c ^ (r & 7)) << 4)));
-                const int cb16 = 2 * lb + (c >> 2), c16 = (c & 3) * 2;
-                const uint32_t dst = dst0 + cb16 * kKBlk + r * 128;
-                uint32_t h[8];
-                e4m3x4_to_f16x4(w0, h[0], h[1]);
-                e4m3x4_to_f16x4(w1, h[2], h[3]);
-                e4m3x4_to_f16x4(w2, h[4], h[5]);
-                e4m3x4_to_f16x4(w3, h[6], h[7]);
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(dst + ((c16 ^ (r & 7)) << 4)), "r"(h[0]),
-                             "r"(h[1]), "r"(h[2]), "r"(h[3])
-                             : "memory");
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(dst + (((c16 + 1) ^ (r & 7)) << 4)),
-                             "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
-                             : "memory");
+                for (int kq = 0; kq < 16; ++kq) {
+                    const int key = 4 * kq + ii;
+                    const uint32_t w = lds32(blk + key * 128 + (((2 * q4 + (g >> 2)) ^ (key & 7)) << 4) + (g & 3) * 4);
+                    const uint32_t x = __byte_perm(w, __shfl_xor_sync(0xffffffffu, w, 2), selA);
+                    const uint32_t y = __byte_perm(x, __shfl_xor_sync(0xffffffffu, x, 1), selB);
+                    e4m3x4_to_f16x4(y, col[2 * kq], col[2 * kq + 1]);
+                }
+                umma::st32(tmem + tlane + kVCol + 64 * vb + 32 * mb, col);
             }
-            umma::fence_async_smem();
-            umma::mbar_arrive(v_full(b));
+            umma::wait_st();
+            umma::fence_before_sync();
+            umma::mbar_arrive(v_full(vb));
             umma::mbar_arrive(empty(st));
         }
     } else {
@@ -412,29 +440,37 @@ __global__ void __launch_bounds__(512, 1)
                 sv[j] = v ? sv[j] * fac : -INFINITY;
                 mt = fmaxf(mt, sv[j]);
             }
-            // move the reference max (warp-wide decision: TMEM access is warp-collective)
+            // move the reference max: every head's O^T column spans all four warps'
+            // lanes, so the four softmax warps agree on it per tile
             const bool exceed = mt > m_ref + kRescaleThreshold;
-            if (__any_sync(0xffffffffu, exceed)) {
+            const bool wx = __any_sync(0xffffffffu, exceed);
+            if (lane == 0)
+                ex_s[b * 4 + warp] = wx;
+            umma::named_bar(1, 128);
+            if (ex_s[b * 4] | ex_s[b * 4 + 1] | ex_s[b * 4 + 2] | ex_s[b * 4 + 3]) {
                 const float mn = exceed ? mt + kHeadroom : m_ref;
-                const float al = (m_ref == -INFINITY || !exceed) ? (exceed ? 0.f : 1.f) : exp2f(m_ref - mn);
+                const float al = !exceed ? 1.f : (m_ref == -INFINITY ? 0.f : exp2f(m_ref - mn));
                 m_ref = mn;
                 l *= al;
+                alpha_s[h] = al;
+                umma::named_bar(1, 128);
                 if (i >= 1) {
-                    // O holds PV(0..i-1): let PV(i-1) finish, then rescale this head's row
+                    // O^T holds PV(0..i-1): let PV(i-1) finish, then scale each head column
                     wait_bar(p_empty((i - 1) & 1), (uint32_t)(((i - 1) >> 1) & 1));
                     umma::fence_after_sync();
 #pragma unroll 1
-                    for (int c = 0; c < kDvHalf; c += 16) {
+                    for (int c = 0; c < 2 * kHeads; c += 16) {
                         uint32_t o[16];
                         umma::ld16(tl + c, o);
                         umma::wait_ld();
 #pragma unroll
                         for (int e = 0; e < 16; ++e)
-                            o[e] = __float_as_uint(__uint_as_float(o[e]) * al);
+                            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha_s[(c + e) & (kHeads - 1)]);
                         umma::st16(tl + c, o);
                     }
                     umma::wait_st();
                 }
+                umma::named_bar(1, 128); // alpha_s is read by all before the next tile writes it
             }
             const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
             uint32_t pw[32];
@@ -444,10 +480,16 @@ __global__ void __launch_bounds__(512, 1)
                 l += p0 + p1;
                 pw[c] = pack_f16x2(p0, p1);
             }
-            if (i >= 2) // PV(i-2) has read P(b)
+            if (i >= 2) // PV(i-2) has read P^T(b)
                 wait_bar(p_empty(b), (uint32_t)(((i - 2) >> 1) & 1));
-            umma::st32(tl + kPCol + 32 * b, pw);
-            umma::wait_st();
+            // this head's row of P^T: 64 keys x fp16 = one 128-byte swizzled row
+            const uint32_t prow = pt_s + b * kPT + h * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow + ((c ^ (h & 7)) << 4)),
+                             "r"(pw[4 * c]), "r"(pw[4 * c + 1]), "r"(pw[4 * c + 2]), "r"(pw[4 * c + 3])
+                             : "memory");
+            umma::fence_async_smem();
             umma::fence_before_sync();
             umma::mbar_arrive(p_full(b));
         };
@@ -457,33 +499,31 @@ __global__ void __launch_bounds__(512, 1)
             step(i0 + 2, xa2, xb2);
             step(i0 + 3, xa3, xb3);
         }
-        // ---- epilogue: this head's 256 output dims and its lse ----
+        // ---- epilogue: O^T / l -> out, lse ----
         if (ntiles > 0) // the last PV (and every earlier one) is done
             wait_bar(p_empty((ntiles - 1) & 1), (uint32_t)(((ntiles - 1) >> 1) & 1));
         umma::fence_after_sync();
-        const float ov = l > 0.f ? kvs / l : 0.f;
-        __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) +
-                              ((int64_t)t * a.H + hg * kHeads + h) * kDv + half * kDvHalf;
-#pragma unroll 1
-        for (int c = 0; c < kDvHalf; c += 16) {
-            uint32_t o[16];
-            umma::ld16(tl + c, o);
-            umma::wait_ld();
-            uint4 u0, u1;
-            auto val = [&](int e) { return l > 0.f ? __uint_as_float(o[e]) * ov : 0.f; };
-            u0.x = pack_bf16x2(val(0), val(1));
-            u0.y = pack_bf16x2(val(2), val(3));
-            u0.z = pack_bf16x2(val(4), val(5));
-            u0.w = pack_bf16x2(val(6), val(7));
-            u1.x = pack_bf16x2(val(8), val(9));
-            u1.y = pack_bf16x2(val(10), val(11));
-            u1.z = pack_bf16x2(val(12), val(13));
-            u1.w = pack_bf16x2(val(14), val(15));
-            reinterpret_cast<uint4 *>(orow + c)[0] = u0;
-            reinterpret_cast<uint4 *>(orow + c)[1] = u1;
-        }
+        alpha_s[h] = l > 0.f ? kvs / l : 0.f; // output factor per head
         if (half == 0 && a.lse != nullptr)
             a.lse[(int64_t)t * a.H + hg * kHeads + h] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+        umma::named_bar(1, 128);
+        // thread = value dim 128 mb + 32 warp + lane; columns = heads
+        __nv_bfloat16 *obase = static_cast<__nv_bfloat16 *>(a.out) + ((int64_t)t * a.H + hg * kHeads) * kDv +
+                               half * kDvHalf + warp * 32 + lane;
+#pragma unroll 1
+        for (int mb = 0; mb < 2; ++mb) {
+#pragma unroll 1
+            for (int c = 0; c < kHeads; c += 16) {
+                uint32_t o[16];
+                umma::ld16(tl + 128 * mb + c, o);
+                umma::wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float f = alpha_s[c + e];
+                    obase[(int64_t)(c + e) * kDv + 128 * mb] = __float2bfloat16_rn(f > 0.f ? __uint_as_float(o[e]) * f : 0.f);
+                }
+            }
+        }
         umma::fence_before_sync();
     }
     __syncthreads();
@@ -527,11 +567,11 @@ cudaError_t launch_fwd_wide(const FwdArgs &a, cudaStream_t stream)
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    // q8 as a 2-D tensor [T*H rows x 576] bytes, copied in boxes of 128 B x 128
-    // rows with the 128-byte swizzle
+    // q8 (latent part) as a 2-D tensor [T*H rows x 512] bytes, copied in boxes
+    // of 128 B x 128 rows with the 128-byte swizzle
     CUtensorMap q8_map;
-    cuuint64_t qdim[2] = {(cuuint64_t)kDqk, (cuuint64_t)a.T * a.H};
-    cuuint64_t qstride[1] = {(cuuint64_t)kDqk};
+    cuuint64_t qdim[2] = {512, (cuuint64_t)a.T * a.H};
+    cuuint64_t qstride[1] = {512};
     cuuint32_t qbox[2] = {128, (cuuint32_t)kHeads};
     if (encode(&q8_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.q8, qdim, qstride, qbox, estride,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -539,7 +579,10 @@ cudaError_t launch_fwd_wide(const FwdArgs &a, cudaStream_t stream)
         return cudaErrorInvalidValue;
     const int64_t qrows = (int64_t)a.T * a.H;
     quantize_q_e4m3_kernel<<<dim3((unsigned)((qrows + 3) / 4)), dim3(128), 0, stream>>>(
-        static_cast<const __nv_bfloat16 *>(a.q), qrows, a.q8, a.q_scale);
+        static_cast<const __nv_bfloat16 *>(a.q), qrows, a.H, a.q8, a.q8_rope, a.q_scale);
+    const cudaError_t qe = cudaGetLastError();
+    if (qe != cudaSuccess)
+        return qe;
     // programmatic dependent launch: the kernel's prologue overlaps the q pass's
     // tail; it waits for it in grid_wait before reading q8
     cudaLaunchConfig_t cfg = {};
@@ -552,9 +595,6 @@ cudaError_t launch_fwd_wide(const FwdArgs &a, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t qe = cudaGetLastError();
-    if (qe != cudaSuccess)
-        return qe;
     return cudaLaunchKernelEx(&cfg, kern, a, kv_map, q8_map);
 }
 

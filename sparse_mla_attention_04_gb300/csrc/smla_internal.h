@@ -21,8 +21,9 @@ struct FwdArgs {
     float *part_o;          // [T, S, H, D_v]   (S > kClusterMaxSplits)
     float *part_lse;        // [T, S, H]        (S > kClusterMaxSplits)
     int *tickets;           // [T, H / 16]      (S > kClusterMaxSplits)
-    uint8_t *q8;            // [T, H, D_qk] E4M3 q codes (128-head kernel)
-    float *q_scale;         // [T, H] their per-(row, head) scales (128-head kernel)
+    uint8_t *q8;            // [T, H, 512] E4M3 codes of q's first 512 columns (128-head kernel)
+    uint8_t *q8_rope;       // [T, H/128] blocks of 8 KB: the last 64 columns, core-matrix order
+    float *q_scale;         // [T, H] per-(row, head) q scales (128-head kernel)
     int64_t num_slots;
     int T, H, D_qk, D_v, topk;
     int S;                  // splits of the top-k list
@@ -53,7 +54,7 @@ constexpr int kTicketSlots = 4096;
 // quantized q and its scales (after the counter region, which every layout
 // leaves zero).
 struct WorkspaceLayout {
-    size_t tickets, part_lse, part_o, q8, q_scale, total;
+    size_t tickets, part_lse, part_o, q8, q8_rope, q_scale, total;
 };
 WorkspaceLayout workspace_layout(int T, int H, int D_qk, int D_v, int S, bool wide);
 
