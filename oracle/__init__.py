@@ -10,8 +10,9 @@ Sources, by page title and section:
   * "Enable AITER sparse MLA on gfx942, including FP8 KV" (vLLM PR 60583),
     Overview and Details ("FP8 KV on gfx942", "Numerics").
   * "Fuse decode QK-RoPE + Q-concat + KV-concat + KV-cache write for sparse
-    MLA" (vLLM PR 47757), Test plan (cache row layout, scaled_fp8_quant
-    convention: stored = x / scale).
+    MLA" (vLLM PR 47757), Summary and Test plan (cache row layout,
+    scaled_fp8_quant convention: stored = x / scale; the fused producer step:
+    RoPE on q_pe / k_pe, q concat, cache write).
 """
 from __future__ import annotations
 
@@ -69,6 +70,13 @@ def _load():
             c.c_int, c.c_int, c.c_int, c.c_int, c.c_int64, c.c_int,
             c.c_float, c.c_int, c.c_void_p, c.c_void_p, c.c_int]
         lib.oracle_sparse_mla.restype = c.c_int64
+        lib.oracle_rope_f64.argtypes = [c.c_void_p, c.c_int, c.c_void_p, c.c_void_p, c.c_int, c.c_void_p]
+        lib.oracle_rope_f64.restype = None
+        lib.oracle_fused_qk_rope_cache.argtypes = [
+            c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p,
+            c.c_int64, c.c_int, c.c_void_p, c.c_void_p, c.c_int, c.c_int64, c.c_float,
+            c.c_void_p, c.c_int, c.c_float, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int]
+        lib.oracle_fused_qk_rope_cache.restype = c.c_int64
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = c.c_int
         _lib = lib
@@ -172,3 +180,53 @@ def sparse_mla(q, kv, indices, scale: float, *, kv_fp8: bool = False,
         T, H, D_qk, D_v, kvb.shape[0], topk, float(np.float32(scale)), int(q_mode),
         _ptr(out), _ptr(lse), int(nthreads))
     return out, lse, int(bad)
+
+
+def rope_f64(x, cos, sin, is_neox: bool) -> np.ndarray:
+    """Rotary embedding of one vector x[R] (fp64) with cos[R/2], sin[R/2]:
+    each pair (a, b) becomes (a cos - b sin, b cos + a sin); neox pairs i with
+    i + R/2, GPT-J pairs 2i with 2i + 1."""
+    xa = np.ascontiguousarray(x, dtype=np.float64)
+    ca = np.ascontiguousarray(cos, dtype=np.float64)
+    sa = np.ascontiguousarray(sin, dtype=np.float64)
+    R = xa.shape[0]
+    assert R % 2 == 0 and ca.shape == (R // 2,) and sa.shape == (R // 2,)
+    out = np.empty(R, dtype=np.float64)
+    _load().oracle_rope_f64(_ptr(xa), R, _ptr(ca), _ptr(sa), 1 if is_neox else 0, _ptr(out))
+    return out
+
+
+def fused_qk_rope_cache(ql_nope, q_pe, kv_c, k_pe, positions, cos_sin, is_neox: bool,
+                        slot_mapping, cache: np.ndarray, *, cache_fp8: bool, kv_scale: float = 1.0,
+                        q_out_fp8: bool = False, q_scale: float = 1.0, mode: int = 1):
+    """The fused producer step over contiguous inputs.
+
+    ql_nope [T, H, Dn], q_pe [T, H, Dr], kv_c [T, Dn], k_pe [T, Dr]: bf16
+    (torch tensors or uint16 bits); positions int64 [T]; cos_sin float32
+    [max_position, Dr] (cos of the Dr/2 angles, then the sines); slot_mapping
+    int64 [T] (negative: no cache row). `cache` (uint16 bf16 bits or uint8
+    E4M3 codes, [num_slots, Dn + Dr]) is updated in place.
+    mode 0: the rotation in fp64, rounded once to bf16; mode 1: binary32
+    products and sums, the precision an fp8 code is decided in.
+    Returns (q_out as uint16 bits or uint8 codes [T, H, Dn + Dr], bad).
+    """
+    qn = _as_bf16_bits(ql_nope)
+    qp = _as_bf16_bits(q_pe)
+    kc = _as_bf16_bits(kv_c)
+    kp = _as_bf16_bits(k_pe)
+    T, H, Dn = qn.shape
+    Dr = qp.shape[2]
+    assert qp.shape == (T, H, Dr) and kc.shape == (T, Dn) and kp.shape == (T, Dr)
+    pos = np.ascontiguousarray(positions.cpu().numpy() if hasattr(positions, "cpu") else positions, dtype=np.int64)
+    cs = np.ascontiguousarray(cos_sin.cpu().numpy() if hasattr(cos_sin, "cpu") else cos_sin, dtype=np.float32)
+    sm = np.ascontiguousarray(slot_mapping.cpu().numpy() if hasattr(slot_mapping, "cpu") else slot_mapping,
+                              dtype=np.int64)
+    assert pos.shape == (T,) and sm.shape == (T,) and cs.ndim == 2 and cs.shape[1] == Dr
+    assert cache.flags.c_contiguous and cache.shape[1] == Dn + Dr
+    assert cache.dtype == (np.uint8 if cache_fp8 else np.uint16)
+    q_out = np.zeros((T, H, Dn + Dr), dtype=np.uint8 if q_out_fp8 else np.uint16)
+    bad = _load().oracle_fused_qk_rope_cache(
+        _ptr(qn), _ptr(qp), _ptr(kc), _ptr(kp), _ptr(pos), _ptr(cs), cs.shape[0], 1 if is_neox else 0,
+        _ptr(sm), _ptr(cache), 1 if cache_fp8 else 0, cache.shape[0], float(np.float32(kv_scale)),
+        _ptr(q_out), 1 if q_out_fp8 else 0, float(np.float32(q_scale)), T, H, Dn, Dr, int(mode))
+    return q_out, int(bad)

@@ -17,6 +17,12 @@
  *    MLA" (vLLM PR 47757), Test plan: the cache row is the latent part
  *    followed by the rope part; fp8 storage follows the scaled_fp8_quant
  *    convention, stored = x / scale, dequantized = code * scale.
+ *  - Same page, Summary and Test plan: the fused producer step. RoPE on the
+ *    pre-RoPE q_pe and k_pe at each token's position (neox or GPT-J pairing),
+ *    q_out = concat(ql_nope, RoPE(q_pe)) in bf16, or its scaled_fp8_quant
+ *    with a per-tensor q_scale, and the cache row concat(kv_c, RoPE(k_pe)).
+ *    The unfused chain stores the rotated values as bf16 before any
+ *    quantization, so the rotation is rounded to bf16 first.
  *  - The forward itself: for each query row t and head h, gather the rows
  *    named by indices[t] (-1 = masked) from the head-shared cache, logits
  *    s_i = scale * q[t,h] . kv[idx_i][:D_qk], softmax over the valid i,
@@ -36,6 +42,16 @@
  * "tile" of the fp8 mode is one (t, h) row of D_qk values with
  * s_q = amax/448 (1.0 when amax == 0); the per-tensor kv scale is
  * amax/448 over the whole source (1.0 when amax == 0); NaN is ignored by amax.
+ *
+ * Readings for the producer step (the page gives no formula): the rotation
+ * of a pair (a, b) by angle theta is (a cos - b sin, b cos + a sin); neox
+ * pairs element i with i + R/2, GPT-J pairs 2i with 2i + 1; the cos/sin cache
+ * row of a position holds cos(theta_0..theta_{R/2-1}) then the sines, as
+ * binary32; the rotation is done in fp64 and rounded once to bf16 (mode 0),
+ * or, where its bf16 value decides an fp8 code, mirrored in binary32 with
+ * each product and the difference or sum rounded (mode 1), the precision the
+ * device computes it in. A position outside [0, max_position) leaves the
+ * token's outputs unwritten; slot -1 skips the cache row.
  *
  * Build: gcc -O2 -fopenmp -shared -fPIC (no fast-math; IEEE semantics needed).
  */
@@ -176,6 +192,146 @@ int64_t oracle_fp8_cache_write(const uint16_t *src, const int64_t *slot_mapping,
         written += 1;
     }
     return written;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The fused producer step (RoPE + q concat + cache write).                 */
+/* ------------------------------------------------------------------------ */
+
+/* bf16 bits of the binary32 value x, rounded to nearest even. */
+static uint16_t float_to_bf16_rne(float x)
+{
+    uint32_t u;
+    memcpy(&u, &x, sizeof u);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0)
+        return (uint16_t)((u >> 16) | 0x0040u); /* NaN stays NaN */
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7FFFu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+/* bf16 bits of the binary64 value x, rounded to nearest even directly (no
+ * intermediate binary32 rounding): keep 8 significant bits. */
+static uint16_t double_to_bf16_rne(double x)
+{
+    if (isnan(x))
+        return 0x7FC0u;
+    if (x == 0.0)
+        return signbit(x) ? 0x8000u : 0x0000u;
+    double a = fabs(x);
+    int e;
+    frexp(a, &e);                       /* a = m * 2^e, m in [0.5, 1) */
+    int q = e - 8;                      /* spacing of 8-bit significands at this binade */
+    if (q < -133)
+        q = -133;                       /* bf16 subnormal spacing 2^-133 */
+    double r = ldexp(nearbyint(ldexp(a, -q)), q); /* default rounding: to nearest even */
+    if (r > 3.3895313892515355e38)     /* above the largest finite bf16: infinity */
+        r = INFINITY;
+    float f = (float)r;                 /* exact: r has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)((u >> 16) | (signbit(x) ? 0x8000u : 0u));
+}
+
+/* Rotary embedding of x[0..R) with cos[0..R/2), sin[0..R/2), in fp64. */
+void oracle_rope_f64(const double *x, int R, const double *cs, const double *sn, int is_neox, double *out)
+{
+    const int half = R / 2;
+    for (int i = 0; i < half; ++i) {
+        const int ia = is_neox ? i : 2 * i;
+        const int ib = is_neox ? i + half : 2 * i + 1;
+        const double a = x[ia], b = x[ib];
+        out[ia] = a * cs[i] - b * sn[i];
+        out[ib] = b * cs[i] + a * sn[i];
+    }
+}
+
+/* One rotated pair as bf16 bits: mode 0 = fp64 rotation rounded once; mode 1 =
+ * binary32 products and difference/sum, each rounded, then rounded to bf16. */
+static void rope_pair_bf16(float a, float b, float c, float sn, int mode, uint16_t *oa, uint16_t *ob)
+{
+    if (mode == 0) {
+        *oa = double_to_bf16_rne((double)a * c - (double)b * sn);
+        *ob = double_to_bf16_rne((double)b * c + (double)a * sn);
+    } else {
+        volatile float p0 = a * c, p1 = b * sn, p2 = b * c, p3 = a * sn;
+        volatile float ra = p0 - p1, rb = p2 + p3;
+        *oa = float_to_bf16_rne(ra);
+        *ob = float_to_bf16_rne(rb);
+    }
+}
+
+/* One output row of Dn + Dr values: nope[0..Dn) copied, rope[0..Dr) rotated at
+ * row `cs_row` of the cos/sin cache; stored as bf16 bits (fp8 == 0) or as the
+ * E4M3 codes of bf16 / scale in binary32 (fp8 == 1). */
+static void producer_row(const uint16_t *nope, int Dn, const uint16_t *rope, int Dr, const float *cs_row,
+                         int is_neox, int mode, int fp8, float scale, void *dst)
+{
+    uint16_t tmp[4096];
+    for (int d = 0; d < Dn; ++d)
+        tmp[d] = nope[d];
+    const int half = Dr / 2;
+    for (int i = 0; i < half; ++i) {
+        const int ia = is_neox ? i : 2 * i;
+        const int ib = is_neox ? i + half : 2 * i + 1;
+        rope_pair_bf16(bf16_to_float(rope[ia]), bf16_to_float(rope[ib]), cs_row[i], cs_row[half + i], mode,
+                       &tmp[Dn + ia], &tmp[Dn + ib]);
+    }
+    const int D = Dn + Dr;
+    if (!fp8) {
+        memcpy(dst, tmp, (size_t)D * sizeof(uint16_t));
+    } else {
+        uint8_t *o = (uint8_t *)dst;
+        for (int d = 0; d < D; ++d) {
+            volatile float x = bf16_to_float(tmp[d]);
+            float y = x / scale;
+            o[d] = oracle_e4m3_encode(y);
+        }
+    }
+}
+
+/* The whole step over contiguous inputs: ql_nope [T,H,Dn], q_pe [T,H,Dr],
+ * kv_c [T,Dn], k_pe [T,Dr] (bf16 bits), positions [T], cos_sin
+ * [max_pos, Dr] binary32. q_out [T,H,Dn+Dr] (bf16 bits or E4M3 codes);
+ * cache [num_slots, Dn+Dr] (bf16 bits or E4M3 codes) row slot_mapping[t]
+ * (negative: skipped). Returns the number of tokens whose position or slot
+ * was out of range (their outputs are left unwritten). */
+int64_t oracle_fused_qk_rope_cache(const uint16_t *ql_nope, const uint16_t *q_pe, const uint16_t *kv_c,
+                                   const uint16_t *k_pe, const int64_t *positions, const float *cos_sin,
+                                   int64_t max_pos, int is_neox, const int64_t *slot_mapping, void *cache,
+                                   int cache_fp8, int64_t num_slots, float kv_scale, void *q_out, int q_out_fp8,
+                                   float q_scale, int T, int H, int Dn, int Dr, int mode)
+{
+    int64_t bad = 0;
+    const int D = Dn + Dr;
+    if (D > 4096 || Dr % 2 != 0)
+        return -1;
+    e4m3_init();
+#pragma omp parallel for reduction(+ : bad) schedule(static)
+    for (int t = 0; t < T; ++t) {
+        const int64_t pos = positions[t];
+        if (pos < 0 || pos >= max_pos) {
+            bad += 1;
+            continue;
+        }
+        const float *cs_row = cos_sin + pos * (int64_t)Dr;
+        for (int h = 0; h < H; ++h) {
+            const int64_t r = (int64_t)t * H + h;
+            void *dst = q_out_fp8 ? (void *)((uint8_t *)q_out + r * D) : (void *)((uint16_t *)q_out + r * D);
+            producer_row(ql_nope + r * Dn, Dn, q_pe + r * Dr, Dr, cs_row, is_neox, mode, q_out_fp8, q_scale, dst);
+        }
+        const int64_t slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        if (slot >= num_slots) {
+            bad += 1;
+            continue;
+        }
+        void *dst = cache_fp8 ? (void *)((uint8_t *)cache + slot * D) : (void *)((uint16_t *)cache + slot * D);
+        producer_row(kv_c + (int64_t)t * Dn, Dn, k_pe + (int64_t)t * Dr, Dr, cs_row, is_neox, mode, cache_fp8,
+                     kv_scale, dst);
+    }
+    return bad;
 }
 
 /* ------------------------------------------------------------------------ */
