@@ -49,7 +49,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode_bf16", choices=sorted(inputs.CONFIGS))
+    ap.add_argument("--workload", default="decode_bf16", choices=sorted(inputs.CONFIGS) + ["producer"],
+                    help="an attention workload, or `producer`: the fused RoPE + q concat + cache write step")
     ap.add_argument("--rotations", type=int, default=0, help="index/q sets (0 = enough for 4x L2)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -543,8 +544,185 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------
+# the fused producer step (RoPE on q_pe / k_pe, q concat, cache write)
+# ----------------------------------------------------------------------------
+
+PRODUCER_T, PRODUCER_H, PRODUCER_POS = 4096, 128, 8192
+PRODUCER_Q_SCALE, PRODUCER_KV_SCALE = 0.0137, 0.0211
+
+
+def producer_bytes(T: int, H: int, cache_rows: int) -> int:
+    """Algorithmic bytes of one call with E4M3 q_out and cache: bf16 ql_nope,
+    q_pe, kv_c, k_pe, the positions and slots, one cos/sin row per token read;
+    q_out and the cache rows written."""
+    reads = T * H * 576 * 2 + T * 576 * 2 + T * 8 * 2 + T * 64 * 4
+    writes = T * H * 576 + cache_rows * 576
+    return reads + writes
+
+
+def run_producer(args):
+    from sparse_mla_attention_04_gb300 import binding
+    rank, world, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist_init(world, "nccl")
+    T, H, P = PRODUCER_T, PRODUCER_H, PRODUCER_POS
+    ql, qp, kc, kp, pos, slots, ns = inputs.producer_inputs(T, H, args.seed + 1 + 1000 * rank, P, num_slots=2 * T)
+    cs = inputs.rope_cos_sin_cache(P)
+    nbytes = producer_bytes(T, H, T)
+    cfg = {"workload": "producer", "T": T, "H": H, "D_latent": 512, "D_rope": 64, "max_position": P,
+           "q_out": "e4m3", "kv_cache": "e4m3", "rope": "neox", "num_slots": ns,
+           "bytes_per_step": nbytes,
+           "l2": "inputs larger than L2: each step reads %.0f MB and writes %.0f MB"
+                 % ((nbytes - T * H * 576 - T * 576) / 1e6, (T * H * 576 + T * 576) / 1e6),
+           "parallelism": "dp%d (independent tokens per GPU, no collective)" % world}
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(producer_reference(args, ql, qp, kc, kp, pos, slots, cs, ns, cfg)), flush=True)
+        return
+    d = [x.to(dev) for x in (ql, qp, kc, kp, pos, slots, cs)]
+    cache = torch.zeros((ns, 576), dtype=torch.uint8, device=dev)
+    q_out = torch.empty((T, H, 576), dtype=torch.uint8, device=dev)
+    kvs = torch.tensor([PRODUCER_KV_SCALE], dtype=torch.float32, device=dev)
+    qs = torch.tensor([PRODUCER_Q_SCALE], dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def call():
+        binding.smla_fused_qk_rope_cache(d[0], d[1], d[2], d[3], d[4], d[6], d[5], cache, is_neox=True,
+                                         kv_scale=kvs, q_out=q_out, q_out_fp8=True, q_scale=qs, stream=stream)
+
+    G = 10
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            call()
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(G):
+                call()
+        graph.replay()
+        stream.synchronize()
+    K = max(G, (args.steps // G) * G)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
+    time.sleep(0.3 if clocks else 0)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(K // G):
+            graph.replay()
+        end.record(stream)
+    end.synchronize()
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    ms = start.elapsed_time(end)
+    ms_max = max_over_ranks(ms, world, dev)
+    gbs = nbytes * K * world / (ms_max * 1e-3) / 1e9
+    hbm, hbm_src = measured_peaks()
+    per_launch = ms / K * 1e-3
+    e2e = None
+    if not args.no_e2e:
+        e2e = producer_e2e(binding, (ql, qp, kc, kp), d, cache, q_out, kvs, qs, stream, nbytes, world, dev)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = producer_reference(args, ql, qp, kc, kp, pos, slots, cs, ns, cfg, cpu_leg=True)
+    if rank == 0:
+        achieved = nbytes / per_launch / 1e9
+        line = {
+            "metric": "fused producer step GB/s (RoPE + q concat + cache write, producer)",
+            "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": max(args.warmup, 3), "ms_per_step": round(ms_max / K, 6),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16 in, e4m3 out (binary32 rotation)",
+            "data": "synthetic (seeded N(0,1) bf16 inputs, uniform positions, distinct slots)",
+            "config": dict(cfg, timing="CUDA graph of %d calls replayed; CUDA events on the launching stream" % G),
+            "tokens_per_s": round(T * K * world / (ms_max * 1e-3), 1),
+            "gpu_launches": K,
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
+                         "frac": round(achieved / hbm, 4), "traffic": ncu_traffic("producer"),
+                         "peak_source": hbm_src, "algorithmic_bytes_per_launch": nbytes},
+            "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def producer_e2e(binding, host_in, d, cache, q_out, kvs, qs, stream, nbytes, world, dev):
+    """The step through the public API with pinned host buffers: the four bf16
+    inputs copied in and q_out read back every step (positions, slots and the
+    cos/sin table stay resident), timed together."""
+    hin = [x.pin_memory() for x in host_in]
+    hout = torch.empty(q_out.shape, dtype=q_out.dtype).pin_memory()
+    steps = 10
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for i in range(steps + 1):
+            if i == 1:
+                a.record(stream)
+            for h, x in zip(hin, d[:4]):
+                x.copy_(h, non_blocking=True)
+            binding.smla_fused_qk_rope_cache(d[0], d[1], d[2], d[3], d[4], d[6], d[5], cache, is_neox=True,
+                                             kv_scale=kvs, q_out=q_out, q_out_fp8=True, q_scale=qs, stream=stream)
+            hout.copy_(q_out, non_blocking=True)
+        b.record(stream)
+    b.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b), world, dev)
+    h2d = sum(x.numel() * x.element_size() for x in hin)
+    d2h = hout.numel() * hout.element_size()
+    return {"value": round(nbytes * steps * world / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "steps": steps,
+            "ms_per_step": round(ms / steps, 6), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def producer_reference(args, ql, qp, kc, kp, pos, slots, cs, ns, cfg, cpu_leg: bool = False):
+    """The oracle (binary32 mirror, OpenMP) on a bounded sample: 16 tokens with
+    all heads per step; the value is scaled to bytes per second of the same
+    per-token work."""
+    import oracle
+    oracle.build()
+    T, H = ql.shape[0], ql.shape[1]
+    n = 16
+    cache = np.zeros((ns, 576), dtype=np.uint8)
+    chunks = []
+    for i in range(0, T, n):
+        chunks.append((ql[i:i + n], qp[i:i + n], kc[i:i + n], kp[i:i + n], pos[i:i + n], slots[i:i + n]))
+    K = 3 if cpu_leg else max(1, args.steps)
+    W = 1 if cpu_leg else max(args.warmup, 3)
+
+    def one(c):
+        oracle.fused_qk_rope_cache(c[0], c[1], c[2], c[3], c[4], cs, True, c[5], cache, cache_fp8=True,
+                                   kv_scale=PRODUCER_KV_SCALE, q_out_fp8=True, q_scale=PRODUCER_Q_SCALE, mode=1)
+
+    for i in range(W):
+        one(chunks[i % len(chunks)])
+    t0 = time.perf_counter()
+    for i in range(K):
+        one(chunks[i % len(chunks)])
+    el = time.perf_counter() - t0
+    value = producer_bytes(n, H, n) * K / el / 1e9
+    sample = "%d step(s) of %d tokens x %d heads (fp32-mirror C + OpenMP)" % (K, n, H)
+    cpu = {"value": round(value, 4), "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+           "sample": sample}
+    if cpu_leg:
+        return cpu
+    return {"impl": "reference", "metric": "fused producer step GB/s (RoPE + q concat + cache write, producer)",
+            "value": round(value, 4), "unit": "GB/s", "n_gpus": 1, "steps": K, "warmup": W,
+            "ms_per_step": round(el * 1e3 / K, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32 mirror", "data": "synthetic (same seeded workload as the GPU arm)",
+            "config": dict(cfg, step="%d tokens (all %d heads) of the workload" % (n, H)),
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
 def main():
     args = parse()
+    if args.workload == "producer":
+        run_producer(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

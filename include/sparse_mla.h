@@ -205,11 +205,13 @@ SMLA_API smla_status sparse_mla_fwd_no_alloc(const void *q, const void *kv_cache
                                              smla_stream_t stream);
 
 /*
- * Error word of the device-side waits (0 = none). The tcgen05 kernels wait on
+ * Error word of the device-side checks (0 = none). The tcgen05 kernels wait on
  * the tensor core and on their own warps with a time limit (about 2 s); a wait
- * that gives up sets a bit here (1 = an awaited barrier never completed),
- * abandons the call's arithmetic, frees its tensor memory and returns, leaving
- * the context usable. Synchronous (copies the word from the device).
+ * that gives up sets a bit here (1 = an awaited barrier never completed,
+ * 2 = the copies or MMAs in flight did not drain), abandons the call's
+ * arithmetic, frees its tensor memory and returns, leaving the context usable.
+ * smla_fused_qk_rope_cache sets 4 for a position outside [0, max_position) and
+ * 8 for a slot >= num_slots. Synchronous (copies the word from the device).
  * reset != 0 clears it.
  */
 SMLA_API smla_status smla_device_error(int *code, int reset);
@@ -240,6 +242,56 @@ SMLA_API smla_status smla_fp8_cache_write(const void *src, const int64_t *slot_m
                                           int64_t N, int D, const float *kv_scale,
                                           void *kv_cache, int64_t num_slots,
                                           smla_stream_t stream);
+
+/*
+ * The fused producer step of sparse MLA decode [P4 Summary: main RoPE on
+ * q_pe/k_pe, the query concat, the KV concat and the fp8 KV-cache write in one
+ * kernel; Test plan: parity with the split chain]. For each token t, with
+ * p = positions[t] and R = the rotation below:
+ *   q_out[t, h, :]  = concat(ql_nope[t, h, 0:512], R_p(q_pe[t, h, 0:64]))   h in [0, H)
+ *   kv_cache[slot_mapping[t], :] = concat(kv_c[t, 0:512], R_p(k_pe[t, 0:64]))
+ * stored as bf16, or (q_out_dtype / kv_dtype = SMLA_KV_FP8_E4M3) as the codes
+ * E4M3_RNE_satfinite(x / *q_scale) resp. (x / *kv_scale), binary32 division of
+ * the bf16 value x (the scaled_fp8_quant convention).
+ * R_p rotates each pair (a, b) to (a cos - b sin, b cos + a sin) with
+ * cos = cos_sin_cache[p, i], sin = cos_sin_cache[p, 32 + i] for pair i: in
+ * binary32, each product and the difference or sum rounded (no fused
+ * multiply-add), then rounded to bf16 before any quantization, as the split
+ * chain stores it. is_neox != 0 pairs element i with i + 32, else 2i with
+ * 2i + 1.
+ *
+ * ql_nope        device, bf16 [T, H, 512], element strides (ql_stride_t,
+ *                ql_stride_h), the last dimension contiguous; strides
+ *                multiples of 8, pointer 16-byte aligned (a transposed
+ *                [H, T, 512] buffer is stride_t = 512, stride_h = T * 512).
+ * q_pe           device, bf16 [T, H, 64] pre-RoPE, strides (qpe_stride_t,
+ *                qpe_stride_h), even, pointer 4-byte aligned.
+ * kv_c           device, bf16 [T, 512], row stride kvc_stride_t (multiple of
+ *                8), 16-byte aligned.
+ * k_pe           device, bf16 [T, 64] pre-RoPE, row stride kpe_stride_t (even),
+ *                4-byte aligned.
+ * positions      device, int64 [T].
+ * cos_sin_cache  device, float [max_position, 64]: 32 cosines then 32 sines.
+ * slot_mapping   device, int64 [T]; a negative slot writes no cache row.
+ * kv_cache       device, [num_slots, 576] bf16 or E4M3 (kv_dtype), 16-byte aligned.
+ * kv_scale       device, one float; required for an E4M3 cache.
+ * q_out          device, [T, H, 576] bf16 or E4M3 (q_out_dtype), contiguous,
+ *                16-byte aligned; must not overlap the inputs.
+ * q_scale        device, one float; required for E4M3 q_out.
+ * H may be 0 (cache rows only; the q pointers may then be NULL).
+ * A token whose position is outside [0, max_position) gets neither its q rows
+ * nor its cache row, and sets bit 4 of smla_device_error; a slot >= num_slots
+ * writes no row and sets bit 8. Asynchronous on `stream`.
+ */
+SMLA_API smla_status smla_fused_qk_rope_cache(const void *ql_nope, int64_t ql_stride_t, int64_t ql_stride_h,
+                                              const void *q_pe, int64_t qpe_stride_t, int64_t qpe_stride_h,
+                                              const void *kv_c, int64_t kvc_stride_t, const void *k_pe,
+                                              int64_t kpe_stride_t, const int64_t *positions,
+                                              const float *cos_sin_cache, int64_t max_position, int is_neox,
+                                              const int64_t *slot_mapping, void *kv_cache, int kv_dtype,
+                                              int64_t num_slots, const float *kv_scale, void *q_out,
+                                              int q_out_dtype, const float *q_scale, int T, int H,
+                                              smla_stream_t stream);
 
 /*
  * Counts the entries of indices [T, topk] that are neither -1 nor inside

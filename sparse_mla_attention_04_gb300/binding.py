@@ -53,6 +53,11 @@ SIGNATURES = {
     "smla_validate_indices": ([_c.c_void_p, _c.c_int, _c.c_int, _c.c_int64, _c.c_void_p,
                                _c.c_void_p], _c.c_int),
     "smla_device_error": ([_c.c_void_p, _c.c_int], _c.c_int),
+    "smla_fused_qk_rope_cache": ([_c.c_void_p, _c.c_int64, _c.c_int64, _c.c_void_p, _c.c_int64, _c.c_int64,
+                                  _c.c_void_p, _c.c_int64, _c.c_void_p, _c.c_int64, _c.c_void_p,
+                                  _c.c_void_p, _c.c_int64, _c.c_int, _c.c_void_p, _c.c_void_p, _c.c_int,
+                                  _c.c_int64, _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_int,
+                                  _c.c_int, _c.c_void_p], _c.c_int),
     "smla_last_error_string": ([], _c.c_char_p),
     "sparse_mla_fwd_no_alloc": ([_c.c_void_p, _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_void_p,
                                  _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int64, _c.c_int,
@@ -246,6 +251,65 @@ def smla_validate_indices(indices: torch.Tensor, num_slots: int, bad_count: Opti
     _check(lib().smla_validate_indices(_ptr(indices), T, topk, int(num_slots), _ptr(bad_count), _stream(stream)),
            "smla_validate_indices")
     return bad_count
+
+
+def _strided(x: torch.Tensor, name: str, ndim: int):
+    """A bf16 CUDA tensor whose last dimension is contiguous (other strides free)."""
+    if not isinstance(x, torch.Tensor) or x.dtype != torch.bfloat16 or not x.is_cuda:
+        raise TypeError("%s must be a CUDA bf16 tensor" % name)
+    if x.dim() != ndim:
+        raise ValueError("%s must have %d dims, got shape %s" % (name, ndim, tuple(x.shape)))
+    if x.stride(-1) != 1:
+        raise ValueError("%s must be contiguous in its last dimension" % name)
+
+
+def smla_fused_qk_rope_cache(ql_nope: torch.Tensor, q_pe: torch.Tensor, kv_c: torch.Tensor, k_pe: torch.Tensor,
+                             positions: torch.Tensor, cos_sin_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                             kv_cache: torch.Tensor, *, is_neox: bool = True, kv_scale: Optional[torch.Tensor] = None,
+                             q_out: Optional[torch.Tensor] = None, q_out_fp8: bool = False,
+                             q_scale: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """The fused producer step: q_out = concat(ql_nope, RoPE(q_pe)) (bf16, or E4M3
+    codes of / q_scale) and kv_cache[slot_mapping[t]] = concat(kv_c, RoPE(k_pe))
+    (bf16 cache, or a 1-byte E4M3 cache with kv_scale). ql_nope [T, H, 512] and
+    q_pe [T, H, 64] may be strided (last dimension contiguous), as may kv_c
+    [T, 512] and k_pe [T, 64]. Returns q_out [T, H, 576]."""
+    _strided(ql_nope, "ql_nope", 3)
+    _strided(q_pe, "q_pe", 3)
+    _strided(kv_c, "kv_c", 2)
+    _strided(k_pe, "k_pe", 2)
+    T, H, Dn = ql_nope.shape
+    if Dn != 512 or tuple(q_pe.shape) != (T, H, 64) or tuple(kv_c.shape) != (T, 512) or tuple(k_pe.shape) != (T, 64):
+        raise ValueError("expected ql_nope [T, H, 512], q_pe [T, H, 64], kv_c [T, 512], k_pe [T, 64]")
+    _need(positions, "positions", torch.int64, 1)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    _need(cos_sin_cache, "cos_sin_cache", torch.float32, 2)
+    if positions.shape[0] != T or slot_mapping.shape[0] != T or cos_sin_cache.shape[1] != 64:
+        raise ValueError("positions and slot_mapping must be [T]; cos_sin_cache [max_position, 64]")
+    _need(kv_cache, "kv_cache", kv_cache.dtype, 2)
+    if kv_cache.shape[1] != 576:
+        raise ValueError("kv_cache must be [num_slots, 576]")
+    if kv_cache.element_size() == 1:
+        kv_dtype = SMLA_KV_FP8_E4M3
+        if kv_scale is None:
+            raise ValueError("an E4M3 cache needs kv_scale")
+    elif kv_cache.dtype == torch.bfloat16:
+        kv_dtype = SMLA_KV_BF16
+    else:
+        raise TypeError("kv_cache must be bf16 or a 1-byte E4M3 cache")
+    if q_out is None:
+        q_out = torch.empty((T, H, 576), dtype=torch.uint8 if q_out_fp8 else torch.bfloat16, device=ql_nope.device)
+    _need(q_out, "q_out", q_out.dtype, 3)
+    if (q_out.element_size() == 1) != bool(q_out_fp8) or tuple(q_out.shape) != (T, H, 576):
+        raise ValueError("q_out must be [T, H, 576], 1-byte when q_out_fp8 else bf16")
+    if q_out_fp8 and q_scale is None:
+        raise ValueError("E4M3 q_out needs q_scale")
+    _check(lib().smla_fused_qk_rope_cache(
+        _ptr(ql_nope), ql_nope.stride(0), ql_nope.stride(1), _ptr(q_pe), q_pe.stride(0), q_pe.stride(1),
+        _ptr(kv_c), kv_c.stride(0), _ptr(k_pe), k_pe.stride(0), _ptr(positions), _ptr(cos_sin_cache),
+        cos_sin_cache.shape[0], 1 if is_neox else 0, _ptr(slot_mapping), _ptr(kv_cache), kv_dtype,
+        kv_cache.shape[0], _ptr(kv_scale), _ptr(q_out), SMLA_KV_FP8_E4M3 if q_out_fp8 else SMLA_KV_BF16,
+        _ptr(q_scale), T, H, _stream(stream)), "smla_fused_qk_rope_cache")
+    return q_out
 
 
 def build_fp8_cache(kv_source: torch.Tensor, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:

@@ -300,13 +300,78 @@ SMLA_API smla_status smla_device_error(int *code, int reset)
 {
     if (code == nullptr)
         return SMLA_ERR_NULL_POINTER;
-    int c16 = 0, cw = 0;
+    int c16 = 0, cw = 0, cp = 0;
     if (const cudaError_t e = smla::read_umma_error(&c16, reset != 0); e != cudaSuccess)
         return cuda_status(e);
     if (const cudaError_t e = smla::read_wide_error(&cw, reset != 0); e != cudaSuccess)
         return cuda_status(e);
-    *code = c16 | cw;
+    if (const cudaError_t e = smla::read_producer_error(&cp, reset != 0); e != cudaSuccess)
+        return cuda_status(e);
+    *code = c16 | cw | cp;
     return SMLA_OK;
+}
+
+SMLA_API smla_status smla_fused_qk_rope_cache(const void *ql_nope, int64_t ql_stride_t, int64_t ql_stride_h,
+                                              const void *q_pe, int64_t qpe_stride_t, int64_t qpe_stride_h,
+                                              const void *kv_c, int64_t kvc_stride_t, const void *k_pe,
+                                              int64_t kpe_stride_t, const int64_t *positions,
+                                              const float *cos_sin_cache, int64_t max_position, int is_neox,
+                                              const int64_t *slot_mapping, void *kv_cache, int kv_dtype,
+                                              int64_t num_slots, const float *kv_scale, void *q_out,
+                                              int q_out_dtype, const float *q_scale, int T, int H,
+                                              smla_stream_t stream)
+{
+    if (T < 0 || H < 0 || num_slots < 0 || max_position < 0 || ql_stride_t < 0 || ql_stride_h < 0 ||
+        qpe_stride_t < 0 || qpe_stride_h < 0 || kvc_stride_t < 0 || kpe_stride_t < 0)
+        return SMLA_ERR_BAD_SHAPE;
+    if ((kv_dtype != SMLA_KV_BF16 && kv_dtype != SMLA_KV_FP8_E4M3) ||
+        (q_out_dtype != SMLA_KV_BF16 && q_out_dtype != SMLA_KV_FP8_E4M3))
+        return SMLA_ERR_BAD_DTYPE;
+    if (T == 0)
+        return SMLA_OK;
+    const bool qrows = H > 0;
+    if ((qrows && (ql_nope == nullptr || q_pe == nullptr || q_out == nullptr)) || kv_c == nullptr ||
+        k_pe == nullptr || positions == nullptr || cos_sin_cache == nullptr || slot_mapping == nullptr ||
+        kv_cache == nullptr || (kv_dtype == SMLA_KV_FP8_E4M3 && kv_scale == nullptr) ||
+        (qrows && q_out_dtype == SMLA_KV_FP8_E4M3 && q_scale == nullptr))
+        return SMLA_ERR_NULL_POINTER;
+    if (max_position == 0)
+        return SMLA_ERR_BAD_SHAPE;
+    // latent rows move as 16-byte vectors, rope pairs as 4-byte words
+    if (ql_stride_t % 8 != 0 || ql_stride_h % 8 != 0 || kvc_stride_t % 8 != 0 || qpe_stride_t % 2 != 0 ||
+        qpe_stride_h % 2 != 0 || kpe_stride_t % 2 != 0)
+        return SMLA_ERR_MISALIGNED;
+    if ((qrows && (!aligned(ql_nope, 16) || !aligned(q_pe, 4) || !aligned(q_out, 16))) || !aligned(kv_c, 16) ||
+        !aligned(k_pe, 4) || !aligned(kv_cache, 16) || !aligned(positions, 8) || !aligned(slot_mapping, 8) ||
+        !aligned(cos_sin_cache, 4) || (kv_scale != nullptr && !aligned(kv_scale, 4)) ||
+        (q_scale != nullptr && !aligned(q_scale, 4)))
+        return SMLA_ERR_MISALIGNED;
+    smla::FusedProducerArgs a;
+    a.ql_nope = ql_nope;
+    a.ql_stride_t = ql_stride_t;
+    a.ql_stride_h = ql_stride_h;
+    a.q_pe = q_pe;
+    a.qpe_stride_t = qpe_stride_t;
+    a.qpe_stride_h = qpe_stride_h;
+    a.kv_c = kv_c;
+    a.kvc_stride_t = kvc_stride_t;
+    a.k_pe = k_pe;
+    a.kpe_stride_t = kpe_stride_t;
+    a.positions = positions;
+    a.cos_sin_cache = cos_sin_cache;
+    a.max_position = max_position;
+    a.slot_mapping = slot_mapping;
+    a.kv_cache = kv_cache;
+    a.num_slots = num_slots;
+    a.kv_scale = kv_scale;
+    a.q_out = q_out;
+    a.q_scale = q_scale;
+    a.T = T;
+    a.H = H;
+    a.is_neox = is_neox != 0;
+    a.q_out_fp8 = q_out_dtype == SMLA_KV_FP8_E4M3;
+    a.cache_fp8 = kv_dtype == SMLA_KV_FP8_E4M3;
+    return cuda_status(smla::launch_fused_producer(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 SMLA_API smla_status smla_compute_fp8_scale(const void *x, int64_t n, float *scale_out, smla_stream_t stream)

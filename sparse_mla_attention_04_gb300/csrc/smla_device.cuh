@@ -104,15 +104,56 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t wa, uint32_t
     return (y & 0x80008000u) | ((y >> 1) & 0x3F803F80u);
 }
 
+// The two reciprocals quant2_e4m3 multiplies by: 1/s rounded to binary32 and
+// scaled by (1 -+ 2^-21), each rounded again; `ok` is false for a reciprocal that is
+// zero, infinite or NaN (then every element is divided).
+struct E4m3Recip {
+    float lo, hi;
+    bool ok;
+};
+__device__ __forceinline__ E4m3Recip e4m3_recip(float s)
+{
+    const float inv = __fdiv_rn(1.0f, s);
+    E4m3Recip r;
+    r.lo = __fmul_rn(inv, 1.0f - 0x1p-21f);
+    r.hi = __fmul_rn(inv, 1.0f + 0x1p-21f);
+    r.ok = fabsf(inv) <= 3.4028234663852886e38f && inv != 0.0f; // finite, nonzero (false for NaN)
+    return r;
+}
+
+// E4M3 codes (round to nearest even, saturating) of x0 / s and x1 / s in
+// IEEE binary32 division, first value in the low byte.
+//
+// The codes are those of the correctly rounded quotients, found without a
+// division for almost every element. x * r.lo and x * r.hi bracket x / s with
+// a relative margin of 2^-21 on each side, while the rounding of 1/s, of the
+// factor (1 -+ 2^-21), of the product and of the quotient itself move a value
+// by at most 2^-24 relative each: the correctly rounded quotient lies between
+// the two products. Rounding onto the E4M3 grid is monotone, so when both
+// products give the same code, so does the quotient; otherwise (they straddle
+// a rounding midpoint, about one element in 10^5) the element is divided.
+__device__ __forceinline__ uint32_t quant2_e4m3(float x0, float x1, float s, const E4m3Recip &r)
+{
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(x0, r.lo), __fmul_rn(x1, r.lo)),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(__fmul_rn(x0, r.hi), __fmul_rn(x1, r.hi)),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    if (r.ok && ((lo ^ hi) & 0xFFFFu) == 0)
+        return lo & 0xFFFFu;
+    const float2 d = make_float2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
+    return __nv_cvt_float2_to_fp8x2(d, __NV_SATFINITE, __NV_E4M3) & 0xFFFFu;
+}
+
 // Four floats divided by `s` (IEEE binary32 division) and rounded to E4M3
-// with saturation, packed lowest index in the lowest byte.
+// with saturation, packed lowest index in the lowest byte; r = e4m3_recip(s).
+__device__ __forceinline__ uint32_t quant4_e4m3(float x0, float x1, float x2, float x3, float s, const E4m3Recip &r)
+{
+    return quant2_e4m3(x0, x1, s, r) | (quant2_e4m3(x2, x3, s, r) << 16);
+}
+
 __device__ __forceinline__ uint32_t quant4_e4m3(float x0, float x1, float x2, float x3, float s)
 {
-    float2 lo = make_float2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
-    float2 hi = make_float2(__fdiv_rn(x2, s), __fdiv_rn(x3, s));
-    uint32_t a = __nv_cvt_float2_to_fp8x2(lo, __NV_SATFINITE, __NV_E4M3);
-    uint32_t b = __nv_cvt_float2_to_fp8x2(hi, __NV_SATFINITE, __NV_E4M3);
-    return (a & 0xFFFFu) | (b << 16);
+    return quant4_e4m3(x0, x1, x2, x3, s, e4m3_recip(s));
 }
 
 // Four E4M3 codes (lowest byte first) as two f16x2 words holding their

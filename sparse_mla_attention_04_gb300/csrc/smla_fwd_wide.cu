@@ -148,6 +148,7 @@ __global__ void __launch_bounds__(128) quantize_q_e4m3_kernel(const __nv_bfloat1
     }
     m = warp_max(m);
     const float s = (m == 0.f) ? 1.0f : __fdiv_rn(m, 448.0f);
+    const E4m3Recip inv = e4m3_recip(s);
     if (lane == 0)
         scale[r] = s;
     if (lane < 24) {
@@ -160,8 +161,8 @@ __global__ void __launch_bounds__(128) quantize_q_e4m3_kernel(const __nv_bfloat1
             const float2 f0 = __bfloat1622float2(b2[0]), f1 = __bfloat1622float2(b2[1]);
             const float2 f2 = __bfloat1622float2(b2[2]), f3 = __bfloat1622float2(b2[3]);
             uint2 o;
-            o.x = quant4_e4m3(f0.x, f0.y, f1.x, f1.y, s);
-            o.y = quant4_e4m3(f2.x, f2.y, f3.x, f3.y, s);
+            o.x = quant4_e4m3(f0.x, f0.y, f1.x, f1.y, s, inv);
+            o.y = quant4_e4m3(f2.x, f2.y, f3.x, f3.y, s, inv);
             const int e0 = 24 * lane + 8 * u; // first column of these 8 codes
             if (e0 < 512) {
                 *reinterpret_cast<uint2 *>(q8 + r * 512 + e0) = o;

@@ -67,6 +67,31 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 cudaError_t read_umma_error(int *out, bool reset);
 cudaError_t read_wide_error(int *out, bool reset);
 
+// The fused producer step (RoPE + q concat + cache write), validated by the ABI layer.
+struct FusedProducerArgs {
+    const void *ql_nope;            // bf16 [T, H, 512], element strides (t, h), rows 16-byte aligned
+    int64_t ql_stride_t, ql_stride_h;
+    const void *q_pe;               // bf16 [T, H, 64], element strides (t, h), rows 4-byte aligned
+    int64_t qpe_stride_t, qpe_stride_h;
+    const void *kv_c;               // bf16 [T, 512], row stride, rows 16-byte aligned
+    int64_t kvc_stride_t;
+    const void *k_pe;               // bf16 [T, 64], row stride, rows 4-byte aligned
+    int64_t kpe_stride_t;
+    const int64_t *positions;       // [T]
+    const float *cos_sin_cache;     // [max_position, 64]: 32 cosines, then 32 sines
+    int64_t max_position;
+    const int64_t *slot_mapping;    // [T], negative = no cache row
+    void *kv_cache;                 // [num_slots, 576] bf16 or E4M3
+    int64_t num_slots;
+    const float *kv_scale;          // device scalar (E4M3 cache)
+    void *q_out;                    // [T, H, 576] bf16 or E4M3, contiguous
+    const float *q_scale;           // device scalar (E4M3 q_out)
+    int T, H;
+    bool is_neox, q_out_fp8, cache_fp8;
+};
+cudaError_t launch_fused_producer(const FusedProducerArgs &a, cudaStream_t stream);
+cudaError_t read_producer_error(int *out, bool reset);
+
 cudaError_t launch_fp8_scale(const void *x, int64_t n, float *scale_out, int sm_count,
                              cudaStream_t stream);
 cudaError_t launch_fp8_cache_write(const void *src, const int64_t *slot_mapping, int64_t N, int D,

@@ -70,6 +70,7 @@ __global__ void __launch_bounds__(256) fp8_cache_write_kernel(const __nv_bfloat1
     if (slot < 0 || slot >= num_slots)
         return;
     const float s = *kv_scale;
+    const E4m3Recip inv = e4m3_recip(s);
     const uint4 *in = reinterpret_cast<const uint4 *>(src + row * D);
     uint2 *outp = reinterpret_cast<uint2 *>(cache + slot * D);
     for (int v = lane; v < D / 8; v += 32) {
@@ -78,8 +79,8 @@ __global__ void __launch_bounds__(256) fp8_cache_write_kernel(const __nv_bfloat1
         const float2 f0 = __bfloat1622float2(b[0]), f1 = __bfloat1622float2(b[1]);
         const float2 f2 = __bfloat1622float2(b[2]), f3 = __bfloat1622float2(b[3]);
         uint2 r;
-        r.x = quant4_e4m3(f0.x, f0.y, f1.x, f1.y, s);
-        r.y = quant4_e4m3(f2.x, f2.y, f3.x, f3.y, s);
+        r.x = quant4_e4m3(f0.x, f0.y, f1.x, f1.y, s, inv);
+        r.y = quant4_e4m3(f2.x, f2.y, f3.x, f3.y, s, inv);
         outp[v] = r;
     }
 }

@@ -176,3 +176,34 @@ def make_q(w: Workload, seed: Optional[int] = None, device="cpu") -> torch.Tenso
 def make_kv_source(w: Workload, device="cpu") -> torch.Tensor:
     """bf16 [num_slots, D_qk]: the cache itself for bf16, the quantizer's input for fp8."""
     return normal_bf16((w.num_slots, w.D_qk), w.seed * 1000003 + 29, device)
+
+
+# --------------------------------------------------------------------------
+# inputs of the fused producer step (RoPE + q concat + cache write)
+# --------------------------------------------------------------------------
+
+def rope_cos_sin_cache(max_position: int, rot_dim: int = 64, base: float = 10000.0) -> torch.Tensor:
+    """float32 [max_position, rot_dim]: for each position p the cosines of
+    p * base^(-2i / rot_dim), i < rot_dim / 2, then their sines (the usual
+    rotary table, an input of the producer step)."""
+    inv = base ** (-np.arange(0, rot_dim, 2, dtype=np.float64) / rot_dim)
+    ang = np.arange(max_position, dtype=np.float64)[:, None] * inv[None, :]
+    return torch.from_numpy(np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32))
+
+
+def producer_inputs(T: int, H: int, seed: int, max_position: int = 4096, num_slots: Optional[int] = None,
+                    skip_every: int = 0):
+    """bf16 ql_nope [T, H, 512], q_pe [T, H, 64], kv_c [T, 512], k_pe [T, 64]
+    (N(0, 1)), int64 positions [T] uniform in [0, max_position), and int64
+    distinct slots [T] in [0, num_slots) (every `skip_every`-th is -1)."""
+    ns = num_slots if num_slots is not None else 2 * T + 7
+    rng = np.random.default_rng(seed)
+    ql = normal_bf16((T, H, 512), seed * 7 + 1)
+    qp = normal_bf16((T, H, 64), seed * 7 + 2)
+    kc = normal_bf16((T, 512), seed * 7 + 3)
+    kp = normal_bf16((T, 64), seed * 7 + 4)
+    pos = rng.integers(0, max_position, T).astype(np.int64)
+    slots = rng.permutation(ns)[:T].astype(np.int64)
+    if skip_every:
+        slots[::skip_every] = -1
+    return ql, qp, kc, kp, torch.from_numpy(pos), torch.from_numpy(slots), ns
