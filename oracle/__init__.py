@@ -70,6 +70,11 @@ def _load():
             c.c_int, c.c_int, c.c_int, c.c_int, c.c_int64, c.c_int,
             c.c_float, c.c_int, c.c_void_p, c.c_void_p, c.c_int]
         lib.oracle_sparse_mla.restype = c.c_int64
+        lib.oracle_sparse_mla_qf64.argtypes = [
+            c.c_void_p, c.c_void_p, c.c_int, c.c_float, c.c_void_p,
+            c.c_int, c.c_int, c.c_int, c.c_int, c.c_int64, c.c_int,
+            c.c_float, c.c_void_p, c.c_void_p, c.c_int]
+        lib.oracle_sparse_mla_qf64.restype = c.c_int64
         lib.oracle_rope_f64.argtypes = [c.c_void_p, c.c_int, c.c_void_p, c.c_void_p, c.c_int, c.c_void_p]
         lib.oracle_rope_f64.restype = None
         lib.oracle_fused_qk_rope_cache.argtypes = [
@@ -179,6 +184,33 @@ def sparse_mla(q, kv, indices, scale: float, *, kv_fp8: bool = False,
         _ptr(qb), _ptr(kvb), 1 if kv_fp8 else 0, float(np.float32(kv_scale)), _ptr(idx),
         T, H, D_qk, D_v, kvb.shape[0], topk, float(np.float32(scale)), int(q_mode),
         _ptr(out), _ptr(lse), int(nthreads))
+    return out, lse, int(bad)
+
+
+def sparse_mla_q8(q8, q_scale, kv, indices, scale: float, *, kv_fp8: bool = True,
+                  kv_scale: float = 1.0, D_v: int = 512, nthreads: int = 0):
+    """Exact (fp64) sparse MLA forward with a pre-quantized q: uint8 E4M3 codes
+    [T, H, D_qk] and one per-tensor scale; q enters the dots as code * q_scale
+    (the oracle's own codec, exact in fp64). kv, indices, returns as sparse_mla."""
+    codes = q8.detach().cpu().numpy() if hasattr(q8, "detach") else np.asarray(q8)
+    codes = np.ascontiguousarray(codes).view(np.uint8)
+    T, H, D_qk = codes.shape
+    table = e4m3_decode_all()
+    qf = np.ascontiguousarray(table[codes] * float(np.float32(q_scale)), dtype=np.float64)
+    if kv_fp8:
+        kvb = kv.detach().contiguous().cpu().numpy() if hasattr(kv, "detach") else np.ascontiguousarray(kv)
+        kvb = kvb.view(np.uint8)
+    else:
+        kvb = _as_bf16_bits(kv)
+    assert kvb.ndim == 2 and kvb.shape[1] == D_qk
+    idx = indices.detach().cpu().numpy() if hasattr(indices, "detach") else indices
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    topk = idx.shape[1]
+    out = np.empty((T, H, D_v), dtype=np.float64)
+    lse = np.empty((T, H), dtype=np.float64)
+    bad = _load().oracle_sparse_mla_qf64(
+        _ptr(qf), _ptr(kvb), 1 if kv_fp8 else 0, float(np.float32(kv_scale)), _ptr(idx),
+        T, H, D_qk, D_v, kvb.shape[0], topk, float(np.float32(scale)), _ptr(out), _ptr(lse), int(nthreads))
     return out, lse, int(bad)
 
 

@@ -361,11 +361,42 @@ static double kv_value(const void *kv, int kv_is_fp8, double kv_scale,
  * out      double [T, H, D_v]; lse double [T, H] (natural log, includes scale)
  * nthreads 0 = OpenMP default. Returns the number of out-of-range indices seen.
  */
+static int64_t sparse_mla_core(const uint16_t *q, const double *qf, const void *kv, int kv_is_fp8,
+                               float kv_scale, const int32_t *indices,
+                               int T, int H, int D_qk, int D_v, int64_t num_slots,
+                               int topk, float scale, int q_mode,
+                               double *out, double *lse, int nthreads);
+
 int64_t oracle_sparse_mla(const uint16_t *q, const void *kv, int kv_is_fp8,
                           float kv_scale, const int32_t *indices,
                           int T, int H, int D_qk, int D_v, int64_t num_slots,
                           int topk, float scale, int q_mode,
                           double *out, double *lse, int nthreads)
+{
+    return sparse_mla_core(q, NULL, kv, kv_is_fp8, kv_scale, indices, T, H, D_qk, D_v, num_slots, topk, scale,
+                           q_mode, out, lse, nthreads);
+}
+
+/*
+ * The same forward with q given as the values that enter the dots, fp64
+ * [T, H, D_qk]: a pre-quantized q is its E4M3 codes times its per-tensor
+ * scale ("Enable AITER sparse MLA on gfx942, including FP8 KV", Details,
+ * "FP8 KV on gfx942": gfx950 keeps the pre-quantized q).
+ */
+int64_t oracle_sparse_mla_qf64(const double *qf, const void *kv, int kv_is_fp8,
+                               float kv_scale, const int32_t *indices,
+                               int T, int H, int D_qk, int D_v, int64_t num_slots,
+                               int topk, float scale, double *out, double *lse, int nthreads)
+{
+    return sparse_mla_core(NULL, qf, kv, kv_is_fp8, kv_scale, indices, T, H, D_qk, D_v, num_slots, topk, scale,
+                           0, out, lse, nthreads);
+}
+
+static int64_t sparse_mla_core(const uint16_t *q, const double *qf, const void *kv, int kv_is_fp8,
+                               float kv_scale, const int32_t *indices,
+                               int T, int H, int D_qk, int D_v, int64_t num_slots,
+                               int topk, float scale, int q_mode,
+                               double *out, double *lse, int nthreads)
 {
     int64_t bad = 0;
     e4m3_init();
@@ -381,11 +412,14 @@ int64_t oracle_sparse_mla(const uint16_t *q, const void *kv, int kv_is_fp8,
 #pragma omp for schedule(dynamic, 1)
         for (int64_t th = 0; th < (int64_t)T * H; ++th) {
             int64_t t = th / H;
-            const uint16_t *qrow = q + th * (int64_t)D_qk;
+            const uint16_t *qrow = q ? q + th * (int64_t)D_qk : NULL;
             double *orow = out + th * (int64_t)D_v;
 
             /* the q row as it enters the dots */
-            if (q_mode == 1) {
+            if (qf != NULL) {
+                for (int d = 0; d < D_qk; ++d)
+                    qv[d] = qf[th * (int64_t)D_qk + d];
+            } else if (q_mode == 1) {
                 float amax = 0.0f;
                 for (int d = 0; d < D_qk; ++d) {
                     float v = fabsf(bf16_to_float(qrow[d]));

@@ -314,3 +314,48 @@ def test_q_quantization_error_is_in_the_pages_range(oracle_mod):
     o1, _, _ = oracle_mod.sparse_mla(q, kv, idx, 1 / math.sqrt(D), q_mode=1, D_v=D)
     rel = np.linalg.norm(o1 - o0) / np.linalg.norm(o0)
     assert 0.005 < rel < 0.045, rel
+
+
+# --------------------------------------------------------------------------
+# pre-quantized q (E4M3 codes and a per-tensor scale)
+# --------------------------------------------------------------------------
+
+def test_prequantized_q_against_torch_codec(oracle_mod):
+    """q given as E4M3 codes with one per-tensor scale enters the dots as
+    code * q_scale: rebuilt with torch's float8 decode and textbook attention."""
+    T, H, Dqk, Dv, N, K = 2, 4, 96, 64, 64, 24
+    rng = np.random.default_rng(21)
+    q8 = rng.integers(0, 256, size=(T, H, Dqk)).astype(np.uint8)
+    q8[(q8 & 0x7F) == 0x7F] = 0x41           # no NaN codes
+    q_scale = np.float32(0.0137)
+    kv = rand_bf16((N, Dqk), 22)
+    idx = np.stack([rng.choice(N, K, replace=False) for _ in range(T)]).astype(np.int32)
+    out, lse, bad = oracle_mod.sparse_mla_q8(q8, q_scale, kv, idx, 0.1, kv_fp8=False, D_v=Dv)
+    assert bad == 0
+    qv = torch.from_numpy(q8).view(torch.float8_e4m3fn).double().numpy() * float(q_scale)
+    kvv = bf16_values(bf16_bits(kv))
+    for t in range(T):
+        ro, rl = dense_attention(qv[t], kvv[idx[t], :Dqk], kvv[idx[t], :Dv], 0.1)
+        np.testing.assert_allclose(out[t], ro, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(lse[t], rl, rtol=1e-13)
+
+
+def test_prequantized_q_equals_bf16_path_and_scales_out(oracle_mod):
+    """Every E4M3 value times a power of two is a bf16 value, so the two input
+    paths must agree to the last bit; and q_scale * 2^k with the softmax scale
+    / 2^k leaves the logits, hence out and lse, unchanged (exact in fp64)."""
+    T, H, D, N, K = 2, 3, 64, 50, 20
+    rng = np.random.default_rng(23)
+    q8 = rng.integers(0, 256, size=(T, H, D)).astype(np.uint8)
+    q8[(q8 & 0x7F) == 0x7F] = 0x30
+    codes_kv = rng.integers(0, 256, size=(N, D)).astype(np.uint8)
+    codes_kv[(codes_kv & 0x7F) == 0x7F] = 0x38
+    idx = np.stack([rng.choice(N, K, replace=False) for _ in range(T)]).astype(np.int32)
+    qvals = oracle_mod.e4m3_decode_all()[q8] * 0.25
+    q_bf16 = torch.from_numpy(qvals.astype(np.float32)).to(torch.bfloat16)
+    assert (q_bf16.double().numpy() == qvals).all()
+    o1, l1, _ = oracle_mod.sparse_mla_q8(q8, 0.25, codes_kv, idx, 0.2, kv_fp8=True, kv_scale=0.5, D_v=D)
+    o2, l2, _ = oracle_mod.sparse_mla(q_bf16, codes_kv, idx, 0.2, kv_fp8=True, kv_scale=0.5, D_v=D)
+    assert (o1 == o2).all() and (l1 == l2).all()
+    o3, l3, _ = oracle_mod.sparse_mla_q8(q8, 0.25 * 8, codes_kv, idx, 0.2 / 8, kv_fp8=True, kv_scale=0.5, D_v=D)
+    assert (o3 == o1).all() and (l3 == l1).all()
