@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--rotations", type=int, default=0, help="index/q sets (0 = enough for 4x L2)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--q8", action="store_true",
+                    help="E4M3 workloads: pass q pre-quantized (codes + a per-tensor scale) to sparse_mla_fwd_q8")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--ctx", type=int, default=0,
                     help="override the per-row context (pool size) of a decode workload, for profiling")
@@ -256,6 +258,11 @@ def run_ours(args):
     w, src, cache, kvs, sets, l2 = build_workload(args.workload, args.seed, args.rotations, dev, rank, args.ctx)
     R = len(sets)
     dot = "fp8" if w.kv_fp8 else "auto"
+    if args.q8:
+        if not w.kv_fp8:
+            raise SystemExit("--q8 needs an E4M3 workload")
+        for s in sets:   # q quantized once per set, outside the timed region, by the library's kernels
+            s["q8"], s["qs"] = quantize_q_per_tensor(binding, s["q"])
     stream = torch.cuda.Stream(device=dev)
     T, H = w.T, w.H
     out = torch.empty((T, H, w.D_v), dtype=torch.bfloat16, device=dev)
@@ -267,8 +274,12 @@ def run_ours(args):
 
     def call(i):
         s = sets[i % R]
-        binding.sparse_mla_fwd(s["q"], cache, s["idx"], w.scale, kv_scale=kvs, dot_precision=dot, D_v=w.D_v,
-                               out=out, lse=lse, workspace=ws, num_splits=splits, stream=stream)
+        if args.q8:
+            binding.sparse_mla_fwd_q8(s["q8"], s["qs"], cache, s["idx"], w.scale, kv_scale=kvs, D_v=w.D_v,
+                                      out=out, lse=lse, workspace=ws, num_splits=splits, stream=stream)
+        else:
+            binding.sparse_mla_fwd(s["q"], cache, s["idx"], w.scale, kv_scale=kvs, dot_precision=dot, D_v=w.D_v,
+                                   out=out, lse=lse, workspace=ws, num_splits=splits, stream=stream)
 
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 3)):
@@ -313,7 +324,7 @@ def run_ours(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(w, cache, kvs, sets, dot, splits, dev, stream, K, world)
+        e2e = run_e2e(w, cache, kvs, sets, dot, splits, dev, stream, K, world, q8=args.q8)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -321,7 +332,7 @@ def run_ours(args):
 
     if rank == 0:
         line = {
-            "metric": "sparse MLA fwd gathered-KV GB/s (%s)" % w.name,
+            "metric": "sparse MLA fwd gathered-KV GB/s (%s%s)" % (w.name, ", pre-quantized q" if args.q8 else ""),
             "value": round(gbs, 2),
             "unit": "GB/s",
             "n_gpus": world,
@@ -355,7 +366,18 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
-def run_e2e(w, cache, kvs, sets, dot, splits, dev, stream, K, world):
+def quantize_q_per_tensor(binding, q):
+    """E4M3 codes of q / s with one per-tensor scale s = amax/448, by the
+    library's own scale and quantizing-write kernels (as a producer would)."""
+    T, H, D = q.shape
+    qs = binding.smla_compute_fp8_scale(q)
+    q8 = torch.empty((T * H, D), dtype=torch.uint8, device=q.device)
+    rows = torch.arange(T * H, dtype=torch.int64, device=q.device)
+    binding.smla_fp8_cache_write(q.reshape(T * H, D), rows, qs, q8)
+    return q8.view(T, H, D), qs
+
+
+def run_e2e(w, cache, kvs, sets, dot, splits, dev, stream, K, world, q8=False):
     """Same metric through the public API with host buffers: every step copies
     that step's q and indices from pinned host memory and reads out and lse
     back into pinned host memory, inside the timed region.
@@ -368,11 +390,12 @@ def run_e2e(w, cache, kvs, sets, dot, splits, dev, stream, K, world):
     from sparse_mla_attention_04_gb300 import binding
     R = len(sets)
     NB = 2
-    hq = [s["q"].cpu().pin_memory() for s in sets]
+    qkey = "q8" if q8 else "q"
+    hq = [s[qkey].cpu().pin_memory() for s in sets]
     hi = [s["idx"].cpu().pin_memory() for s in sets]
     ho = [torch.empty((w.T, w.H, w.D_v), dtype=torch.bfloat16).pin_memory() for _ in range(NB)]
     hl = [torch.empty((w.T, w.H), dtype=torch.float32).pin_memory() for _ in range(NB)]
-    dq = [torch.empty_like(sets[0]["q"]) for _ in range(NB)]
+    dq = [torch.empty_like(sets[0][qkey]) for _ in range(NB)]
     di = [torch.empty_like(sets[0]["idx"]) for _ in range(NB)]
     out = [torch.empty((w.T, w.H, w.D_v), dtype=torch.bfloat16, device=dev) for _ in range(NB)]
     lse = [torch.empty((w.T, w.H), dtype=torch.float32, device=dev) for _ in range(NB)]
@@ -396,8 +419,12 @@ def run_e2e(w, cache, kvs, sets, dot, splits, dev, stream, K, world):
         stream.wait_event(ev_in[k])
         if not first:
             stream.wait_event(ev_out[k])
-        binding.sparse_mla_fwd(dq[k], cache, di[k], w.scale, kv_scale=kvs, dot_precision=dot, D_v=w.D_v,
-                               out=out[k], lse=lse[k], workspace=ws, num_splits=splits, stream=stream)
+        if q8:
+            binding.sparse_mla_fwd_q8(dq[k], sets[i % R]["qs"], cache, di[k], w.scale, kv_scale=kvs, D_v=w.D_v,
+                                      out=out[k], lse=lse[k], workspace=ws, num_splits=splits, stream=stream)
+        else:
+            binding.sparse_mla_fwd(dq[k], cache, di[k], w.scale, kv_scale=kvs, dot_precision=dot, D_v=w.D_v,
+                                   out=out[k], lse=lse[k], workspace=ws, num_splits=splits, stream=stream)
         ev_k[k].record(stream)
         s_out.wait_event(ev_k[k])
         with torch.cuda.stream(s_out):
@@ -441,7 +468,7 @@ def run_e2e(w, cache, kvs, sets, dot, splits, dev, stream, K, world):
     ms = max_over_ranks(a.elapsed_time(b), world, dev)
     reps, rem = divmod(steps, R)
     nbytes = reps * sum(s["bytes"] for s in sets) + sum(s["bytes"] for s in sets[:rem])
-    h2d = sets[0]["q"].numel() * 2 + sets[0]["idx"].numel() * 4
+    h2d = sets[0][qkey].numel() * sets[0][qkey].element_size() + sets[0]["idx"].numel() * 4
     d2h = out[0].numel() * 2 + lse[0].numel() * 4
     return {"value": round(nbytes * world / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "steps": steps,
             "ms_per_step": round(ms / steps, 6), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -173,6 +173,24 @@ SMLA_API smla_status sparse_mla_fwd(const void *q, const void *kv_cache, int kv_
                                     int num_splits, smla_stream_t stream);
 
 /*
+ * The same forward with a pre-quantized q [P1 Details, "FP8 KV on gfx942":
+ * gfx950 keeps the pre-quantized q]: q8 holds E4M3 codes [T, H, D_qk] (as
+ * written, for example, by smla_fused_qk_rope_cache with an E4M3 q_out) and
+ * *q_scale is their per-tensor scale, so q enters the dots as code * q_scale.
+ * The cache must be E4M3 (kv_scale as above); the dots run in fp8, as with
+ * SMLA_DOT_FP8, without quantizing q again. Every other argument, the
+ * workspace and the kernels are as for sparse_mla_fwd.
+ * q8       device, uint8 [T, H, D_qk], 16-byte aligned.
+ * q_scale  device, one float, 4-byte aligned.
+ */
+SMLA_API smla_status sparse_mla_fwd_q8(const void *q8, const float *q_scale, const void *kv_cache,
+                                       const float *kv_scale, const int32_t *indices, int T, int H, int D_qk,
+                                       int D_v, int64_t num_slots, int topk, float scale, void *out, float *lse,
+                                       void *workspace, size_t workspace_bytes, int num_splits,
+                                       smla_stream_t stream);
+
+
+/*
  * Maximum workspace bytes sparse_mla_fwd_no_alloc can serve from its static
  * device array (8 MiB): every GPU that loads the library holds this much.
  */

@@ -47,6 +47,9 @@ SIGNATURES = {
                         _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int64, _c.c_int,
                         _c.c_float, _c.c_int, _c.c_void_p, _c.c_void_p,
                         _c.c_void_p, _c.c_size_t, _c.c_int, _c.c_void_p], _c.c_int),
+    "sparse_mla_fwd_q8": ([_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                           _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int64, _c.c_int, _c.c_float,
+                           _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_size_t, _c.c_int, _c.c_void_p], _c.c_int),
     "smla_compute_fp8_scale": ([_c.c_void_p, _c.c_int64, _c.c_void_p, _c.c_void_p], _c.c_int),
     "smla_fp8_cache_write": ([_c.c_void_p, _c.c_void_p, _c.c_int64, _c.c_int, _c.c_void_p,
                               _c.c_void_p, _c.c_int64, _c.c_void_p], _c.c_int),
@@ -212,6 +215,49 @@ def sparse_mla_fwd(q: torch.Tensor, kv_cache: torch.Tensor, indices: torch.Tenso
         T, H, D_qk, D_v, kv_cache.shape[0], topk, float(scale), _DOT[dot_precision],
         _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, int(num_splits), sh)
     _check(st, "sparse_mla_fwd")
+    return out, lse
+
+
+def sparse_mla_fwd_q8(q8: torch.Tensor, q_scale: torch.Tensor, kv_cache: torch.Tensor, indices: torch.Tensor,
+                      scale: float, *, kv_scale: torch.Tensor, D_v: int = 512, out: Optional[torch.Tensor] = None,
+                      lse: Optional[torch.Tensor] = None, return_lse: bool = True,
+                      workspace: Optional[torch.Tensor] = None, num_splits: int = 0,
+                      stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """The forward with a pre-quantized q: q8 E4M3 codes [T, H, D_qk] (uint8 or
+    float8_e4m3fn) and q_scale, its per-tensor fp32 device scalar; an E4M3 cache
+    with kv_scale; fp8 dots."""
+    if q8.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise TypeError("q8 must be E4M3 codes (uint8 / float8_e4m3fn), got %s" % q8.dtype)
+    _need(q8, "q8", q8.dtype, 3)
+    T, H, D_qk = q8.shape
+    if kv_cache.dtype not in (torch.float8_e4m3fn, torch.uint8):
+        raise TypeError("kv_cache must be E4M3 (float8_e4m3fn / uint8), got %s" % kv_cache.dtype)
+    _need(kv_cache, "kv_cache", kv_cache.dtype, 2)
+    if kv_cache.shape[1] != D_qk:
+        raise ValueError("kv_cache row width %d != D_qk %d" % (kv_cache.shape[1], D_qk))
+    _need(indices, "indices", torch.int32, 2)
+    if indices.shape[0] != T:
+        raise ValueError("indices has %d rows, q8 has %d" % (indices.shape[0], T))
+    _need(q_scale.reshape(1), "q_scale", torch.float32, 1)
+    _need(kv_scale.reshape(1), "kv_scale", torch.float32, 1)
+    topk = indices.shape[1]
+    if out is None:
+        out = torch.empty((T, H, D_v), dtype=torch.bfloat16, device=q8.device)
+    _need(out, "out", torch.bfloat16, 3)
+    if lse is None and return_lse:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q8.device)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    sh = _stream(stream)
+    need = sparse_mla_fwd_workspace_size(T, H, D_qk, D_v, topk, SMLA_KV_FP8_E4M3, num_splits)
+    if workspace is None:
+        workspace = workspace_for(need, q8.device, sh)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().sparse_mla_fwd_q8(
+        _ptr(q8), _ptr(q_scale), _ptr(kv_cache), _ptr(kv_scale), _ptr(indices),
+        T, H, D_qk, D_v, kv_cache.shape[0], topk, float(scale),
+        _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, int(num_splits), sh)
+    _check(st, "sparse_mla_fwd_q8")
     return out, lse
 
 

@@ -201,15 +201,17 @@ SMLA_API size_t sparse_mla_fwd_workspace_size(int T, int H, int D_qk, int D_v, i
     return smla::workspace_layout(T, H, D_qk, D_v, S, wide).total;
 }
 
-SMLA_API smla_status sparse_mla_fwd(const void *q, const void *kv_cache, int kv_dtype, const float *kv_scale,
-                                    const int32_t *indices, int T, int H, int D_qk, int D_v, int64_t num_slots,
-                                    int topk, float scale, int dot_precision, void *out, float *lse,
-                                    void *workspace, size_t workspace_bytes, int num_splits,
-                                    smla_stream_t stream)
+// The forward for a bf16 q, or (q_fp8_in) for E4M3 codes of q with one
+// per-tensor scale q_scale_in.
+static smla_status fwd_impl(const void *q, bool q_fp8_in, const float *q_scale_in, const void *kv_cache,
+                            int kv_dtype, const float *kv_scale, const int32_t *indices, int T, int H, int D_qk,
+                            int D_v, int64_t num_slots, int topk, float scale, int dot_precision, void *out,
+                            float *lse, void *workspace, size_t workspace_bytes, int num_splits,
+                            smla_stream_t stream)
 {
     // 1. pointers
     if (kv_cache == nullptr || ((q == nullptr || out == nullptr) && T > 0) ||
-        (indices == nullptr && (int64_t)T * topk > 0))
+        (indices == nullptr && (int64_t)T * topk > 0) || (q_fp8_in && q_scale_in == nullptr))
         return SMLA_ERR_NULL_POINTER;
     if (kv_dtype == SMLA_KV_FP8_E4M3 && kv_scale == nullptr)
         return SMLA_ERR_NULL_POINTER;
@@ -234,7 +236,8 @@ SMLA_API smla_status sparse_mla_fwd(const void *q, const void *kv_cache, int kv_
         return SMLA_ERR_UNSUPPORTED;
     // 5. alignment
     if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(indices, 4) ||
-        (lse != nullptr && !aligned(lse, 4)) || (kv_scale != nullptr && !aligned(kv_scale, 4)))
+        (lse != nullptr && !aligned(lse, 4)) || (kv_scale != nullptr && !aligned(kv_scale, 4)) ||
+        (q_scale_in != nullptr && !aligned(q_scale_in, 4)))
         return SMLA_ERR_MISALIGNED;
     if (T == 0)
         return SMLA_OK;
@@ -285,6 +288,8 @@ SMLA_API smla_status sparse_mla_fwd(const void *q, const void *kv_cache, int kv_
     a.keys_per_split = topk > 0 ? keys_per_split(topk, S, tile_keys(path)) : tile_keys(path);
     a.scale = scale;
     a.kv_fp8 = kv_dtype == SMLA_KV_FP8_E4M3;
+    a.q_fp8_in = q_fp8_in;
+    a.q_scale_in = q_scale_in;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     switch (path) {
     case Path::Umma16:
@@ -294,6 +299,26 @@ SMLA_API smla_status sparse_mla_fwd(const void *q, const void *kv_cache, int kv_
     default:
         return cuda_status(smla::launch_fwd_mma(a, st));
     }
+}
+
+SMLA_API smla_status sparse_mla_fwd(const void *q, const void *kv_cache, int kv_dtype, const float *kv_scale,
+                                    const int32_t *indices, int T, int H, int D_qk, int D_v, int64_t num_slots,
+                                    int topk, float scale, int dot_precision, void *out, float *lse,
+                                    void *workspace, size_t workspace_bytes, int num_splits,
+                                    smla_stream_t stream)
+{
+    return fwd_impl(q, false, nullptr, kv_cache, kv_dtype, kv_scale, indices, T, H, D_qk, D_v, num_slots, topk,
+                    scale, dot_precision, out, lse, workspace, workspace_bytes, num_splits, stream);
+}
+
+SMLA_API smla_status sparse_mla_fwd_q8(const void *q8, const float *q_scale, const void *kv_cache,
+                                       const float *kv_scale, const int32_t *indices, int T, int H, int D_qk,
+                                       int D_v, int64_t num_slots, int topk, float scale, void *out, float *lse,
+                                       void *workspace, size_t workspace_bytes, int num_splits,
+                                       smla_stream_t stream)
+{
+    return fwd_impl(q8, true, q_scale, kv_cache, SMLA_KV_FP8_E4M3, kv_scale, indices, T, H, D_qk, D_v, num_slots,
+                    topk, scale, SMLA_DOT_FP8, out, lse, workspace, workspace_bytes, num_splits, stream);
 }
 
 SMLA_API smla_status smla_device_error(int *code, int reset)

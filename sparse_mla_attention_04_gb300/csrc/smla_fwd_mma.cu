@@ -81,6 +81,7 @@ struct Cfg {
 template <bool FP8, int DQK>
 __device__ __forceinline__ void load_q_frags(uint32_t (&qa)[Cfg<FP8, DQK>::KS_MAX][4],
                                              const __nv_bfloat16 *__restrict__ q0, // head (group base + g)
+                                             const uint8_t *__restrict__ c0, // pre-quantized codes of that head, or null
                                              const float *sq, int g, int c, int ks0, int ks1)
 {
     using C = Cfg<FP8, DQK>;
@@ -89,7 +90,15 @@ __device__ __forceinline__ void load_q_frags(uint32_t (&qa)[Cfg<FP8, DQK>::KS_MA
     for (int i = 0; i < C::KS_MAX; ++i) {
         const int ks = ks0 + i;
         if (ks < ks1) {
-            if constexpr (!FP8) {
+            if (FP8 && c0 != nullptr) {
+                // pre-quantized q: the m16n8k32 A fragment takes 4 consecutive codes per register
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int d = ks * 32 + half * 16 + 4 * c;
+                    qa[i][2 * half + 0] = *reinterpret_cast<const uint32_t *>(c0 + d);
+                    qa[i][2 * half + 1] = *reinterpret_cast<const uint32_t *>(c0 + 8 * DQK + d);
+                }
+            } else if constexpr (!FP8) {
                 const int d = ks * 16 + 2 * c;
                 qa[i][0] = *reinterpret_cast<const uint32_t *>(q0 + d);
                 qa[i][1] = *reinterpret_cast<const uint32_t *>(q8 + d);
@@ -175,7 +184,10 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_fwd_mma_kernel(const F
     };
 
     // ---- q: per-head fp8 scales, then this warp's A fragments ---------------
-    if constexpr (FP8) {
+    if (FP8 && a.q_fp8_in) {
+        if (tid < kHeads) // one per-tensor scale for every head
+            sq[tid] = *a.q_scale_in;
+    } else if constexpr (FP8) {
 #pragma unroll
         for (int hh = 0; hh < kHeads / kWarps; ++hh) {
             const int h = warp * (kHeads / kWarps) + hh;
@@ -204,7 +216,9 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_fwd_mma_kernel(const F
     __syncthreads(); // sq visible
     const int ks0 = warp * C::KS / kWarps, ks1 = (warp + 1) * C::KS / kWarps;
     uint32_t qa[C::KS_MAX][4];
-    load_q_frags<FP8, DQK>(qa, qg + (int64_t)g * DQK, sq, g, c, ks0, ks1);
+    const uint8_t *cg = a.q_fp8_in ? static_cast<const uint8_t *>(a.q) + (qg - static_cast<const __nv_bfloat16 *>(a.q))
+                                   : nullptr; // the same row and head offset, in codes
+    load_q_frags<FP8, DQK>(qa, qg + (int64_t)g * DQK, cg ? cg + (int64_t)g * DQK : nullptr, sq, g, c, ks0, ks1);
 #pragma unroll
     for (int j = 0; j < C::STAGES - 1; ++j) {
         if (j < ntiles)

@@ -283,6 +283,14 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
                 const int h = e >> 6, c = e & 63;
                 cp_async_16(q_s + (h >> 3) * C::QGRP + c * 128 + (h & 7) * 16, qg + h * kD + c * 8, 16);
             }
+        } else if (a.q_fp8_in) {
+            // pre-quantized q: each head's 512 codes straight into core matrices
+            // (a core-matrix row holds 16 codes)
+            const uint8_t *q8g = static_cast<const uint8_t *>(a.q) + (int64_t)t * kHeads * kD;
+            for (int e = pt; e < kHeads * (kD / 16); e += kProducerThreads) {
+                const int h = e / (kD / 16), c = e % (kD / 16);
+                cp_async_16(q_s + (h >> 3) * C::QGRP + c * 128 + (h & 7) * 16, q8g + h * kD + c * 16, 16);
+            }
         } else {
             // bf16 q staged row-major: this thread's 64 elements of head pt/8,
             // the ones it quantizes
@@ -295,7 +303,10 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
         bool q_pending = true;
         auto publish_q = [&] {
             cp_async_wait<0>();
-            if constexpr (FP8) {
+            if (FP8 && a.q_fp8_in) {
+                if (pt < kHeads) // one per-tensor scale for every head
+                    sq_s[pt] = *a.q_scale_in;
+            } else if constexpr (FP8) {
                 // thread pt quantizes the 64 elements of head pt/8 it staged
                 const int h = pt >> 3;
                 uint4 qraw[8];

@@ -121,14 +121,40 @@ constexpr uint32_t kIdescPV = umma::idesc(128, 128, 0, 0, 0, 0);
 // reads (per (row t, group of 128 heads) an 8 KB block: 8-head groups of 4
 // chunks of 8 heads x 16 B), and the per-row scale. One warp per row; lanes
 // 0-23 hold 24 elements each.
+//
+// With a pre-quantized q (codes [rows x 576] and one per-tensor scale) the
+// codes are only rearranged and the scale copied to every row.
 __global__ void __launch_bounds__(128) quantize_q_e4m3_kernel(const __nv_bfloat16 *__restrict__ q, int64_t rows, int H,
                                                              uint8_t *__restrict__ q8, uint8_t *__restrict__ q8_rope,
-                                                             float *__restrict__ scale)
+                                                             float *__restrict__ scale,
+                                                             const uint8_t *__restrict__ codes_in,
+                                                             const float *__restrict__ scale_in)
 {
     const int64_t r = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (r >= rows)
         return;
+    if (codes_in != nullptr) {
+        if (lane == 0)
+            scale[r] = *scale_in;
+        if (lane < 24) {
+            const int64_t t = r / H;
+            const int h = (int)(r % H), hg = h / kHeads, hl = h % kHeads;
+            uint8_t *rope = q8_rope + (t * (H / kHeads) + hg) * kQRope;
+#pragma unroll
+            for (int u = 0; u < 3; ++u) {
+                const int e0 = 24 * lane + 8 * u;
+                const uint2 o = __ldg(reinterpret_cast<const uint2 *>(codes_in + r * kDqk + e0));
+                if (e0 < 512) {
+                    *reinterpret_cast<uint2 *>(q8 + r * 512 + e0) = o;
+                } else {
+                    const int d = e0 - 512;
+                    *reinterpret_cast<uint2 *>(rope + ((hl >> 3) * 4 + (d >> 4)) * 128 + (hl & 7) * 16 + (d & 15)) = o;
+                }
+            }
+        }
+        return;
+    }
     const uint4 *src = reinterpret_cast<const uint4 *>(q + r * kDqk);
     uint4 v[3];
     float m = 0.f;
@@ -580,7 +606,8 @@ cudaError_t launch_fwd_wide(const FwdArgs &a, cudaStream_t stream)
         return cudaErrorInvalidValue;
     const int64_t qrows = (int64_t)a.T * a.H;
     quantize_q_e4m3_kernel<<<dim3((unsigned)((qrows + 3) / 4)), dim3(128), 0, stream>>>(
-        static_cast<const __nv_bfloat16 *>(a.q), qrows, a.H, a.q8, a.q8_rope, a.q_scale);
+        static_cast<const __nv_bfloat16 *>(a.q), qrows, a.H, a.q8, a.q8_rope, a.q_scale,
+        a.q_fp8_in ? static_cast<const uint8_t *>(a.q) : nullptr, a.q_scale_in);
     const cudaError_t qe = cudaGetLastError();
     if (qe != cudaSuccess)
         return qe;
