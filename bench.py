@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--rotations", type=int, default=0, help="index/q sets (0 = enough for 4x L2)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--bf16-dots", action="store_true",
+                    help="E4M3 workloads: keep q in bf16 and dot it with the cache values (dot_precision bf16)")
     ap.add_argument("--q8", action="store_true",
                     help="E4M3 workloads: pass q pre-quantized (codes + a per-tensor scale) to sparse_mla_fwd_q8")
     ap.add_argument("--seed", type=int, default=0)
@@ -258,6 +260,10 @@ def run_ours(args):
     w, src, cache, kvs, sets, l2 = build_workload(args.workload, args.seed, args.rotations, dev, rank, args.ctx)
     R = len(sets)
     dot = "fp8" if w.kv_fp8 else "auto"
+    if args.bf16_dots:
+        if not w.kv_fp8 or args.q8:
+            raise SystemExit("--bf16-dots needs an E4M3 workload and a bf16 q")
+        dot = "bf16"
     if args.q8:
         if not w.kv_fp8:
             raise SystemExit("--q8 needs an E4M3 workload")
@@ -269,6 +275,8 @@ def run_ours(args):
     lse = torch.empty((T, H), dtype=torch.float32, device=dev)
     splits = binding.smla_plan_num_splits(T, H, w.D_qk, w.topk, int(w.kv_fp8),
                                           torch.cuda.get_device_properties(dev).multi_processor_count)
+    if args.bf16_dots:
+        splits = 0   # bf16 dots run on the warp-MMA kernel: its own automatic plan
     need = binding.sparse_mla_fwd_workspace_size(T, H, w.D_qk, w.D_v, w.topk, int(w.kv_fp8), splits)
     ws = torch.zeros(max(need, 1), dtype=torch.uint8, device=dev)
 
@@ -332,7 +340,8 @@ def run_ours(args):
 
     if rank == 0:
         line = {
-            "metric": "sparse MLA fwd gathered-KV GB/s (%s%s)" % (w.name, ", pre-quantized q" if args.q8 else ""),
+            "metric": "sparse MLA fwd gathered-KV GB/s (%s%s)" % (
+                w.name, ", pre-quantized q" if args.q8 else (", bf16 dots" if args.bf16_dots else "")),
             "value": round(gbs, 2),
             "unit": "GB/s",
             "n_gpus": world,
@@ -342,7 +351,8 @@ def run_ours(args):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "fp8-e4m3 QK / fp16 PV" if w.kv_fp8 else "bf16",
+            "dtype": ("bf16 QK over e4m3 / fp16 PV" if args.bf16_dots else "fp8-e4m3 QK / fp16 PV") if w.kv_fp8
+                     else "bf16",
             "data": "synthetic (seeded N(0,1) bf16 q and KV, uniform distinct top-k over paged contexts)",
             "config": {
                 "workload": w.name, "T": T, "H": H, "D_qk": w.D_qk, "D_v": w.D_v, "topk": w.topk,

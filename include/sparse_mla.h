@@ -67,7 +67,8 @@ typedef enum {
 /* Precision of the QK dot products [P1 Details: optional dot_precision; when
  * omitted the precision follows q's dtype, which is bf16 here].
  *   AUTO = BF16.
- *   BF16: bf16 q . bf16 K (a bf16 cache).
+ *   BF16: bf16 q . K, with K the bf16 cache or the fp8 cache's values
+ *         code * kv_scale.
  *   FP8 : q quantized inside the kernel per (row, head) tile to E4M3 with
  *         s_q = amax|q[t,h,:]| / 448 (1.0 if amax == 0), q8 = RNE_sat(q / s_q),
  *         dotted with the E4M3 cache; requires an fp8 cache.
@@ -132,8 +133,11 @@ SMLA_API size_t sparse_mla_fwd_workspace_size(int T, int H, int D_qk, int D_v, i
  *              supported: H a multiple of 16, D_v = 512, D_qk in {512, 576}.
  *              T = 0 is a no-op. topk = 0 gives empty rows.
  * scale        softmax scale (e.g. 1/sqrt(D_qk)).
- * dot_precision smla_dot_precision (FP8 needs an fp8 cache; bf16 dots over an
- *              fp8 cache return SMLA_ERR_UNSUPPORTED in this version).
+ * dot_precision smla_dot_precision (FP8 needs an fp8 cache). AUTO or BF16
+ *              with an fp8 cache keeps q in bf16 and dots it with the cache
+ *              values code * kv_scale ([P1 Details, "Numerics": the BF16-dots
+ *              option]); this runs on the warp-MMA kernel, with at most 8
+ *              automatic splits.
  * out          device, bf16 [T, H, D_v], 16-byte aligned, written.
  * lse          device, float [T, H], or NULL to skip.
  * workspace    device, >= sparse_mla_fwd_workspace_size(...) bytes, 256-byte

@@ -230,8 +230,6 @@ static smla_status fwd_impl(const void *q, bool q_fp8_in, const float *q_scale_i
     // 4. what this build has kernels for
     if (!shape_supported(H, D_qk, D_v))
         return SMLA_ERR_UNSUPPORTED;
-    if (kv_dtype == SMLA_KV_FP8_E4M3 && !fp8_dots)
-        return SMLA_ERR_UNSUPPORTED; // bf16 dots over an fp8 cache: not built yet
     if (num_splits > kMaxSplits)
         return SMLA_ERR_UNSUPPORTED;
     // 5. alignment
@@ -242,15 +240,20 @@ static smla_status fwd_impl(const void *q, bool q_fp8_in, const float *q_scale_i
     if (T == 0)
         return SMLA_OK;
     // 6. split plan and workspace
+    const bool bf16_dots = kv_dtype == SMLA_KV_FP8_E4M3 && !fp8_dots; // bf16 q . dequantized K
     Path path = choose_path(H, D_qk, D_v, kv_dtype == SMLA_KV_FP8_E4M3);
     if (path == Path::Wide && num_splits > 1)
         path = Path::Mma; // the 128-head kernel does not split the top-k list
+    if (bf16_dots)
+        path = Path::Mma; // the warp-MMA kernel serves bf16 dots over an E4M3 cache
     int S = num_splits;
     if (S == 0) {
         int sms = 0;
         if (const cudaError_t e = current_sm_count(&sms); e != cudaSuccess)
             return cuda_status(e);
         S = plan_splits(T, H, topk, sms, path);
+        if (bf16_dots && S > kClusterMaxSplits)
+            S = kClusterMaxSplits; // merged in a cluster: no workspace beyond the E4M3 query's
     }
     if (S > kClusterMaxSplits && (int64_t)T * (H / 16) > kTicketSlots)
         return SMLA_ERR_UNSUPPORTED;
@@ -288,6 +291,7 @@ static smla_status fwd_impl(const void *q, bool q_fp8_in, const float *q_scale_i
     a.keys_per_split = topk > 0 ? keys_per_split(topk, S, tile_keys(path)) : tile_keys(path);
     a.scale = scale;
     a.kv_fp8 = kv_dtype == SMLA_KV_FP8_E4M3;
+    a.bf16_dots = bf16_dots;
     a.q_fp8_in = q_fp8_in;
     a.q_scale_in = q_scale_in;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

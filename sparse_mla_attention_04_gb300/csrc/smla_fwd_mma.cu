@@ -31,6 +31,12 @@
 //       s_q = amax|q[t,h,:]| / 448 per (row, head); PV in fp16 with P in fp16
 //       and V = code * 2^-8 formed exactly from the code bits in registers
 //       (the 2^8 and kv_scale fold into the epilogue).
+//   fp8 cache with bf16 dots ("Enable AITER sparse MLA on gfx942, including
+//       FP8 KV", Details, "Numerics": the BF16-dots option): q stays bf16; each
+//       register of four key codes (k = 4c..4c+3) becomes two bf16 pairs
+//       code * 2^-8 (exact) feeding two bf16 m16n8k16 MMAs, with q's fragments
+//       loaded in the same order of k; the 2^8 * kv_scale folds into the
+//       logit factor. PV as for the fp8 cache.
 #include "smla_device.cuh"
 #include "smla_epilogue.cuh"
 #include "smla_internal.h"
@@ -77,9 +83,22 @@ struct Cfg {
     static_assert(kWarps * 4 * 32 * 16 >= 128 * kHeads * 4, "merge weights must fit");
 };
 
+// Four E4M3 codes (k = 4c..4c+3 of one key) as two bf16x2 words holding
+// code * 2^-8 exactly: (k0, k1) and (k2, k3), the lower k in the low half.
+__device__ __forceinline__ void e4m3x4_to_bf16x4_scaled(uint32_t w, uint32_t &lo, uint32_t &hi)
+{
+    // binary16 code * 2^-8: the sign to bit 15, exponent and mantissa to bits 14..7
+    const uint32_t h01 = ((w & 0x80u) << 8) | ((w & 0x7Fu) << 7) | ((w & 0x8000u) << 16) | ((w & 0x7F00u) << 15);
+    const uint32_t h23 = ((w & 0x800000u) >> 8) | ((w & 0x7F0000u) >> 9) | (w & 0x80000000u) | ((w & 0x7F000000u) >> 1);
+    const float2 f01 = __half22float2(*reinterpret_cast<const __half2 *>(&h01));
+    const float2 f23 = __half22float2(*reinterpret_cast<const __half2 *>(&h23));
+    lo = pack_bf16x2(f01.x, f01.y);
+    hi = pack_bf16x2(f23.x, f23.y);
+}
+
 // q fragments (A operand) for this warp's share of the QK reduction.
-template <bool FP8, int DQK>
-__device__ __forceinline__ void load_q_frags(uint32_t (&qa)[Cfg<FP8, DQK>::KS_MAX][4],
+template <bool FP8, int DQK, bool BD = false>
+__device__ __forceinline__ void load_q_frags(uint32_t (&qa)[Cfg<FP8, DQK>::KS_MAX][BD ? 8 : 4],
                                              const __nv_bfloat16 *__restrict__ q0, // head (group base + g)
                                              const uint8_t *__restrict__ c0, // pre-quantized codes of that head, or null
                                              const float *sq, int g, int c, int ks0, int ks1)
@@ -90,7 +109,22 @@ __device__ __forceinline__ void load_q_frags(uint32_t (&qa)[Cfg<FP8, DQK>::KS_MA
     for (int i = 0; i < C::KS_MAX; ++i) {
         const int ks = ks0 + i;
         if (ks < ks1) {
-            if (FP8 && c0 != nullptr) {
+            if constexpr (BD) {
+                // bf16 q against an E4M3 key tile: for the k32 step, MMA 0 takes
+                // k = 4c..4c+3 and MMA 1 k = 16 + 4c..16 + 4c+3, in the order the
+                // key registers are split (slot 2c, 2c+1 <- 4c, 4c+1; slot 8+2c,
+                // 9+2c <- 4c+2, 4c+3)
+#pragma unroll
+                for (int mm = 0; mm < 2; ++mm) {
+                    const int d = ks * 32 + mm * 16 + 4 * c;
+                    const uint2 u0 = *reinterpret_cast<const uint2 *>(q0 + d);
+                    const uint2 u1 = *reinterpret_cast<const uint2 *>(q8 + d);
+                    qa[i][4 * mm + 0] = u0.x;
+                    qa[i][4 * mm + 1] = u1.x;
+                    qa[i][4 * mm + 2] = u0.y;
+                    qa[i][4 * mm + 3] = u1.y;
+                }
+            } else if (FP8 && c0 != nullptr) {
                 // pre-quantized q: the m16n8k32 A fragment takes 4 consecutive codes per register
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
@@ -120,12 +154,14 @@ __device__ __forceinline__ void load_q_frags(uint32_t (&qa)[Cfg<FP8, DQK>::KS_MA
                 }
             }
         } else {
-            qa[i][0] = qa[i][1] = qa[i][2] = qa[i][3] = 0u;
+#pragma unroll
+            for (int r = 0; r < (BD ? 8 : 4); ++r)
+                qa[i][r] = 0u;
         }
     }
 }
 
-template <bool FP8, int DQK>
+template <bool FP8, int DQK, bool BD = false>
 __global__ void __launch_bounds__(kThreads, 2) sparse_mla_fwd_mma_kernel(const FwdArgs a)
 {
     using C = Cfg<FP8, DQK>;
@@ -184,7 +220,9 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_fwd_mma_kernel(const F
     };
 
     // ---- q: per-head fp8 scales, then this warp's A fragments ---------------
-    if (FP8 && a.q_fp8_in) {
+    if constexpr (BD) {
+        // q stays bf16: no q scales
+    } else if (FP8 && a.q_fp8_in) {
         if (tid < kHeads) // one per-tensor scale for every head
             sq[tid] = *a.q_scale_in;
     } else if constexpr (FP8) {
@@ -215,10 +253,10 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_fwd_mma_kernel(const F
         pre[j] = fetch_idx(j);
     __syncthreads(); // sq visible
     const int ks0 = warp * C::KS / kWarps, ks1 = (warp + 1) * C::KS / kWarps;
-    uint32_t qa[C::KS_MAX][4];
+    uint32_t qa[C::KS_MAX][BD ? 8 : 4];
     const uint8_t *cg = a.q_fp8_in ? static_cast<const uint8_t *>(a.q) + (qg - static_cast<const __nv_bfloat16 *>(a.q))
                                    : nullptr; // the same row and head offset, in codes
-    load_q_frags<FP8, DQK>(qa, qg + (int64_t)g * DQK, cg ? cg + (int64_t)g * DQK : nullptr, sq, g, c, ks0, ks1);
+    load_q_frags<FP8, DQK, BD>(qa, qg + (int64_t)g * DQK, cg ? cg + (int64_t)g * DQK : nullptr, sq, g, c, ks0, ks1);
 #pragma unroll
     for (int j = 0; j < C::STAGES - 1; ++j) {
         if (j < ntiles)
@@ -228,7 +266,10 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_fwd_mma_kernel(const F
     int idx_next = pre[C::STAGES - 1];
 
     float qk_fac0 = a.scale * kLog2e, qk_fac1 = qk_fac0;
-    if constexpr (FP8) {
+    if constexpr (BD) {
+        qk_fac0 *= 256.0f * kvs; // keys entered the dots as code * 2^-8
+        qk_fac1 = qk_fac0;
+    } else if constexpr (FP8) {
         qk_fac0 *= sq[g] * kvs;
         qk_fac1 *= sq[g + 8] * kvs;
     }
@@ -264,7 +305,18 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_fwd_mma_kernel(const F
                         const int chunk = 2 * ks + (mtx & 1);
                         uint32_t b[4];
                         ldmatrix_x4(b, sbase + row * C::PITCH + chunk * 16);
-                        if constexpr (FP8) {
+                        if constexpr (BD) {
+#pragma unroll
+                            for (int nb = 0; nb < 2; ++nb) {
+#pragma unroll
+                                for (int mm = 0; mm < 2; ++mm) {
+                                    uint32_t lo, hi;
+                                    e4m3x4_to_bf16x4_scaled(b[2 * nb + mm], lo, hi);
+                                    const uint32_t(&aq)[4] = *reinterpret_cast<const uint32_t(*)[4]>(&qa[i][4 * mm]);
+                                    mma_bf16_16816(sacc[2 * nbp + nb], aq, lo, hi);
+                                }
+                            }
+                        } else if constexpr (FP8) {
                             mma_e4m3_16832(sacc[2 * nbp], qa[i], b[0], b[1]);
                             mma_e4m3_16832(sacc[2 * nbp + 1], qa[i], b[2], b[3]);
                         } else {
@@ -450,11 +502,11 @@ __global__ void __launch_bounds__(kThreads, 2) sparse_mla_fwd_mma_kernel(const F
     finish_tile<kThreads>(a, ost, lse_s, reinterpret_cast<float *>(smem + C::OFF_RED), flag_s, t, hg, s, tid);
 }
 
-template <bool FP8, int DQK>
+template <bool FP8, int DQK, bool BD = false>
 cudaError_t launch_one(const FwdArgs &a, cudaStream_t stream)
 {
     using C = Cfg<FP8, DQK>;
-    auto kern = sparse_mla_fwd_mma_kernel<FP8, DQK>;
+    auto kern = sparse_mla_fwd_mma_kernel<FP8, DQK, BD>;
     // The shared-memory opt-in is per function and per device: set it on the
     // first launch on each device (before any stream capture of that device).
     static std::atomic<uint64_t> attr_done{0};
@@ -496,6 +548,8 @@ cudaError_t launch_one(const FwdArgs &a, cudaStream_t stream)
 
 cudaError_t launch_fwd_mma(const FwdArgs &a, cudaStream_t stream)
 {
+    if (a.kv_fp8 && a.bf16_dots)
+        return a.D_qk == 512 ? launch_one<true, 512, true>(a, stream) : launch_one<true, 576, true>(a, stream);
     if (a.kv_fp8)
         return a.D_qk == 512 ? launch_one<true, 512>(a, stream) : launch_one<true, 576>(a, stream);
     return a.D_qk == 512 ? launch_one<false, 512>(a, stream) : launch_one<false, 576>(a, stream);

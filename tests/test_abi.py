@@ -87,7 +87,8 @@ def test_argument_checks_return_before_any_launch(L):
     assert _call(L, kvd=0, dot=2) == b.SMLA_ERR_BAD_DTYPE            # fp8 dots need an fp8 cache
     assert _call(L, H=8) == b.SMLA_ERR_UNSUPPORTED
     assert _call(L, Dqk=256, Dv=256) == b.SMLA_ERR_UNSUPPORTED
-    assert _call(L, kvd=1, kvs=0x5000, dot=0) == b.SMLA_ERR_UNSUPPORTED
+    assert _call(L, kvd=1, kvs=0x5000, dot=0, q=0x1002) == b.SMLA_ERR_MISALIGNED  # bf16 dots over fp8: accepted
+    assert _call(L, kvd=1, kvs=0x5000, dot=1, T=0) == b.SMLA_OK
     assert _call(L, splits=129) == b.SMLA_ERR_UNSUPPORTED
     assert _call(L, q=0x1002) == b.SMLA_ERR_MISALIGNED
     assert _call(L, out=0x4008) == b.SMLA_ERR_MISALIGNED
