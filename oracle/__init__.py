@@ -75,6 +75,11 @@ def _load():
             c.c_int, c.c_int, c.c_int, c.c_int, c.c_int64, c.c_int,
             c.c_float, c.c_void_p, c.c_void_p, c.c_int]
         lib.oracle_sparse_mla_qf64.restype = c.c_int64
+        lib.oracle_sparse_mla_sinks.argtypes = [
+            c.c_void_p, c.c_void_p, c.c_void_p, c.c_int, c.c_float, c.c_void_p,
+            c.c_int, c.c_int, c.c_int, c.c_int, c.c_int64, c.c_int,
+            c.c_float, c.c_int, c.c_void_p, c.c_void_p, c.c_void_p, c.c_int]
+        lib.oracle_sparse_mla_sinks.restype = c.c_int64
         lib.oracle_rope_f64.argtypes = [c.c_void_p, c.c_int, c.c_void_p, c.c_void_p, c.c_int, c.c_void_p]
         lib.oracle_rope_f64.restype = None
         lib.oracle_fused_qk_rope_cache.argtypes = [
@@ -158,7 +163,7 @@ def fp8_quantize(src, kv_scale) -> np.ndarray:
 
 def sparse_mla(q, kv, indices, scale: float, *, kv_fp8: bool = False,
                kv_scale: float = 1.0, D_v: int = 512, q_mode: int = 0,
-               nthreads: int = 0):
+               nthreads: int = 0, sinks=None):
     """Exact (fp64) sparse MLA forward.
 
     q        bf16 [T, H, D_qk] (torch bf16 tensor or uint16 bits)
@@ -180,15 +185,23 @@ def sparse_mla(q, kv, indices, scale: float, *, kv_fp8: bool = False,
     topk = idx.shape[1]
     out = np.empty((T, H, D_v), dtype=np.float64)
     lse = np.empty((T, H), dtype=np.float64)
-    bad = _load().oracle_sparse_mla(
-        _ptr(qb), _ptr(kvb), 1 if kv_fp8 else 0, float(np.float32(kv_scale)), _ptr(idx),
-        T, H, D_qk, D_v, kvb.shape[0], topk, float(np.float32(scale)), int(q_mode),
-        _ptr(out), _ptr(lse), int(nthreads))
+    if sinks is None:
+        bad = _load().oracle_sparse_mla(
+            _ptr(qb), _ptr(kvb), 1 if kv_fp8 else 0, float(np.float32(kv_scale)), _ptr(idx),
+            T, H, D_qk, D_v, kvb.shape[0], topk, float(np.float32(scale)), int(q_mode),
+            _ptr(out), _ptr(lse), int(nthreads))
+    else:
+        sk = np.ascontiguousarray(sinks.cpu().numpy() if hasattr(sinks, "cpu") else sinks, dtype=np.float32)
+        assert sk.shape == (H,)
+        bad = _load().oracle_sparse_mla_sinks(
+            _ptr(qb), None, _ptr(kvb), 1 if kv_fp8 else 0, float(np.float32(kv_scale)), _ptr(idx),
+            T, H, D_qk, D_v, kvb.shape[0], topk, float(np.float32(scale)), int(q_mode), _ptr(sk),
+            _ptr(out), _ptr(lse), int(nthreads))
     return out, lse, int(bad)
 
 
 def sparse_mla_q8(q8, q_scale, kv, indices, scale: float, *, kv_fp8: bool = True,
-                  kv_scale: float = 1.0, D_v: int = 512, nthreads: int = 0):
+                  kv_scale: float = 1.0, D_v: int = 512, nthreads: int = 0, sinks=None):
     """Exact (fp64) sparse MLA forward with a pre-quantized q: uint8 E4M3 codes
     [T, H, D_qk] and one per-tensor scale; q enters the dots as code * q_scale
     (the oracle's own codec, exact in fp64). kv, indices, returns as sparse_mla."""
@@ -208,9 +221,17 @@ def sparse_mla_q8(q8, q_scale, kv, indices, scale: float, *, kv_fp8: bool = True
     topk = idx.shape[1]
     out = np.empty((T, H, D_v), dtype=np.float64)
     lse = np.empty((T, H), dtype=np.float64)
-    bad = _load().oracle_sparse_mla_qf64(
-        _ptr(qf), _ptr(kvb), 1 if kv_fp8 else 0, float(np.float32(kv_scale)), _ptr(idx),
-        T, H, D_qk, D_v, kvb.shape[0], topk, float(np.float32(scale)), _ptr(out), _ptr(lse), int(nthreads))
+    if sinks is None:
+        bad = _load().oracle_sparse_mla_qf64(
+            _ptr(qf), _ptr(kvb), 1 if kv_fp8 else 0, float(np.float32(kv_scale)), _ptr(idx),
+            T, H, D_qk, D_v, kvb.shape[0], topk, float(np.float32(scale)), _ptr(out), _ptr(lse), int(nthreads))
+    else:
+        sk = np.ascontiguousarray(sinks.cpu().numpy() if hasattr(sinks, "cpu") else sinks, dtype=np.float32)
+        assert sk.shape == (H,)
+        bad = _load().oracle_sparse_mla_sinks(
+            None, _ptr(qf), _ptr(kvb), 1 if kv_fp8 else 0, float(np.float32(kv_scale)), _ptr(idx),
+            T, H, D_qk, D_v, kvb.shape[0], topk, float(np.float32(scale)), 0, _ptr(sk),
+            _ptr(out), _ptr(lse), int(nthreads))
     return out, lse, int(bad)
 
 

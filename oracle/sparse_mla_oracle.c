@@ -53,6 +53,13 @@
  * device computes it in. A position outside [0, max_position) leaves the
  * token's outputs unwritten; slot -1 skips the cache row.
  *
+ * Attention sinks ("Enable AITER sparse MLA on gfx942, including FP8 KV",
+ * Limitations: sinks are passed through; the page gives no formula). Reading:
+ * a per-head sink logit, in the units of scale * q.k, joins the softmax
+ * denominator and has no value row: out = sum_i e^{s_i} v_i / (e^{sink} +
+ * sum_j e^{s_j}), lse = log(e^{sink} + sum_j e^{s_j}); a row with no valid
+ * index gives out = 0 and lse = sink.
+ *
  * Build: gcc -O2 -fopenmp -shared -fPIC (no fast-math; IEEE semantics needed).
  */
 #include <math.h>
@@ -364,7 +371,7 @@ static double kv_value(const void *kv, int kv_is_fp8, double kv_scale,
 static int64_t sparse_mla_core(const uint16_t *q, const double *qf, const void *kv, int kv_is_fp8,
                                float kv_scale, const int32_t *indices,
                                int T, int H, int D_qk, int D_v, int64_t num_slots,
-                               int topk, float scale, int q_mode,
+                               int topk, float scale, int q_mode, const float *sinks,
                                double *out, double *lse, int nthreads);
 
 int64_t oracle_sparse_mla(const uint16_t *q, const void *kv, int kv_is_fp8,
@@ -374,7 +381,20 @@ int64_t oracle_sparse_mla(const uint16_t *q, const void *kv, int kv_is_fp8,
                           double *out, double *lse, int nthreads)
 {
     return sparse_mla_core(q, NULL, kv, kv_is_fp8, kv_scale, indices, T, H, D_qk, D_v, num_slots, topk, scale,
-                           q_mode, out, lse, nthreads);
+                           q_mode, NULL, out, lse, nthreads);
+}
+
+/* The forward with per-head sink logits sinks[H] (see the reading above);
+ * sinks == NULL is the plain forward. q as in oracle_sparse_mla (q != NULL)
+ * or as fp64 values (qf != NULL). */
+int64_t oracle_sparse_mla_sinks(const uint16_t *q, const double *qf, const void *kv, int kv_is_fp8,
+                                float kv_scale, const int32_t *indices,
+                                int T, int H, int D_qk, int D_v, int64_t num_slots,
+                                int topk, float scale, int q_mode, const float *sinks,
+                                double *out, double *lse, int nthreads)
+{
+    return sparse_mla_core(q, qf, kv, kv_is_fp8, kv_scale, indices, T, H, D_qk, D_v, num_slots, topk, scale,
+                           q_mode, sinks, out, lse, nthreads);
 }
 
 /*
@@ -389,13 +409,13 @@ int64_t oracle_sparse_mla_qf64(const double *qf, const void *kv, int kv_is_fp8,
                                int topk, float scale, double *out, double *lse, int nthreads)
 {
     return sparse_mla_core(NULL, qf, kv, kv_is_fp8, kv_scale, indices, T, H, D_qk, D_v, num_slots, topk, scale,
-                           0, out, lse, nthreads);
+                           0, NULL, out, lse, nthreads);
 }
 
 static int64_t sparse_mla_core(const uint16_t *q, const double *qf, const void *kv, int kv_is_fp8,
                                float kv_scale, const int32_t *indices,
                                int T, int H, int D_qk, int D_v, int64_t num_slots,
-                               int topk, float scale, int q_mode,
+                               int topk, float scale, int q_mode, const float *sinks,
                                double *out, double *lse, int nthreads)
 {
     int64_t bad = 0;
@@ -450,10 +470,12 @@ static int64_t sparse_mla_core(const uint16_t *q, const double *qf, const void *
                 }
                 sel[n++] = j;
             }
+            /* the head's sink logit (-inf: none) */
+            const double sink = sinks ? (double)sinks[th % H] : -INFINITY;
             if (n == 0) {
                 for (int d = 0; d < D_v; ++d)
                     orow[d] = 0.0;
-                lse[th] = -INFINITY;
+                lse[th] = sink;
                 continue;
             }
 
@@ -467,8 +489,10 @@ static int64_t sparse_mla_core(const uint16_t *q, const double *qf, const void *
                 if (s[i] > m)
                     m = s[i];
             }
-            /* softmax normaliser and lse */
-            double l = 0.0;
+            /* softmax normaliser (the sink joins it) and lse */
+            if (sink > m)
+                m = sink;
+            double l = (sink == -INFINITY) ? 0.0 : exp(sink - m);
             for (int i = 0; i < n; ++i)
                 l += exp(s[i] - m);
             lse[th] = m + log(l);

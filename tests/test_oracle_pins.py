@@ -359,3 +359,53 @@ def test_prequantized_q_equals_bf16_path_and_scales_out(oracle_mod):
     assert (o1 == o2).all() and (l1 == l2).all()
     o3, l3, _ = oracle_mod.sparse_mla_q8(q8, 0.25 * 8, codes_kv, idx, 0.2 / 8, kv_fp8=True, kv_scale=0.5, D_v=D)
     assert (o3 == o1).all() and (l3 == l1).all()
+
+
+# --------------------------------------------------------------------------
+# attention sinks (a per-head logit in the softmax denominator)
+# --------------------------------------------------------------------------
+
+def test_sinks_against_textbook_softmax(oracle_mod):
+    """softmax over [s_1..s_n, sink] with the sink's value row zero."""
+    T, H, Dqk, Dv, N, K = 2, 4, 96, 64, 64, 24
+    q = rand_bf16((T, H, Dqk), 31)
+    kv = rand_bf16((N, Dqk), 32)
+    rng = np.random.default_rng(33)
+    idx = np.stack([rng.choice(N, K, replace=False) for _ in range(T)]).astype(np.int32)
+    sinks = np.array([-1.5, 0.0, 2.0, 7.0], dtype=np.float32)   # from negligible to dominant
+    out, lse, _ = oracle_mod.sparse_mla(q, kv, idx, 0.1, D_v=Dv, sinks=sinks)
+    qv, kvv = bf16_values(bf16_bits(q)), bf16_values(bf16_bits(kv))
+    for t in range(T):
+        for h in range(H):
+            s = f32(0.1) * (kvv[idx[t], :Dqk] @ qv[t, h])
+            z = np.concatenate([s, [float(sinks[h])]])
+            e = np.exp(z - z.max())
+            p = e / e.sum()
+            np.testing.assert_allclose(out[t, h], p[:-1] @ kvv[idx[t], :Dv], rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(lse[t, h], z.max() + np.log(e.sum()), rtol=1e-13)
+
+
+def test_sinks_special_cases(oracle_mod):
+    """-inf sinks change nothing; one key gives v * sigmoid(s - sink); an empty
+    row gives 0 and lse = sink."""
+    T, H, D, N = 3, 2, 64, 40
+    q = rand_bf16((T, H, D), 34)
+    kv = rand_bf16((N, D), 35)
+    rng = np.random.default_rng(36)
+    idx = np.stack([rng.choice(N, 10, replace=False) for _ in range(T)]).astype(np.int32)
+    o0, l0, _ = oracle_mod.sparse_mla(q, kv, idx, 0.2, D_v=D)
+    o1, l1, _ = oracle_mod.sparse_mla(q, kv, idx, 0.2, D_v=D, sinks=np.full(H, -np.inf, np.float32))
+    assert (o0 == o1).all() and (l0 == l1).all()
+    one = np.full((T, 10), -1, dtype=np.int32)
+    one[:, 0] = idx[:, 0]
+    one[2, 0] = -1                                        # row 2: empty
+    sinks = np.array([0.7, -0.4], dtype=np.float32)
+    o, l, _ = oracle_mod.sparse_mla(q, kv, one, 0.2, D_v=D, sinks=sinks)
+    qv, kvv = bf16_values(bf16_bits(q)), bf16_values(bf16_bits(kv))
+    for t in range(2):
+        for h in range(H):
+            s = f32(0.2) * (kvv[one[t, 0]] @ qv[t, h])
+            sig = 1.0 / (1.0 + math.exp(float(sinks[h]) - s))
+            np.testing.assert_allclose(o[t, h], kvv[one[t, 0]][:D] * sig, rtol=1e-12, atol=1e-14)
+            np.testing.assert_allclose(l[t, h], np.logaddexp(s, float(sinks[h])), rtol=1e-13)
+    assert (o[2] == 0).all() and (l[2] == sinks.astype(np.float64)).all()
