@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--rotations", type=int, default=0, help="index/q sets (0 = enough for 4x L2)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sinks", action="store_true",
+                    help="give every head a sink logit (seeded, uniform in [-2, 4])")
     ap.add_argument("--bf16-dots", action="store_true",
                     help="E4M3 workloads: keep q in bf16 and dot it with the cache values (dot_precision bf16)")
     ap.add_argument("--q8", action="store_true",
@@ -264,6 +266,10 @@ def run_ours(args):
         if not w.kv_fp8 or args.q8:
             raise SystemExit("--bf16-dots needs an E4M3 workload and a bf16 q")
         dot = "bf16"
+    sinks = None
+    if args.sinks:
+        g = np.random.default_rng(args.seed + 7)
+        sinks = torch.from_numpy(g.uniform(-2.0, 4.0, w.H).astype(np.float32)).to(dev)
     if args.q8:
         if not w.kv_fp8:
             raise SystemExit("--q8 needs an E4M3 workload")
@@ -284,10 +290,10 @@ def run_ours(args):
         s = sets[i % R]
         if args.q8:
             binding.sparse_mla_fwd_q8(s["q8"], s["qs"], cache, s["idx"], w.scale, kv_scale=kvs, D_v=w.D_v,
-                                      out=out, lse=lse, workspace=ws, num_splits=splits, stream=stream)
+                                      out=out, lse=lse, workspace=ws, num_splits=splits, stream=stream, sinks=sinks)
         else:
             binding.sparse_mla_fwd(s["q"], cache, s["idx"], w.scale, kv_scale=kvs, dot_precision=dot, D_v=w.D_v,
-                                   out=out, lse=lse, workspace=ws, num_splits=splits, stream=stream)
+                                   out=out, lse=lse, workspace=ws, num_splits=splits, stream=stream, sinks=sinks)
 
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 3)):
@@ -340,8 +346,9 @@ def run_ours(args):
 
     if rank == 0:
         line = {
-            "metric": "sparse MLA fwd gathered-KV GB/s (%s%s)" % (
-                w.name, ", pre-quantized q" if args.q8 else (", bf16 dots" if args.bf16_dots else "")),
+            "metric": "sparse MLA fwd gathered-KV GB/s (%s%s%s)" % (
+                w.name, ", pre-quantized q" if args.q8 else (", bf16 dots" if args.bf16_dots else ""),
+                ", sinks" if args.sinks else ""),
             "value": round(gbs, 2),
             "unit": "GB/s",
             "n_gpus": world,

@@ -177,6 +177,45 @@ SMLA_API smla_status sparse_mla_fwd(const void *q, const void *kv_cache, int kv_
                                     int num_splits, smla_stream_t stream);
 
 /*
+ * The forward with every option in one versioned structure (set `size` to
+ * sizeof(smla_fwd_params)); the fields mean what sparse_mla_fwd's arguments
+ * mean, plus:
+ *   q_scale  NULL for a bf16 q; else q holds E4M3 codes [T, H, D_qk] with this
+ *            per-tensor scale (as sparse_mla_fwd_q8: an E4M3 cache, fp8 dots;
+ *            dot_precision AUTO or FP8, else SMLA_ERR_BAD_DTYPE).
+ *   sinks    NULL, or device float [H], 4-byte aligned: per-head attention
+ *            sink logits [P1 Limitations: sinks are passed through], in the
+ *            units of scale * q.k. The sink joins each row's softmax
+ *            denominator and has no value row:
+ *              out = sum_i e^{s_i} v_i / (e^{sink_h} + sum_j e^{s_j}),
+ *              lse = log(e^{sink_h} + sum_j e^{s_j});
+ *            a row with no valid index gives out = 0 and lse = sink_h.
+ */
+typedef struct smla_fwd_params {
+    size_t size;
+    const void *q;
+    const float *q_scale;
+    const void *kv_cache;
+    int kv_dtype;
+    const float *kv_scale;
+    const int32_t *indices;
+    int T, H, D_qk, D_v;
+    int64_t num_slots;
+    int topk;
+    float scale;
+    int dot_precision;
+    const float *sinks;
+    void *out;
+    float *lse;
+    void *workspace;
+    size_t workspace_bytes;
+    int num_splits;
+    smla_stream_t stream;
+} smla_fwd_params;
+
+SMLA_API smla_status sparse_mla_fwd_ex(const smla_fwd_params *params);
+
+/*
  * The same forward with a pre-quantized q [P1 Details, "FP8 KV on gfx942":
  * gfx950 keeps the pre-quantized q]: q8 holds E4M3 codes [T, H, D_qk] (as
  * written, for example, by smla_fused_qk_rope_cache with an E4M3 q_out) and

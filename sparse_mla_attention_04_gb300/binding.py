@@ -50,6 +50,7 @@ SIGNATURES = {
     "sparse_mla_fwd_q8": ([_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
                            _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int64, _c.c_int, _c.c_float,
                            _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_size_t, _c.c_int, _c.c_void_p], _c.c_int),
+    "sparse_mla_fwd_ex": ([_c.c_void_p], _c.c_int),
     "smla_compute_fp8_scale": ([_c.c_void_p, _c.c_int64, _c.c_void_p, _c.c_void_p], _c.c_int),
     "smla_fp8_cache_write": ([_c.c_void_p, _c.c_void_p, _c.c_int64, _c.c_int, _c.c_void_p,
                               _c.c_void_p, _c.c_int64, _c.c_void_p], _c.c_int),
@@ -67,6 +68,18 @@ SIGNATURES = {
                                  _c.c_float, _c.c_int, _c.c_void_p, _c.c_void_p, _c.c_int,
                                  _c.c_void_p], _c.c_int),
 }
+
+
+
+class SmlaFwdParams(ctypes.Structure):
+    """smla_fwd_params of include/sparse_mla.h."""
+    _fields_ = [("size", _c.c_size_t), ("q", _c.c_void_p), ("q_scale", _c.c_void_p),
+                ("kv_cache", _c.c_void_p), ("kv_dtype", _c.c_int), ("kv_scale", _c.c_void_p),
+                ("indices", _c.c_void_p), ("T", _c.c_int), ("H", _c.c_int), ("D_qk", _c.c_int), ("D_v", _c.c_int),
+                ("num_slots", _c.c_int64), ("topk", _c.c_int), ("scale", _c.c_float), ("dot_precision", _c.c_int),
+                ("sinks", _c.c_void_p), ("out", _c.c_void_p), ("lse", _c.c_void_p), ("workspace", _c.c_void_p),
+                ("workspace_bytes", _c.c_size_t), ("num_splits", _c.c_int), ("stream", _c.c_void_p)]
+
 
 _lock = threading.Lock()
 _lib = None
@@ -171,8 +184,10 @@ def sparse_mla_fwd(q: torch.Tensor, kv_cache: torch.Tensor, indices: torch.Tenso
                    kv_scale: Optional[torch.Tensor] = None, dot_precision: str = "auto",
                    D_v: int = 512, out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                    return_lse: bool = True, workspace: Optional[torch.Tensor] = None,
-                   num_splits: int = 0, stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
-    """out[T,H,D_v] (bf16), lse[T,H] (fp32) of the sparse MLA forward.
+                   num_splits: int = 0, stream=None,
+                   sinks: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """out[T,H,D_v] (bf16), lse[T,H] (fp32) of the sparse MLA forward
+    (sinks: optional fp32 [H] per-head sink logits).
 
     q bf16 [T,H,D_qk]; kv_cache [num_slots, D_qk] bf16 or torch.float8_e4m3fn/uint8
     (E4M3 codes, then kv_scale: fp32 device scalar); indices int32 [T, topk].
@@ -210,19 +225,34 @@ def sparse_mla_fwd(q: torch.Tensor, kv_cache: torch.Tensor, indices: torch.Tenso
     if workspace is None:
         workspace = workspace_for(need, q.device, sh)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib().sparse_mla_fwd(
-        _ptr(q), _ptr(kv_cache), kv_dtype, _ptr(kv_scale), _ptr(indices),
-        T, H, D_qk, D_v, kv_cache.shape[0], topk, float(scale), _DOT[dot_precision],
-        _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, int(num_splits), sh)
-    _check(st, "sparse_mla_fwd")
+    if sinks is None:
+        st = lib().sparse_mla_fwd(
+            _ptr(q), _ptr(kv_cache), kv_dtype, _ptr(kv_scale), _ptr(indices),
+            T, H, D_qk, D_v, kv_cache.shape[0], topk, float(scale), _DOT[dot_precision],
+            _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, int(num_splits), sh)
+        _check(st, "sparse_mla_fwd")
+    else:
+        _need(sinks, "sinks", torch.float32, 1)
+        if sinks.shape[0] != H:
+            raise ValueError("sinks must be [H]")
+        _fwd_ex(q, None, kv_cache, kv_dtype, kv_scale, indices, T, H, D_qk, D_v, topk, scale,
+                _DOT[dot_precision], sinks, out, lse, workspace, ws_bytes, num_splits, sh)
     return out, lse
+
+
+def _fwd_ex(q, q_scale, kv_cache, kv_dtype, kv_scale, indices, T, H, D_qk, D_v, topk, scale, dot, sinks,
+            out, lse, workspace, ws_bytes, num_splits, sh):
+    p = SmlaFwdParams(ctypes.sizeof(SmlaFwdParams), _ptr(q), _ptr(q_scale), _ptr(kv_cache), kv_dtype,
+                      _ptr(kv_scale), _ptr(indices), T, H, D_qk, D_v, kv_cache.shape[0], topk, float(scale), dot,
+                      _ptr(sinks), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, int(num_splits), sh)
+    _check(lib().sparse_mla_fwd_ex(ctypes.byref(p)), "sparse_mla_fwd_ex")
 
 
 def sparse_mla_fwd_q8(q8: torch.Tensor, q_scale: torch.Tensor, kv_cache: torch.Tensor, indices: torch.Tensor,
                       scale: float, *, kv_scale: torch.Tensor, D_v: int = 512, out: Optional[torch.Tensor] = None,
                       lse: Optional[torch.Tensor] = None, return_lse: bool = True,
                       workspace: Optional[torch.Tensor] = None, num_splits: int = 0,
-                      stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+                      stream=None, sinks: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """The forward with a pre-quantized q: q8 E4M3 codes [T, H, D_qk] (uint8 or
     float8_e4m3fn) and q_scale, its per-tensor fp32 device scalar; an E4M3 cache
     with kv_scale; fp8 dots."""
@@ -253,11 +283,18 @@ def sparse_mla_fwd_q8(q8: torch.Tensor, q_scale: torch.Tensor, kv_cache: torch.T
     if workspace is None:
         workspace = workspace_for(need, q8.device, sh)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib().sparse_mla_fwd_q8(
-        _ptr(q8), _ptr(q_scale), _ptr(kv_cache), _ptr(kv_scale), _ptr(indices),
-        T, H, D_qk, D_v, kv_cache.shape[0], topk, float(scale),
-        _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, int(num_splits), sh)
-    _check(st, "sparse_mla_fwd_q8")
+    if sinks is None:
+        st = lib().sparse_mla_fwd_q8(
+            _ptr(q8), _ptr(q_scale), _ptr(kv_cache), _ptr(kv_scale), _ptr(indices),
+            T, H, D_qk, D_v, kv_cache.shape[0], topk, float(scale),
+            _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, int(num_splits), sh)
+        _check(st, "sparse_mla_fwd_q8")
+    else:
+        _need(sinks, "sinks", torch.float32, 1)
+        if sinks.shape[0] != H:
+            raise ValueError("sinks must be [H]")
+        _fwd_ex(q8, q_scale, kv_cache, SMLA_KV_FP8_E4M3, kv_scale, indices, T, H, D_qk, D_v, topk, scale,
+                SMLA_DOT_FP8, sinks, out, lse, workspace, ws_bytes, num_splits, sh)
     return out, lse
 
 

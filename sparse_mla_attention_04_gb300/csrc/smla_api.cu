@@ -207,7 +207,7 @@ static smla_status fwd_impl(const void *q, bool q_fp8_in, const float *q_scale_i
                             int kv_dtype, const float *kv_scale, const int32_t *indices, int T, int H, int D_qk,
                             int D_v, int64_t num_slots, int topk, float scale, int dot_precision, void *out,
                             float *lse, void *workspace, size_t workspace_bytes, int num_splits,
-                            smla_stream_t stream)
+                            smla_stream_t stream, const float *sinks = nullptr)
 {
     // 1. pointers
     if (kv_cache == nullptr || ((q == nullptr || out == nullptr) && T > 0) ||
@@ -235,7 +235,7 @@ static smla_status fwd_impl(const void *q, bool q_fp8_in, const float *q_scale_i
     // 5. alignment
     if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(indices, 4) ||
         (lse != nullptr && !aligned(lse, 4)) || (kv_scale != nullptr && !aligned(kv_scale, 4)) ||
-        (q_scale_in != nullptr && !aligned(q_scale_in, 4)))
+        (q_scale_in != nullptr && !aligned(q_scale_in, 4)) || (sinks != nullptr && !aligned(sinks, 4)))
         return SMLA_ERR_MISALIGNED;
     if (T == 0)
         return SMLA_OK;
@@ -292,6 +292,7 @@ static smla_status fwd_impl(const void *q, bool q_fp8_in, const float *q_scale_i
     a.scale = scale;
     a.kv_fp8 = kv_dtype == SMLA_KV_FP8_E4M3;
     a.bf16_dots = bf16_dots;
+    a.sinks = sinks;
     a.q_fp8_in = q_fp8_in;
     a.q_scale_in = q_scale_in;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -313,6 +314,21 @@ SMLA_API smla_status sparse_mla_fwd(const void *q, const void *kv_cache, int kv_
 {
     return fwd_impl(q, false, nullptr, kv_cache, kv_dtype, kv_scale, indices, T, H, D_qk, D_v, num_slots, topk,
                     scale, dot_precision, out, lse, workspace, workspace_bytes, num_splits, stream);
+}
+
+SMLA_API smla_status sparse_mla_fwd_ex(const smla_fwd_params *p)
+{
+    if (p == nullptr)
+        return SMLA_ERR_NULL_POINTER;
+    if (p->size < sizeof(smla_fwd_params))
+        return SMLA_ERR_BAD_SHAPE; // a caller built against a different layout
+    const bool q8 = p->q_scale != nullptr;
+    if (q8 && (p->kv_dtype != SMLA_KV_FP8_E4M3 ||
+               (p->dot_precision != SMLA_DOT_AUTO && p->dot_precision != SMLA_DOT_FP8)))
+        return SMLA_ERR_BAD_DTYPE; // E4M3 q codes are dotted in fp8 with an E4M3 cache
+    return fwd_impl(p->q, q8, p->q_scale, p->kv_cache, p->kv_dtype, p->kv_scale, p->indices, p->T, p->H, p->D_qk,
+                    p->D_v, p->num_slots, p->topk, p->scale, q8 ? SMLA_DOT_FP8 : p->dot_precision, p->out, p->lse,
+                    p->workspace, p->workspace_bytes, p->num_splits, p->stream, p->sinks);
 }
 
 SMLA_API smla_status sparse_mla_fwd_q8(const void *q8, const float *q_scale, const void *kv_cache,

@@ -7,6 +7,12 @@
 // distributed shared memory (LSE weights). With more splits the partials go
 // to the workspace and the split that draws the last ticket (one atomic; no
 // spinning) merges them.
+//
+// Attention sinks: a per-head sink logit (natural-log units, like the lse)
+// joins the softmax denominator once per row: with one split the staged
+// output is scaled by 1 / (1 + e^{sink - lse}) and the lse becomes
+// log(e^lse + e^sink); with several, the sink enters the merge's total as a
+// partial with no output.
 #pragma once
 
 #include "smla_device.cuh"
@@ -26,19 +32,34 @@ __device__ __forceinline__ void finish_tile(const FwdArgs &a, float *ost, const 
     const int G = a.H / kHeads;
     const int hbase = hg * kHeads;
     __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out) + ((int64_t)t * a.H + hbase) * kDv;
+    // the row's sink logit of head `h` of this group (-inf: none)
+    auto sink = [&](int h) { return a.sinks != nullptr ? a.sinks[hbase + h] : -INFINITY; };
     if (a.S == 1) {
+        if (a.sinks != nullptr) {
+            if (tid < kHeads) {
+                const float l = lse_s[tid], sk = sink(tid);
+                const float M = fmaxf(l, sk);
+                // e^lse / (e^lse + e^sink), and the lse with the sink
+                const float el = l == -INFINITY ? 0.f : expf(l - M), es = sk == -INFINITY ? 0.f : expf(sk - M);
+                wts[tid] = el + es > 0.f ? el / (el + es) : 0.f;
+                if (a.lse != nullptr)
+                    a.lse[(int64_t)t * a.H + hbase + tid] = M == -INFINITY ? -INFINITY : M + logf(el + es);
+            }
+            __syncthreads();
+        }
         for (int e = tid; e < kHeads * kDv / 8; e += kThreads) {
             const int h = e / (kDv / 8), d = (e % (kDv / 8)) * 8;
+            const float f = a.sinks != nullptr ? wts[h] : 1.0f;
             const float4 x = *reinterpret_cast<const float4 *>(ost + h * kDv + d);
             const float4 y = *reinterpret_cast<const float4 *>(ost + h * kDv + d + 4);
             uint4 u;
-            u.x = pack_bf16x2(x.x, x.y);
-            u.y = pack_bf16x2(x.z, x.w);
-            u.z = pack_bf16x2(y.x, y.y);
-            u.w = pack_bf16x2(y.z, y.w);
+            u.x = pack_bf16x2(x.x * f, x.y * f);
+            u.y = pack_bf16x2(x.z * f, x.w * f);
+            u.z = pack_bf16x2(y.x * f, y.y * f);
+            u.w = pack_bf16x2(y.z * f, y.w * f);
             *reinterpret_cast<uint4 *>(out + (int64_t)h * kDv + d) = u;
         }
-        if (a.lse != nullptr && tid < kHeads)
+        if (a.sinks == nullptr && a.lse != nullptr && tid < kHeads)
             a.lse[(int64_t)t * a.H + hbase + tid] = lse_s[tid];
         return;
     }
@@ -54,11 +75,12 @@ __device__ __forceinline__ void finish_tile(const FwdArgs &a, float *ost, const 
 #pragma unroll
             for (int j = 0; j < kClusterMaxSplits; ++j)
                 lj[j] = j < a.S ? *cluster.map_shared_rank(lse_s + tid, j) : -INFINITY;
-            float mx = -INFINITY;
+            const float sk = sink(tid);
+            float mx = sk;
 #pragma unroll
             for (int j = 0; j < kClusterMaxSplits; ++j)
                 mx = fmaxf(mx, lj[j]);
-            float tot = 0.f;
+            float tot = (mx == -INFINITY || sk == -INFINITY) ? 0.f : expf(sk - mx); // the sink: no output
 #pragma unroll
             for (int j = 0; j < kClusterMaxSplits; ++j) {
                 lj[j] = (mx == -INFINITY || j >= a.S) ? 0.f : expf(lj[j] - mx);
@@ -142,10 +164,11 @@ __device__ __forceinline__ void finish_tile(const FwdArgs &a, float *ost, const 
 
     // ---- last CTA of the row: LSE merge of the S partials ----
     if (tid < kHeads) {
-        float mx = -INFINITY;
+        const float sk = sink(tid);
+        float mx = sk;
         for (int j = 0; j < a.S; ++j)
             mx = fmaxf(mx, __ldcg(a.part_lse + ((int64_t)t * a.S + j) * a.H + hbase + tid));
-        float tot = 0.f;
+        float tot = (mx == -INFINITY || sk == -INFINITY) ? 0.f : expf(sk - mx); // the sink: no output
         for (int j = 0; j < a.S; ++j) {
             const float lj = __ldcg(a.part_lse + ((int64_t)t * a.S + j) * a.H + hbase + tid);
             const float e = (mx == -INFINITY) ? 0.f : expf(lj - mx);

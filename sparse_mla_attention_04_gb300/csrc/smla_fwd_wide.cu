@@ -530,9 +530,23 @@ __global__ void __launch_bounds__(512, 1)
         if (ntiles > 0) // the last PV (and every earlier one) is done
             wait_bar(p_empty((ntiles - 1) & 1), (uint32_t)(((ntiles - 1) >> 1) & 1));
         umma::fence_after_sync();
-        alpha_s[h] = l > 0.f ? kvs / l : 0.f; // output factor per head
-        if (half == 0 && a.lse != nullptr)
-            a.lse[(int64_t)t * a.H + hg * kHeads + h] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+        {
+            // output factor and lse per head; a sink logit (base-2 units sk) joins the
+            // denominator: l 2^m_ref + 2^sk, taken relative to M = max(m_ref, sk)
+            const float sk = a.sinks != nullptr ? a.sinks[hg * kHeads + h] * kLog2e : -INFINITY;
+            float f = 0.f, lse_h = -INFINITY;
+            if (l > 0.f) {
+                const float M = fmaxf(m_ref, sk);
+                const float lt = l * exp2f(m_ref - M) + (sk == -INFINITY ? 0.f : exp2f(sk - M));
+                f = kvs * exp2f(m_ref - M) / lt;
+                lse_h = (M + log2f(lt)) * kLn2;
+            } else if (sk != -INFINITY) {
+                lse_h = sk * kLn2; // no valid key: the sink alone
+            }
+            alpha_s[h] = f; // output factor per head
+            if (half == 0 && a.lse != nullptr)
+                a.lse[(int64_t)t * a.H + hg * kHeads + h] = lse_h;
+        }
         umma::named_bar(1, 128);
         // thread = value dim 128 mb + 32 warp + lane; columns = heads
         __nv_bfloat16 *obase = static_cast<__nv_bfloat16 *>(a.out) + ((int64_t)t * a.H + hg * kHeads) * kDv +

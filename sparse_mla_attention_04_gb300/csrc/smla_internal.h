@@ -30,6 +30,7 @@ struct FwdArgs {
     int keys_per_split;     // multiple of the key tile
     float scale;
     bool kv_fp8;            // E4M3 cache with fp8 QK dots
+    const float *sinks;     // [H] per-head sink logits (natural-log units), or nullptr
     bool bf16_dots;         // E4M3 cache with bf16 q . dequantized K dots (warp-MMA kernel)
     bool q_fp8_in;          // q holds E4M3 codes [T, H, D_qk] with one per-tensor scale
     const float *q_scale_in; // that scale (device scalar), or nullptr

@@ -123,3 +123,21 @@ def test_binding_rejects_strided_and_wrong_dtypes():
         b._need(q.float(), "q", torch.bfloat16, 3)
     with pytest.raises(ValueError):
         b._need(q, "q", torch.bfloat16, 3)   # not a CUDA tensor
+
+
+def test_fwd_ex_structure_size_and_checks(L):
+    """The ctypes structure matches the header's size check; the checks run
+    before any launch (fake pointers, T = 0 or failing checks)."""
+    import ctypes
+    from sparse_mla_attention_04_gb300 import binding as b
+    p = b.SmlaFwdParams(ctypes.sizeof(b.SmlaFwdParams), 0x1000, None, 0x2000, 0, None, 0x3000, 0, 16, 512, 512,
+                        100, 8, 0.1, 0, None, 0x4000, None, None, 0, 1, None)
+    assert L.sparse_mla_fwd_ex(ctypes.byref(p)) == b.SMLA_OK           # T = 0: a no-op
+    p.size = 8
+    assert L.sparse_mla_fwd_ex(ctypes.byref(p)) == b.SMLA_ERR_BAD_SHAPE
+    p.size = ctypes.sizeof(b.SmlaFwdParams)
+    p.T, p.q_scale = 2, 0x5000                                          # E4M3 q codes with a bf16 cache
+    assert L.sparse_mla_fwd_ex(ctypes.byref(p)) == b.SMLA_ERR_BAD_DTYPE
+    p.q_scale, p.sinks = None, 0x6002                                   # misaligned sinks
+    assert L.sparse_mla_fwd_ex(ctypes.byref(p)) == b.SMLA_ERR_MISALIGNED
+    assert L.sparse_mla_fwd_ex(None) == b.SMLA_ERR_NULL_POINTER
