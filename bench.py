@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--rotations", type=int, default=0, help="index/q sets (0 = enough for 4x L2)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="the per-call sweep: rows x fan-out grid (H=16, D=512, bf16), automatic vs fixed splits")
     ap.add_argument("--sinks", action="store_true",
                     help="give every head a sink logit (seeded, uniform in [-2, 4])")
     ap.add_argument("--bf16-dots", action="store_true",
@@ -762,8 +764,88 @@ def producer_reference(args, ql, qp, kc, kp, pos, slots, cs, ns, cfg, cpu_leg: b
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# ----------------------------------------------------------------------------
+# the per-call sweep (rows x fan-out), automatic split plan against fixed ones
+# ----------------------------------------------------------------------------
+
+SWEEP_ROWS = (2, 16, 256, 512, 1024, 2048, 16384)
+SWEEP_FANOUT = (128, 512, 2048)
+SWEEP_SPLITS = (1, 2, 3, 4, 6, 8, 16)
+SWEEP_POOL = 2 * 1024 * 1024
+
+
+def run_sweep(args):
+    """Per-call device time over the grid the pages measure per call (16 heads,
+    D=512, bf16 cache; each row gathers `fan-out` uniform random slots of a
+    shared 2M-slot pool), for the automatic split plan and for fixed split
+    counts; reports where the plan is not the fastest."""
+    from sparse_mla_attention_04_gb300 import binding
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    H, D = 16, 512
+    scale = 1.0 / math.sqrt(D)
+    pool = inputs.normal_bf16((SWEEP_POOL, D), 11, dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    stream = torch.cuda.Stream(device=dev)
+    points = []
+    for rows in SWEEP_ROWS:
+        q = inputs.normal_bf16((rows, H, D), 12 + rows, dev)
+        out = torch.empty((rows, H, D), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((rows, H), dtype=torch.float32, device=dev)
+        for fan in SWEEP_FANOUT:
+            g = torch.Generator(device=dev)
+            g.manual_seed(rows * 7919 + fan)
+            # uniform random slots per row (a duplicate, rare here, counts with multiplicity)
+            idx = torch.randint(0, SWEEP_POOL, (rows, fan), generator=g, device=dev)
+            idx = idx.to(torch.int32).contiguous()
+            auto_s = binding.smla_plan_num_splits(rows, H, D, fan, 0, sms)
+            choices = sorted(set(SWEEP_SPLITS) | {auto_s})
+            times = {}
+            for S in choices:
+                try:
+                    need = binding.sparse_mla_fwd_workspace_size(rows, H, D, D, fan, 0, S)
+                except binding.SmlaError:
+                    continue   # more than 8 splits need rows * H / 16 <= 4096
+                ws = torch.zeros(max(need, 1), dtype=torch.uint8, device=dev)
+
+                def call():
+                    binding.sparse_mla_fwd(q, pool, idx, scale, out=out, lse=lse, workspace=ws, num_splits=S,
+                                           stream=stream)
+                with torch.cuda.stream(stream):
+                    for _ in range(3):
+                        call()
+                    stream.synchronize()
+                    reps = max(3, min(50, int(2e9 / max(1, rows * fan * D * 2))))
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    for _ in range(reps):
+                        call()
+                    b.record(stream)
+                b.synchronize()
+                times[S] = a.elapsed_time(b) / reps * 1000.0
+            best = min(times, key=times.get)
+            points.append({"rows": rows, "fanout": fan, "auto_splits": auto_s,
+                           "us_auto": round(times[auto_s], 2), "best_splits": best,
+                           "us_best": round(times[best], 2),
+                           "auto_over_best": round(times[auto_s] / times[best], 3),
+                           "us_by_splits": {str(k): round(v, 2) for k, v in times.items()},
+                           "gbs_auto": round(rows * fan * D * 2 / (times[auto_s] * 1e-6) / 1e9, 1)})
+    worst = max(points, key=lambda p: p["auto_over_best"])
+    line = {"metric": "sparse MLA fwd per-call time sweep (H=16, D=512, bf16)", "unit": "us",
+            "higher_is_better": False, "n_gpus": 1, "points": points,
+            "auto_over_best_worst": worst["auto_over_best"], "worst_point": [worst["rows"], worst["fanout"]],
+            "config": {"workload": "sweep", "rows": list(SWEEP_ROWS), "fanout": list(SWEEP_FANOUT),
+                       "splits_tried": list(SWEEP_SPLITS), "pool_slots": SWEEP_POOL,
+                       "timing": "CUDA events around repeated calls on one stream after 3 warm-up calls"}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.workload == "producer":
         run_producer(args)
         return

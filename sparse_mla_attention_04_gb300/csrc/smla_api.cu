@@ -81,8 +81,16 @@ Path choose_path(int H, int D_qk, int D_v, bool kv_fp8)
 int ctas_per_sm(Path p) { return p == Path::Mma ? 2 : 1; }
 int tile_keys(Path p) { return p == Path::Umma16 ? smla::kUmma16TileKeys : smla::kMmaTileKeys; }
 
-// A split keeps at least this many keys.
-constexpr int kMinKeysPerSplit = 64;
+// Split plan, from the per-call sweep (rows {2..16K} x fan-out {128, 512,
+// 2048}, 16 heads, bf16): a split keeps at least two key tiles (128 keys);
+// the automatic plan stays within one cluster merge (up to 8 splits: the
+// workspace merge of more splits cost up to 2x at 2 rows x 2048 keys); and
+// 8-CTA clusters, fast when few (2 rows), were slower than 6-CTA ones once
+// rows x splits passed 64 (16 rows: 28 us at 8 splits, 17.6 us at 6).
+constexpr int kMinKeysPerSplit = 128;
+constexpr int kAutoMaxSplits = smla::kClusterMaxSplits;
+constexpr int kWideClusterSplits = 6;
+constexpr int64_t kWideClusterRowSplits = 64;
 using smla::kClusterMaxSplits;
 using smla::kMaxSplits;
 using smla::kTicketSlots;
@@ -97,8 +105,10 @@ int plan_splits(int T, int H, int topk, int sm_count, Path path)
     const int64_t by_keys = topk / kMinKeysPerSplit;
     if (S > by_keys)
         S = by_keys;
-    if (S > kMaxSplits)
-        S = kMaxSplits;
+    if (S > kAutoMaxSplits)
+        S = kAutoMaxSplits;
+    if (S > kWideClusterSplits && units * S > kWideClusterRowSplits)
+        S = kWideClusterSplits;
     return S < 1 ? 1 : (int)S;
 }
 

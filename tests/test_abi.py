@@ -43,10 +43,13 @@ def test_split_plan(L):
     from sparse_mla_attention_04_gb300 import binding as b
     assert b.smla_plan_num_splits(64, 16, 512, 2048, 0, 152) == 2     # decode bf16, tcgen05 kernel: 1 CTA/SM
     assert b.smla_plan_num_splits(64, 16, 512, 2048, 1, 152) == 2     # decode fp8, tcgen05 kernel: 1 CTA/SM
-    assert b.smla_plan_num_splits(4, 16, 512, 128, 0, 152) == 2       # capped by keys per split
+    assert b.smla_plan_num_splits(4, 16, 512, 128, 0, 152) == 1       # a split keeps two key tiles
+    assert b.smla_plan_num_splits(2, 16, 512, 2048, 0, 152) == 8      # few rows: up to one 8-CTA cluster
+    assert b.smla_plan_num_splits(16, 16, 512, 2048, 0, 152) == 6     # many 8-CTA clusters: 6 instead
+    assert b.smla_plan_num_splits(16, 16, 512, 512, 0, 152) == 4      # capped by keys per split
     assert b.smla_plan_num_splits(8192, 16, 512, 2048, 0, 152) == 1   # prefill: no split
     assert b.smla_plan_num_splits(128, 128, 576, 2048, 1, 152) == 1
-    assert b.smla_plan_num_splits(1, 16, 512, 100000, 0, 152) == 128  # capped
+    assert b.smla_plan_num_splits(1, 16, 512, 100000, 0, 152) == 8    # automatic plans stay in one cluster
     assert b.smla_plan_num_splits(4, 15, 512, 128, 0, 152) == 0       # invalid H
 
 
