@@ -46,7 +46,9 @@
 //     shortens the time each stage is held. Commits signal the softmax (S
 //     full), the producers (stage empty) and the P buffers.
 //   converters (E4M3 only, warps 11-14, one per quarter of the TMEM lanes):
-//     tile i -> V^T in tensor memory buffer i%2 once PV(i-2) has read it;
+//     tile i -> V^T in tensor memory buffer i%3 once PV(i-3) has read it
+//     (three buffers: the conversion of a tile overlaps the PV of the two
+//     before it, so neither waits on the other in steady state);
 //     lane d of M-block b holds dim 128b + d, two keys per column. Each
 //     thread loads 4-byte words (4 dims of one key), transposes 4x4 bytes
 //     within its lane quad by two shuffles, converts, and stores 32 columns.
@@ -135,13 +137,14 @@ struct Cfg {
     static constexpr int OFF_MISC = OFF_ALPHA + 16 * 4; // flag, tmem address, abort
     static constexpr int OFF_MBAR = (OFF_MISC + 16 + 7) & ~7;
     // full[S], empty[S], s_full[2] (a commit per QK issuer), p_full[2], p_empty[2] (a
-    // commit per PV issuer), q_full, drain (a commit per MMA issuer), v_full[2] (E4M3:
-    // V^T buffer written)
-    static constexpr int NBAR = 2 * STAGES + 10;
-    // tensor memory: O^T 0..63, S^T 64..127; E4M3: V^T buffers at 256 + 128 v
+    // commit per PV issuer), q_full, drain (a commit per MMA issuer), v_full[3] (E4M3:
+    // V^T buffer written), v_free[3] (E4M3: a commit per PV issuer, V^T buffer read)
+    static constexpr int VBUFS = 3;
+    static constexpr int NBAR = 2 * STAGES + 8 + 2 * VBUFS;
+    // tensor memory: O^T 0..63, S^T 64..127; E4M3: V^T buffers at 128 + 128 v
     static constexpr int TMEM_COLS = FP8 ? 512 : 128;
-    static constexpr int VCOL = 256;
-    static_assert(!FP8 || VCOL + 2 * 128 <= TMEM_COLS, "two V^T buffers fit in tensor memory");
+    static constexpr int VCOL = 128;
+    static_assert(!FP8 || VCOL + VBUFS * 128 <= TMEM_COLS, "the V^T buffers fit in tensor memory");
     static constexpr int SMEM = OFF_MBAR + NBAR * 8;
     static constexpr int SMEM_ALLOC = SMEM + 1024; // the base is aligned up to 1 KB in the kernel
     static constexpr int THREADS = 32 * (FP8 ? kConverterWarp0 + 4 : kConverterWarp0);
@@ -195,6 +198,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
     const uint32_t q_full = bar0 + 8 * (2 * S_ + 6);
     const uint32_t drain = bar0 + 8 * (2 * S_ + 7);
     auto v_full = [&](int vb) { return bar0 + 8 * (2 * S_ + 8 + vb); };
+    auto v_free = [&](int vb) { return bar0 + 8 * (2 * S_ + 8 + C::VBUFS + vb); };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int s = blockIdx.x % a.S;
@@ -216,8 +220,10 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
         }
         umma::mbar_init(q_full, kProducerThreads);
         umma::mbar_init(drain, C::QK_ISSUERS + C::PV_ISSUERS);
-        for (int vb = 0; vb < 2; ++vb)
+        for (int vb = 0; vb < C::VBUFS; ++vb) {
             umma::mbar_init(v_full(vb), kConverterThreads);
+            umma::mbar_init(v_free(vb), C::PV_ISSUERS);
+        }
         umma::mbar_init_fence();
         *abort_s = 0;
     }
@@ -438,15 +444,16 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
                 for (int i = 0; i < ntiles; ++i) {
                     const int b = i & 1, st = i % S_;
                     wait_bar(p_full(b), (uint32_t)((i >> 1) & 1));
-                    if constexpr (FP8) // V^T buffer b holds tile i
-                        wait_bar(v_full(b), (uint32_t)((i >> 1) & 1));
+                    const int vb = i % C::VBUFS;
+                    if constexpr (FP8) // V^T buffer vb holds tile i
+                        wait_bar(v_full(vb), (uint32_t)((i / C::VBUFS) & 1));
                     if (*(volatile int *)abort_s)
                         break;
                     umma::fence_after_sync();
                     const uint64_t bd = umma::desc(p_s + b * 2048, 256, 128);
                     if constexpr (FP8) {
                         // V^T in tensor memory: M-block blk at +32 blk, 16 keys = 8 columns
-                        const uint32_t va = tmem + C::VCOL + 128 * b;
+                        const uint32_t va = tmem + C::VCOL + 128 * vb;
                         for (int blk = blk0; blk < blk1; ++blk)
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
@@ -466,7 +473,9 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
                     // PV(0..i): each issuer's commit covers all its earlier MMAs.
                     if constexpr (!FP8)
                         umma::commit(empty(st));
-                    umma::commit(p_empty(b)); // E4M3: also frees V^T buffer b
+                    else
+                        umma::commit(v_free(vb));
+                    umma::commit(p_empty(b));
                 }
             }
             // every MMA issued has completed before TMEM is released
@@ -486,10 +495,10 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
             const uint32_t selB = ii & 1 ? 0x3715u : 0x6240u; // interleave bytes (xor 1)
             const uint32_t tlane = (uint32_t)(32 * q4) << 16;
             for (int i = 0; i < ntiles; ++i) {
-                const int st = i % S_, vb = i & 1;
+                const int st = i % S_, vb = i % C::VBUFS;
                 wait_bar(full(st), (uint32_t)((i / S_) & 1));
-                if (i >= 2) // PV(i-2) has read V^T buffer vb
-                    wait_bar(p_empty(vb), (uint32_t)(((i - 2) >> 1) & 1));
+                if (i >= C::VBUFS) // PV(i-3) has read V^T buffer vb
+                    wait_bar(v_free(vb), (uint32_t)((i / C::VBUFS - 1) & 1));
                 const uint32_t src0 = ring + st * C::TILE;
 #pragma unroll 1
                 for (int mb = 0; mb < 4; ++mb) {
