@@ -339,7 +339,8 @@ SMLA_API smla_status smla_fp8_cache_write(const void *src, const int64_t *slot_m
  * q_out          device, [T, H, 576] bf16 or E4M3 (q_out_dtype), contiguous,
  *                16-byte aligned; must not overlap the inputs.
  * q_scale        device, one float; required for E4M3 q_out.
- * H may be 0 (cache rows only; the q pointers may then be NULL).
+ * H may be 0 (cache rows only; the q pointers may then be NULL); H above
+ * 524279 is SMLA_ERR_BAD_SHAPE.
  * A token whose position is outside [0, max_position) gets neither its q rows
  * nor its cache row, and sets bit 4 of smla_device_error; a slot >= num_slots
  * writes no row and sets bit 8. Asynchronous on `stream`.

@@ -376,6 +376,8 @@ SMLA_API smla_status smla_fused_qk_rope_cache(const void *ql_nope, int64_t ql_st
                                               int q_out_dtype, const float *q_scale, int T, int H,
                                               smla_stream_t stream)
 {
+    // a token's H + 1 rows run as blocks of 8 along the grid's y (at most 65535)
+    constexpr int kMaxProducerHeads = 65535 * 8 - 1;
     if (T < 0 || H < 0 || num_slots < 0 || max_position < 0 || ql_stride_t < 0 || ql_stride_h < 0 ||
         qpe_stride_t < 0 || qpe_stride_h < 0 || kvc_stride_t < 0 || kpe_stride_t < 0)
         return SMLA_ERR_BAD_SHAPE;
@@ -390,7 +392,7 @@ SMLA_API smla_status smla_fused_qk_rope_cache(const void *ql_nope, int64_t ql_st
         kv_cache == nullptr || (kv_dtype == SMLA_KV_FP8_E4M3 && kv_scale == nullptr) ||
         (qrows && q_out_dtype == SMLA_KV_FP8_E4M3 && q_scale == nullptr))
         return SMLA_ERR_NULL_POINTER;
-    if (max_position == 0)
+    if (max_position == 0 || H > kMaxProducerHeads)
         return SMLA_ERR_BAD_SHAPE;
     // latent rows move as 16-byte vectors, rope pairs as 4-byte words
     if (ql_stride_t % 8 != 0 || ql_stride_h % 8 != 0 || kvc_stride_t % 8 != 0 || qpe_stride_t % 2 != 0 ||

@@ -17,8 +17,10 @@
 // cosines, then the 32 sines, in binary32.
 //
 // Work: one warp per output row, i.e. per (token, head) of q_out plus one per
-// token for its cache row; a warp issues all its loads whose addresses do not
-// depend on a loaded value before using any. The 512 latent columns move as
+// token for its cache row; a block holds 8 rows of one token (blockIdx.x is
+// the token, blockIdx.y the group of 8 rows), so no index is divided. A warp
+// issues all its loads whose addresses do not depend on a loaded value before
+// using any. The 512 latent columns move as
 // 16-byte vectors (two per lane); the 64 rope columns as one rotary pair per
 // lane. Per q row 1,152 bytes are read and 1,152 (bf16) or 576 (E4M3) written.
 #include "smla_device.cuh"
@@ -80,15 +82,13 @@ __device__ __forceinline__ uint2 quant8(const uint4 v, float s, const E4m3Recip 
     return o;
 }
 
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) fused_qk_rope_cache_kernel(const ProducerArgs a)
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, 8) fused_qk_rope_cache_kernel(const ProducerArgs a)
 {
     const int lane = threadIdx.x & 31;
-    const int64_t item = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-    const int64_t items = (int64_t)a.T * (a.H + 1);
-    if (item >= items)
+    const int t = blockIdx.x;
+    const int j = blockIdx.y * kWarpsPerBlock + (threadIdx.x >> 5); // j < H: q row of head j; j == H: the cache row
+    if (j > a.H)
         return;
-    const int t = (int)(item / (a.H + 1));
-    const int j = (int)(item % (a.H + 1)); // j < H: q row of head j; j == H: the cache row
     const bool qrow = j < a.H;
     // every load whose address does not depend on a loaded value is issued
     // before any is used: the row's latent vectors, its rope pair, the position
@@ -199,13 +199,12 @@ cudaError_t launch_fused_producer(const FusedProducerArgs &f, cudaStream_t strea
     a.neox = f.is_neox;
     a.q_fp8 = f.q_out_fp8;
     a.cache_fp8 = f.cache_fp8;
-    const int64_t items = (int64_t)f.T * (f.H + 1);
-    if (items == 0)
+    if (f.T == 0)
         return cudaSuccess;
-    const int64_t blocks = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    if (blocks > INT_MAX)
+    const int64_t groups = ((int64_t)f.H + 1 + kWarpsPerBlock - 1) / kWarpsPerBlock; // rows of a token, in blocks
+    if (groups > 65535)
         return cudaErrorInvalidValue;
-    fused_qk_rope_cache_kernel<<<dim3((unsigned)blocks), dim3(kWarpsPerBlock * 32), 0, stream>>>(a);
+    fused_qk_rope_cache_kernel<<<dim3((unsigned)f.T, (unsigned)groups), dim3(kWarpsPerBlock * 32), 0, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -144,3 +144,32 @@ def test_fwd_ex_structure_size_and_checks(L):
     p.q_scale, p.sinks = None, 0x6002                                   # misaligned sinks
     assert L.sparse_mla_fwd_ex(ctypes.byref(p)) == b.SMLA_ERR_MISALIGNED
     assert L.sparse_mla_fwd_ex(None) == b.SMLA_ERR_NULL_POINTER
+
+
+def test_fused_producer_argument_checks(L):
+    """Host-side checks of smla_fused_qk_rope_cache: each bad argument is
+    refused before any launch (fake device addresses, nothing dereferenced)."""
+    from sparse_mla_attention_04_gb300 import binding as b
+
+    def call(**kw):
+        a = dict(ql=0x1000, ql_st=128 * 512, ql_sh=512, qpe=0x2000, qpe_st=128 * 64, qpe_sh=64, kvc=0x3000,
+                 kvc_st=512, kpe=0x4000, kpe_st=64, pos=0x5000, cs=0x6000, maxpos=4096, neox=1, slots=0x7000,
+                 cache=0x8000, kvdt=b.SMLA_KV_FP8_E4M3, nslots=100, kvs=0x9000, qout=0xA000,
+                 qdt=b.SMLA_KV_FP8_E4M3, qs=0xB000, T=4, H=128)
+        a.update(kw)
+        return L.smla_fused_qk_rope_cache(a["ql"], a["ql_st"], a["ql_sh"], a["qpe"], a["qpe_st"], a["qpe_sh"],
+                                          a["kvc"], a["kvc_st"], a["kpe"], a["kpe_st"], a["pos"], a["cs"],
+                                          a["maxpos"], a["neox"], a["slots"], a["cache"], a["kvdt"], a["nslots"],
+                                          a["kvs"], a["qout"], a["qdt"], a["qs"], a["T"], a["H"], None)
+
+    assert call(T=-1) == b.SMLA_ERR_BAD_SHAPE
+    assert call(H=-1) == b.SMLA_ERR_BAD_SHAPE
+    assert call(kvdt=7) == b.SMLA_ERR_BAD_DTYPE
+    assert call(T=0) == b.SMLA_OK                          # no-op, nothing launched
+    assert call(ql=None) == b.SMLA_ERR_NULL_POINTER
+    assert call(kvs=None) == b.SMLA_ERR_NULL_POINTER       # an E4M3 cache needs its scale
+    assert call(maxpos=0) == b.SMLA_ERR_BAD_SHAPE
+    assert call(H=65535 * 8) == b.SMLA_ERR_BAD_SHAPE       # H + 1 rows exceed the grid
+    assert call(ql_st=4) == b.SMLA_ERR_MISALIGNED          # latent rows move as 16-byte vectors
+    assert call(ql=0x1008) == b.SMLA_ERR_MISALIGNED
+    assert call(qpe_sh=3) == b.SMLA_ERR_MISALIGNED
