@@ -54,7 +54,7 @@ typedef enum {
     SMLA_ERR_BAD_SHAPE = 2,           /* a size is negative or inconsistent            */
     SMLA_ERR_BAD_DTYPE = 3,           /* unknown dtype / precision, or a bad pairing    */
     SMLA_ERR_MISALIGNED = 4,          /* a pointer lacks the alignment stated below    */
-    SMLA_ERR_UNSUPPORTED = 5,         /* valid arguments this build has no kernel for  */
+    SMLA_ERR_UNSUPPORTED = 5,         /* valid arguments the library has no kernel for */
     SMLA_ERR_WORKSPACE_TOO_SMALL = 6, /* workspace_bytes below the required size       */
     SMLA_ERR_CUDA = 7                 /* CUDA runtime error (device query or launch)   */
 } smla_status;
@@ -104,8 +104,8 @@ SMLA_API size_t sparse_mla_fwd_workspace_size(int T, int H, int D_qk, int D_v, i
                                               int kv_dtype, int num_splits);
 
 /*
- * Sparse MLA attention forward (north star of the build; [P1] Overview and
- * Details, [P3] per-call benchmark shapes, [P4] cache layout).
+ * Sparse MLA attention forward ([P1] Overview and Details, [P3] per-call
+ * benchmark shapes, [P4] cache layout).
  *
  * For each query row t in [0, T) and head h in [0, H):
  *   I      = { indices[t, i] : indices[t, i] != -1 }            (order free,

@@ -237,7 +237,7 @@ static smla_status fwd_impl(const void *q, bool q_fp8_in, const float *q_scale_i
     const bool fp8_dots = dot_precision == SMLA_DOT_FP8;
     if (fp8_dots && kv_dtype != SMLA_KV_FP8_E4M3)
         return SMLA_ERR_BAD_DTYPE;
-    // 4. what this build has kernels for
+    // 4. the shapes the library has kernels for
     if (!shape_supported(H, D_qk, D_v))
         return SMLA_ERR_UNSUPPORTED;
     if (num_splits > kMaxSplits)

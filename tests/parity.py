@@ -1,7 +1,7 @@
 """Helpers of the GPU parity tests: run the CUDA path through the C ABI and
 the fp64 oracle on the same seeded inputs, and compare.
 
-Tolerances (stated by the build's target and fixed here):
+Tolerances (the accuracy targets of the forward, fixed here):
   bf16 cache              : rel-L2 <= 5e-3, max-abs <= 2e-2, lse abs <= 1e-2
   fp8 dots vs the oracle on the dequantized values the kernel uses (q8 * s_q,
     code * kv_scale; q_mode=1): rel-L2 <= 5e-3, max-abs <= 2e-2, lse <= 1e-2
