@@ -94,6 +94,17 @@ def max_over_ranks(x: float, world: int, device) -> float:
     return float(t.item())
 
 
+def rank_seed(seed: int, r: int, rank: int) -> int:
+    """Seed of input set r on `rank`: every rank draws its own rows (weak scaling)."""
+    return seed + 1 + r + 1000 * rank
+
+
+def job_rate(units_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job units per second: each of `world` ranks processed
+    `units_per_rank` in the timed region, which took the slowest rank ms_max."""
+    return units_per_rank * world / (ms_max * 1e-3)
+
+
 # ----------------------------------------------------------------------------
 # measurement helpers
 # ----------------------------------------------------------------------------
@@ -235,7 +246,7 @@ def build_workload(name: str, seed: int, rotations: int, device, rank: int, ctx:
     total = 0
     r = 0
     while True:
-        s = seed + 1 + r + 1000 * rank
+        s = rank_seed(seed, r, rank)
         idx = inputs.make_indices(w, seed=s)
         q = inputs.make_q(w, seed=s, device=device)
         gathered = inputs.valid_count(idx) * w.D_qk * w.kv_bytes_per_elem
@@ -333,7 +344,7 @@ def run_ours(args):
     ms_max = max_over_ranks(ms, world, dev)
     ms_per_step = ms_max / K
     rows = sum(int((s["idx_np"] != -1).any(axis=1).sum()) for s in sets) / R   # rows with work (all, here)
-    gbs = total_bytes * world / (ms_max * 1e-3) / 1e9
+    gbs = job_rate(total_bytes, world, ms_max) / 1e9
     per_launch_bytes = total_bytes / K
     valid_per_step = [int((s["idx_np"] != -1).sum()) for s in sets]
     valid_per_launch = (reps * sum(valid_per_step) + sum(valid_per_step[:rem])) / K
@@ -373,7 +384,7 @@ def run_ours(args):
                 "parallelism": "dp%d (independent rows per GPU, no collective)" % world,
                 "timing": "CUDA graph of %d calls replayed; CUDA events on the launching stream" % R,
             },
-            "query_rows_per_s": round(rows * world / (ms_max * 1e-3 / K), 1),
+            "query_rows_per_s": round(job_rate(rows * K, world, ms_max), 1),
             "gpu_launches": K,
             "roofline": roofline(w, per_launch_bytes, valid_per_launch, ms / K * 1e-3, ncu_traffic(w.name)),
             "clocks": clk,
@@ -489,7 +500,7 @@ def run_e2e(w, cache, kvs, sets, dot, splits, dev, stream, K, world, q8=False):
     nbytes = reps * sum(s["bytes"] for s in sets) + sum(s["bytes"] for s in sets[:rem])
     h2d = sets[0][qkey].numel() * sets[0][qkey].element_size() + sets[0]["idx"].numel() * 4
     d2h = out[0].numel() * 2 + lse[0].numel() * 4
-    return {"value": round(nbytes * world / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "steps": steps,
+    return {"value": round(job_rate(nbytes, world, ms) / 1e9, 2), "unit": "GB/s", "steps": steps,
             "ms_per_step": round(ms / steps, 6), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "pipelining": "2 buffer sets; copies in and out on their own streams overlap the neighbouring "
                           "steps' calls; sequences of %d steps replayed from a CUDA graph" % G}
@@ -614,7 +625,7 @@ def run_producer(args):
     torch.cuda.set_device(dev)
     dist_init(world, "nccl")
     T, H, P = PRODUCER_T, PRODUCER_H, PRODUCER_POS
-    ql, qp, kc, kp, pos, slots, ns = inputs.producer_inputs(T, H, args.seed + 1 + 1000 * rank, P, num_slots=2 * T)
+    ql, qp, kc, kp, pos, slots, ns = inputs.producer_inputs(T, H, rank_seed(args.seed, 0, rank), P, num_slots=2 * T)
     cs = inputs.rope_cos_sin_cache(P)
     nbytes = producer_bytes(T, H, T)
     cfg = {"workload": "producer", "T": T, "H": H, "D_latent": 512, "D_rope": 64, "max_position": P,
@@ -666,7 +677,7 @@ def run_producer(args):
     clk = clocks.stop() if clocks else None
     ms = start.elapsed_time(end)
     ms_max = max_over_ranks(ms, world, dev)
-    gbs = nbytes * K * world / (ms_max * 1e-3) / 1e9
+    gbs = job_rate(nbytes * K, world, ms_max) / 1e9
     hbm, hbm_src = measured_peaks()
     per_launch = ms / K * 1e-3
     e2e = None
@@ -685,7 +696,7 @@ def run_producer(args):
             "dtype": "bf16 in, e4m3 out (binary32 rotation)",
             "data": "synthetic (seeded N(0,1) bf16 inputs, uniform positions, distinct slots)",
             "config": dict(cfg, timing="CUDA graph of %d calls replayed; CUDA events on the launching stream" % G),
-            "tokens_per_s": round(T * K * world / (ms_max * 1e-3), 1),
+            "tokens_per_s": round(job_rate(T * K, world, ms_max), 1),
             "gpu_launches": K,
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
                          "frac": round(achieved / hbm, 4), "traffic": ncu_traffic("producer"),
@@ -720,7 +731,7 @@ def producer_e2e(binding, host_in, d, cache, q_out, kvs, qs, stream, nbytes, wor
     ms = max_over_ranks(a.elapsed_time(b), world, dev)
     h2d = sum(x.numel() * x.element_size() for x in hin)
     d2h = hout.numel() * hout.element_size()
-    return {"value": round(nbytes * steps * world / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "steps": steps,
+    return {"value": round(job_rate(nbytes * steps, world, ms) / 1e9, 2), "unit": "GB/s", "steps": steps,
             "ms_per_step": round(ms / steps, 6), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
