@@ -23,6 +23,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -204,13 +205,21 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+def _code_only(text: str) -> str:
+    """C/CUDA source without comments, trailing blanks or empty lines (a
+    comment-only edit leaves the kernels, and so their counters, unchanged)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(ln.rstrip() for ln in text.splitlines() if ln.strip())
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_mla_attention_04_gb300", "csrc")
     for n in sorted(os.listdir(csrc)):
         if n.endswith((".cu", ".cuh", ".h")):
             h.update(n.encode())
-            h.update(open(os.path.join(csrc, n), "rb").read())
+            h.update(_code_only(open(os.path.join(csrc, n), encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -28,7 +28,7 @@
 // E4M3 (kind::f8f6f4) on the gathered tile and the logits are scaled by
 // scale * s_q * kv_scale. PV needs 16-bit operands of one type, so four
 // converter warps turn each tile's values into binary16 (exact) and write
-// V^T straight into tensor memory (double-buffered), where PV reads its A
+// V^T straight into tensor memory (three buffers), where PV reads its A
 // operand; P is kept in fp16 and kv_scale is applied with 1/l. Keeping V^T
 // out of shared memory matters: a binary16 copy there costs 128 KB of
 // shared-memory traffic per 32 KB tile, more than the rest of the tile.
