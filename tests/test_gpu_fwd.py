@@ -324,3 +324,20 @@ def test_large_logits_take_the_rescale_path(kernel):
     idx[0] = idx[0][np.argsort(logits0.numpy())]
     for S in (1, 2, 3):
         parity.case(w, idx=idx, kv_src=kv, q=q, num_splits=S)
+
+
+@pytest.mark.parametrize("topk", [5, 20])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_more_splits_than_keys(topk, fp8, kernel):
+    """Explicit split counts above the number of keys leave most splits empty
+    (no tile, lse -inf): the cluster merge (8), the workspace merge (16) and
+    the maximum (128) must all give the single-split result."""
+    w = inputs.Workload("split_empty", 3, 16, 512, 512, 700, topk, fp8, 1 / math.sqrt(512), "uniform", seed=topk)
+    outs = []
+    for s in (1, 8, 16, 128):
+        res, out, lse = parity.case(w, num_splits=s)
+        assert np.isfinite(out).all() and np.isfinite(lse).all()
+        outs.append(out)
+    for o in outs[1:]:
+        rel = np.linalg.norm(o - outs[0]) / np.linalg.norm(outs[0])
+        assert rel < 5e-3, rel
