@@ -66,6 +66,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--ctx", type=int, default=0,
                     help="override the per-row context (pool size) of a decode workload, for profiling")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only --workload (skip the other configurations, the ceilings and the L2 probe)")
     return ap.parse_args()
 
 
@@ -132,7 +134,7 @@ def measured_bf16_tflops():
         return FALLBACK_BF16_TFLOPS, "fallback (1.9 PFLOP/s bf16)"
 
 
-def roofline(w, per_launch_bytes, valid_per_launch, sec_per_launch, traffic):
+def roofline(w, per_launch_bytes, valid_per_launch, sec_per_launch, traffic, l2_gbs=None):
     """The bound of one launch: HBM (gathered bytes / copy bandwidth) or the
     tensor cores (QK at 2*H*D_qk and PV at 2*H*D_v FLOP per valid index, QK
     at the E4M3 rate for an fp8 cache, PV at the bf16 rate), whichever takes
@@ -144,6 +146,18 @@ def roofline(w, per_launch_bytes, valid_per_launch, sec_per_launch, traffic):
     qk_peak = bf16 * (FP8_OVER_BF16 if w.kv_fp8 else 1.0)
     t_tensor = qk_flop / (qk_peak * 1e12) + pv_flop / (bf16 * 1e12)
     t_hbm = per_launch_bytes / (hbm * 1e9)
+    if l2_gbs is not None:
+        # the pool sits in L2: the gathered bytes move L2 -> SM, bound by the
+        # L2 read bandwidth this run measured; the HBM formula rides along
+        t_l2 = per_launch_bytes / (l2_gbs * 1e9)
+        if t_l2 >= t_tensor:
+            achieved = per_launch_bytes / sec_per_launch / 1e9
+            return {"bound": "l2", "achieved": round(achieved, 2), "peak": round(l2_gbs, 1), "unit": "GB/s",
+                    "frac": round(achieved / l2_gbs, 4), "traffic": traffic,
+                    "peak_source": "measured in this run (smla_l2_read_probe: L2 -> SM streaming read)",
+                    "algorithmic_bytes_per_launch": per_launch_bytes,
+                    "hbm_formula_frac": round(per_launch_bytes / sec_per_launch / 1e9 / hbm, 4),
+                    "tensor_frac": round(t_tensor / sec_per_launch, 4)}
     if t_tensor > t_hbm:
         flop = qk_flop + pv_flop
         peak = flop / t_tensor / 1e12   # the mix's peak: fp8 QK share at 2x
@@ -275,29 +289,20 @@ def build_workload(name: str, seed: int, rotations: int, device, rank: int, ctx:
 # our arm
 # ----------------------------------------------------------------------------
 
-def run_ours(args):
-    from sparse_mla_attention_04_gb300 import binding
-    rank, world, local = dist_env()
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    dist_init(world, "nccl")
-    w, src, cache, kvs, sets, l2 = build_workload(args.workload, args.seed, args.rotations, dev, rank, args.ctx)
+def forward_setup(binding, w, cache, kvs, sets, dev, stream, args, sinks=None):
+    """Buffers, split plan and the call of one workload (call(i) runs the
+    forward on input set i % R on `stream`)."""
     R = len(sets)
     dot = "fp8" if w.kv_fp8 else "auto"
     if args.bf16_dots:
         if not w.kv_fp8 or args.q8:
             raise SystemExit("--bf16-dots needs an E4M3 workload and a bf16 q")
         dot = "bf16"
-    sinks = None
-    if args.sinks:
-        g = np.random.default_rng(args.seed + 7)
-        sinks = torch.from_numpy(g.uniform(-2.0, 4.0, w.H).astype(np.float32)).to(dev)
     if args.q8:
         if not w.kv_fp8:
             raise SystemExit("--q8 needs an E4M3 workload")
         for s in sets:   # q quantized once per set, outside the timed region, by the library's kernels
             s["q8"], s["qs"] = quantize_q_per_tensor(binding, s["q"])
-    stream = torch.cuda.Stream(device=dev)
     T, H = w.T, w.H
     out = torch.empty((T, H, w.D_v), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((T, H), dtype=torch.float32, device=dev)
@@ -316,9 +321,13 @@ def run_ours(args):
         else:
             binding.sparse_mla_fwd(s["q"], cache, s["idx"], w.scale, kv_scale=kvs, dot_precision=dot, D_v=w.D_v,
                                    out=out, lse=lse, workspace=ws, num_splits=splits, stream=stream, sinks=sinks)
+    return call, dot, splits
 
+
+def graph_of(call, R, warmup, stream):
+    """W warm-up calls, then a CUDA graph of R consecutive calls (replayed once)."""
     with torch.cuda.stream(stream):
-        for i in range(max(args.warmup, 3)):
+        for i in range(max(warmup, 3)):
             call(i)
         stream.synchronize()
         graph = torch.cuda.CUDAGraph()
@@ -327,17 +336,14 @@ def run_ours(args):
                 call(i)
         graph.replay()
         stream.synchronize()
+    return graph
 
-    K = args.steps
+
+def time_steps(graph, call, R, K, stream):
+    """Device milliseconds of exactly K calls (whole graphs, then the rest)."""
     reps, rem = divmod(K, R)
-    bytes_per_step = [s["bytes"] for s in sets]
-    total_bytes = reps * sum(bytes_per_step) + sum(bytes_per_step[:rem])
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    clocks = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
-    time.sleep(0.3 if clocks else 0)
     with torch.cuda.stream(stream):
         start.record(stream)
         for _ in range(reps):
@@ -346,10 +352,158 @@ def run_ours(args):
             call(i)
         end.record(stream)
     end.synchronize()
+    return start.elapsed_time(end)
+
+
+def time_isolated(call, stream, flush, n=9):
+    """Median device time of single calls, each after a write of a buffer
+    larger than L2 (cold L2, nothing else in flight), with CUDA events on the
+    launching stream."""
+    times = []
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            flush.zero_()
+            a.record(stream)
+            call(i)
+            b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+    return statistics.median(times)
+
+
+def ceiling_configs(row_bytes: int):
+    """(CTAs per SM, stages) pairs of the gather-ceiling sweep: for each CTA
+    count the most 64-row tiles that fit (as the probe pads its CTAs)."""
+    tile = 64 * 128 * ((row_bytes + 127) // 128)
+    out = []
+    for k in (1, 2, 3, 4):
+        st = min(8, (233472 // k - 1024 - 1024 - 256) // tile)
+        if st >= 1:
+            out.append((k, st))
+    return out
+
+
+def gather_ceiling(binding, cache, sets, stream, reps: int = 4):
+    """The pure indexed-row copy probe on this workload's own pool and index
+    sets, for 1-4 CTAs per SM: rows/s and GB/s of the valid rows."""
+    row_bytes = cache.shape[1] * cache.element_size()
+    valid = sum(int((s["idx_np"] != -1).sum()) for s in sets)
+    sms = torch.cuda.get_device_properties(cache.device).multi_processor_count
+    res = []
+    for k, st in ceiling_configs(row_bytes):
+        ck = torch.zeros(sms * k, dtype=torch.int32, device=cache.device)
+
+        def probe(i, k=k, st=st, ck=ck):
+            binding.smla_gather_probe(cache, sets[i % len(sets)]["idx"], ctas_per_sm=k, stages=st, checksum=ck,
+                                      stream=stream)
+        g = graph_of(probe, len(sets), 3, stream)
+        ms = time_steps(g, probe, len(sets), reps * len(sets), stream)
+        sec = ms * 1e-3 / reps
+        res.append({"ctas_per_sm": k, "stages": st, "rows_per_s": round(valid / sec, 1),
+                    "gbs": round(valid * row_bytes / sec / 1e9, 1)})
+    best = max(res, key=lambda r: r["gbs"])
+    return {"row_bytes": row_bytes, "best_gbs": best["gbs"], "best_rows_per_s": best["rows_per_s"],
+            "best": [best["ctas_per_sm"], best["stages"]], "sweep": res,
+            "kernel": "smla_gather_probe (TMA tile::gather4 into a shared-memory ring, 64-row tiles, no arithmetic)"}
+
+
+def l2_read_gbs(binding, dev, stream, mb: int = 32, reps: int = 16):
+    """L2 -> SM streaming read bandwidth (best of several launches over an
+    L2-resident buffer)."""
+    buf = torch.ones(mb << 18, dtype=torch.int32, device=dev)   # mb MiB
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ck = torch.zeros(sms * 4, dtype=torch.int32, device=dev)
+    best = 0.0
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for i in range(8):
+            a.record(stream)
+            binding.smla_l2_read_probe(buf, reps, sms * 4, checksum=ck, stream=stream)
+            b.record(stream)
+            b.synchronize()
+            if i >= 2:
+                best = max(best, buf.numel() * 4 * reps / (a.elapsed_time(b) * 1e-3) / 1e9)
+    return best
+
+
+def measure_config(binding, name, args, dev, stream, flush, l2_gbs):
+    """One configuration timed in this process (the same way as the headline)
+    with its roofline, isolated-launch time and gather ceiling."""
+    w, src, cache, kvs, sets, l2 = build_workload(name, args.seed, 0, dev, 0)
+    R = len(sets)
+    call, dot, splits = forward_setup(binding, w, cache, kvs, sets, dev, stream, args)
+    graph = graph_of(call, R, args.warmup, stream)
+    K = max(args.steps, 2 * R)
+    ms = time_steps(graph, call, R, K, stream)
+    reps, rem = divmod(K, R)
+    b_per = [s["bytes"] for s in sets]
+    v_per = [int((s["idx_np"] != -1).sum()) for s in sets]
+    nbytes = reps * sum(b_per) + sum(b_per[:rem])
+    nvalid = reps * sum(v_per) + sum(v_per[:rem])
+    sec = ms * 1e-3 / K
+    iso = time_isolated(call, stream, flush)
+    flop = 2.0 * w.H * (w.D_qk + w.D_v) * nvalid / K
+    ceil = gather_ceiling(binding, cache, sets, stream)
+    gbs = nbytes / K / sec / 1e9
+    entry = {
+        "config": {"workload": w.name, "T": w.T, "H": w.H, "D_qk": w.D_qk, "D_v": w.D_v, "topk": w.topk,
+                   "num_slots": w.num_slots, "kv_dtype": "e4m3" if w.kv_fp8 else "bf16", "dot_precision": dot,
+                   "context_per_row": w.ctx, "splits": splits, "rotating_sets": R,
+                   "gathered_bytes_per_call": nbytes / K},
+        "steps": K, "ms_per_call": round(ms / K, 6), "ms_isolated_launch": round(iso, 6),
+        "gathered_gbs": round(gbs, 2), "query_rows_per_s": round(w.T / sec, 1),
+        "tflops": round(flop / sec / 1e12, 2),
+        "roofline": roofline(w, nbytes / K, nvalid / K, sec, ncu_traffic(w.name),
+                             l2_gbs=l2_gbs if w.kind == "prefill" else None),
+        "gather_ceiling": ceil,
+        "frac_of_gather_ceiling": round(gbs / ceil["best_gbs"], 4),
+        "gpu_launches_per_call": 2 if (w.kind == "wide" and not args.bf16_dots) else 1,
+    }
+    if w.kind == "prefill":
+        entry["l2_bound"] = {"l2_read_gbs": round(l2_gbs, 1), "bound_ms": round(nbytes / K / (l2_gbs * 1e9) * 1e3, 4),
+                             "note": "the %.0f MiB pool is L2-resident: gathered bytes / measured L2 read bandwidth"
+                                     % (w.num_slots * w.D_qk * w.kv_bytes_per_elem / 2 ** 20)}
+    del graph, sets, cache, src, kvs
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return entry
+
+
+PER_CONFIG = ("decode_bf16", "decode_fp8", "prefill_bf16", "wide_fp8")
+
+
+def run_ours(args):
+    from sparse_mla_attention_04_gb300 import binding
+    rank, world, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist_init(world, "nccl")
+    w, src, cache, kvs, sets, l2 = build_workload(args.workload, args.seed, args.rotations, dev, rank, args.ctx)
+    R = len(sets)
+    sinks = None
+    if args.sinks:
+        g = np.random.default_rng(args.seed + 7)
+        sinks = torch.from_numpy(g.uniform(-2.0, 4.0, w.H).astype(np.float32)).to(dev)
+    stream = torch.cuda.Stream(device=dev)
+    T, H = w.T, w.H
+    call, dot, splits = forward_setup(binding, w, cache, kvs, sets, dev, stream, args, sinks)
+    graph = graph_of(call, R, args.warmup, stream)
+
+    K = args.steps
+    reps, rem = divmod(K, R)
+    bytes_per_step = [s["bytes"] for s in sets]
+    total_bytes = reps * sum(bytes_per_step) + sum(bytes_per_step[:rem])
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0) if rank == 0 else None
+    time.sleep(0.3 if clocks else 0)
+    ms = time_steps(graph, call, R, K, stream)
     torch.cuda.synchronize(dev)
     barrier(world)
     clk = clocks.stop() if clocks else None
-    ms = start.elapsed_time(end)
     ms_max = max_over_ranks(ms, world, dev)
     ms_per_step = ms_max / K
     rows = sum(int((s["idx_np"] != -1).any(axis=1).sum()) for s in sets) / R   # rows with work (all, here)
@@ -358,6 +512,12 @@ def run_ours(args):
     valid_per_step = [int((s["idx_np"] != -1).sum()) for s in sets]
     valid_per_launch = (reps * sum(valid_per_step) + sum(valid_per_step[:rem])) / K
 
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    iso = time_isolated(call, stream, flush)
+    per_config = (world == 1 and not args.no_per_config and not (args.q8 or args.bf16_dots or args.sinks)
+                  and args.ctx == 0)
+    ceil = gather_ceiling(binding, cache, sets, stream) if per_config else None
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(w, cache, kvs, sets, dot, splits, dev, stream, K, world, q8=args.q8)
@@ -365,6 +525,17 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, src, sets[0])
+
+    pcs = None
+    if per_config:
+        del graph, sets, cache, src, kvs
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+        l2_gbs = l2_read_gbs(binding, dev, stream)
+        pcs = {"l2_read_gbs": round(l2_gbs, 1)}
+        for name in PER_CONFIG:
+            if name != args.workload:
+                pcs[name] = measure_config(binding, name, args, dev, stream, flush, l2_gbs)
 
     if rank == 0:
         line = {
@@ -394,12 +565,18 @@ def run_ours(args):
                 "timing": "CUDA graph of %d calls replayed; CUDA events on the launching stream" % R,
             },
             "query_rows_per_s": round(job_rate(rows * K, world, ms_max), 1),
-            "gpu_launches": K,
+            "gpu_launches": K * (2 if (w.kind == "wide" and not args.bf16_dots) else 1),
             "roofline": roofline(w, per_launch_bytes, valid_per_launch, ms / K * 1e-3, ncu_traffic(w.name)),
+            "ms_isolated_launch": round(iso, 6),
             "clocks": clk,
             "e2e": e2e,
             "cpu_baseline": cpu,
         }
+        if ceil is not None:
+            line["gather_ceiling"] = ceil
+            line["frac_of_gather_ceiling"] = round(gbs / ceil["best_gbs"], 4)
+        if pcs is not None:
+            line["per_config"] = pcs
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -544,11 +721,11 @@ def oracle_inputs(w, src, s, rows, kvs_val):
     return q, kv_rows, remap, nbytes
 
 
-def time_oracle(w, q, kv_rows, remap, kvs_val):
+def time_oracle(w, q, kv_rows, remap, kvs_val, nthreads: int = 0):
     import oracle
     t0 = time.perf_counter()
     oracle.sparse_mla(q, kv_rows, remap, w.scale, kv_fp8=w.kv_fp8, kv_scale=kvs_val, D_v=w.D_v,
-                      q_mode=1 if w.kv_fp8 else 0)
+                      q_mode=1 if w.kv_fp8 else 0, nthreads=nthreads)
     return time.perf_counter() - t0
 
 
@@ -562,10 +739,20 @@ def cpu_baseline(w, src, s, budget_s: float = 10.0):
         el += time_oracle(w, q, kv_rows, remap, kvs_val)
         done += nbytes
         reps += 1
+    # the same oracle on one core, over a few rows of the same set
+    rows1 = list(range(min(8, w.T)))
+    q1, kv1, remap1, nbytes1 = oracle_inputs(w, src, s, rows1, kvs_val)
+    done1, el1, reps1 = 0, 0.0, 0
+    while el1 < budget_s / 4 and reps1 < 20:
+        el1 += time_oracle(w, q1, kv1, remap1, kvs_val, nthreads=1)
+        done1 += nbytes1
+        reps1 += 1
     return {"value": round(done / el / 1e9, 4), "unit": "GB/s", "cores": oracle.max_threads(),
             "kind": "oracle",
             "sample": "%d pass(es) over all %d rows of one index set (%d heads, fp64 C + OpenMP), %.1f s"
-                      % (reps, w.T, w.H, el)}
+                      % (reps, w.T, w.H, el),
+            "value_1core": round(done1 / el1 / 1e9, 4),
+            "sample_1core": "%d pass(es) over %d rows of the same set on 1 thread, %.1f s" % (reps1, len(rows1), el1)}
 
 
 def run_reference(args):

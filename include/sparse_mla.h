@@ -79,6 +79,16 @@ typedef enum {
     SMLA_DOT_FP8 = 2
 } smla_dot_precision;
 
+/* Which kernel serves a forward call (smla_fwd_params.kernel).
+ *   AUTO     : the library's choice (described under sparse_mla_fwd).
+ *   WARP_MMA : the warp-level mma.sync kernel, for every supported shape and
+ *              precision (a comparison path: slower, same results within the
+ *              stated tolerances). */
+typedef enum {
+    SMLA_KERNEL_AUTO = 0,
+    SMLA_KERNEL_WARP_MMA = 1
+} smla_kernel_choice;
+
 /* Human-readable name of a status. Never NULL. */
 SMLA_API const char *smla_status_string(int status);
 
@@ -98,8 +108,12 @@ SMLA_API int smla_plan_num_splits(int T, int H, int D_qk, int topk, int kv_dtype
 
 /* Bytes of workspace sparse_mla_fwd needs with `num_splits` splits
  * (num_splits == 0: the automatic plan for the current device, which queries
- * the device). 0 means no workspace is needed. Returns (size_t)-1 on invalid
- * arguments or a failed device query. */
+ * the device), for any dot precision the cache allows (the largest of their
+ * needs). 0 means no workspace is needed. Returns (size_t)-1 on invalid
+ * arguments or a failed device query. (The boundary's first sketch took
+ * (T, H, D_v, topk, sm_count); D_qk and kv_dtype are needed because the
+ * 128-head E4M3 kernel keeps its quantized q in the workspace, and
+ * num_splits because an explicit split count decides the merge path.) */
 SMLA_API size_t sparse_mla_fwd_workspace_size(int T, int H, int D_qk, int D_v, int topk,
                                               int kv_dtype, int num_splits);
 
@@ -160,9 +174,9 @@ SMLA_API size_t sparse_mla_fwd_workspace_size(int T, int H, int D_qk, int D_v, i
  *              call does not ask for more than one split, on a tcgen05 kernel
  *              with heads on M (two CTAs per row, each owning half of the
  *              value dims; a first pass quantizes q into the workspace); every
- *              other supported shape runs on a warp-MMA (mma.sync) kernel.
- *              Setting SMLA_KERNEL=mma in the environment routes every call to
- *              the warp-MMA kernel (a comparison and test switch).
+ *              other supported shape runs on a warp-MMA (mma.sync) kernel
+ *              (sparse_mla_fwd_ex can ask for it for any shape: its `kernel`
+ *              field).
  * num_splits   0 = automatic (smla_plan_num_splits for the current device);
  *              otherwise the number of top-k splits to use, 1..128. More than 8
  *              splits need T * H / 16 <= 4096 (else SMLA_ERR_UNSUPPORTED).
@@ -211,9 +225,17 @@ typedef struct smla_fwd_params {
     size_t workspace_bytes;
     int num_splits;
     smla_stream_t stream;
+    int kernel;          /* smla_kernel_choice (ABI 1.1; a structure of the 1.0
+                            size, without this field, means AUTO) */
 } smla_fwd_params;
 
 SMLA_API smla_status sparse_mla_fwd_ex(const smla_fwd_params *params);
+
+/* The exact workspace bytes the call described by `params` needs (its dot
+ * precision, q form, kernel choice and split count; pointers are not read).
+ * 0 = none. Returns (size_t)-1 for arguments sparse_mla_fwd_ex would reject
+ * or a failed device query. */
+SMLA_API size_t sparse_mla_fwd_ex_workspace_size(const smla_fwd_params *params);
 
 /*
  * The same forward with a pre-quantized q [P1 Details, "FP8 KV on gfx942":
@@ -247,16 +269,24 @@ SMLA_API smla_status sparse_mla_fwd_q8(const void *q8, const float *q_scale, con
  * the buffers it hands over).
  *
  * Arguments and results are those of sparse_mla_fwd; q, kv_cache, indices,
- * out and lse remain the caller's. When the split plan needs a workspace
- * (more than 8 splits of a row), the library uses a static device array of
- * SMLA_NO_ALLOC_SCRATCH_BYTES instead, and returns
- * SMLA_ERR_WORKSPACE_TOO_SMALL (nothing launched) when the call would need
- * more. Nothing is allocated or freed. The first call on a device, made with
- * that device current, looks the array's device address up once
- * (cudaGetSymbolAddress); make that first call before any stream capture.
- * Each call clears the array's merge counters on `stream` before launching.
- * All calls share the one array: calls that can run at the same time on the
- * GPU (unordered streams) race on it and must not overlap.
+ * out and lse remain the caller's. When the call's own plan needs a workspace
+ * the library uses a static device array of SMLA_NO_ALLOC_SCRATCH_BYTES
+ * instead, and returns SMLA_ERR_WORKSPACE_TOO_SMALL (nothing launched) when
+ * the call would need more. Two kinds of call need it:
+ *   - more than 8 splits of a row (merge counters, then T * S * H * 2 KB of
+ *     partial results);
+ *   - the 128-head E4M3 kernel with fp8 dots (H a multiple of 128, D_qk = 576,
+ *     one split), at any split plan: its quantized q, T * H * 580 bytes after
+ *     a 16 KB counter region. T * H must stay below about 14,400: 128 rows of
+ *     128 heads (9.5 MB) do not fit and are rejected.
+ * Calls with bf16 dots or a bf16 cache and at most 8 splits use no workspace
+ * and never touch the array. Nothing is allocated or freed. Each call looks
+ * the array's device address up (cudaGetSymbolAddress) with its device
+ * current; make a device's first call before any stream capture, since that
+ * lookup may load the module. A call that merges through the counters clears
+ * them on `stream` before launching. All calls share the one array: calls
+ * that can run at the same time on the GPU (unordered streams) race on it and
+ * must not overlap.
  */
 SMLA_API smla_status sparse_mla_fwd_no_alloc(const void *q, const void *kv_cache, int kv_dtype,
                                              const float *kv_scale, const int32_t *indices,
@@ -272,8 +302,9 @@ SMLA_API smla_status sparse_mla_fwd_no_alloc(const void *q, const void *kv_cache
  * 2 = the copies or MMAs in flight did not drain), abandons the call's
  * arithmetic, frees its tensor memory and returns, leaving the context usable.
  * smla_fused_qk_rope_cache sets 4 for a position outside [0, max_position) and
- * 8 for a slot >= num_slots. Synchronous (copies the word from the device).
- * reset != 0 clears it.
+ * 8 for a slot >= num_slots. Synchronous (copies the word from the device):
+ * unlike every other entry point it waits for the device, since the word is
+ * read on the host. reset != 0 clears it.
  */
 SMLA_API smla_status smla_device_error(int *code, int reset);
 
@@ -354,6 +385,34 @@ SMLA_API smla_status smla_fused_qk_rope_cache(const void *ql_nope, int64_t ql_st
                                               int64_t num_slots, const float *kv_scale, void *q_out,
                                               int q_out_dtype, const float *q_scale, int T, int H,
                                               smla_stream_t stream);
+
+/*
+ * Measurement kernels (not part of the forward; bench.py reports them beside
+ * the forward's rate as the ceilings it is held against).
+ *
+ * smla_gather_probe: a pure indexed-row copy at the forward kernels' gather
+ * pattern. The n_indices entries of `indices` are taken as consecutive tiles
+ * of 64 rows, split evenly over ctas_per_sm CTAs on each SM; each CTA copies
+ * its tiles' rows [idx, 0:row_bytes) of the pool [num_rows, row_bytes]
+ * (row_bytes a multiple of 16, at most 1024) into a ring of `stages` tiles in
+ * shared memory by TMA tile::gather4 (128-byte boxes, 128-byte swizzle); -1
+ * and out-of-range entries are zero-filled without a read. A consumer folds
+ * the first 4 bytes of each row into checksum[cta] (XOR, written; device
+ * uint32 [sm_count * ctas_per_sm]) and holds each tile hold_ns nanoseconds
+ * before releasing it. SMLA_ERR_UNSUPPORTED when `stages` tiles do not fit
+ * ctas_per_sm CTAs on one SM; ctas_per_sm in 1..4, stages in 1..8.
+ *
+ * smla_l2_read_probe: `blocks` blocks of 512 threads read the first `bytes`
+ * of `buf` (a multiple of 16, 16-byte aligned) `reps` times with 16-byte
+ * loads that bypass L1, and write one word per block to checksum[block]. With
+ * a buffer smaller than L2 its rate is the L2 -> SM read bandwidth.
+ */
+SMLA_API smla_status smla_gather_probe(const void *pool, int64_t num_rows, int row_bytes,
+                                       const int32_t *indices, int64_t n_indices, int ctas_per_sm,
+                                       int stages, int hold_ns, uint32_t *checksum,
+                                       smla_stream_t stream);
+SMLA_API smla_status smla_l2_read_probe(const void *buf, int64_t bytes, int reps, uint32_t *checksum,
+                                        int blocks, smla_stream_t stream);
 
 /*
  * Counts the entries of indices [T, topk] that are neither -1 nor inside

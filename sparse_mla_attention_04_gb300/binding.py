@@ -35,6 +35,9 @@ SMLA_DOT_AUTO = 0
 SMLA_DOT_BF16 = 1
 SMLA_DOT_FP8 = 2
 _DOT = {"auto": SMLA_DOT_AUTO, "bf16": SMLA_DOT_BF16, "fp8": SMLA_DOT_FP8}
+SMLA_KERNEL_AUTO = 0
+SMLA_KERNEL_WARP_MMA = 1
+_KERNEL = {"auto": SMLA_KERNEL_AUTO, "mma": SMLA_KERNEL_WARP_MMA}
 
 # every function the header declares, with its ctypes signature
 _c = ctypes
@@ -51,6 +54,10 @@ SIGNATURES = {
                            _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int64, _c.c_int, _c.c_float,
                            _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_size_t, _c.c_int, _c.c_void_p], _c.c_int),
     "sparse_mla_fwd_ex": ([_c.c_void_p], _c.c_int),
+    "sparse_mla_fwd_ex_workspace_size": ([_c.c_void_p], _c.c_size_t),
+    "smla_gather_probe": ([_c.c_void_p, _c.c_int64, _c.c_int, _c.c_void_p, _c.c_int64, _c.c_int, _c.c_int,
+                           _c.c_int, _c.c_void_p, _c.c_void_p], _c.c_int),
+    "smla_l2_read_probe": ([_c.c_void_p, _c.c_int64, _c.c_int, _c.c_void_p, _c.c_int, _c.c_void_p], _c.c_int),
     "smla_compute_fp8_scale": ([_c.c_void_p, _c.c_int64, _c.c_void_p, _c.c_void_p], _c.c_int),
     "smla_fp8_cache_write": ([_c.c_void_p, _c.c_void_p, _c.c_int64, _c.c_int, _c.c_void_p,
                               _c.c_void_p, _c.c_int64, _c.c_void_p], _c.c_int),
@@ -78,7 +85,8 @@ class SmlaFwdParams(ctypes.Structure):
                 ("indices", _c.c_void_p), ("T", _c.c_int), ("H", _c.c_int), ("D_qk", _c.c_int), ("D_v", _c.c_int),
                 ("num_slots", _c.c_int64), ("topk", _c.c_int), ("scale", _c.c_float), ("dot_precision", _c.c_int),
                 ("sinks", _c.c_void_p), ("out", _c.c_void_p), ("lse", _c.c_void_p), ("workspace", _c.c_void_p),
-                ("workspace_bytes", _c.c_size_t), ("num_splits", _c.c_int), ("stream", _c.c_void_p)]
+                ("workspace_bytes", _c.c_size_t), ("num_splits", _c.c_int), ("stream", _c.c_void_p),
+                ("kernel", _c.c_int)]
 
 
 _lock = threading.Lock()
@@ -185,9 +193,11 @@ def sparse_mla_fwd(q: torch.Tensor, kv_cache: torch.Tensor, indices: torch.Tenso
                    D_v: int = 512, out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                    return_lse: bool = True, workspace: Optional[torch.Tensor] = None,
                    num_splits: int = 0, stream=None,
-                   sinks: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+                   sinks: Optional[torch.Tensor] = None,
+                   kernel: str = "auto") -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """out[T,H,D_v] (bf16), lse[T,H] (fp32) of the sparse MLA forward
-    (sinks: optional fp32 [H] per-head sink logits).
+    (sinks: optional fp32 [H] per-head sink logits; kernel: "auto", or "mma"
+    for the warp-MMA kernel).
 
     q bf16 [T,H,D_qk]; kv_cache [num_slots, D_qk] bf16 or torch.float8_e4m3fn/uint8
     (E4M3 codes, then kv_scale: fp32 device scalar); indices int32 [T, topk].
@@ -212,6 +222,8 @@ def sparse_mla_fwd(q: torch.Tensor, kv_cache: torch.Tensor, indices: torch.Tenso
         _need(kv_scale.reshape(1), "kv_scale", torch.float32, 1)
     if dot_precision not in _DOT:
         raise ValueError("dot_precision must be one of %s" % sorted(_DOT))
+    if kernel not in _KERNEL:
+        raise ValueError("kernel must be one of %s" % sorted(_KERNEL))
     topk = indices.shape[1]
     if out is None:
         out = torch.empty((T, H, D_v), dtype=torch.bfloat16, device=q.device)
@@ -225,26 +237,28 @@ def sparse_mla_fwd(q: torch.Tensor, kv_cache: torch.Tensor, indices: torch.Tenso
     if workspace is None:
         workspace = workspace_for(need, q.device, sh)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    if sinks is None:
+    if sinks is None and kernel == "auto":
         st = lib().sparse_mla_fwd(
             _ptr(q), _ptr(kv_cache), kv_dtype, _ptr(kv_scale), _ptr(indices),
             T, H, D_qk, D_v, kv_cache.shape[0], topk, float(scale), _DOT[dot_precision],
             _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, int(num_splits), sh)
         _check(st, "sparse_mla_fwd")
     else:
-        _need(sinks, "sinks", torch.float32, 1)
-        if sinks.shape[0] != H:
-            raise ValueError("sinks must be [H]")
+        if sinks is not None:
+            _need(sinks, "sinks", torch.float32, 1)
+            if sinks.shape[0] != H:
+                raise ValueError("sinks must be [H]")
         _fwd_ex(q, None, kv_cache, kv_dtype, kv_scale, indices, T, H, D_qk, D_v, topk, scale,
-                _DOT[dot_precision], sinks, out, lse, workspace, ws_bytes, num_splits, sh)
+                _DOT[dot_precision], sinks, out, lse, workspace, ws_bytes, num_splits, sh, _KERNEL[kernel])
     return out, lse
 
 
 def _fwd_ex(q, q_scale, kv_cache, kv_dtype, kv_scale, indices, T, H, D_qk, D_v, topk, scale, dot, sinks,
-            out, lse, workspace, ws_bytes, num_splits, sh):
+            out, lse, workspace, ws_bytes, num_splits, sh, kernel=SMLA_KERNEL_AUTO):
     p = SmlaFwdParams(ctypes.sizeof(SmlaFwdParams), _ptr(q), _ptr(q_scale), _ptr(kv_cache), kv_dtype,
                       _ptr(kv_scale), _ptr(indices), T, H, D_qk, D_v, kv_cache.shape[0], topk, float(scale), dot,
-                      _ptr(sinks), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, int(num_splits), sh)
+                      _ptr(sinks), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, int(num_splits), sh,
+                      int(kernel))
     _check(lib().sparse_mla_fwd_ex(ctypes.byref(p)), "sparse_mla_fwd_ex")
 
 
@@ -252,7 +266,8 @@ def sparse_mla_fwd_q8(q8: torch.Tensor, q_scale: torch.Tensor, kv_cache: torch.T
                       scale: float, *, kv_scale: torch.Tensor, D_v: int = 512, out: Optional[torch.Tensor] = None,
                       lse: Optional[torch.Tensor] = None, return_lse: bool = True,
                       workspace: Optional[torch.Tensor] = None, num_splits: int = 0,
-                      stream=None, sinks: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+                      stream=None, sinks: Optional[torch.Tensor] = None,
+                      kernel: str = "auto") -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """The forward with a pre-quantized q: q8 E4M3 codes [T, H, D_qk] (uint8 or
     float8_e4m3fn) and q_scale, its per-tensor fp32 device scalar; an E4M3 cache
     with kv_scale; fp8 dots."""
@@ -283,19 +298,67 @@ def sparse_mla_fwd_q8(q8: torch.Tensor, q_scale: torch.Tensor, kv_cache: torch.T
     if workspace is None:
         workspace = workspace_for(need, q8.device, sh)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    if sinks is None:
+    if kernel not in _KERNEL:
+        raise ValueError("kernel must be one of %s" % sorted(_KERNEL))
+    if sinks is None and kernel == "auto":
         st = lib().sparse_mla_fwd_q8(
             _ptr(q8), _ptr(q_scale), _ptr(kv_cache), _ptr(kv_scale), _ptr(indices),
             T, H, D_qk, D_v, kv_cache.shape[0], topk, float(scale),
             _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, int(num_splits), sh)
         _check(st, "sparse_mla_fwd_q8")
     else:
-        _need(sinks, "sinks", torch.float32, 1)
-        if sinks.shape[0] != H:
-            raise ValueError("sinks must be [H]")
+        if sinks is not None:
+            _need(sinks, "sinks", torch.float32, 1)
+            if sinks.shape[0] != H:
+                raise ValueError("sinks must be [H]")
         _fwd_ex(q8, q_scale, kv_cache, SMLA_KV_FP8_E4M3, kv_scale, indices, T, H, D_qk, D_v, topk, scale,
-                SMLA_DOT_FP8, sinks, out, lse, workspace, ws_bytes, num_splits, sh)
+                SMLA_DOT_FP8, sinks, out, lse, workspace, ws_bytes, num_splits, sh, _KERNEL[kernel])
     return out, lse
+
+
+def smla_gather_probe(pool: torch.Tensor, indices: torch.Tensor, *, ctas_per_sm: int = 1, stages: int = 1,
+                      hold_ns: int = 0, checksum: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """The pure indexed-row copy probe: rows `indices` (int32, any shape,
+    taken flat) of `pool` [num_rows, row_bytes] (any 1- or 2-byte dtype)
+    gathered by TMA into shared memory and folded into per-CTA checksums
+    (uint32 device tensor [sm_count * ctas_per_sm], returned)."""
+    if pool.dim() != 2 or not pool.is_contiguous() or not pool.is_cuda:
+        raise ValueError("pool must be a contiguous CUDA tensor [num_rows, row]")
+    _need(indices.reshape(-1), "indices", torch.int32, 1)
+    row_bytes = pool.shape[1] * pool.element_size()
+    sms = torch.cuda.get_device_properties(pool.device).multi_processor_count
+    if checksum is None:
+        checksum = torch.zeros(sms * ctas_per_sm, dtype=torch.int32, device=pool.device)
+    _check(lib().smla_gather_probe(_ptr(pool), pool.shape[0], row_bytes, _ptr(indices), indices.numel(),
+                                   int(ctas_per_sm), int(stages), int(hold_ns), _ptr(checksum), _stream(stream)),
+           "smla_gather_probe")
+    return checksum
+
+
+def smla_l2_read_probe(buf: torch.Tensor, reps: int, blocks: int, checksum: Optional[torch.Tensor] = None,
+                       stream=None) -> torch.Tensor:
+    """Stream `buf` (contiguous CUDA tensor) `reps` times from `blocks` blocks."""
+    if not buf.is_contiguous() or not buf.is_cuda:
+        raise ValueError("buf must be a contiguous CUDA tensor")
+    if checksum is None:
+        checksum = torch.zeros(blocks, dtype=torch.int32, device=buf.device)
+    nbytes = buf.numel() * buf.element_size()
+    _check(lib().smla_l2_read_probe(_ptr(buf), nbytes - nbytes % 16, int(reps), _ptr(checksum), int(blocks),
+                                    _stream(stream)), "smla_l2_read_probe")
+    return checksum
+
+
+def sparse_mla_fwd_ex_workspace_size(T: int, H: int, D_qk: int, D_v: int, topk: int, kv_dtype: int, *,
+                                     dot_precision: str = "auto", q8: bool = False, num_splits: int = 0,
+                                     kernel: str = "auto") -> int:
+    """Exact workspace bytes of one call (its dot precision, q form, kernel and splits)."""
+    p = SmlaFwdParams(ctypes.sizeof(SmlaFwdParams), None, 1 if q8 else None, None, kv_dtype, None, None,
+                      T, H, D_qk, D_v, 0, topk, 1.0, _DOT[dot_precision], None, None, None, None, 0,
+                      int(num_splits), None, _KERNEL[kernel])
+    n = lib().sparse_mla_fwd_ex_workspace_size(ctypes.byref(p))
+    if n == ctypes.c_size_t(-1).value:
+        raise SmlaError(SMLA_ERR_BAD_SHAPE, "sparse_mla_fwd_ex_workspace_size")
+    return int(n)
 
 
 def smla_compute_fp8_scale(x: torch.Tensor, scale_out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:

@@ -6,9 +6,8 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstddef>
 #include <cstdint>
-#include <cstdlib>
-#include <cstring>
 
 namespace {
 
@@ -55,22 +54,12 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // Which kernel serves a call.
 enum class Path { Mma, Umma16, Wide };
 
-// SMLA_KERNEL=mma in the environment routes every shape to the warp-MMA
-// kernel (a comparison and test switch).
-bool force_mma()
-{
-    const char *v = getenv("SMLA_KERNEL");
-    return v != nullptr && strcmp(v, "mma") == 0;
-}
-
 // 16 heads with D_qk = D_v = 512 (bf16 cache, or E4M3 cache with fp8 dots):
 // the tcgen05 16-head kernel; a multiple of 128 heads with D_qk = 576,
 // D_v = 512 and an E4M3 cache: the tcgen05 128-head kernel (no split of the
 // top-k list); every other shape: the warp-MMA kernel.
 Path choose_path(int H, int D_qk, int D_v, bool kv_fp8)
 {
-    if (force_mma())
-        return Path::Mma;
     if (H == 16 && D_qk == 512 && D_v == 512)
         return Path::Umma16;
     if (H % 128 == 0 && D_qk == 576 && D_v == 512 && kv_fp8)
@@ -127,6 +116,42 @@ bool shape_supported(int H, int D_qk, int D_v)
 
 namespace smla {
 
+// The plan of one forward call whose arguments have passed the checks: the
+// kernel, the split count and the workspace layout. Queries the device's SM
+// count only for the automatic split plan (num_splits == 0).
+smla_status plan_forward(int T, int H, int D_qk, int D_v, int topk, int kv_dtype, int dot_precision,
+                         int num_splits, int kernel, FwdPlan *out)
+{
+    const bool kv_fp8 = kv_dtype == SMLA_KV_FP8_E4M3;
+    const bool bf16_dots = kv_fp8 && dot_precision != SMLA_DOT_FP8; // bf16 q . dequantized K
+    Path path = kernel == SMLA_KERNEL_WARP_MMA ? Path::Mma : choose_path(H, D_qk, D_v, kv_fp8);
+    if (path == Path::Wide && num_splits > 1)
+        path = Path::Mma; // the 128-head kernel does not split the top-k list
+    if (bf16_dots)
+        path = Path::Mma; // the warp-MMA kernel serves bf16 dots over an E4M3 cache
+    int S = num_splits;
+    if (S == 0) {
+        int sms = 0;
+        if (const cudaError_t e = current_sm_count(&sms); e != cudaSuccess)
+            return cuda_status(e);
+        S = plan_splits(T, H, topk, sms, path);
+        if (bf16_dots && S > kClusterMaxSplits)
+            S = kClusterMaxSplits; // merged in a cluster: no workspace beyond the E4M3 query's
+    }
+    if (S > kClusterMaxSplits && (int64_t)T * (H / 16) > kTicketSlots)
+        return SMLA_ERR_UNSUPPORTED;
+    out->path = static_cast<int>(path);
+    out->S = S;
+    out->bf16_dots = bf16_dots;
+    out->layout = workspace_layout(T, H, D_qk, D_v, S, path == Path::Wide);
+    out->uses_tickets = S > kClusterMaxSplits;
+    return SMLA_OK;
+}
+
+} // namespace smla
+
+namespace smla {
+
 WorkspaceLayout workspace_layout(int T, int H, int D_qk, int D_v, int S, bool wide)
 {
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
@@ -176,7 +201,7 @@ SMLA_API const char *smla_status_string(int status)
     }
 }
 
-SMLA_API int smla_version(void) { return (1 << 16) | 0; }
+SMLA_API int smla_version(void) { return (1 << 16) | 1; }
 
 SMLA_API const char *smla_last_error_string(void)
 {
@@ -195,20 +220,45 @@ SMLA_API int smla_plan_num_splits(int T, int H, int D_qk, int topk, int kv_dtype
 SMLA_API size_t sparse_mla_fwd_workspace_size(int T, int H, int D_qk, int D_v, int topk, int kv_dtype,
                                               int num_splits)
 {
-    if (T < 0 || topk < 0 || num_splits < 0 || !shape_supported(H, D_qk, D_v) ||
+    if (T < 0 || topk < 0 || num_splits < 0 || num_splits > kMaxSplits || !shape_supported(H, D_qk, D_v) ||
         (kv_dtype != SMLA_KV_BF16 && kv_dtype != SMLA_KV_FP8_E4M3))
         return (size_t)-1;
-    int S = num_splits;
-    if (S == 0) {
-        int sms = 0;
-        if (current_sm_count(&sms) != cudaSuccess)
+    // the most any dot precision valid for this cache needs
+    size_t most = 0;
+    const int dots[3] = {SMLA_DOT_AUTO, SMLA_DOT_BF16, SMLA_DOT_FP8};
+    for (int dp : dots) {
+        if (dp == SMLA_DOT_FP8 && kv_dtype != SMLA_KV_FP8_E4M3)
+            continue;
+        smla::FwdPlan pl;
+        if (smla::plan_forward(T, H, D_qk, D_v, topk, kv_dtype, dp, num_splits, SMLA_KERNEL_AUTO, &pl) != SMLA_OK)
             return (size_t)-1;
-        S = plan_splits(T, H, topk, sms, choose_path(H, D_qk, D_v, kv_dtype == SMLA_KV_FP8_E4M3));
+        if (pl.layout.total > most)
+            most = pl.layout.total;
     }
-    if (S > kMaxSplits || (S > kClusterMaxSplits && (int64_t)T * (H / 16) > kTicketSlots))
+    return most;
+}
+
+SMLA_API size_t sparse_mla_fwd_ex_workspace_size(const smla_fwd_params *p)
+{
+    if (p == nullptr || p->size < offsetof(smla_fwd_params, kernel))
         return (size_t)-1;
-    const bool wide = choose_path(H, D_qk, D_v, kv_dtype == SMLA_KV_FP8_E4M3) == Path::Wide && S == 1;
-    return smla::workspace_layout(T, H, D_qk, D_v, S, wide).total;
+    const int kernel = p->size >= sizeof(smla_fwd_params) ? p->kernel : SMLA_KERNEL_AUTO;
+    const bool q8 = p->q_scale != nullptr;
+    const int dot = q8 ? SMLA_DOT_FP8 : p->dot_precision;
+    if (p->T < 0 || p->topk < 0 || p->num_splits < 0 || p->num_splits > kMaxSplits ||
+        !shape_supported(p->H, p->D_qk, p->D_v) ||
+        (p->kv_dtype != SMLA_KV_BF16 && p->kv_dtype != SMLA_KV_FP8_E4M3) ||
+        (dot != SMLA_DOT_AUTO && dot != SMLA_DOT_BF16 && dot != SMLA_DOT_FP8) ||
+        (dot == SMLA_DOT_FP8 && p->kv_dtype != SMLA_KV_FP8_E4M3) ||
+        (kernel != SMLA_KERNEL_AUTO && kernel != SMLA_KERNEL_WARP_MMA))
+        return (size_t)-1;
+    if (p->T == 0)
+        return 0;
+    smla::FwdPlan pl;
+    if (smla::plan_forward(p->T, p->H, p->D_qk, p->D_v, p->topk, p->kv_dtype, dot, p->num_splits, kernel, &pl) !=
+        SMLA_OK)
+        return (size_t)-1;
+    return pl.layout.total;
 }
 
 // The forward for a bf16 q, or (q_fp8_in) for E4M3 codes of q with one
@@ -217,7 +267,7 @@ static smla_status fwd_impl(const void *q, bool q_fp8_in, const float *q_scale_i
                             int kv_dtype, const float *kv_scale, const int32_t *indices, int T, int H, int D_qk,
                             int D_v, int64_t num_slots, int topk, float scale, int dot_precision, void *out,
                             float *lse, void *workspace, size_t workspace_bytes, int num_splits,
-                            smla_stream_t stream, const float *sinks = nullptr)
+                            smla_stream_t stream, const float *sinks = nullptr, int kernel = SMLA_KERNEL_AUTO)
 {
     // 1. pointers
     if (kv_cache == nullptr || ((q == nullptr || out == nullptr) && T > 0) ||
@@ -242,6 +292,8 @@ static smla_status fwd_impl(const void *q, bool q_fp8_in, const float *q_scale_i
         return SMLA_ERR_UNSUPPORTED;
     if (num_splits > kMaxSplits)
         return SMLA_ERR_UNSUPPORTED;
+    if (kernel != SMLA_KERNEL_AUTO && kernel != SMLA_KERNEL_WARP_MMA)
+        return SMLA_ERR_BAD_SHAPE;
     // 5. alignment
     if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(indices, 4) ||
         (lse != nullptr && !aligned(lse, 4)) || (kv_scale != nullptr && !aligned(kv_scale, 4)) ||
@@ -250,24 +302,15 @@ static smla_status fwd_impl(const void *q, bool q_fp8_in, const float *q_scale_i
     if (T == 0)
         return SMLA_OK;
     // 6. split plan and workspace
-    const bool bf16_dots = kv_dtype == SMLA_KV_FP8_E4M3 && !fp8_dots; // bf16 q . dequantized K
-    Path path = choose_path(H, D_qk, D_v, kv_dtype == SMLA_KV_FP8_E4M3);
-    if (path == Path::Wide && num_splits > 1)
-        path = Path::Mma; // the 128-head kernel does not split the top-k list
-    if (bf16_dots)
-        path = Path::Mma; // the warp-MMA kernel serves bf16 dots over an E4M3 cache
-    int S = num_splits;
-    if (S == 0) {
-        int sms = 0;
-        if (const cudaError_t e = current_sm_count(&sms); e != cudaSuccess)
-            return cuda_status(e);
-        S = plan_splits(T, H, topk, sms, path);
-        if (bf16_dots && S > kClusterMaxSplits)
-            S = kClusterMaxSplits; // merged in a cluster: no workspace beyond the E4M3 query's
-    }
-    if (S > kClusterMaxSplits && (int64_t)T * (H / 16) > kTicketSlots)
-        return SMLA_ERR_UNSUPPORTED;
-    const smla::WorkspaceLayout wl = smla::workspace_layout(T, H, D_qk, D_v, S, path == Path::Wide);
+    smla::FwdPlan plan;
+    if (const smla_status st = smla::plan_forward(T, H, D_qk, D_v, topk, kv_dtype, dot_precision, num_splits,
+                                                  kernel, &plan);
+        st != SMLA_OK)
+        return st;
+    const Path path = static_cast<Path>(plan.path);
+    const int S = plan.S;
+    const bool bf16_dots = plan.bf16_dots;
+    const smla::WorkspaceLayout wl = plan.layout;
     if (wl.total > 0) {
         if (workspace == nullptr)
             return SMLA_ERR_NULL_POINTER;
@@ -330,15 +373,17 @@ SMLA_API smla_status sparse_mla_fwd_ex(const smla_fwd_params *p)
 {
     if (p == nullptr)
         return SMLA_ERR_NULL_POINTER;
-    if (p->size < sizeof(smla_fwd_params))
+    // callers built against ABI 1.0 pass the structure without `kernel`
+    if (p->size < offsetof(smla_fwd_params, kernel))
         return SMLA_ERR_BAD_SHAPE; // a caller built against a different layout
+    const int kernel = p->size >= sizeof(smla_fwd_params) ? p->kernel : SMLA_KERNEL_AUTO;
     const bool q8 = p->q_scale != nullptr;
     if (q8 && (p->kv_dtype != SMLA_KV_FP8_E4M3 ||
                (p->dot_precision != SMLA_DOT_AUTO && p->dot_precision != SMLA_DOT_FP8)))
         return SMLA_ERR_BAD_DTYPE; // E4M3 q codes are dotted in fp8 with an E4M3 cache
     return fwd_impl(p->q, q8, p->q_scale, p->kv_cache, p->kv_dtype, p->kv_scale, p->indices, p->T, p->H, p->D_qk,
                     p->D_v, p->num_slots, p->topk, p->scale, q8 ? SMLA_DOT_FP8 : p->dot_precision, p->out, p->lse,
-                    p->workspace, p->workspace_bytes, p->num_splits, p->stream, p->sinks);
+                    p->workspace, p->workspace_bytes, p->num_splits, p->stream, p->sinks, kernel);
 }
 
 SMLA_API smla_status sparse_mla_fwd_q8(const void *q8, const float *q_scale, const void *kv_cache,
@@ -355,14 +400,16 @@ SMLA_API smla_status smla_device_error(int *code, int reset)
 {
     if (code == nullptr)
         return SMLA_ERR_NULL_POINTER;
-    int c16 = 0, cw = 0, cp = 0;
+    int c16 = 0, cw = 0, cp = 0, cg = 0;
     if (const cudaError_t e = smla::read_umma_error(&c16, reset != 0); e != cudaSuccess)
+        return cuda_status(e);
+    if (const cudaError_t e = smla::read_probe_error(&cg, reset != 0); e != cudaSuccess)
         return cuda_status(e);
     if (const cudaError_t e = smla::read_wide_error(&cw, reset != 0); e != cudaSuccess)
         return cuda_status(e);
     if (const cudaError_t e = smla::read_producer_error(&cp, reset != 0); e != cudaSuccess)
         return cuda_status(e);
-    *code = c16 | cw | cp;
+    *code = c16 | cw | cp | cg;
     return SMLA_OK;
 }
 
@@ -457,6 +504,41 @@ SMLA_API smla_status smla_fp8_cache_write(const void *src, const int64_t *slot_m
         return SMLA_ERR_MISALIGNED;
     return cuda_status(smla::launch_fp8_cache_write(src, slot_mapping, N, D, kv_scale, kv_cache, num_slots,
                                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+SMLA_API smla_status smla_gather_probe(const void *pool, int64_t num_rows, int row_bytes, const int32_t *indices,
+                                       int64_t n_indices, int ctas_per_sm, int stages, int hold_ns,
+                                       uint32_t *checksum, smla_stream_t stream)
+{
+    if (pool == nullptr || checksum == nullptr || (indices == nullptr && n_indices > 0))
+        return SMLA_ERR_NULL_POINTER;
+    if (num_rows < 0 || n_indices < 0 || row_bytes < 16 || row_bytes > 1024 || row_bytes % 16 != 0 ||
+        ctas_per_sm < 1 || ctas_per_sm > 4 || stages < 1 || stages > 8 || hold_ns < 0)
+        return SMLA_ERR_BAD_SHAPE;
+    if (!aligned(pool, 16) || !aligned(indices, 4) || !aligned(checksum, 4))
+        return SMLA_ERR_MISALIGNED;
+    int sms = 0;
+    if (const cudaError_t e = current_sm_count(&sms); e != cudaSuccess)
+        return cuda_status(e);
+    const cudaError_t e = smla::launch_gather_probe(pool, num_rows, row_bytes, indices, n_indices, ctas_per_sm,
+                                                    stages, hold_ns, checksum, sms,
+                                                    reinterpret_cast<cudaStream_t>(stream));
+    if (e == cudaErrorInvalidValue)
+        return SMLA_ERR_UNSUPPORTED; // the stages do not fit ctas_per_sm CTAs on an SM
+    return cuda_status(e);
+}
+
+SMLA_API smla_status smla_l2_read_probe(const void *buf, int64_t bytes, int reps, uint32_t *checksum, int blocks,
+                                        smla_stream_t stream)
+{
+    if (buf == nullptr || checksum == nullptr)
+        return SMLA_ERR_NULL_POINTER;
+    if (bytes < 16 || bytes % 16 != 0 || reps < 1 || blocks < 1)
+        return SMLA_ERR_BAD_SHAPE;
+    if (!aligned(buf, 16) || !aligned(checksum, 4))
+        return SMLA_ERR_MISALIGNED;
+    return cuda_status(smla::launch_l2_read_probe(buf, bytes, reps, checksum, blocks,
+                                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
 SMLA_API smla_status smla_validate_indices(const int32_t *indices, int T, int topk, int64_t num_slots,

@@ -8,6 +8,8 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include "../../include/sparse_mla.h"
+
 namespace smla {
 
 // Everything a forward launch needs, already validated by the ABI layer.
@@ -62,6 +64,19 @@ struct WorkspaceLayout {
 };
 WorkspaceLayout workspace_layout(int T, int H, int D_qk, int D_v, int S, bool wide);
 
+// The plan of one forward call (see plan_forward in smla_api.cu).
+struct FwdPlan {
+    int path;            // the kernel that serves the call
+    int S;               // splits of each row's top-k list
+    bool bf16_dots;      // E4M3 cache with bf16 dots
+    bool uses_tickets;   // the workspace's merge counters take part (S > kClusterMaxSplits)
+    WorkspaceLayout layout;
+};
+// Plans a call whose arguments are valid; returns SMLA_OK or the status that
+// rejects it (SMLA_ERR_UNSUPPORTED, or SMLA_ERR_CUDA for a failed device query).
+smla_status plan_forward(int T, int H, int D_qk, int D_v, int topk, int kv_dtype, int dot_precision,
+                         int num_splits, int kernel, FwdPlan *out);
+
 cudaError_t launch_fwd_mma(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_fwd_wide(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_fwd_umma16(const FwdArgs &a, cudaStream_t stream);
@@ -95,6 +110,15 @@ struct FusedProducerArgs {
 };
 cudaError_t launch_fused_producer(const FusedProducerArgs &a, cudaStream_t stream);
 cudaError_t read_producer_error(int *out, bool reset);
+
+// Measurement kernels: a pure indexed-row copy at the forward kernels' gather
+// pattern, and an L2 -> SM streaming read.
+cudaError_t launch_gather_probe(const void *pool, int64_t num_rows, int row_bytes, const int32_t *indices,
+                                int64_t n_indices, int ctas_per_sm, int stages, int hold_ns, uint32_t *checksum,
+                                int sm_count, cudaStream_t stream);
+cudaError_t launch_l2_read_probe(const void *buf, int64_t bytes, int reps, uint32_t *checksum, int blocks,
+                                 cudaStream_t stream);
+cudaError_t read_probe_error(int *out, bool reset);
 
 cudaError_t launch_fp8_scale(const void *x, int64_t n, float *scale_out, int sm_count,
                              cudaStream_t stream);

@@ -5,53 +5,31 @@
 // reserved nearly all of HBM for its KV-cache pool up front has nothing left
 // to cudaMalloc from, and a host framework that loads this library as a
 // plug-in may only let it use the buffers it hands over. For them the
-// workspace that sparse_mla_fwd needs when a row's top-k list is split more
-// than 8 ways lives in a fixed array inside the library instead.
+// workspace that sparse_mla_fwd needs (the merge counters and partial results
+// when a row's top-k list is split more than 8 ways, or the quantized q of the
+// 128-head E4M3 kernel) lives in a fixed array inside the library instead.
 //
 // The array is a file-scope device variable: every GPU that loads the library
 // holds it until the process exits. Host code cannot use its name as an
-// address (it is a host-side stand-in), so the device address is looked up
-// once per device with cudaGetSymbolAddress on the first call made with that
-// device current. Each call clears the merge counters at the start of the
-// array before launching; all calls share the array, so calls that overlap
-// on the GPU (different streams, no ordering between them) race on it.
+// address (it is a host-side stand-in), so every call looks the device address
+// up with cudaGetSymbolAddress, with the call's device current (a lookup
+// cached across calls could outlive a context reset that moves the module).
+// The call's workspace need comes from the same plan the forward itself
+// makes (its dot precision and split count included), so a call that needs no
+// workspace never touches the array. A call that merges through the array's
+// counters clears them on its stream first. All calls share the array, so
+// calls that overlap on the GPU (different streams, no ordering between them)
+// race on it.
 #include "../../include/sparse_mla.h"
 #include "smla_internal.h"
 
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 namespace {
 
 constexpr size_t kScratchBytes = SMLA_NO_ALLOC_SCRATCH_BYTES;
 
 static __device__ __align__(256) unsigned char g_no_alloc_scratch[kScratchBytes];
-
-constexpr int kMaxDevices = 64;
-std::mutex g_mutex;
-void *g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (looked up once).
-cudaError_t scratch_address(void **out)
-{
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return e;
-    if (dev < 0 || dev >= kMaxDevices)
-        return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_no_alloc_scratch);
-        if (e != cudaSuccess)
-            return e;
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
-    return cudaSuccess;
-}
 
 } // namespace
 
@@ -61,24 +39,45 @@ extern "C" SMLA_API smla_status sparse_mla_fwd_no_alloc(const void *q, const voi
                                                         int dot_precision, void *out, float *lse, int num_splits,
                                                         smla_stream_t stream)
 {
-    if (T == 0 || num_splits < 0)
-        return sparse_mla_fwd(q, kv_cache, kv_dtype, kv_scale, indices, T, H, D_qk, D_v, num_slots, topk, scale,
-                              dot_precision, out, lse, nullptr, 0, num_splits, stream);
-    const size_t need = sparse_mla_fwd_workspace_size(T, H, D_qk, D_v, topk, kv_dtype, num_splits);
-    if (need == (size_t)-1) // invalid shape or plan: let the full checks report why
-        return sparse_mla_fwd(q, kv_cache, kv_dtype, kv_scale, indices, T, H, D_qk, D_v, num_slots, topk, scale,
-                              dot_precision, out, lse, nullptr, 0, num_splits, stream);
+    smla_fwd_params p{};
+    p.size = sizeof(smla_fwd_params);
+    p.q = q;
+    p.kv_cache = kv_cache;
+    p.kv_dtype = kv_dtype;
+    p.kv_scale = kv_scale;
+    p.indices = indices;
+    p.T = T;
+    p.H = H;
+    p.D_qk = D_qk;
+    p.D_v = D_v;
+    p.num_slots = num_slots;
+    p.topk = topk;
+    p.scale = scale;
+    p.dot_precision = dot_precision;
+    p.out = out;
+    p.lse = lse;
+    p.num_splits = num_splits;
+    p.stream = stream;
+    p.kernel = SMLA_KERNEL_AUTO;
+    const size_t need = sparse_mla_fwd_ex_workspace_size(&p);
+    if (need == (size_t)-1 || need == 0) // invalid (the full checks report why), or no workspace needed
+        return sparse_mla_fwd_ex(&p);
     if (need > kScratchBytes)
         return SMLA_ERR_WORKSPACE_TOO_SMALL;
+    smla::FwdPlan plan;
+    if (const smla_status st = smla::plan_forward(T, H, D_qk, D_v, topk, kv_dtype, dot_precision, num_splits,
+                                                  SMLA_KERNEL_AUTO, &plan);
+        st != SMLA_OK)
+        return st;
     void *ws = nullptr;
-    if (need > 0) {
-        if (scratch_address(&ws) != cudaSuccess)
-            return SMLA_ERR_CUDA;
-        // the merge counters must start at zero whatever an earlier call left
-        if (cudaMemsetAsync(ws, 0, (size_t)smla::kTicketSlots * sizeof(int),
-                            reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-            return SMLA_ERR_CUDA;
-    }
-    return sparse_mla_fwd(q, kv_cache, kv_dtype, kv_scale, indices, T, H, D_qk, D_v, num_slots, topk, scale,
-                          dot_precision, out, lse, ws, need > 0 ? kScratchBytes : 0, num_splits, stream);
+    if (cudaGetSymbolAddress(&ws, g_no_alloc_scratch) != cudaSuccess)
+        return SMLA_ERR_CUDA;
+    // merge counters must start at zero whatever an earlier call left there
+    if (plan.uses_tickets &&
+        cudaMemsetAsync(ws, 0, (size_t)smla::kTicketSlots * sizeof(int), reinterpret_cast<cudaStream_t>(stream)) !=
+            cudaSuccess)
+        return SMLA_ERR_CUDA;
+    p.workspace = ws;
+    p.workspace_bytes = kScratchBytes;
+    return sparse_mla_fwd_ex(&p);
 }

@@ -44,10 +44,20 @@ def oracle_cache(kv_src_cpu: torch.Tensor, fp8: bool):
     return oracle.fp8_quantize(kv_src_cpu, s), float(s)
 
 
-def run_gpu(q, cache, kvs, idx, scale, *, fp8: bool, num_splits: int = 0, D_v: int = 512):
+def fwd(kernel, *args, **kw):
+    """binding.sparse_mla_fwd on the named kernel ("auto" or "mma")."""
+    return binding.sparse_mla_fwd(*args, kernel=kernel, **kw)
+
+
+def fwd_q8(kernel, *args, **kw):
+    """binding.sparse_mla_fwd_q8 on the named kernel ("auto" or "mma")."""
+    return binding.sparse_mla_fwd_q8(*args, kernel=kernel, **kw)
+
+
+def run_gpu(q, cache, kvs, idx, scale, *, fp8: bool, num_splits: int = 0, D_v: int = 512, kernel: str = "auto"):
     dot = "fp8" if fp8 else "auto"
     out, lse = binding.sparse_mla_fwd(q, cache, idx, scale, kv_scale=kvs, dot_precision=dot, D_v=D_v,
-                                      num_splits=num_splits)
+                                      num_splits=num_splits, kernel=kernel)
     torch.cuda.synchronize()
     return out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
 
@@ -76,7 +86,7 @@ def compare(out, lse, ref_o, ref_l, tol, what=""):
 
 
 def case(w: inputs.Workload, *, num_splits=0, idx=None, kv_src=None, q=None, check_mirror=True,
-         check_plain=True):
+         check_plain=True, kernel: str = "auto"):
     """Run workload `w` (small enough for the whole-pool oracle) on both sides.
 
     For an E4M3 cache the plain comparison (oracle with unquantized q, the
@@ -89,7 +99,7 @@ def case(w: inputs.Workload, *, num_splits=0, idx=None, kv_src=None, q=None, che
     idx = inputs.make_indices(w) if idx is None else idx
     cache, kvs = gpu_cache(kv_src.to(DEV), w.kv_fp8)
     out, lse = run_gpu(q.to(DEV), cache, kvs, torch.from_numpy(idx).to(DEV), w.scale,
-                       fp8=w.kv_fp8, num_splits=num_splits, D_v=w.D_v)
+                       fp8=w.kv_fp8, num_splits=num_splits, D_v=w.D_v, kernel=kernel)
     ocache, oscale = oracle_cache(kv_src, w.kv_fp8)
     ref_o, ref_l, _ = oracle.sparse_mla(q, ocache, idx, w.scale, kv_fp8=w.kv_fp8, kv_scale=oscale, D_v=w.D_v)
     res = {}

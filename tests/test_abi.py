@@ -173,3 +173,38 @@ def test_fused_producer_argument_checks(L):
     assert call(ql_st=4) == b.SMLA_ERR_MISALIGNED          # latent rows move as 16-byte vectors
     assert call(ql=0x1008) == b.SMLA_ERR_MISALIGNED
     assert call(qpe_sh=3) == b.SMLA_ERR_MISALIGNED
+
+
+def test_probe_host_checks(L):
+    """The measurement kernels reject bad arguments before any launch."""
+    from sparse_mla_attention_04_gb300 import binding as b
+    P = 1 << 12   # fake, never dereferenced: every call below fails its host checks
+    lib = b.lib()
+    assert lib.smla_gather_probe(None, 10, 1024, P, 64, 1, 1, 0, P, None) == b.SMLA_ERR_NULL_POINTER
+    assert lib.smla_gather_probe(P, 10, 1000, P, 64, 1, 1, 0, P, None) == b.SMLA_ERR_BAD_SHAPE   # not 16-byte rows
+    assert lib.smla_gather_probe(P, 10, 2048, P, 64, 1, 1, 0, P, None) == b.SMLA_ERR_BAD_SHAPE   # > 1 KB rows
+    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 5, 1, 0, P, None) == b.SMLA_ERR_BAD_SHAPE   # > 4 CTAs/SM
+    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 1, 9, 0, P, None) == b.SMLA_ERR_BAD_SHAPE   # > 8 stages
+    assert lib.smla_gather_probe(P + 8, 10, 1024, P, 64, 1, 1, 0, P, None) == b.SMLA_ERR_MISALIGNED
+    assert lib.smla_l2_read_probe(P, 1000, 1, P, 4, None) == b.SMLA_ERR_BAD_SHAPE
+    assert lib.smla_l2_read_probe(None, 1024, 1, P, 4, None) == b.SMLA_ERR_NULL_POINTER
+
+
+def test_exact_workspace_follows_the_call(L):
+    """The exact per-call workspace query follows the dot precision: the
+    128-head E4M3 kernel (fp8 dots) keeps its quantized q in the workspace,
+    bf16 dots over the same cache run on the warp-MMA kernel with none."""
+    from sparse_mla_attention_04_gb300 import binding as b
+    fp8 = b.sparse_mla_fwd_ex_workspace_size(128, 128, 576, 512, 2048, 1, dot_precision="fp8", num_splits=1)
+    bd = b.sparse_mla_fwd_ex_workspace_size(128, 128, 576, 512, 2048, 1, dot_precision="bf16", num_splits=1)
+    q8 = b.sparse_mla_fwd_ex_workspace_size(128, 128, 576, 512, 2048, 1, q8=True, num_splits=1)
+    mma = b.sparse_mla_fwd_ex_workspace_size(128, 128, 576, 512, 2048, 1, dot_precision="fp8", num_splits=1,
+                                             kernel="mma")
+    assert fp8 == q8 == b.sparse_mla_fwd_workspace_size(128, 128, 576, 512, 2048, 1, 1) > (8 << 20)
+    assert bd == 0 and mma == 0
+    # more than 8 splits: counters and partials whatever the dot precision
+    for dp in ("auto", "fp8"):
+        assert b.sparse_mla_fwd_ex_workspace_size(4, 16, 512, 512, 2048, 1, dot_precision=dp, num_splits=16) == \
+            b.sparse_mla_fwd_workspace_size(4, 16, 512, 512, 2048, 1, 16)
+    with pytest.raises(b.SmlaError):
+        b.sparse_mla_fwd_ex_workspace_size(4, 16, 512, 512, 2048, 0, dot_precision="fp8", num_splits=1)

@@ -17,34 +17,32 @@ from sparse_mla_attention_04_gb300 import binding, inputs
 pytestmark = pytest.mark.gpu
 
 # both kernels that serve 16 heads with a bf16 cache: the tcgen05 one (default)
-# and the warp-MMA one (SMLA_KERNEL=mma)
+# and the warp-MMA one (the forward's kernel-choice field)
 KERNELS = ["tcgen05", "mma"]
 
 
 @pytest.fixture(params=KERNELS)
-def kernel(request, monkeypatch):
-    if request.param == "mma":
-        monkeypatch.setenv("SMLA_KERNEL", "mma")
-    else:
-        monkeypatch.delenv("SMLA_KERNEL", raising=False)
-    yield request.param
+def kernel(request):
+    """The kernel a test runs on: the library's own choice, or the warp-MMA
+    kernel (asked for through the forward's kernel-choice field)."""
+    yield "auto" if request.param == "tcgen05" else "mma"
     assert binding.smla_device_error() == 0
 
 
 def test_tiny_config(kernel):
-    res, _, _ = parity.case(inputs.tiny(seed=0))
+    res, _, _ = parity.case(inputs.tiny(seed=0), kernel=kernel)
     print(res)
 
 
 @pytest.mark.parametrize("splits", [0, 1, 2, 3, 4, 8, 9, 16, 32])
 def test_decode_bf16_small(splits, kernel):
     w = inputs.decode(n_seqs=8, ctx=8192, topk=2048, name="decode_bf16_small")
-    parity.case(w, num_splits=splits)
+    parity.case(w, kernel=kernel, num_splits=splits)
 
 
 def test_split_counts_agree(kernel):
     w = inputs.decode(n_seqs=4, ctx=8192, topk=1000, name="decode_ragged")
-    outs = [parity.case(w, num_splits=s)[1] for s in (1, 2, 5, 6, 7, 11)]
+    outs = [parity.case(w, kernel=kernel, num_splits=s)[1] for s in (1, 2, 5, 6, 7, 11)]
     for o in outs[1:]:
         # each split count rounds P to bf16 against its own running max, so
         # runs differ by the bf16 tolerance, not by fp32 noise
@@ -61,7 +59,7 @@ def test_decode_fp8_small(splits):
 
 def test_prefill_small(kernel):
     w = inputs.prefill(T=384, topk=128, name="prefill_small")
-    parity.case(w)
+    parity.case(w, kernel=kernel)
 
 
 def test_wide_head_small():
@@ -158,7 +156,7 @@ def test_topk_edges(topk, fp8, kernel):
     w = inputs.Workload("edge", 3, 16, 512, 512, 1000, topk, fp8, 1 / math.sqrt(512), "uniform", seed=topk)
     for s in (1, 2):
         if s <= max(1, topk // 32):
-            parity.case(w, num_splits=s)
+            parity.case(w, kernel=kernel, num_splits=s)
 
 
 def test_masks_anywhere_and_empty_rows(kernel):
@@ -170,7 +168,7 @@ def test_masks_anywhere_and_empty_rows(kernel):
     idx[2, :199] = -1                                      # one index, at the end
     idx[3, ::2] = -1
     for s in (1, 3, 7):
-        res, out, lse = parity.case(w, idx=idx, num_splits=s)
+        res, out, lse = parity.case(w, kernel=kernel, idx=idx, num_splits=s)
         assert (out[1] == 0).all() and np.isneginf(lse[1]).all()
 
 
@@ -183,7 +181,7 @@ def test_single_index_is_bit_exact(kernel):
     q = inputs.make_q(w)
     kv = inputs.make_kv_source(w)
     for s in (1, 2):
-        out, lse = binding.sparse_mla_fwd(q.to(DEV), kv.to(DEV), torch.from_numpy(idx).to(DEV), w.scale,
+        out, lse = parity.fwd(kernel, q.to(DEV), kv.to(DEV), torch.from_numpy(idx).to(DEV), w.scale,
                                           num_splits=s)
         out = out.cpu()
         for t, j in ((0, 17), (1, 499), (2, 0)):
@@ -192,7 +190,7 @@ def test_single_index_is_bit_exact(kernel):
 
 def test_scale_zero_gives_mean(kernel):
     w = inputs.Workload("scale0", 2, 16, 512, 512, 800, 96, False, 0.0, "uniform", seed=5)
-    parity.case(w, num_splits=2)
+    parity.case(w, kernel=kernel, num_splits=2)
 
 
 def test_duplicate_indices_count(kernel):
@@ -200,7 +198,7 @@ def test_duplicate_indices_count(kernel):
     idx = inputs.make_indices(w)
     idx[0, 64:] = idx[0, :64]          # every slot twice
     idx[1, 1:40] = idx[1, 0]           # one slot 40 times
-    parity.case(w, idx=idx, num_splits=2)
+    parity.case(w, kernel=kernel, idx=idx, num_splits=2)
 
 
 @pytest.mark.parametrize("fp8", [False, True])
@@ -221,14 +219,14 @@ def test_nan_poison_in_unreferenced_slots(fp8, kernel):
     ti = torch.from_numpy(idx).to(DEV)
     dot = "fp8" if fp8 else "auto"
     for s in (1, 3):
-        o1, l1 = binding.sparse_mla_fwd(q, cache, ti, w.scale, kv_scale=kvs, dot_precision=dot, num_splits=s)
+        o1, l1 = parity.fwd(kernel, q, cache, ti, w.scale, kv_scale=kvs, dot_precision=dot, num_splits=s)
         o1, l1 = o1.clone(), l1.clone()
         poisoned = cache.clone()
         if fp8:
             poisoned[unused] = 0x7F
         else:
             poisoned[unused] = float("nan")
-        o2, l2 = binding.sparse_mla_fwd(q, poisoned, ti, w.scale, kv_scale=kvs, dot_precision=dot, num_splits=s)
+        o2, l2 = parity.fwd(kernel, q, poisoned, ti, w.scale, kv_scale=kvs, dot_precision=dot, num_splits=s)
         torch.cuda.synchronize()
         assert torch.isfinite(o2.float()).all()
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
@@ -246,8 +244,8 @@ def test_out_of_range_indices_are_masked_and_reported(kernel):
     clean[(clean < -1) | (clean >= 1000)] = -1
     q = inputs.make_q(w).to(DEV)
     kv = inputs.make_kv_source(w).to(DEV)
-    o1, l1 = binding.sparse_mla_fwd(q, kv, torch.from_numpy(bad).to(DEV), w.scale, num_splits=2)
-    o2, l2 = binding.sparse_mla_fwd(q, kv, torch.from_numpy(clean).to(DEV), w.scale, num_splits=2)
+    o1, l1 = parity.fwd(kernel, q, kv, torch.from_numpy(bad).to(DEV), w.scale, num_splits=2)
+    o2, l2 = parity.fwd(kernel, q, kv, torch.from_numpy(clean).to(DEV), w.scale, num_splits=2)
     n_bad = binding.smla_validate_indices(torch.from_numpy(bad).to(DEV), 1000)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
@@ -272,7 +270,7 @@ def test_topk_zero_gives_empty_rows(kernel):
     q = inputs.make_q(w).to(DEV)
     kv = inputs.make_kv_source(w).to(DEV)
     idx = torch.empty((4, 0), dtype=torch.int32, device=DEV)
-    out, lse = binding.sparse_mla_fwd(q, kv, idx, w.scale)
+    out, lse = parity.fwd(kernel, q, kv, idx, w.scale)
     torch.cuda.synchronize()
     assert (out == 0).all() and torch.isneginf(lse).all()
 
@@ -303,7 +301,7 @@ def test_workspace_reuse_across_shapes(kernel):
         q = inputs.make_q(w)
         kv = inputs.make_kv_source(w)
         idx = inputs.make_indices(w)
-        out, lse = binding.sparse_mla_fwd(q.to(DEV), kv.to(DEV), torch.from_numpy(idx).to(DEV), w.scale,
+        out, lse = parity.fwd(kernel, q.to(DEV), kv.to(DEV), torch.from_numpy(idx).to(DEV), w.scale,
                                           num_splits=S, workspace=ws)
         torch.cuda.synchronize()
         ref_o, ref_l, _ = oracle.sparse_mla(q, kv, idx, w.scale)
@@ -323,7 +321,7 @@ def test_large_logits_take_the_rescale_path(kernel):
     logits0 = kv[idx[0]].float() @ q[0, 0].float()
     idx[0] = idx[0][np.argsort(logits0.numpy())]
     for S in (1, 2, 3):
-        parity.case(w, idx=idx, kv_src=kv, q=q, num_splits=S)
+        parity.case(w, kernel=kernel, idx=idx, kv_src=kv, q=q, num_splits=S)
 
 
 @pytest.mark.parametrize("topk", [5, 20])
@@ -335,7 +333,7 @@ def test_more_splits_than_keys(topk, fp8, kernel):
     w = inputs.Workload("split_empty", 3, 16, 512, 512, 700, topk, fp8, 1 / math.sqrt(512), "uniform", seed=topk)
     outs = []
     for s in (1, 8, 16, 128):
-        res, out, lse = parity.case(w, num_splits=s)
+        res, out, lse = parity.case(w, kernel=kernel, num_splits=s)
         assert np.isfinite(out).all() and np.isfinite(lse).all()
         outs.append(out)
     for o in outs[1:]:

@@ -20,15 +20,13 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.fixture(params=["tcgen05", "mma"])
-def kernel(request, monkeypatch):
-    if request.param == "mma":
-        monkeypatch.setenv("SMLA_KERNEL", "mma")
-    else:
-        monkeypatch.delenv("SMLA_KERNEL", raising=False)
-    return request.param
+def kernel(request):
+    """The kernel a test runs on: the library's own choice, or the warp-MMA
+    kernel (asked for through the forward's kernel-choice field)."""
+    return "auto" if request.param == "tcgen05" else "mma"
 
 
-def _run(w, q_scale, *, num_splits=0, idx=None):
+def _run(w, q_scale, *, num_splits=0, idx=None, kernel="auto"):
     q = inputs.make_q(w)
     T, H, D = q.shape
     codes = oracle.fp8_quantize(q.reshape(-1, D), q_scale).reshape(T, H, D)   # the pinned quantizer
@@ -39,7 +37,7 @@ def _run(w, q_scale, *, num_splits=0, idx=None):
     out, lse = binding.sparse_mla_fwd_q8(torch.from_numpy(codes).to(DEV),
                                          torch.tensor([q_scale], dtype=torch.float32, device=DEV), cache,
                                          torch.from_numpy(idx).to(DEV), w.scale, kv_scale=kvs, D_v=w.D_v,
-                                         num_splits=num_splits)
+                                         num_splits=num_splits, kernel=kernel)
     torch.cuda.synchronize()
     ref_o, ref_l, _ = oracle.sparse_mla_q8(codes, q_scale, ocache, idx, w.scale, kv_fp8=True, kv_scale=oscale,
                                            D_v=w.D_v)
@@ -49,18 +47,18 @@ def _run(w, q_scale, *, num_splits=0, idx=None):
 
 def test_q8_decode_16_heads(kernel):
     w = inputs.decode(n_seqs=8, ctx=8192, topk=2048, fp8=True, short_rows=2, name="decode_fp8_q8")
-    _run(w, np.float32(0.0137))
+    _run(w, np.float32(0.0137), kernel=kernel)
 
 
 def test_q8_decode_splits(kernel):
     w = inputs.decode(n_seqs=4, ctx=8192, topk=2048, fp8=True, name="decode_fp8_q8_splits")
     for s in (1, 3, 12):
-        _run(w, np.float32(0.011), num_splits=s)
+        _run(w, np.float32(0.011), num_splits=s, kernel=kernel)
 
 
 def test_q8_wide_128_heads(kernel):
     w = inputs.wide(T=4, ctx=4096, topk=2048, name="wide_q8")
-    _run(w, np.float32(0.0093))
+    _run(w, np.float32(0.0093), kernel=kernel)
 
 
 def test_q8_ragged_and_masked():

@@ -29,21 +29,19 @@ def _sinks(H, seed):
 
 
 @pytest.fixture(params=["tcgen05", "mma"])
-def kernel(request, monkeypatch):
-    if request.param == "mma":
-        monkeypatch.setenv("SMLA_KERNEL", "mma")
-    else:
-        monkeypatch.delenv("SMLA_KERNEL", raising=False)
-    return request.param
+def kernel(request):
+    """The kernel a test runs on: the library's own choice, or the warp-MMA
+    kernel (asked for through the forward's kernel-choice field)."""
+    return "auto" if request.param == "tcgen05" else "mma"
 
 
-def _bf16_case(w, sinks, num_splits, idx=None):
+def _bf16_case(w, sinks, num_splits, idx=None, kernel="auto"):
     q = inputs.make_q(w)
     src = inputs.make_kv_source(w)
     idx = inputs.make_indices(w) if idx is None else idx
     out, lse = binding.sparse_mla_fwd(q.to(DEV), src.to(DEV), torch.from_numpy(idx).to(DEV), w.scale,
                                       D_v=w.D_v, num_splits=num_splits,
-                                      sinks=torch.from_numpy(sinks).to(DEV))
+                                      sinks=torch.from_numpy(sinks).to(DEV), kernel=kernel)
     torch.cuda.synchronize()
     ref_o, ref_l, _ = oracle.sparse_mla(q, src, idx, w.scale, D_v=w.D_v, sinks=sinks)
     return (out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), ref_o, ref_l)
@@ -52,7 +50,7 @@ def _bf16_case(w, sinks, num_splits, idx=None):
 @pytest.mark.parametrize("splits", [1, 2, 12])
 def test_sinks_decode_bf16(kernel, splits):
     w = inputs.decode(n_seqs=6, ctx=8192, topk=2048, name="decode_bf16_sinks")
-    o, l, ro, rl = _bf16_case(w, _sinks(16, 1), splits)
+    o, l, ro, rl = _bf16_case(w, _sinks(16, 1), splits, kernel=kernel)
     compare(o, l, ro, rl, TOL_BF16, "sinks, %d split(s)" % splits)
 
 
@@ -62,7 +60,7 @@ def test_sinks_empty_rows_give_the_sink(kernel):
     idx[2, :] = -1
     sinks = _sinks(16, 2)
     for splits in (1, 3, 10):
-        o, l, ro, rl = _bf16_case(w, sinks, splits, idx=idx)
+        o, l, ro, rl = _bf16_case(w, sinks, splits, idx=idx, kernel=kernel)
         compare(o, l, ro, rl, TOL_BF16, "sinks, empty row")
         assert (o[2] == 0).all()
         fin = np.isfinite(sinks)
