@@ -66,6 +66,9 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--ctx", type=int, default=0,
                     help="override the per-row context (pool size) of a decode workload, for profiling")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "mma", "basic"],
+                    help="kernel choice of the forward (auto: the library's; mma: the warp-MMA kernel; basic: the "
+                         "tcgen05 kernels that take a whole SM per CTA)")
     ap.add_argument("--no-per-config", action="store_true",
                     help="time only --workload (skip the other configurations, the ceilings and the L2 probe)")
     return ap.parse_args()
@@ -304,12 +307,13 @@ def forward_setup(binding, w, cache, kvs, sets, dev, stream, args, sinks=None):
         for s in sets:   # q quantized once per set, outside the timed region, by the library's kernels
             s["q8"], s["qs"] = quantize_q_per_tensor(binding, s["q"])
     T, H = w.T, w.H
+    kernel = getattr(args, "kernel", "auto")
     out = torch.empty((T, H, w.D_v), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((T, H), dtype=torch.float32, device=dev)
     splits = binding.smla_plan_num_splits(T, H, w.D_qk, w.topk, int(w.kv_fp8),
                                           torch.cuda.get_device_properties(dev).multi_processor_count)
-    if args.bf16_dots:
-        splits = 0   # bf16 dots run on the warp-MMA kernel: its own automatic plan
+    if args.bf16_dots or kernel != "auto":
+        splits = 0   # another kernel than the default: its own automatic plan
     need = binding.sparse_mla_fwd_workspace_size(T, H, w.D_qk, w.D_v, w.topk, int(w.kv_fp8), splits)
     ws = torch.zeros(max(need, 1), dtype=torch.uint8, device=dev)
 
@@ -317,10 +321,12 @@ def forward_setup(binding, w, cache, kvs, sets, dev, stream, args, sinks=None):
         s = sets[i % R]
         if args.q8:
             binding.sparse_mla_fwd_q8(s["q8"], s["qs"], cache, s["idx"], w.scale, kv_scale=kvs, D_v=w.D_v,
-                                      out=out, lse=lse, workspace=ws, num_splits=splits, stream=stream, sinks=sinks)
+                                      out=out, lse=lse, workspace=ws, num_splits=splits, stream=stream, sinks=sinks,
+                                      kernel=kernel)
         else:
             binding.sparse_mla_fwd(s["q"], cache, s["idx"], w.scale, kv_scale=kvs, dot_precision=dot, D_v=w.D_v,
-                                   out=out, lse=lse, workspace=ws, num_splits=splits, stream=stream, sinks=sinks)
+                                   out=out, lse=lse, workspace=ws, num_splits=splits, stream=stream, sinks=sinks,
+                                   kernel=kernel)
     return call, dot, splits
 
 

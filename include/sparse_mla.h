@@ -83,10 +83,16 @@ typedef enum {
  *   AUTO     : the library's choice (described under sparse_mla_fwd).
  *   WARP_MMA : the warp-level mma.sync kernel, for every supported shape and
  *              precision (a comparison path: slower, same results within the
- *              stated tolerances). */
+ *              stated tolerances).
+ *   TCGEN05_BASIC : the first tcgen05 kernels, whose CTAs take a whole SM and
+ *              share nothing: for 16 heads over an E4M3 cache one CTA per SM
+ *              (AUTO runs two lean ones per SM), for 128 heads two CTAs per row
+ *              that each gather every key (AUTO pairs them in a cluster that
+ *              gathers each key once); otherwise as AUTO. */
 typedef enum {
     SMLA_KERNEL_AUTO = 0,
-    SMLA_KERNEL_WARP_MMA = 1
+    SMLA_KERNEL_WARP_MMA = 1,
+    SMLA_KERNEL_TCGEN05_BASIC = 2
 } smla_kernel_choice;
 
 /* Human-readable name of a status. Never NULL. */
@@ -167,9 +173,11 @@ SMLA_API size_t sparse_mla_fwd_workspace_size(int T, int H, int D_qk, int D_v, i
  *              that region: q quantized per (row, head), T*H*D_qk bytes, and
  *              its T*H scales.
  *              Calls that overlap in time must not share a workspace.
- * Kernels: 16 heads with D_qk = D_v = 512 (bf16 cache, or E4M3 with fp8
- *              dots) run on a tcgen05 kernel (keys on the MMA's M axis,
- *              accumulators in tensor memory, TMA row gathers); H a multiple of
+ * Kernels: 16 heads with D_qk = D_v = 512 run on tcgen05 kernels (keys on
+ *              the MMA's M axis, accumulators in tensor memory, TMA row
+ *              gathers): a bf16 cache on one that takes a whole SM per CTA,
+ *              an E4M3 cache with fp8 dots on a lean one that runs two CTAs
+ *              per SM (its splits fill twice as many CTAs); H a multiple of
  *              128 with D_qk = 576, D_v = 512 and an E4M3 cache runs, when the
  *              call does not ask for more than one split, on a tcgen05 kernel
  *              with heads on M (two CTAs per row, each owning half of the

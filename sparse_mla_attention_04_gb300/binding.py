@@ -37,7 +37,8 @@ SMLA_DOT_FP8 = 2
 _DOT = {"auto": SMLA_DOT_AUTO, "bf16": SMLA_DOT_BF16, "fp8": SMLA_DOT_FP8}
 SMLA_KERNEL_AUTO = 0
 SMLA_KERNEL_WARP_MMA = 1
-_KERNEL = {"auto": SMLA_KERNEL_AUTO, "mma": SMLA_KERNEL_WARP_MMA}
+SMLA_KERNEL_TCGEN05_BASIC = 2
+_KERNEL = {"auto": SMLA_KERNEL_AUTO, "mma": SMLA_KERNEL_WARP_MMA, "basic": SMLA_KERNEL_TCGEN05_BASIC}
 
 # every function the header declares, with its ctypes signature
 _c = ctypes
@@ -196,8 +197,9 @@ def sparse_mla_fwd(q: torch.Tensor, kv_cache: torch.Tensor, indices: torch.Tenso
                    sinks: Optional[torch.Tensor] = None,
                    kernel: str = "auto") -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """out[T,H,D_v] (bf16), lse[T,H] (fp32) of the sparse MLA forward
-    (sinks: optional fp32 [H] per-head sink logits; kernel: "auto", or "mma"
-    for the warp-MMA kernel).
+    (sinks: optional fp32 [H] per-head sink logits; kernel: "auto", "mma" for
+    the warp-MMA kernel, or "basic" for the tcgen05 kernels that take a
+    whole SM per CTA).
 
     q bf16 [T,H,D_qk]; kv_cache [num_slots, D_qk] bf16 or torch.float8_e4m3fn/uint8
     (E4M3 codes, then kv_scale: fp32 device scalar); indices int32 [T, topk].

@@ -52,23 +52,34 @@ cudaError_t current_sm_count(int *out)
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // Which kernel serves a call.
-enum class Path { Mma, Umma16, Wide };
+enum class Path { Mma, Umma16, Wide, Lean16, Wide2 };
 
-// 16 heads with D_qk = D_v = 512 (bf16 cache, or E4M3 cache with fp8 dots):
-// the tcgen05 16-head kernel; a multiple of 128 heads with D_qk = 576,
-// D_v = 512 and an E4M3 cache: the tcgen05 128-head kernel (no split of the
-// top-k list); every other shape: the warp-MMA kernel.
-Path choose_path(int H, int D_qk, int D_v, bool kv_fp8)
+// 16 heads with D_qk = D_v = 512: an E4M3 cache with fp8 dots runs on the
+// lean tcgen05 16-head kernel (two CTAs per SM: its random 512-byte row
+// gathers complete faster with more CTAs per SM), a bf16 cache on the
+// tcgen05 16-head kernel that takes a whole SM per CTA (its 1 KB row gathers
+// reach the DRAM bound already); a multiple of 128 heads with D_qk = 576,
+// D_v = 512 and an E4M3 cache with fp8 dots: the tcgen05 128-head kernel (no
+// split of the top-k list) whose two CTAs per row form a cluster that
+// gathers each key row once; every other shape or precision: the warp-MMA
+// kernel. `kernel` (smla_kernel_choice) can ask for the warp-MMA kernel, or
+// for the first tcgen05 kernels (whole SM per CTA, nothing shared).
+Path choose_path(int H, int D_qk, int D_v, bool kv_fp8, bool fp8_dots, int kernel)
 {
+    if (kernel == SMLA_KERNEL_WARP_MMA || (kv_fp8 && !fp8_dots))
+        return Path::Mma;
     if (H == 16 && D_qk == 512 && D_v == 512)
-        return Path::Umma16;
+        return kv_fp8 && kernel != SMLA_KERNEL_TCGEN05_BASIC ? Path::Lean16 : Path::Umma16;
     if (H % 128 == 0 && D_qk == 576 && D_v == 512 && kv_fp8)
-        return Path::Wide;
+        return kernel == SMLA_KERNEL_TCGEN05_BASIC ? Path::Wide : Path::Wide2;
     return Path::Mma;
 }
 
-int ctas_per_sm(Path p) { return p == Path::Mma ? 2 : 1; }
-int tile_keys(Path p) { return p == Path::Umma16 ? smla::kUmma16TileKeys : smla::kMmaTileKeys; }
+int ctas_per_sm(Path p) { return (p == Path::Mma || p == Path::Lean16) ? 2 : 1; }
+int tile_keys(Path p)
+{
+    return (p == Path::Umma16 || p == Path::Lean16) ? smla::kUmma16TileKeys : smla::kMmaTileKeys;
+}
 
 // Split plan, from the per-call sweep (rows {2..16K} x fan-out {128, 512,
 // 2048}, 16 heads, bf16): a split keeps at least two key tiles (128 keys);
@@ -86,7 +97,7 @@ using smla::kTicketSlots;
 
 int plan_splits(int T, int H, int topk, int sm_count, Path path)
 {
-    if (T <= 0 || H <= 0 || topk <= 0 || sm_count <= 0 || path == Path::Wide)
+    if (T <= 0 || H <= 0 || topk <= 0 || sm_count <= 0 || path == Path::Wide || path == Path::Wide2)
         return 1;
     const int64_t units = (int64_t)T * (H / 16);
     const int64_t slots = (int64_t)sm_count * ctas_per_sm(path);
@@ -124,11 +135,9 @@ smla_status plan_forward(int T, int H, int D_qk, int D_v, int topk, int kv_dtype
 {
     const bool kv_fp8 = kv_dtype == SMLA_KV_FP8_E4M3;
     const bool bf16_dots = kv_fp8 && dot_precision != SMLA_DOT_FP8; // bf16 q . dequantized K
-    Path path = kernel == SMLA_KERNEL_WARP_MMA ? Path::Mma : choose_path(H, D_qk, D_v, kv_fp8);
-    if (path == Path::Wide && num_splits > 1)
-        path = Path::Mma; // the 128-head kernel does not split the top-k list
-    if (bf16_dots)
-        path = Path::Mma; // the warp-MMA kernel serves bf16 dots over an E4M3 cache
+    Path path = choose_path(H, D_qk, D_v, kv_fp8, !bf16_dots, kernel);
+    if ((path == Path::Wide || path == Path::Wide2) && num_splits > 1)
+        path = Path::Mma; // the 128-head kernels do not split the top-k list
     int S = num_splits;
     if (S == 0) {
         int sms = 0;
@@ -143,7 +152,7 @@ smla_status plan_forward(int T, int H, int D_qk, int D_v, int topk, int kv_dtype
     out->path = static_cast<int>(path);
     out->S = S;
     out->bf16_dots = bf16_dots;
-    out->layout = workspace_layout(T, H, D_qk, D_v, S, path == Path::Wide);
+    out->layout = workspace_layout(T, H, D_qk, D_v, S, path == Path::Wide || path == Path::Wide2);
     out->uses_tickets = S > kClusterMaxSplits;
     return SMLA_OK;
 }
@@ -214,7 +223,8 @@ SMLA_API int smla_plan_num_splits(int T, int H, int D_qk, int topk, int kv_dtype
     (void)kv_dtype;
     if (T < 0 || H <= 0 || H % 16 != 0 || topk < 0 || sm_count <= 0)
         return 0;
-    return plan_splits(T, H, topk, sm_count, choose_path(H, D_qk, 512, kv_dtype == SMLA_KV_FP8_E4M3));
+    const bool fp8 = kv_dtype == SMLA_KV_FP8_E4M3;
+    return plan_splits(T, H, topk, sm_count, choose_path(H, D_qk, 512, fp8, fp8, SMLA_KERNEL_AUTO));
 }
 
 SMLA_API size_t sparse_mla_fwd_workspace_size(int T, int H, int D_qk, int D_v, int topk, int kv_dtype,
@@ -250,7 +260,7 @@ SMLA_API size_t sparse_mla_fwd_ex_workspace_size(const smla_fwd_params *p)
         (p->kv_dtype != SMLA_KV_BF16 && p->kv_dtype != SMLA_KV_FP8_E4M3) ||
         (dot != SMLA_DOT_AUTO && dot != SMLA_DOT_BF16 && dot != SMLA_DOT_FP8) ||
         (dot == SMLA_DOT_FP8 && p->kv_dtype != SMLA_KV_FP8_E4M3) ||
-        (kernel != SMLA_KERNEL_AUTO && kernel != SMLA_KERNEL_WARP_MMA))
+        (kernel != SMLA_KERNEL_AUTO && kernel != SMLA_KERNEL_WARP_MMA && kernel != SMLA_KERNEL_TCGEN05_BASIC))
         return (size_t)-1;
     if (p->T == 0)
         return 0;
@@ -292,7 +302,7 @@ static smla_status fwd_impl(const void *q, bool q_fp8_in, const float *q_scale_i
         return SMLA_ERR_UNSUPPORTED;
     if (num_splits > kMaxSplits)
         return SMLA_ERR_UNSUPPORTED;
-    if (kernel != SMLA_KERNEL_AUTO && kernel != SMLA_KERNEL_WARP_MMA)
+    if (kernel != SMLA_KERNEL_AUTO && kernel != SMLA_KERNEL_WARP_MMA && kernel != SMLA_KERNEL_TCGEN05_BASIC)
         return SMLA_ERR_BAD_SHAPE;
     // 5. alignment
     if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(indices, 4) ||
@@ -331,9 +341,10 @@ static smla_status fwd_impl(const void *q, bool q_fp8_in, const float *q_scale_i
     a.part_o = wl.total ? reinterpret_cast<float *>(ws + wl.part_o) : nullptr;
     a.part_lse = wl.total ? reinterpret_cast<float *>(ws + wl.part_lse) : nullptr;
     a.tickets = wl.total ? reinterpret_cast<int *>(ws + wl.tickets) : nullptr;
-    a.q8 = path == Path::Wide ? ws + wl.q8 : nullptr;
-    a.q8_rope = path == Path::Wide ? ws + wl.q8_rope : nullptr;
-    a.q_scale = path == Path::Wide ? reinterpret_cast<float *>(ws + wl.q_scale) : nullptr;
+    const bool wide = path == Path::Wide || path == Path::Wide2;
+    a.q8 = wide ? ws + wl.q8 : nullptr;
+    a.q8_rope = wide ? ws + wl.q8_rope : nullptr;
+    a.q_scale = wide ? reinterpret_cast<float *>(ws + wl.q_scale) : nullptr;
     a.num_slots = num_slots;
     a.T = T;
     a.H = H;
@@ -352,8 +363,12 @@ static smla_status fwd_impl(const void *q, bool q_fp8_in, const float *q_scale_i
     switch (path) {
     case Path::Umma16:
         return cuda_status(smla::launch_fwd_umma16(a, st));
+    case Path::Lean16:
+        return cuda_status(smla::launch_fwd_lean16(a, st));
     case Path::Wide:
         return cuda_status(smla::launch_fwd_wide(a, st));
+    case Path::Wide2:
+        return cuda_status(smla::launch_fwd_wide2(a, st));
     default:
         return cuda_status(smla::launch_fwd_mma(a, st));
     }
@@ -400,8 +415,12 @@ SMLA_API smla_status smla_device_error(int *code, int reset)
 {
     if (code == nullptr)
         return SMLA_ERR_NULL_POINTER;
-    int c16 = 0, cw = 0, cp = 0, cg = 0;
+    int c16 = 0, cw = 0, cp = 0, cg = 0, cl = 0, cw2 = 0;
     if (const cudaError_t e = smla::read_umma_error(&c16, reset != 0); e != cudaSuccess)
+        return cuda_status(e);
+    if (const cudaError_t e = smla::read_lean_error(&cl, reset != 0); e != cudaSuccess)
+        return cuda_status(e);
+    if (const cudaError_t e = smla::read_wide2_error(&cw2, reset != 0); e != cudaSuccess)
         return cuda_status(e);
     if (const cudaError_t e = smla::read_probe_error(&cg, reset != 0); e != cudaSuccess)
         return cuda_status(e);
@@ -409,7 +428,7 @@ SMLA_API smla_status smla_device_error(int *code, int reset)
         return cuda_status(e);
     if (const cudaError_t e = smla::read_producer_error(&cp, reset != 0); e != cudaSuccess)
         return cuda_status(e);
-    *code = c16 | cw | cp | cg;
+    *code = c16 | cw | cp | cg | cl | cw2;
     return SMLA_OK;
 }
 

@@ -574,6 +574,17 @@ __global__ void __launch_bounds__(512, 1)
 
 } // namespace
 
+cudaError_t launch_quantize_q_wide(const FwdArgs &a, cudaStream_t stream)
+{
+    const int64_t qrows = (int64_t)a.T * a.H;
+    if (qrows == 0)
+        return cudaSuccess;
+    quantize_q_e4m3_kernel<<<dim3((unsigned)((qrows + 3) / 4)), dim3(128), 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(a.q), qrows, a.H, a.q8, a.q8_rope, a.q_scale,
+        a.q_fp8_in ? static_cast<const uint8_t *>(a.q) : nullptr, a.q_scale_in);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_fwd_wide(const FwdArgs &a, cudaStream_t stream)
 {
     auto kern = sparse_mla_fwd_wide_kernel;
@@ -618,12 +629,7 @@ cudaError_t launch_fwd_wide(const FwdArgs &a, cudaStream_t stream)
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    const int64_t qrows = (int64_t)a.T * a.H;
-    quantize_q_e4m3_kernel<<<dim3((unsigned)((qrows + 3) / 4)), dim3(128), 0, stream>>>(
-        static_cast<const __nv_bfloat16 *>(a.q), qrows, a.H, a.q8, a.q8_rope, a.q_scale,
-        a.q_fp8_in ? static_cast<const uint8_t *>(a.q) : nullptr, a.q_scale_in);
-    const cudaError_t qe = cudaGetLastError();
-    if (qe != cudaSuccess)
+    if (const cudaError_t qe = launch_quantize_q_wide(a, stream); qe != cudaSuccess)
         return qe;
     // programmatic dependent launch: the kernel's prologue overlaps the q pass's
     // tail; it waits for it in grid_wait before reading q8

@@ -80,11 +80,18 @@ smla_status plan_forward(int T, int H, int D_qk, int D_v, int topk, int kv_dtype
 cudaError_t launch_fwd_mma(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_fwd_wide(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_fwd_umma16(const FwdArgs &a, cudaStream_t stream);
+cudaError_t launch_fwd_lean16(const FwdArgs &a, cudaStream_t stream);
+cudaError_t launch_fwd_wide2(const FwdArgs &a, cudaStream_t stream);
+// The 128-head kernels' q pass: per (row, head) E4M3 codes and scales of q
+// (or the pre-quantized codes rearranged) into the workspace.
+cudaError_t launch_quantize_q_wide(const FwdArgs &a, cudaStream_t stream);
 // cuTensorMapEncodeTiled from the driver (resolved once; nullptr if unavailable).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 // First error code recorded by a bounded device-side wait that gave up (0 = none).
 cudaError_t read_umma_error(int *out, bool reset);
 cudaError_t read_wide_error(int *out, bool reset);
+cudaError_t read_lean_error(int *out, bool reset);
+cudaError_t read_wide2_error(int *out, bool reset);
 
 // The fused producer step (RoPE + q concat + cache write), validated by the ABI layer.
 struct FusedProducerArgs {

@@ -69,6 +69,16 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
                  "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
+// Arrive once on the mbarrier at shared-memory offset `mbar` of every CTA of
+// the cluster in `cta_mask` when every tcgen05 op issued so far by this
+// thread is done.
+__device__ __forceinline__ void commit_multicast(uint32_t mbar, uint16_t cta_mask)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n" ::"r"(mbar),
+                 "h"(cta_mask)
+                 : "memory");
+}
+
 // Arrive once on `mbar` when every tcgen05 op issued so far by this thread is done.
 __device__ __forceinline__ void commit(uint32_t mbar)
 {
@@ -100,6 +110,21 @@ __device__ __forceinline__ void ld16(uint32_t taddr, uint32_t (&r)[16])
                    "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
                    "=r"(r[15])
                  : "r"(taddr));
+}
+
+// 32 lanes x 8 consecutive 32-bit columns (warp-wide).
+__device__ __forceinline__ void ld8(uint32_t taddr, uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+
+__device__ __forceinline__ void st8(uint32_t taddr, const uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
 }
 
 __device__ __forceinline__ void st16(uint32_t taddr, const uint32_t (&r)[16])
@@ -150,6 +175,18 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int 
                  : "memory");
 }
 
+// tma_gather4 delivered to the same shared-memory offset (dst) in every CTA
+// of the cluster in `cta_mask`; each destination CTA counts the bytes on its
+// own mbarrier at offset `mbar`.
+__device__ __forceinline__ void tma_gather4_multicast(uint32_t dst, const void *tmap, int x, int r0, int r1, int r2,
+                                                      int r3, uint32_t mbar, uint16_t cta_mask)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.multicast::cluster"
+                 " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;\n" ::"r"(dst),
+                 "l"(tmap), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(mbar), "h"(cta_mask)
+                 : "memory");
+}
+
 // TMA tile load of the box at (x, y) of a 2-D tensor map into shared memory at
 // dst (in the map's swizzle), bytes counted on mbar; out-of-range parts of the
 // box are filled with zeros.
@@ -173,6 +210,28 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uin
 __device__ __forceinline__ void mbar_arrive(uint32_t mbar)
 {
     asm volatile("{\n.reg .b64 st;\nmbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(mbar) : "memory");
+}
+
+// Arrive once, with release semantics at cluster scope, on the mbarrier at
+// shared-memory offset `mbar` of cluster CTA `rank` (which may be this CTA).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t mbar, uint32_t rank)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(mbar), "r"(rank));
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(remote) : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
+}
+
+// Barrier over every thread of every CTA of the cluster (release / acquire).
+__device__ __forceinline__ void cluster_barrier()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
 __device__ __forceinline__ uint64_t globaltimer()

@@ -42,7 +42,7 @@ def test_status_strings(L):
 def test_split_plan(L):
     from sparse_mla_attention_04_gb300 import binding as b
     assert b.smla_plan_num_splits(64, 16, 512, 2048, 0, 152) == 2     # decode bf16, tcgen05 kernel: 1 CTA/SM
-    assert b.smla_plan_num_splits(64, 16, 512, 2048, 1, 152) == 2     # decode fp8, tcgen05 kernel: 1 CTA/SM
+    assert b.smla_plan_num_splits(64, 16, 512, 2048, 1, 152) == 4     # decode fp8, lean tcgen05 kernel: 2 CTAs/SM
     assert b.smla_plan_num_splits(4, 16, 512, 128, 0, 152) == 1       # a split keeps two key tiles
     assert b.smla_plan_num_splits(2, 16, 512, 2048, 0, 152) == 8      # few rows: up to one 8-CTA cluster
     assert b.smla_plan_num_splits(16, 16, 512, 2048, 0, 152) == 6     # many 8-CTA clusters: 6 instead

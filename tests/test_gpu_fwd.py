@@ -16,16 +16,18 @@ from sparse_mla_attention_04_gb300 import binding, inputs
 
 pytestmark = pytest.mark.gpu
 
-# both kernels that serve 16 heads with a bf16 cache: the tcgen05 one (default)
-# and the warp-MMA one (the forward's kernel-choice field)
-KERNELS = ["tcgen05", "mma"]
+# the kernels that serve 16 heads: the library's choice (the lean tcgen05
+# kernel for an E4M3 cache, the whole-SM one for bf16), the warp-MMA kernel,
+# and the whole-SM tcgen05 kernel for E4M3 too (the forward's kernel-choice field)
+KERNELS = ["tcgen05", "mma", "basic"]
 
 
 @pytest.fixture(params=KERNELS)
 def kernel(request):
-    """The kernel a test runs on: the library's own choice, or the warp-MMA
-    kernel (asked for through the forward's kernel-choice field)."""
-    yield "auto" if request.param == "tcgen05" else "mma"
+    """The kernel a test runs on: the library's own choice, the warp-MMA
+    kernel, or the tcgen05 kernels that take a whole SM per CTA (asked for
+    through the forward's kernel-choice field)."""
+    yield {"tcgen05": "auto", "mma": "mma", "basic": "basic"}[request.param]
     assert binding.smla_device_error() == 0
 
 
@@ -51,9 +53,9 @@ def test_split_counts_agree(kernel):
 
 
 @pytest.mark.parametrize("splits", [0, 1, 4, 12])
-def test_decode_fp8_small(splits):
+def test_decode_fp8_small(splits, kernel):
     w = inputs.decode(n_seqs=8, ctx=8192, topk=2048, fp8=True, short_rows=2, name="decode_fp8_small")
-    res, _, _ = parity.case(w, num_splits=splits)
+    res, _, _ = parity.case(w, num_splits=splits, kernel=kernel)
     print(res)
 
 
@@ -62,35 +64,43 @@ def test_prefill_small(kernel):
     parity.case(w, kernel=kernel)
 
 
-def test_wide_head_small():
+@pytest.fixture(params=["auto", "basic"])
+def wide_kernel(request):
+    """The 128-head kernels: the cluster pair that gathers each key once
+    (auto), and the first one whose two CTAs per row each gather every key."""
+    yield request.param
+    assert binding.smla_device_error() == 0
+
+
+def test_wide_head_small(wide_kernel):
     w = inputs.wide(T=4, ctx=4096, topk=2048, name="wide_small")
-    res, _, _ = parity.case(w)
+    res, _, _ = parity.case(w, kernel=wide_kernel)
     print(res)
 
 
 # --- 128-head kernel (E4M3 cache, D_qk = 576): ragged top-k, masks, the
 # rescale path, several head groups, and the fallback for explicit splits ---
 
-@pytest.mark.parametrize("topk", [1, 63, 65, 700])
-def test_wide_head_ragged_topk(topk):
+@pytest.mark.parametrize("topk", [1, 31, 33, 63, 65, 700])
+def test_wide_head_ragged_topk(topk, wide_kernel):
     w = inputs.Workload("wide_ragged", 3, 128, 576, 512, 3000, topk, True, 1 / math.sqrt(576), "uniform",
                         seed=topk)
-    parity.case(w)
+    parity.case(w, kernel=wide_kernel)
     assert binding.smla_device_error() == 0
 
 
-def test_wide_head_masks_and_empty_rows():
+def test_wide_head_masks_and_empty_rows(wide_kernel):
     w = inputs.Workload("wide_masks", 4, 128, 576, 512, 3000, 300, True, 1 / math.sqrt(576), "uniform", seed=9)
     idx = inputs.make_indices(w)
     rng = np.random.default_rng(11)
     idx[0, rng.choice(300, 200, replace=False)] = -1   # scattered
     idx[1, :] = -1                                      # empty row
     idx[2, :299] = -1                                   # one index, at the end
-    res, out, lse = parity.case(w, idx=idx)
+    res, out, lse = parity.case(w, idx=idx, kernel=wide_kernel)
     assert (out[1] == 0).all() and np.isneginf(lse[1]).all()
 
 
-def test_wide_head_rescale_path():
+def test_wide_head_rescale_path(wide_kernel):
     """Row 0 lists its keys in ascending order of head 0's logit with q
     scaled up, so the running max of most heads climbs by more than 2^8
     several times and the kernel rescales O rows in tensor memory. Scaled-up
@@ -102,13 +112,13 @@ def test_wide_head_rescale_path():
     idx = inputs.make_indices(w)
     logits0 = kv[idx[0]].float() @ q[0, 0].float()
     idx[0] = idx[0][np.argsort(logits0.numpy())]
-    res, _, _ = parity.case(w, idx=idx, kv_src=kv, q=q, check_plain=False)
+    res, _, _ = parity.case(w, idx=idx, kv_src=kv, q=q, check_plain=False, kernel=wide_kernel)
     assert "mirror" in res
 
 
-def test_wide_head_two_head_groups():
+def test_wide_head_two_head_groups(wide_kernel):
     w = inputs.Workload("wide_h256", 2, 256, 576, 512, 3000, 300, True, 1 / math.sqrt(576), "uniform", seed=5)
-    parity.case(w)
+    parity.case(w, kernel=wide_kernel)
 
 
 def test_wide_head_explicit_splits():

@@ -28,11 +28,12 @@ def _sinks(H, seed):
     return s
 
 
-@pytest.fixture(params=["tcgen05", "mma"])
+@pytest.fixture(params=["tcgen05", "mma", "basic"])
 def kernel(request):
-    """The kernel a test runs on: the library's own choice, or the warp-MMA
-    kernel (asked for through the forward's kernel-choice field)."""
-    return "auto" if request.param == "tcgen05" else "mma"
+    """The kernel a test runs on: the library's own choice, the warp-MMA
+    kernel, or the tcgen05 kernels that take a whole SM per CTA (asked for
+    through the forward's kernel-choice field)."""
+    return {"tcgen05": "auto", "mma": "mma", "basic": "basic"}[request.param]
 
 
 def _bf16_case(w, sinks, num_splits, idx=None, kernel="auto"):
