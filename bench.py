@@ -310,10 +310,10 @@ def forward_setup(binding, w, cache, kvs, sets, dev, stream, args, sinks=None):
     kernel = getattr(args, "kernel", "auto")
     out = torch.empty((T, H, w.D_v), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((T, H), dtype=torch.float32, device=dev)
-    splits = binding.smla_plan_num_splits(T, H, w.D_qk, w.topk, int(w.kv_fp8),
-                                          torch.cuda.get_device_properties(dev).multi_processor_count)
-    if args.bf16_dots or kernel != "auto":
-        splits = 0   # another kernel than the default: its own automatic plan
+    # the library's automatic plan (0); the split count it takes is reported
+    planned = binding.smla_plan_num_splits(T, H, w.D_qk, w.topk, int(w.kv_fp8),
+                                           torch.cuda.get_device_properties(dev).multi_processor_count)
+    splits = 0
     need = binding.sparse_mla_fwd_workspace_size(T, H, w.D_qk, w.D_v, w.topk, int(w.kv_fp8), splits)
     ws = torch.zeros(max(need, 1), dtype=torch.uint8, device=dev)
 
@@ -327,7 +327,7 @@ def forward_setup(binding, w, cache, kvs, sets, dev, stream, args, sinks=None):
             binding.sparse_mla_fwd(s["q"], cache, s["idx"], w.scale, kv_scale=kvs, dot_precision=dot, D_v=w.D_v,
                                    out=out, lse=lse, workspace=ws, num_splits=splits, stream=stream, sinks=sinks,
                                    kernel=kernel)
-    return call, dot, splits
+    return call, dot, planned
 
 
 def graph_of(call, R, warmup, stream):
@@ -380,14 +380,18 @@ def time_isolated(call, stream, flush, n=9):
 
 
 def ceiling_configs(row_bytes: int):
-    """(CTAs per SM, stages) pairs of the gather-ceiling sweep: for each CTA
-    count the most 64-row tiles that fit (as the probe pads its CTAs)."""
+    """(CTAs per SM, stages, pair mode) of the gather-ceiling sweep: for each
+    CTA count the most 64-row tiles that fit (as the probe pads its CTAs), and
+    CTA pairs that share each tile (1: cluster multicast, 2: bulk copy into
+    the peer)."""
     tile = 64 * 128 * ((row_bytes + 127) // 128)
     out = []
     for k in (1, 2, 3, 4):
         st = min(8, (233472 // k - 1024 - 1024 - 256) // tile)
         if st >= 1:
-            out.append((k, st))
+            out.append((k, st, 0))
+    for pm in (1, 2):
+        out.append((1, min(8, (233472 - 1024 - 1024 - 256) // tile), pm))
     return out
 
 
@@ -398,18 +402,18 @@ def gather_ceiling(binding, cache, sets, stream, reps: int = 4):
     valid = sum(int((s["idx_np"] != -1).sum()) for s in sets)
     sms = torch.cuda.get_device_properties(cache.device).multi_processor_count
     res = []
-    for k, st in ceiling_configs(row_bytes):
+    for k, st, pm in ceiling_configs(row_bytes):
         ck = torch.zeros(sms * k, dtype=torch.int32, device=cache.device)
 
-        def probe(i, k=k, st=st, ck=ck):
-            binding.smla_gather_probe(cache, sets[i % len(sets)]["idx"], ctas_per_sm=k, stages=st, checksum=ck,
-                                      stream=stream)
+        def probe(i, k=k, st=st, pm=pm, ck=ck):
+            binding.smla_gather_probe(cache, sets[i % len(sets)]["idx"], ctas_per_sm=k, stages=st, pair_mode=pm,
+                                      checksum=ck, stream=stream)
         g = graph_of(probe, len(sets), 3, stream)
         ms = time_steps(g, probe, len(sets), reps * len(sets), stream)
         sec = ms * 1e-3 / reps
-        res.append({"ctas_per_sm": k, "stages": st, "rows_per_s": round(valid / sec, 1),
+        res.append({"ctas_per_sm": k, "stages": st, "pair_mode": pm, "rows_per_s": round(valid / sec, 1),
                     "gbs": round(valid * row_bytes / sec / 1e9, 1)})
-    best = max(res, key=lambda r: r["gbs"])
+    best = max((r for r in res if not r["pair_mode"]), key=lambda r: r["gbs"])
     return {"row_bytes": row_bytes, "best_gbs": best["gbs"], "best_rows_per_s": best["rows_per_s"],
             "best": [best["ctas_per_sm"], best["stages"]], "sweep": res,
             "kernel": "smla_gather_probe (TMA tile::gather4 into a shared-memory ring, 64-row tiles, no arithmetic)"}
@@ -526,7 +530,7 @@ def run_ours(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(w, cache, kvs, sets, dot, splits, dev, stream, K, world, q8=args.q8)
+        e2e = run_e2e(w, cache, kvs, sets, dot, 0, dev, stream, K, world, q8=args.q8)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

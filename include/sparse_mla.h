@@ -84,11 +84,9 @@ typedef enum {
  *   WARP_MMA : the warp-level mma.sync kernel, for every supported shape and
  *              precision (a comparison path: slower, same results within the
  *              stated tolerances).
- *   TCGEN05_BASIC : the first tcgen05 kernels, whose CTAs take a whole SM and
- *              share nothing: for 16 heads over an E4M3 cache one CTA per SM
- *              (AUTO runs two lean ones per SM), for 128 heads two CTAs per row
- *              that each gather every key (AUTO pairs them in a cluster that
- *              gathers each key once); otherwise as AUTO. */
+ *   TCGEN05_BASIC : the first tcgen05 kernels, whose CTAs take a whole SM:
+ *              for 16 heads over an E4M3 cache one CTA per SM (AUTO runs two
+ *              lean ones per SM); otherwise as AUTO. */
 typedef enum {
     SMLA_KERNEL_AUTO = 0,
     SMLA_KERNEL_WARP_MMA = 1,
@@ -162,13 +160,18 @@ SMLA_API size_t sparse_mla_fwd_workspace_size(int T, int H, int D_qk, int D_v, i
  * lse          device, float [T, H], or NULL to skip.
  * workspace    device, >= sparse_mla_fwd_workspace_size(...) bytes, 256-byte
  *              aligned; may be NULL when that size is 0, which is the case for
- *              up to 8 splits (the splits of a row then form one thread-block
- *              cluster and merge through distributed shared memory). With more
- *              splits it holds the partial results and, in a fixed region at
- *              its start, one merge counter per (row, 16-head group). It must
- *              be zero-filled before its first use; every call returns its
- *              counters to zero and never writes partials into that region, so
- *              one buffer serves later calls of any shape on the same stream.
+ *              up to 8 splits with 16 heads: the splits of a row form one
+ *              thread-block cluster and merge through distributed shared
+ *              memory. The workspace opens with a fixed region of merge
+ *              counters, which must be zero-filled before the buffer's first
+ *              use; every call leaves that region zero, so one buffer serves
+ *              later calls of any shape on the same stream. With more than 8
+ *              splits, after the region, every split writes its partial output
+ *              in binary16 (T*H*S*D_v*2 bytes in all) and its lse, then takes a
+ *              counter ticket; the split that takes a row's last ticket merges
+ *              the row's partials (no split waits for another). The binary16
+ *              partials hold averages of value rows: a bf16 cache with values
+ *              beyond +-65504 is not supported with more than 8 splits.
  *              The 128-head E4M3 kernel (below) also needs a workspace, after
  *              that region: q quantized per (row, head), T*H*D_qk bytes, and
  *              its T*H scales.
@@ -187,7 +190,12 @@ SMLA_API size_t sparse_mla_fwd_workspace_size(int T, int H, int D_qk, int D_v, i
  *              field).
  * num_splits   0 = automatic (smla_plan_num_splits for the current device);
  *              otherwise the number of top-k splits to use, 1..128. More than 8
- *              splits need T * H / 16 <= 4096 (else SMLA_ERR_UNSUPPORTED).
+ *              splits need T * H / 16 <= 16384 (else SMLA_ERR_UNSUPPORTED).
+ *              For 128 heads over an E4M3 cache with fp8 dots the automatic
+ *              plan (0) also spreads the rows' key tiles evenly over pairs of
+ *              SMs when the rows outnumber the pairs (a row cut between two
+ *              pairs is merged through the workspace); 1 keeps one pair of
+ *              CTAs per row.
  * stream       CUDA stream.
  */
 SMLA_API smla_status sparse_mla_fwd(const void *q, const void *kv_cache, int kv_dtype,
@@ -281,11 +289,11 @@ SMLA_API smla_status sparse_mla_fwd_q8(const void *q8, const float *q_scale, con
  * the library uses a static device array of SMLA_NO_ALLOC_SCRATCH_BYTES
  * instead, and returns SMLA_ERR_WORKSPACE_TOO_SMALL (nothing launched) when
  * the call would need more. Two kinds of call need it:
- *   - more than 8 splits of a row (merge counters, then T * S * H * 2 KB of
- *     partial results);
+ *   - more than 8 splits of a row (merge counters, then T * S * H * 1 KB of
+ *     binary16 partial results);
  *   - the 128-head E4M3 kernel with fp8 dots (H a multiple of 128, D_qk = 576,
  *     one split), at any split plan: its quantized q, T * H * 580 bytes after
- *     a 16 KB counter region. T * H must stay below about 14,400: 128 rows of
+ *     a 64 KB counter region. T * H must stay below about 14,300: 128 rows of
  *     128 heads (9.5 MB) do not fit and are rejected.
  * Calls with bf16 dots or a bf16 cache and at most 8 splits use no workspace
  * and never touch the array. Nothing is allocated or freed. Each call looks
@@ -409,6 +417,19 @@ SMLA_API smla_status smla_fused_qk_rope_cache(const void *ql_nope, int64_t ql_st
  * uint32 [sm_count * ctas_per_sm]) and holds each tile hold_ns nanoseconds
  * before releasing it. SMLA_ERR_UNSUPPORTED when `stages` tiles do not fit
  * ctas_per_sm CTAs on one SM; ctas_per_sm in 1..4, stages in 1..8.
+ * pair_mode (with ctas_per_sm = 1): 0 = single CTAs; 1 or 2 = CTAs in pairs,
+ * each pair a thread-block cluster of two that takes the tiles one CTA would:
+ * each CTA gathers half of every tile's rows (so every row is read once) and
+ * delivers it to both CTAs, by cluster multicast of its gathers (1) or by a
+ * bulk copy of its landed half into the peer's ring (2); a stage is refilled
+ * once both consumers released it (the patterns of a pair that shares its key
+ * rows). Only the first CTA of a pair writes its checksum (the second writes
+ * 0). 3 = single CTAs launched in clusters of two (a control for 1 and 2).
+ * issue_warps: 0 = copy c of a tile (c < 16 * boxes per row, boxes =
+ * row_bytes / 128 rounded up; half that in pair modes 1 and 2) is issued by
+ * producer thread c of four warps; 1..8 = the copies are spread evenly over
+ * that many warps, ceil(copies / issue_warps) lanes each, which must not
+ * exceed 32 (else SMLA_ERR_BAD_SHAPE).
  *
  * smla_l2_read_probe: `blocks` blocks of 512 threads read the first `bytes`
  * of `buf` (a multiple of 16, 16-byte aligned) `reps` times with 16-byte
@@ -417,8 +438,8 @@ SMLA_API smla_status smla_fused_qk_rope_cache(const void *ql_nope, int64_t ql_st
  */
 SMLA_API smla_status smla_gather_probe(const void *pool, int64_t num_rows, int row_bytes,
                                        const int32_t *indices, int64_t n_indices, int ctas_per_sm,
-                                       int stages, int hold_ns, uint32_t *checksum,
-                                       smla_stream_t stream);
+                                       int stages, int hold_ns, int pair_mode, int issue_warps,
+                                       uint32_t *checksum, smla_stream_t stream);
 SMLA_API smla_status smla_l2_read_probe(const void *buf, int64_t bytes, int reps, uint32_t *checksum,
                                         int blocks, smla_stream_t stream);
 

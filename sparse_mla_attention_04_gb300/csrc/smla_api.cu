@@ -52,7 +52,7 @@ cudaError_t current_sm_count(int *out)
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // Which kernel serves a call.
-enum class Path { Mma, Umma16, Wide, Lean16, Wide2 };
+enum class Path { Mma, Umma16, Wide, Lean16 };
 
 // 16 heads with D_qk = D_v = 512: an E4M3 cache with fp8 dots runs on the
 // lean tcgen05 16-head kernel (two CTAs per SM: its random 512-byte row
@@ -60,8 +60,7 @@ enum class Path { Mma, Umma16, Wide, Lean16, Wide2 };
 // tcgen05 16-head kernel that takes a whole SM per CTA (its 1 KB row gathers
 // reach the DRAM bound already); a multiple of 128 heads with D_qk = 576,
 // D_v = 512 and an E4M3 cache with fp8 dots: the tcgen05 128-head kernel (no
-// split of the top-k list) whose two CTAs per row form a cluster that
-// gathers each key row once; every other shape or precision: the warp-MMA
+// split of the top-k list); every other shape or precision: the warp-MMA
 // kernel. `kernel` (smla_kernel_choice) can ask for the warp-MMA kernel, or
 // for the first tcgen05 kernels (whole SM per CTA, nothing shared).
 Path choose_path(int H, int D_qk, int D_v, bool kv_fp8, bool fp8_dots, int kernel)
@@ -71,7 +70,7 @@ Path choose_path(int H, int D_qk, int D_v, bool kv_fp8, bool fp8_dots, int kerne
     if (H == 16 && D_qk == 512 && D_v == 512)
         return kv_fp8 && kernel != SMLA_KERNEL_TCGEN05_BASIC ? Path::Lean16 : Path::Umma16;
     if (H % 128 == 0 && D_qk == 576 && D_v == 512 && kv_fp8)
-        return kernel == SMLA_KERNEL_TCGEN05_BASIC ? Path::Wide : Path::Wide2;
+        return Path::Wide;
     return Path::Mma;
 }
 
@@ -88,16 +87,15 @@ int tile_keys(Path p)
 // 8-CTA clusters, fast when few (2 rows), were slower than 6-CTA ones once
 // rows x splits passed 64 (16 rows: 28 us at 8 splits, 17.6 us at 6).
 constexpr int kMinKeysPerSplit = 128;
-constexpr int kAutoMaxSplits = smla::kClusterMaxSplits;
+using smla::kClusterMaxSplits;
 constexpr int kWideClusterSplits = 6;
 constexpr int64_t kWideClusterRowSplits = 64;
-using smla::kClusterMaxSplits;
 using smla::kMaxSplits;
 using smla::kTicketSlots;
 
 int plan_splits(int T, int H, int topk, int sm_count, Path path)
 {
-    if (T <= 0 || H <= 0 || topk <= 0 || sm_count <= 0 || path == Path::Wide || path == Path::Wide2)
+    if (T <= 0 || H <= 0 || topk <= 0 || sm_count <= 0 || path == Path::Wide)
         return 1;
     const int64_t units = (int64_t)T * (H / 16);
     const int64_t slots = (int64_t)sm_count * ctas_per_sm(path);
@@ -105,8 +103,8 @@ int plan_splits(int T, int H, int topk, int sm_count, Path path)
     const int64_t by_keys = topk / kMinKeysPerSplit;
     if (S > by_keys)
         S = by_keys;
-    if (S > kAutoMaxSplits)
-        S = kAutoMaxSplits;
+    if (S > kClusterMaxSplits)
+        S = kClusterMaxSplits;
     if (S > kWideClusterSplits && units * S > kWideClusterRowSplits)
         S = kWideClusterSplits;
     return S < 1 ? 1 : (int)S;
@@ -136,7 +134,7 @@ smla_status plan_forward(int T, int H, int D_qk, int D_v, int topk, int kv_dtype
     const bool kv_fp8 = kv_dtype == SMLA_KV_FP8_E4M3;
     const bool bf16_dots = kv_fp8 && dot_precision != SMLA_DOT_FP8; // bf16 q . dequantized K
     Path path = choose_path(H, D_qk, D_v, kv_fp8, !bf16_dots, kernel);
-    if ((path == Path::Wide || path == Path::Wide2) && num_splits > 1)
+    if ((path == Path::Wide) && num_splits > 1)
         path = Path::Mma; // the 128-head kernels do not split the top-k list
     int S = num_splits;
     if (S == 0) {
@@ -145,15 +143,43 @@ smla_status plan_forward(int T, int H, int D_qk, int D_v, int topk, int kv_dtype
             return cuda_status(e);
         S = plan_splits(T, H, topk, sms, path);
         if (bf16_dots && S > kClusterMaxSplits)
-            S = kClusterMaxSplits; // merged in a cluster: no workspace beyond the E4M3 query's
+            S = kClusterMaxSplits;
     }
     if (S > kClusterMaxSplits && (int64_t)T * (H / 16) > kTicketSlots)
         return SMLA_ERR_UNSUPPORTED;
+    // 128 heads: in the automatic plan the rows' (row, key tile) sequence is
+    // spread over pairs of CTAs, one pair per two SMs when the rows outnumber
+    // them (shared rows merge through the workspace's tickets; a CTA's tiles
+    // stay below 2^30); with an explicit single split, the first kernels, or
+    // no keys, one pair per row
+    int pairs = 0;
+    bool shared_rows = false;
+    if (path == Path::Wide) {
+        const int64_t rows = (int64_t)T * (H / 128);
+        const int64_t ntiles = (topk + 63) / 64;
+        pairs = (int)rows;
+        int sms = 0;
+        if (num_splits == 0 && kernel != SMLA_KERNEL_TCGEN05_BASIC && topk > 0 && rows * 2 <= kTicketSlots) {
+            if (const cudaError_t e = current_sm_count(&sms); e != cudaSuccess)
+                return cuda_status(e);
+            // spread only when one pair per row would leave many pairs idle in
+            // its last wave: the pieces of shared rows cost about as much as
+            // a sixth of a wave (128 rows on 76 pairs, 84% of the slots busy:
+            // 107 us per row pair against 109 us spread)
+            const int64_t P = sms / 2;
+            const int64_t waves = P > 0 ? (rows + P - 1) / P : 0;
+            if (P > 0 && rows > P && rows * 5 < waves * P * 4 && rows * ntiles / P + ntiles < (int64_t(1) << 30)) {
+                pairs = (int)P;
+                shared_rows = rows % pairs != 0;
+            }
+        }
+    }
     out->path = static_cast<int>(path);
     out->S = S;
     out->bf16_dots = bf16_dots;
-    out->layout = workspace_layout(T, H, D_qk, D_v, S, path == Path::Wide || path == Path::Wide2);
-    out->uses_tickets = S > kClusterMaxSplits;
+    out->wide_pairs = pairs;
+    out->layout = workspace_layout(T, H, D_qk, D_v, S, path == Path::Wide, shared_rows ? pairs : 0);
+    out->uses_tickets = S > kClusterMaxSplits || shared_rows;
     return SMLA_OK;
 }
 
@@ -161,7 +187,7 @@ smla_status plan_forward(int T, int H, int D_qk, int D_v, int topk, int kv_dtype
 
 namespace smla {
 
-WorkspaceLayout workspace_layout(int T, int H, int D_qk, int D_v, int S, bool wide)
+WorkspaceLayout workspace_layout(int T, int H, int D_qk, int D_v, int S, bool wide, int wide_pairs)
 {
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
     WorkspaceLayout w{};
@@ -171,14 +197,20 @@ WorkspaceLayout workspace_layout(int T, int H, int D_qk, int D_v, int S, bool wi
         w.q8_rope = up(w.q8 + (size_t)T * H * 512);
         w.q_scale = up(w.q8_rope + (size_t)T * H * (D_qk - 512));
         w.total = up(w.q_scale + (size_t)T * H * sizeof(float));
+        if (wide_pairs > 0) {
+            // two partial slots per pair and value half: [256 dims][128 heads] binary16 and 128 lse
+            w.wide_part_lse = w.total;
+            w.wide_part = up(w.wide_part_lse + (size_t)wide_pairs * 2 * 2 * 128 * sizeof(float));
+            w.total = up(w.wide_part + (size_t)wide_pairs * 2 * 2 * 128 * 256 * sizeof(uint16_t));
+        }
         return w;
     }
     if (S <= kClusterMaxSplits)
         return w;
     w.tickets = 0;
     w.part_lse = up((size_t)kTicketSlots * sizeof(int));
-    w.part_o = up(w.part_lse + (size_t)T * S * H * sizeof(float));
-    w.total = up(w.part_o + (size_t)T * S * H * D_v * sizeof(float));
+    w.part_o16 = up(w.part_lse + (size_t)T * S * H * sizeof(float));
+    w.total = up(w.part_o16 + (size_t)T * S * H * D_v * sizeof(uint16_t));
     return w;
 }
 
@@ -330,6 +362,7 @@ static smla_status fwd_impl(const void *q, bool q_fp8_in, const float *q_scale_i
             return SMLA_ERR_MISALIGNED;
     }
 
+    const bool wide = path == Path::Wide;
     smla::FwdArgs a{};
     a.q = q;
     a.kv = kv_cache;
@@ -338,10 +371,10 @@ static smla_status fwd_impl(const void *q, bool q_fp8_in, const float *q_scale_i
     a.out = out;
     a.lse = lse;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    a.part_o = wl.total ? reinterpret_cast<float *>(ws + wl.part_o) : nullptr;
-    a.part_lse = wl.total ? reinterpret_cast<float *>(ws + wl.part_lse) : nullptr;
-    a.tickets = wl.total ? reinterpret_cast<int *>(ws + wl.tickets) : nullptr;
-    const bool wide = path == Path::Wide || path == Path::Wide2;
+    const bool split_merge = S > kClusterMaxSplits && !wide;
+    a.part_o16 = split_merge ? reinterpret_cast<uint16_t *>(ws + wl.part_o16) : nullptr;
+    a.part_lse = split_merge ? reinterpret_cast<float *>(ws + wl.part_lse) : nullptr;
+    a.tickets = split_merge ? reinterpret_cast<int *>(ws + wl.tickets) : nullptr;
     a.q8 = wide ? ws + wl.q8 : nullptr;
     a.q8_rope = wide ? ws + wl.q8_rope : nullptr;
     a.q_scale = wide ? reinterpret_cast<float *>(ws + wl.q_scale) : nullptr;
@@ -359,6 +392,10 @@ static smla_status fwd_impl(const void *q, bool q_fp8_in, const float *q_scale_i
     a.sinks = sinks;
     a.q_fp8_in = q_fp8_in;
     a.q_scale_in = q_scale_in;
+    a.wide_pairs = plan.wide_pairs;
+    a.wide_part = wl.wide_part ? reinterpret_cast<uint16_t *>(ws + wl.wide_part) : nullptr;
+    a.wide_part_lse = wl.wide_part ? reinterpret_cast<float *>(ws + wl.wide_part_lse) : nullptr;
+    a.wide_tickets = wl.wide_part ? reinterpret_cast<int *>(ws) : nullptr;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     switch (path) {
     case Path::Umma16:
@@ -367,8 +404,6 @@ static smla_status fwd_impl(const void *q, bool q_fp8_in, const float *q_scale_i
         return cuda_status(smla::launch_fwd_lean16(a, st));
     case Path::Wide:
         return cuda_status(smla::launch_fwd_wide(a, st));
-    case Path::Wide2:
-        return cuda_status(smla::launch_fwd_wide2(a, st));
     default:
         return cuda_status(smla::launch_fwd_mma(a, st));
     }
@@ -415,12 +450,10 @@ SMLA_API smla_status smla_device_error(int *code, int reset)
 {
     if (code == nullptr)
         return SMLA_ERR_NULL_POINTER;
-    int c16 = 0, cw = 0, cp = 0, cg = 0, cl = 0, cw2 = 0;
+    int c16 = 0, cw = 0, cp = 0, cg = 0, cl = 0;
     if (const cudaError_t e = smla::read_umma_error(&c16, reset != 0); e != cudaSuccess)
         return cuda_status(e);
     if (const cudaError_t e = smla::read_lean_error(&cl, reset != 0); e != cudaSuccess)
-        return cuda_status(e);
-    if (const cudaError_t e = smla::read_wide2_error(&cw2, reset != 0); e != cudaSuccess)
         return cuda_status(e);
     if (const cudaError_t e = smla::read_probe_error(&cg, reset != 0); e != cudaSuccess)
         return cuda_status(e);
@@ -428,7 +461,7 @@ SMLA_API smla_status smla_device_error(int *code, int reset)
         return cuda_status(e);
     if (const cudaError_t e = smla::read_producer_error(&cp, reset != 0); e != cudaSuccess)
         return cuda_status(e);
-    *code = c16 | cw | cp | cg | cl | cw2;
+    *code = c16 | cw | cp | cg | cl;
     return SMLA_OK;
 }
 
@@ -526,21 +559,27 @@ SMLA_API smla_status smla_fp8_cache_write(const void *src, const int64_t *slot_m
 }
 
 SMLA_API smla_status smla_gather_probe(const void *pool, int64_t num_rows, int row_bytes, const int32_t *indices,
-                                       int64_t n_indices, int ctas_per_sm, int stages, int hold_ns,
-                                       uint32_t *checksum, smla_stream_t stream)
+                                       int64_t n_indices, int ctas_per_sm, int stages, int hold_ns, int pair_mode,
+                                       int issue_warps, uint32_t *checksum, smla_stream_t stream)
 {
     if (pool == nullptr || checksum == nullptr || (indices == nullptr && n_indices > 0))
         return SMLA_ERR_NULL_POINTER;
     if (num_rows < 0 || n_indices < 0 || row_bytes < 16 || row_bytes > 1024 || row_bytes % 16 != 0 ||
-        ctas_per_sm < 1 || ctas_per_sm > 4 || stages < 1 || stages > 8 || hold_ns < 0)
+        ctas_per_sm < 1 || ctas_per_sm > 4 || stages < 1 || stages > 8 || hold_ns < 0 ||
+        pair_mode < 0 || pair_mode > 3 || issue_warps < 0 || issue_warps > 8)
         return SMLA_ERR_BAD_SHAPE;
+    const int copies = (pair_mode == 1 || pair_mode == 2 ? 8 : 16) * ((row_bytes + 127) / 128);
+    if (issue_warps > 0 && (copies + issue_warps - 1) / issue_warps > 32)
+        return SMLA_ERR_BAD_SHAPE;
+    if (pair_mode && ctas_per_sm != 1)
+        return SMLA_ERR_UNSUPPORTED;
     if (!aligned(pool, 16) || !aligned(indices, 4) || !aligned(checksum, 4))
         return SMLA_ERR_MISALIGNED;
     int sms = 0;
     if (const cudaError_t e = current_sm_count(&sms); e != cudaSuccess)
         return cuda_status(e);
     const cudaError_t e = smla::launch_gather_probe(pool, num_rows, row_bytes, indices, n_indices, ctas_per_sm,
-                                                    stages, hold_ns, checksum, sms,
+                                                    stages, hold_ns, pair_mode, issue_warps, checksum, sms,
                                                     reinterpret_cast<cudaStream_t>(stream));
     if (e == cudaErrorInvalidValue)
         return SMLA_ERR_UNSUPPORTED; // the stages do not fit ctas_per_sm CTAs on an SM

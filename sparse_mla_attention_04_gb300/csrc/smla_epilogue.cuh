@@ -5,8 +5,9 @@
 // kClusterMaxSplits splits the row's CTAs form one thread-block cluster and
 // each merges a slice of the tile from every split's staging through
 // distributed shared memory (LSE weights). With more splits the partials go
-// to the workspace and the split that draws the last ticket (one atomic; no
-// spinning) merges them.
+// to the workspace in binary16 and the split that draws the last ticket (one
+// atomic; no spinning) merges them, summing the splits in index order from
+// the same binary16 values whichever split that is.
 //
 // Attention sinks: a per-head sink logit (natural-log units, like the lse)
 // joins the softmax denominator once per row: with one split the staged
@@ -141,12 +142,24 @@ __device__ __forceinline__ void finish_tile(const FwdArgs &a, float *ost, const 
         return;
     }
 
-    // ---- many splits: (o_j, lse_j) to the workspace, then take a ticket ----
-    float *po = a.part_o + (((int64_t)t * a.S + s) * a.H + hbase) * kDv;
-    for (int e = tid; e < kHeads * kDv / 4; e += kThreads)
-        __stcg(reinterpret_cast<float4 *>(po) + e, reinterpret_cast<const float4 *>(ost)[e]);
+    // ---- many splits: (o_s, lse_s) to the workspace (o_s in binary16), then
+    // take a ticket; the split that draws the row's last ticket merges (no
+    // split waits for another: more splits than a cluster holds need not be
+    // co-resident).
+    const int64_t rowbase = (int64_t)t * a.S;
+    uint4 *po = reinterpret_cast<uint4 *>(a.part_o16 + ((rowbase + s) * a.H + hbase) * kDv);
+    for (int e = tid; e < kHeads * kDv / 8; e += kThreads) {
+        const float4 x = reinterpret_cast<const float4 *>(ost)[2 * e];
+        const float4 y = reinterpret_cast<const float4 *>(ost)[2 * e + 1];
+        uint4 u;
+        u.x = pack_f16x2(x.x, x.y);
+        u.y = pack_f16x2(x.z, x.w);
+        u.z = pack_f16x2(y.x, y.y);
+        u.w = pack_f16x2(y.z, y.w);
+        __stcg(po + e, u);
+    }
     if (tid < kHeads)
-        __stcg(a.part_lse + ((int64_t)t * a.S + s) * a.H + hbase + tid, lse_s[tid]);
+        __stcg(a.part_lse + (rowbase + s) * a.H + hbase + tid, lse_s[tid]);
     __threadfence();
     __syncthreads();
     if (tid == 0) {
@@ -162,16 +175,19 @@ __device__ __forceinline__ void finish_tile(const FwdArgs &a, float *ost, const 
         return;
     __threadfence();
 
-    // ---- last CTA of the row: LSE merge of the S partials ----
+    // ---- last split of the row: LSE merge of the S partials ----
+    // every split's lse (loaded in parallel), then the weights per (split, head)
+    for (int i = tid; i < a.S * kHeads; i += kThreads)
+        wts[i] = __ldcg(a.part_lse + (rowbase + i / kHeads) * a.H + hbase + i % kHeads);
+    __syncthreads();
     if (tid < kHeads) {
         const float sk = sink(tid);
         float mx = sk;
         for (int j = 0; j < a.S; ++j)
-            mx = fmaxf(mx, __ldcg(a.part_lse + ((int64_t)t * a.S + j) * a.H + hbase + tid));
+            mx = fmaxf(mx, wts[j * kHeads + tid]);
         float tot = (mx == -INFINITY || sk == -INFINITY) ? 0.f : expf(sk - mx); // the sink: no output
         for (int j = 0; j < a.S; ++j) {
-            const float lj = __ldcg(a.part_lse + ((int64_t)t * a.S + j) * a.H + hbase + tid);
-            const float e = (mx == -INFINITY) ? 0.f : expf(lj - mx);
+            const float e = (mx == -INFINITY) ? 0.f : expf(wts[j * kHeads + tid] - mx);
             wts[j * kHeads + tid] = e;
             tot += e;
         }
@@ -182,24 +198,71 @@ __device__ __forceinline__ void finish_tile(const FwdArgs &a, float *ost, const 
             a.lse[(int64_t)t * a.H + hbase + tid] = (mx == -INFINITY) ? -INFINITY : mx + logf(tot);
     }
     __syncthreads();
-    for (int e = tid; e < kHeads * kDv / 4; e += kThreads) {
-        const int h = e / (kDv / 4);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < a.S; ++j) {
-            const float w = wts[j * kHeads + h];
-            const float4 x = (j == s) ? reinterpret_cast<const float4 *>(ost)[e]
-                                      : __ldcg(reinterpret_cast<const float4 *>(
-                                                   a.part_o + (((int64_t)t * a.S + j) * a.H + hbase) * kDv) +
-                                               e);
-            acc.x += w * x.x;
-            acc.y += w * x.y;
-            acc.z += w * x.z;
-            acc.w += w * x.w;
+    // groups of 8 values; a thread takes kU groups and, two splits at a time,
+    // issues all their loads before accumulating. This split's own partial is
+    // rounded to binary16 from shared memory, exactly as the others stored
+    // theirs, and the splits are summed in index order: whichever split merges,
+    // the result is the same bits.
+    constexpr int E8 = kHeads * kDv / 8;
+    constexpr int kU = 4;
+    const uint4 *pall = reinterpret_cast<const uint4 *>(a.part_o16 + (rowbase * a.H + hbase) * kDv);
+    const int64_t split_stride = (int64_t)a.H * kDv / 8; // uint4 per split
+    auto own16 = [&](int e) {
+        const float4 x = reinterpret_cast<const float4 *>(ost)[2 * e];
+        const float4 y = reinterpret_cast<const float4 *>(ost)[2 * e + 1];
+        return make_uint4(pack_f16x2(x.x, x.y), pack_f16x2(x.z, x.w), pack_f16x2(y.x, y.y), pack_f16x2(y.z, y.w));
+    };
+    for (int e0 = tid; e0 < E8; e0 += kU * kThreads) {
+        float acc[kU][8];
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                acc[u][c] = 0.f;
+        for (int j0 = 0; j0 < a.S; j0 += 2) {
+            uint4 raw[2][kU];
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const int j = j0 + jj;
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int e = e0 + u * kThreads;
+                    raw[jj][u] = (j >= a.S || e >= E8) ? make_uint4(0u, 0u, 0u, 0u)
+                                 : (j == s)              ? own16(e)
+                                                         : __ldcg(pall + j * split_stride + e);
+                }
+            }
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const int j = j0 + jj;
+                if (j >= a.S)
+                    continue;
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int e = min(e0 + u * kThreads, E8 - 1);
+                    const float w = wts[j * kHeads + e / (kDv / 8)];
+                    const uint32_t q[4] = {raw[jj][u].x, raw[jj][u].y, raw[jj][u].z, raw[jj][u].w};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&q[c]));
+                        acc[u][2 * c] += w * f.x;
+                        acc[u][2 * c + 1] += w * f.y;
+                    }
+                }
+            }
         }
-        uint2 u;
-        u.x = pack_bf16x2(acc.x, acc.y);
-        u.y = pack_bf16x2(acc.z, acc.w);
-        *reinterpret_cast<uint2 *>(out + (int64_t)e * 4) = u;
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int e = e0 + u * kThreads;
+            if (e < E8) {
+                uint4 v;
+                v.x = pack_bf16x2(acc[u][0], acc[u][1]);
+                v.y = pack_bf16x2(acc[u][2], acc[u][3]);
+                v.z = pack_bf16x2(acc[u][4], acc[u][5]);
+                v.w = pack_bf16x2(acc[u][6], acc[u][7]);
+                *reinterpret_cast<uint4 *>(out + (int64_t)e * 8) = v;
+            }
+        }
     }
 }
 

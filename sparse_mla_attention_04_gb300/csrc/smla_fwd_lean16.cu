@@ -615,6 +615,7 @@ cudaError_t launch_fwd_lean16(const FwdArgs &a, cudaStream_t stream)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (a.S > 1 && a.S <= kClusterMaxSplits) {
+        // the S splits of a (row, head group) are consecutive blocks: one cluster
         attr[1].id = cudaLaunchAttributeClusterDimension;
         attr[1].val.clusterDim.x = (unsigned)a.S;
         attr[1].val.clusterDim.y = 1;

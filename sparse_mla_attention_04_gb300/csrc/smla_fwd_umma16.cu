@@ -38,13 +38,14 @@
 //     then per tile one gather4 per thread into the stage ring, completing
 //     the stage's "full" barrier by transaction bytes. A stage is refilled
 //     once everything that reads it is done ("empty").
-//   MMA issuers (one thread each in warps 4, 9, 10): two issue the halves
-//     of QK(i) as soon as tile i has landed (and the softmax is done with the
-//     S buffer), one issues PV(i) as soon as the softmax has written P(i). A
-//     single thread issues small MMAs at about one per 26 ns; two threads
-//     issue in parallel, so splitting a tile's MMAs across three issuers
-//     shortens the time each stage is held. Commits signal the softmax (S
-//     full), the producers (stage empty) and the P buffers.
+//   MMA issuers (one thread each in warps 4, 9, 10, and 11 for bf16): QK(i)
+//     as soon as tile i has landed (and the softmax is done with the S
+//     buffer), in two halves for bf16; PV(i) as soon as the softmax has
+//     written P(i), two threads each taking half of the value dims. A single
+//     thread issues small MMAs at about one per 26 ns; threads issue in
+//     parallel, so splitting a tile's MMAs across issuers shortens the time
+//     each stage is held and the chain of the last tile. Commits signal the
+//     softmax (S full), the producers (stage empty) and the P buffers.
 //   converters (E4M3 only, warps 11-14, one per quarter of the TMEM lanes):
 //     tile i -> V^T in tensor memory buffer i%3 once PV(i-3) has read it
 //     (three buffers: the conversion of a tile overlaps the PV of the two
@@ -94,7 +95,7 @@ constexpr int kMmaWarp = 4;       // QK, first half of the columns
 constexpr int kProducerWarp0 = 5;
 constexpr int kProducerWarps = 4;
 constexpr int kProducerThreads = 32 * kProducerWarps;
-constexpr int kMmaWarp2 = kProducerWarp0 + kProducerWarps; // QK second half; PV in the next warp
+constexpr int kMmaWarp2 = kProducerWarp0 + kProducerWarps; // more MMA issuers: warps 9, 10 (and 11 for bf16)
 constexpr int kConverterWarp0 = kMmaWarp2 + 2;             // E4M3 only
 constexpr int kConverterThreads = 128;
 // tensor memory columns: O^T 0..63, S^T partial p of buffer b at kSCol + 32 p + 16 b
@@ -121,7 +122,7 @@ struct Cfg {
     static constexpr int KSTEP = FP8 ? 32 : 16;   // reduction depth of one QK MMA
     static constexpr int QK_MMAS = kD / KSTEP;    // per tile (32 | 16)
     static constexpr int QK_ISSUERS = FP8 ? 1 : 2; // threads issuing QK (S partial sums)
-    static constexpr int PV_ISSUERS = FP8 ? 2 : 1; // threads issuing PV (halves of the 512 dims)
+    static constexpr int PV_ISSUERS = 2;           // threads issuing PV (halves of the 512 dims)
     static constexpr int OFF_QSTG = STAGES * TILE; // E4M3: bf16 q staged for the quantizer (16 KB)
     static constexpr int OFF_Q = OFF_QSTG + (FP8 ? kHeads * kD * 2 : 0); // q [16 x 512] in core matrices
     static constexpr int QGRP = 8 * ROW;          // q: 8 heads x 512 elements
@@ -147,12 +148,12 @@ struct Cfg {
     static_assert(!FP8 || VCOL + VBUFS * 128 <= TMEM_COLS, "the V^T buffers fit in tensor memory");
     static constexpr int SMEM = OFF_MBAR + NBAR * 8;
     static constexpr int SMEM_ALLOC = SMEM + 1024; // the base is aligned up to 1 KB in the kernel
-    static constexpr int THREADS = 32 * (FP8 ? kConverterWarp0 + 4 : kConverterWarp0);
+    static constexpr int THREADS = 32 * (FP8 ? kConverterWarp0 + 4 : kMmaWarp2 + 3);
     // E4M3: 15 warps share the register file, so at most 128 registers a thread
     static constexpr int BOUND_THREADS = FP8 ? 512 : THREADS;
-    // stage "empty" arrivals: the PV commit (bf16), or the QK commits and every
+    // stage "empty" arrivals: the PV commits (bf16), or the QK commits and every
     // converter thread (E4M3: PV reads V^T from tensor memory, not the stage)
-    static constexpr int EMPTY_COUNT = FP8 ? QK_ISSUERS + kConverterThreads : 1;
+    static constexpr int EMPTY_COUNT = FP8 ? QK_ISSUERS + kConverterThreads : PV_ISSUERS;
     static_assert(STAGES * TILE >= kHeads * kD * 4, "epilogue staging fits in the ring");
     static_assert(2 * QGRP >= 128 * kHeads * 4, "merge weights fit in the q area");
     static_assert(COPIES <= kProducerThreads, "one copy per producer thread at most");
@@ -284,28 +285,31 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
         fetch(3, r3);
         // q [16 x 512] -> core matrices (8 heads x 16 B): LBO 128 (K), SBO = 8 heads;
         // published once the first tile's copies are in flight, so both latencies overlap
-        if constexpr (!FP8) {
-            for (int e = pt; e < kHeads * 64; e += kProducerThreads) {
-                const int h = e >> 6, c = e & 63;
-                cp_async_16(q_s + (h >> 3) * C::QGRP + c * 128 + (h & 7) * 16, qg + h * kD + c * 8, 16);
-            }
-        } else if (a.q_fp8_in) {
-            // pre-quantized q: each head's 512 codes straight into core matrices
-            // (a core-matrix row holds 16 codes)
-            const uint8_t *q8g = static_cast<const uint8_t *>(a.q) + (int64_t)t * kHeads * kD;
-            for (int e = pt; e < kHeads * (kD / 16); e += kProducerThreads) {
-                const int h = e / (kD / 16), c = e % (kD / 16);
-                cp_async_16(q_s + (h >> 3) * C::QGRP + c * 128 + (h & 7) * 16, q8g + h * kD + c * 16, 16);
-            }
-        } else {
-            // bf16 q staged row-major: this thread's 64 elements of head pt/8,
-            // the ones it quantizes
-            const int h = pt >> 3, e0 = h * kD + (pt & 7) * 64;
+        auto issue_q = [&] {
+            if constexpr (!FP8) {
+                for (int e = pt; e < kHeads * 64; e += kProducerThreads) {
+                    const int h = e >> 6, c = e & 63;
+                    cp_async_16(q_s + (h >> 3) * C::QGRP + c * 128 + (h & 7) * 16, qg + h * kD + c * 8, 16);
+                }
+            } else if (a.q_fp8_in) {
+                // pre-quantized q: each head's 512 codes straight into core matrices
+                // (a core-matrix row holds 16 codes)
+                const uint8_t *q8g = static_cast<const uint8_t *>(a.q) + (int64_t)t * kHeads * kD;
+                for (int e = pt; e < kHeads * (kD / 16); e += kProducerThreads) {
+                    const int h = e / (kD / 16), c = e % (kD / 16);
+                    cp_async_16(q_s + (h >> 3) * C::QGRP + c * 128 + (h & 7) * 16, q8g + h * kD + c * 16, 16);
+                }
+            } else {
+                // bf16 q staged row-major: this thread's 64 elements of head pt/8,
+                // the ones it quantizes
+                const int h = pt >> 3, e0 = h * kD + (pt & 7) * 64;
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                cp_async_16(sbase + C::OFF_QSTG + (e0 + 8 * u) * 2, qg + e0 + 8 * u, 16);
-        }
-        cp_async_commit();
+                for (int u = 0; u < 8; ++u)
+                    cp_async_16(sbase + C::OFF_QSTG + (e0 + 8 * u) * 2, qg + e0 + 8 * u, 16);
+            }
+            cp_async_commit();
+        };
+        issue_q();
         bool q_pending = true;
         auto publish_q = [&] {
             cp_async_wait<0>();
@@ -402,13 +406,13 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
             for (int j = max(0, issued - S_); j < issued; ++j)
                 wait_issued(full(j % S_), (uint32_t)((j / S_) & 1));
         }
-    } else if (warp == kMmaWarp || warp == kMmaWarp2 || warp == kMmaWarp2 + 1) {
+    } else if (warp == kMmaWarp || (warp >= kMmaWarp2 && warp < kMmaWarp2 + C::QK_ISSUERS + C::PV_ISSUERS - 1)) {
         // ======================= MMA issuers =======================
         if (lane == 0) {
-            // role 0: QK part 0; role 1: QK part 1 (bf16) or PV dims 256..511 (E4M3);
-            // role 2: PV (bf16) or PV dims 0..255 (E4M3)
+            // roles 0 .. QK_ISSUERS-1: parts of QK; the next PV_ISSUERS: PV over
+            // halves of the value dims (M-blocks 2 v, 2 v + 1 for PV issuer v)
             const int role = warp == kMmaWarp ? 0 : 1 + warp - kMmaWarp2;
-            const bool is_pv = role == 2 || (role == 1 && C::PV_ISSUERS == 2);
+            const bool is_pv = role >= C::QK_ISSUERS;
             if (role < C::QK_ISSUERS) {
                 wait_bar(q_full, 0);
                 const uint64_t qdesc = umma::desc(q_s, 128, C::QGRP);
@@ -439,8 +443,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
                         umma::commit(empty(st)); // this half of QK(i) no longer reads the stage
                 }
             } else if (is_pv) {
-                const int blk0 = C::PV_ISSUERS == 2 && role == 1 ? 2 : 0;
-                const int blk1 = C::PV_ISSUERS == 2 && role == 2 ? 2 : 4;
+                const int blk0 = 2 * (role - C::QK_ISSUERS), blk1 = blk0 + 2;
                 for (int i = 0; i < ntiles; ++i) {
                     const int b = i & 1, st = i % S_;
                     wait_bar(p_full(b), (uint32_t)((i >> 1) & 1));
@@ -472,7 +475,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
                     // p_empty(b) also tells the softmax (and the converters) that O^T holds
                     // PV(0..i): each issuer's commit covers all its earlier MMAs.
                     if constexpr (!FP8)
-                        umma::commit(empty(st));
+                        umma::commit(empty(st)); // this half of PV(i) no longer reads the stage
                     else
                         umma::commit(v_free(vb));
                     umma::commit(p_empty(b));
@@ -739,8 +742,7 @@ cudaError_t launch(const FwdArgs &a, cudaStream_t stream)
         return cudaErrorInvalidValue;
 
     // programmatic dependent launch (the kernel waits for its predecessor in
-    // grid_wait after a prologue that reads no global memory), and the row's
-    // splits as one cluster when they merge through distributed shared memory
+    // grid_wait after a prologue that reads no global memory)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(C::THREADS);
@@ -752,6 +754,7 @@ cudaError_t launch(const FwdArgs &a, cudaStream_t stream)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (a.S > 1 && a.S <= kClusterMaxSplits) {
+        // the S splits of a (row, head group) are consecutive blocks: one cluster
         attr[1].id = cudaLaunchAttributeClusterDimension;
         attr[1].val.clusterDim.x = (unsigned)a.S;
         attr[1].val.clusterDim.y = 1;

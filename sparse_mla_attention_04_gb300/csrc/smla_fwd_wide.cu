@@ -6,9 +6,23 @@
 //   S   [128 heads x 64 keys]  = q8 [128 x 576] . K_tile^T          (E4M3, 18 MMAs, M=128 N=64)
 //   O^T [256 dims x 128 heads] += V^T[half] [256 x 64] . P^T        (fp16, 8 MMAs, 2 x M=128 N=128)
 // The fp32 output for 128 heads x 512 dims alone would fill an SM's tensor
-// memory (256 KB), so each query row runs as two CTAs, each owning one half
-// of the value dims; both compute the full QK and softmax (identical inputs,
-// identical P).
+// memory (256 KB), so each query row runs on a pair of CTAs, each owning one
+// half of the value dims; both compute the full QK and softmax (identical
+// inputs, identical P), and the second gather of each key row mostly hits L2.
+//
+// Work is spread over the pairs stream-K style: the sequence of (row, 64-key
+// tile) units is cut into as many contiguous ranges as there are pairs (one
+// pair per two SMs when the rows outnumber them), so no SM idles in a second
+// wave. A range of at least a row's length holds whole rows and at most two
+// pieces of rows it shares with a neighbouring pair: the end of its first row
+// (run first) and the beginning of its last (run last). A piece of a shared
+// row that finds the other piece finished merges at once, its own half
+// straight from tensor memory and the other from the workspace; otherwise it
+// stores a normalised partial (binary16, in units of the cache's codes) with
+// its lse and marks itself finished, and whichever of the two sees the other
+// finished merges (one atomic per piece, no spinning).
+// At each new piece a CTA reloads that row's q8 and starts a fresh
+// accumulation in tensor memory once the previous piece has been read out.
 //
 // Tensor memory (512 columns): O^T in 0..255 (two M-blocks of 128 dims x 128
 // heads), S in 256 + 64 b (double-buffered), V^T in 384 + 64 b (binary16,
@@ -24,10 +38,15 @@
 // CTA copies its 128 heads with four TMA tile loads and one bulk copy.
 //
 // Warp roles, handing tiles over through mbarriers (every wait bounded):
-//   producers (warps 5-8): per 64-key tile 80 TMA tile::gather4 copies (16
+//   producers (warps 6-11): per 64-key tile 80 TMA tile::gather4 copies (16
 //     key quads x 5 column blocks of 128 B; the last block reaches past
-//     column 576 and is zero filled). Masked and out-of-range indices are
-//     passed as row -1 (zero fill, no memory read).
+//     column 576 and is zero filled), 13 or 14 from each warp: the copies of
+//     one warp are issued one after another, so six warps start a tile's
+//     gathers well over twice as soon as two and a half would. Each warp adds
+//     its own bytes to the stage's barrier. (Six, not eight: with 16 warps an
+//     SM sub-partition holds four, which leaves 128 registers a thread.)
+//     Masked and out-of-range indices are passed as row -1 (zero fill, no
+//     memory read).
 //   QK issuer (warp 4): S(i) once tile i has landed and the softmax has read
 //     S(i-2).
 //   softmax (warps 0-3, thread = head, whole S row in the thread): masks,
@@ -36,10 +55,10 @@
 //     O^T columns are rescaled in tensor memory) only when a logit exceeds
 //     it by more than 2^8, and then to 2^8 above the tile max; writes its
 //     row of P^T (fp16).
-//   converters (warps 10-13, one per quarter of the TMEM lanes): the tile's
+//   converters (warps 12-15, one per quarter of the TMEM lanes): the tile's
 //     half of the value columns, E4M3 -> binary16 (exact), as V^T into
 //     tensor memory (4x4 byte transposes within lane quads).
-//   PV issuer (warp 9): O^T += V^T(i) . P^T(i) once both are written.
+//   PV issuer (warp 5): O^T += V^T(i) . P^T(i) once both are written.
 //
 // Method sources (page titles and sections):
 //   "Enable AITER sparse MLA on gfx942, including FP8 KV" — Overview, Details
@@ -69,8 +88,6 @@ constexpr int kKeys = 64;      // keys per tile (N of QK)
 constexpr int kQkSteps = kDqk / 32;   // 18 E4M3 k-steps of 32
 constexpr int kCB = 5;                // 128-byte column blocks per cache row (the last half used)
 constexpr int kStages = 3;
-constexpr int kCopies = 16 * kCB;     // gather4 copies per tile
-constexpr int kIdxAhead = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f; // log2 units a logit may exceed the reference by
@@ -78,12 +95,15 @@ constexpr float kHeadroom = 8.0f;         // a moved reference sits this far abo
 
 // warps 0-3: softmax
 constexpr int kQkWarp = 4;
-constexpr int kProducerWarp0 = 5;     // warps 5-8
-constexpr int kPvWarp = 9;
-constexpr int kConverterWarp0 = 10;   // warps 10-13
-constexpr int kThreads = 14 * 32;
-constexpr int kProducerThreads = 128;
+constexpr int kPvWarp = 5;
+constexpr int kProducerWarp0 = 6;     // warps 6-11
+constexpr int kProducerWarps = 6;
+constexpr int kCopies = 16 * kCB;     // gather4 copies per tile
+constexpr int kCopiesPerWarp = (kCopies + kProducerWarps - 1) / kProducerWarps; // 14 (the last warp 10)
+constexpr int kConverterWarp0 = kProducerWarp0 + kProducerWarps; // warps 12-15
+constexpr int kThreads = (kConverterWarp0 + 4) * 32;
 constexpr int kConverterThreads = 128;
+constexpr int kIdxAhead = 4;          // tiles of index look-ahead in the producers
 
 // shared memory (bytes from a 1 KB-aligned base)
 constexpr int kQBlk = kHeads * 128;           // one swizzled column block of q8 (16 KB)
@@ -97,14 +117,17 @@ constexpr int kPT = kHeads * 128;             // P^T: 128 heads x 64 keys fp16 (
 constexpr int kOffPT = kOffRing + kStages * kTile;
 constexpr int kOffAlpha = kOffPT + 2 * kPT;   // [128] per-head factors (rescale, then 1/l)
 constexpr int kOffEx = kOffAlpha + kHeads * 4;// [2][4] exceed flags
-constexpr int kOffMisc = kOffEx + 32;         // tmem address, abort, go[2]
-constexpr int kOffMbar = kOffMisc + 32;
-// full[3], empty[3], s_full[2], p_full[2], p_empty[2], v_full[2], q_full, drain
-constexpr int kNBar = 16;
+constexpr int kOffWts = kOffEx + 32;          // [2][128] merge weights of a shared row
+constexpr int kOffMisc = kOffWts + 2 * kHeads * 4; // tmem address, abort, last
+constexpr int kOffSeg = kOffMisc + 32;        // the CTA's work segments
+constexpr int kOffMbar = kOffSeg + 64;
+// full[3], empty[3], s_full[2], p_full[2], p_empty[2], v_full[2], q_full, drain, q_free, o_free
+constexpr int kNBar = 18;
 constexpr int kSmem = kOffMbar + kNBar * 8;
 constexpr int kSmemAlloc = kSmem + 1024;
 static_assert(kOffRing % 1024 == 0 && kOffPT % 1024 == 0, "swizzle atoms need 1 KB alignment");
 static_assert(kSmemAlloc <= 227 * 1024, "shared memory budget");
+static_assert(kCopies * 512 == kTile && kCopiesPerWarp <= 32, "the producer warps fill a tile");
 
 // tensor memory columns
 constexpr int kTmemCols = 512;
@@ -200,7 +223,59 @@ __global__ void __launch_bounds__(128) quantize_q_e4m3_kernel(const __nv_bfloat1
     }
 }
 
-__global__ void __launch_bounds__(512, 1)
+// A CTA's work: up to three segments of consecutive (row, key tile) units,
+// run in this order: the end of the first row of its range, the whole rows
+// between (a segment may run over many rows), then the beginning of the last
+// row. The neighbour that holds the other piece of a shared row runs that
+// piece first, so it has usually finished by the time this CTA reaches the
+// row's beginning, which then merges straight from tensor memory.
+struct SegTab {
+    int64_t t[3];
+    int hg[3], k[3], len[3];
+    int n;
+};
+static_assert(sizeof(SegTab) <= 64, "segment table fits its shared-memory slot");
+
+// A walk over the segments: the current unit (row t, head group hg, key tile
+// k), the units left in its segment, and whether a piece (a run of one row's
+// tiles) starts here.
+struct Cur {
+    int64_t t;
+    int hg, k, left, seg;
+    bool begin;
+};
+
+__device__ __forceinline__ void cur_load(Cur &c, const SegTab &s, int i)
+{
+    c.seg = i;
+    c.left = 0;
+    if (i < s.n) {
+        c.t = s.t[i];
+        c.hg = s.hg[i];
+        c.k = s.k[i];
+        c.left = s.len[i];
+        c.begin = true;
+    }
+}
+
+__device__ __forceinline__ void cur_next(Cur &c, const SegTab &s, int ntiles, int G)
+{
+    if (--c.left > 0) {
+        c.begin = false;
+        if (++c.k == ntiles) {
+            c.k = 0;
+            c.begin = true;
+            if (++c.hg == G) {
+                c.hg = 0;
+                ++c.t;
+            }
+        }
+    } else {
+        cur_load(c, s, c.seg + 1);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
     sparse_mla_fwd_wide_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap kv_map,
                                const __grid_constant__ CUtensorMap q8_map)
 {
@@ -214,7 +289,9 @@ __global__ void __launch_bounds__(512, 1)
     int *ex_s = reinterpret_cast<int *>(smem + kOffEx);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     int *abort_s = reinterpret_cast<int *>(smem + kOffMisc + 4);
-    volatile int *go_s = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
+    volatile int *last_s = reinterpret_cast<volatile int *>(smem + kOffMisc + 8);
+    float *wts_s = reinterpret_cast<float *>(smem + kOffWts); // [2][128] merge weights
+    SegTab &sg = *reinterpret_cast<SegTab *>(smem + kOffSeg);
     const uint32_t bar0 = sbase + kOffMbar;
     auto full = [&](int st) { return bar0 + 8 * st; };
     auto empty = [&](int st) { return bar0 + 8 * (3 + st); };
@@ -224,18 +301,18 @@ __global__ void __launch_bounds__(512, 1)
     auto v_full = [&](int b) { return bar0 + 8 * (12 + b); };
     const uint32_t q_full = bar0 + 8 * 14;
     const uint32_t drain = bar0 + 8 * 15;
+    const uint32_t q_free = bar0 + 8 * 16; // the QK MMAs of a finished piece no longer read q8
+    const uint32_t o_free = bar0 + 8 * 17; // a finished piece's O^T has been read out
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = a.H / kHeads;
     const int half = blockIdx.x & 1;
-    const int hg = (blockIdx.x >> 1) % G;
-    const int t = (blockIdx.x >> 1) / G;
+    const int64_t pair = blockIdx.x >> 1;
     const int ntiles = (a.topk + kKeys - 1) / kKeys;
-    const int32_t *__restrict__ row_idx = a.indices + (int64_t)t * a.topk;
 
     if (tid == 0) {
         for (int st = 0; st < kStages; ++st) {
-            umma::mbar_init(full(st), 1);
+            umma::mbar_init(full(st), kProducerWarps);      // each producer warp: its bytes
             umma::mbar_init(empty(st), 1 + kConverterThreads); // QK commit + converters
         }
         for (int b = 0; b < 2; ++b) {
@@ -246,8 +323,46 @@ __global__ void __launch_bounds__(512, 1)
         }
         umma::mbar_init(q_full, 1);
         umma::mbar_init(drain, 2);
+        umma::mbar_init(q_free, 1);
+        umma::mbar_init(o_free, 128);
         umma::mbar_init_fence();
         *abort_s = 0;
+        // this pair's range [u0, u1) of the (row, key tile) sequence and its segments
+        const int64_t rows = (int64_t)a.T * G, P = a.wide_pairs;
+        int64_t u0 = 0, u1 = 0;
+        if (P == rows) {
+            u0 = pair * ntiles;
+            u1 = u0 + ntiles;
+        } else {
+            const int64_t U = rows * ntiles;
+            u0 = pair * U / P;
+            u1 = (pair + 1) * U / P;
+        }
+        sg.n = 0;
+        auto add = [&](int64_t r, int k, int64_t len) {
+            if (len <= 0)
+                return;
+            sg.t[sg.n] = r / G;
+            sg.hg[sg.n] = (int)(r % G);
+            sg.k[sg.n] = k;
+            sg.len[sg.n] = (int)len;
+            ++sg.n;
+        };
+        if (u1 > u0) {
+            const int64_t rf = u0 / ntiles, rl = (u1 - 1) / ntiles;
+            const int kf = (int)(u0 % ntiles), kl = (int)((u1 - 1) % ntiles);
+            if (rf == rl) {
+                add(rf, kf, u1 - u0);
+            } else {
+                if (kf != 0)
+                    add(rf, kf, ntiles - kf); // the end of the first row
+                const int64_t w0 = kf != 0 ? rf + 1 : rf, w1 = kl != ntiles - 1 ? rl - 1 : rl;
+                if (w1 >= w0)
+                    add(w0, 0, (w1 - w0 + 1) * ntiles);
+                if (kl != ntiles - 1)
+                    add(rl, 0, kl + 1);       // the beginning of the last
+            }
+        }
     }
     if (warp == kQkWarp)
         umma::alloc(smem_u32(tmem_slot), kTmemCols);
@@ -255,21 +370,15 @@ __global__ void __launch_bounds__(512, 1)
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    int n = 0; // tiles of this CTA
+    for (int i = 0; i < sg.n; ++i)
+        n += sg.len[i];
     // the prologue above touches no global memory: from here on the previous
     // kernel in the stream (which may produce this call's inputs, or still
     // read this call's outputs) must be complete; the next one may start its
     // own prologue on free SMs meanwhile
     umma::grid_launch_dependents();
     umma::grid_wait();
-
-    // ---- q8 of this CTA's 128 heads: four TMA tile loads and one bulk copy ----
-    if (tid == 0) {
-        umma::mbar_arrive_expect_tx(q_full, 4 * kQBlk + kQRope);
-        const int qrow = t * a.H + hg * kHeads;
-        for (int cb = 0; cb < 4; ++cb)
-            umma::tma_load_2d(q8_s + cb * kQBlk, &q8_map, 128 * cb, qrow, q_full);
-        umma::bulk_copy_g2s(qrope_s, a.q8_rope + ((int64_t)t * G + hg) * kQRope, kQRope, q_full);
-    }
 
     auto wait_bar = [&](uint32_t mbar, uint32_t parity) {
         if (*(volatile int *)abort_s)
@@ -284,53 +393,75 @@ __global__ void __launch_bounds__(512, 1)
             atomicOr(&g_wide_error, 2);
     };
 
-    if (warp >= kProducerWarp0 && warp < kProducerWarp0 + 4) {
+    if (ntiles == 0) {
+        // no keys (topk = 0): one pair per row; the softmax threads write the
+        // row's half of zeros and its lse (the sink alone, or -inf)
+        if (warp < 4) {
+            const int64_t t = pair / G;
+            const int hg = (int)(pair % G), h = tid;
+            uint4 *o = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) +
+                                                 ((t * a.H + hg * kHeads + h) * kDv + half * kDvHalf));
+#pragma unroll 4
+            for (int i = 0; i < kDvHalf / 8; ++i)
+                o[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (half == 0 && a.lse != nullptr)
+                a.lse[t * a.H + hg * kHeads + h] = a.sinks != nullptr ? a.sinks[hg * kHeads + h] : -INFINITY;
+        }
+    } else if (warp >= kProducerWarp0 && warp < kProducerWarp0 + kProducerWarps) {
         // ======================= producers =======================
-        const int pt = tid - kProducerWarp0 * 32;
-        // copy cid (20 per warp): key quad qd, column block cb
-        const bool copier = (pt & 31) < kCopies / 4;
-        const int cid = (pt >> 5) * (kCopies / 4) + (pt & 31);
-        const int qd = cid / kCB, cb = cid % kCB;
-        auto fetch = [&](int tile, int (&r)[4]) {
+        // warp pw issues copies 14 pw .. 14 pw + 13 of every tile (fewer in the
+        // last warp): copy c = key quad c / 5, column block c % 5; each copier
+        // lane loads its quad's four indices, kIdxAhead tiles ahead
+        const int pw = warp - kProducerWarp0;
+        const int cid = pw * kCopiesPerWarp + lane;
+        const bool copier = lane < kCopiesPerWarp && cid < kCopies;
+        const int quad = cid / kCB, cb = cid % kCB;
+        const int warp_copies = min(kCopiesPerWarp, kCopies - pw * kCopiesPerWarp);
+        Cur cf;
+        cur_load(cf, sg, 0);
+        auto fetch = [&](int (&r)[4]) {
+            const bool live = cf.seg < sg.n;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int p = tile * kKeys + 4 * qd + u;
-                r[u] = (copier && tile < ntiles && p < a.topk) ? __ldg(row_idx + p) : -1;
+                const int p = cf.k * kKeys + 4 * quad + u;
+                r[u] = (live && copier && p < a.topk) ? __ldg(a.indices + cf.t * (int64_t)a.topk + p) : -1;
             }
+            if (live)
+                cur_next(cf, sg, ntiles, G);
         };
         auto row = [&](int x) { return (x >= 0 && (int64_t)x < a.num_slots) ? x : -1; };
-        int r0[4], r1[4], r2[4], r3[4];
         static_assert(kIdxAhead == 4, "one register slot per tile of look-ahead");
-        fetch(0, r0);
-        fetch(1, r1);
-        fetch(2, r2);
-        fetch(3, r3);
+        int r0[4], r1[4], r2[4], r3[4];
+        fetch(r0);
+        fetch(r1);
+        fetch(r2);
+        fetch(r3);
         int issued = 0;
         bool stop = false;
-        auto step = [&](int j, int(&r)[4]) {
-            if (stop || j >= ntiles) {
+        auto step = [&](int j, int (&r)[4]) {
+            if (stop || j >= n) {
                 stop = true;
                 return;
             }
             const int st = j % kStages;
-            if (pt == 0) {
+            int go = 0;
+            if (lane == 0) {
                 if (j >= kStages)
                     wait_bar(empty(st), (uint32_t)((j / kStages - 1) & 1));
-                const int go = !*(volatile int *)abort_s;
+                go = !*(volatile int *)abort_s;
                 if (go)
-                    umma::mbar_arrive_expect_tx(full(st), kTile);
-                go_s[j & 1] = go;
+                    umma::mbar_arrive_expect_tx(full(st), (uint32_t)(warp_copies * 512));
             }
-            umma::named_bar(2, kProducerThreads);
-            if (!go_s[j & 1]) {
+            go = __shfl_sync(0xffffffffu, go, 0);
+            if (!go) {
                 stop = true;
                 return;
             }
             if (copier)
-                umma::tma_gather4(ring + st * kTile + cb * kKBlk + qd * 512, &kv_map, 128 * cb, row(r[0]),
+                umma::tma_gather4(ring + st * kTile + cb * kKBlk + quad * 512, &kv_map, 128 * cb, row(r[0]),
                                   row(r[1]), row(r[2]), row(r[3]), full(st));
             issued = j + 1;
-            fetch(j + kIdxAhead, r);
+            fetch(r);
         };
         for (int j0 = 0; !stop; j0 += kIdxAhead) {
             step(j0, r0);
@@ -338,20 +469,54 @@ __global__ void __launch_bounds__(512, 1)
             step(j0 + 2, r2);
             step(j0 + 3, r3);
         }
-        if (pt == 0) {
-            wait_issued(q_full, 0); // the q8 copies have landed (also after an abort)
+        // this warp's copies in flight have landed (also after an abort)
+        if (lane == 0) {
             for (int j = max(0, issued - kStages); j < issued; ++j)
                 wait_issued(full(j % kStages), (uint32_t)((j / kStages) & 1));
         }
+        __syncwarp();
     } else if (warp == kQkWarp) {
         // ======================= QK issuer =======================
         if (lane == 0) {
-            wait_bar(q_full, 0);
-            for (int i = 0; i < ntiles; ++i) {
-                const int b = i & 1, st = i % kStages;
-                wait_bar(full(st), (uint32_t)((i / kStages) & 1));
-                if (i >= 2) // the softmax has read S(i-2)
-                    wait_bar(p_full(b), (uint32_t)(((i - 2) >> 1) & 1));
+            Cur cu;
+            cur_load(cu, sg, 0);
+            int piece = -1; // the piece whose q8 was loaded last
+            for (int j = 0; j < n; ++j) {
+                const int b = j & 1, st = j % kStages;
+                if (cu.begin) {
+                    // this piece's row: its q8 (once the previous piece's QK MMAs are done with q8)
+                    if (piece >= 0) {
+                        umma::commit(q_free);
+                        wait_bar(q_free, (uint32_t)(piece & 1));
+                    }
+                    if (*(volatile int *)abort_s)
+                        break;
+                    ++piece;
+                    umma::mbar_arrive_expect_tx(q_full, 4 * kQBlk + kQRope);
+                    const int qrow = (int)(cu.t * a.H + cu.hg * kHeads);
+                    for (int c = 0; c < 4; ++c)
+                        umma::tma_load_2d(q8_s + c * kQBlk, &q8_map, 128 * c, qrow, q_full);
+                    umma::bulk_copy_g2s(qrope_s, a.q8_rope + (cu.t * G + cu.hg) * kQRope, kQRope, q_full);
+                    // the next piece's q8 into L2 meanwhile: the next row of this
+                    // segment, or the next segment's first
+                    int64_t nt = -1;
+                    int nhg = 0;
+                    if (cu.left > ntiles - cu.k) {
+                        nt = cu.t + (cu.hg + 1 == G ? 1 : 0);
+                        nhg = cu.hg + 1 == G ? 0 : cu.hg + 1;
+                    } else if (cu.seg + 1 < sg.n) {
+                        nt = sg.t[cu.seg + 1];
+                        nhg = sg.hg[cu.seg + 1];
+                    }
+                    if (nt >= 0) {
+                        umma::prefetch_l2(a.q8 + (nt * a.H + nhg * kHeads) * 512, kHeads * 512);
+                        umma::prefetch_l2(a.q8_rope + (nt * G + nhg) * kQRope, kQRope);
+                    }
+                    wait_bar(q_full, (uint32_t)(piece & 1));
+                }
+                wait_bar(full(st), (uint32_t)((j / kStages) & 1));
+                if (j >= 2) // the softmax has read S(j-2)
+                    wait_bar(p_full(b), (uint32_t)(((j - 2) >> 1) & 1));
                 if (*(volatile int *)abort_s)
                     break;
                 umma::fence_after_sync();
@@ -367,7 +532,11 @@ __global__ void __launch_bounds__(512, 1)
                 }
                 umma::commit(s_full(b));
                 umma::commit(empty(st));
+                cur_next(cu, sg, ntiles, G);
             }
+            // the q8 copies in flight have landed (also after an abort)
+            if (piece >= 0)
+                wait_issued(q_full, (uint32_t)(piece & 1));
             umma::commit(drain);
             wait_issued(drain, 0);
         }
@@ -375,10 +544,21 @@ __global__ void __launch_bounds__(512, 1)
     } else if (warp == kPvWarp) {
         // ======================= PV issuer =======================
         if (lane == 0) {
-            for (int i = 0; i < ntiles; ++i) {
-                const int b = i & 1;
-                wait_bar(p_full(b), (uint32_t)((i >> 1) & 1));
-                wait_bar(v_full(b), (uint32_t)((i >> 1) & 1));
+            Cur cu;
+            cur_load(cu, sg, 0);
+            int piece = -1;
+            bool first = false; // the piece's first PV overwrites O^T
+            for (int j = 0; j < n; ++j) {
+                const int b = j & 1;
+                if (cu.begin) {
+                    // O^T is overwritten by this piece: the previous piece's O^T has been read out
+                    if (piece >= 0)
+                        wait_bar(o_free, (uint32_t)(piece & 1));
+                    ++piece;
+                    first = true;
+                }
+                wait_bar(p_full(b), (uint32_t)((j >> 1) & 1));
+                wait_bar(v_full(b), (uint32_t)((j >> 1) & 1));
                 if (*(volatile int *)abort_s)
                     break;
                 umma::fence_after_sync();
@@ -389,8 +569,10 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         umma::mma_f16_ts(tmem + 128 * mb, tmem + kVCol + 64 * b + 32 * mb + 8 * kk,
-                                         bd + (uint64_t)((kk * 32) >> 4), kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+                                         bd + (uint64_t)((kk * 32) >> 4), kIdescPV, (!first || kk > 0) ? 1u : 0u);
+                first = false;
                 umma::commit(p_empty(b));
+                cur_next(cu, sg, ntiles, G);
             }
             umma::commit(drain);
             wait_issued(drain, 0);
@@ -404,7 +586,7 @@ __global__ void __launch_bounds__(512, 1)
         const uint32_t selA = ii < 2 ? 0x5410u : 0x3276u; // keep / take 16-bit halves (xor 2)
         const uint32_t selB = ii & 1 ? 0x3715u : 0x6240u; // interleave bytes (xor 1)
         const uint32_t tlane = (uint32_t)(32 * q4) << 16;
-        for (int i = 0; i < ntiles; ++i) {
+        for (int i = 0; i < n; ++i) {
             const int st = i % kStages, vb = i & 1;
             wait_bar(full(st), (uint32_t)((i / kStages) & 1));
             if (i >= 2) // PV(i-2) has read V^T buffer vb
@@ -429,44 +611,267 @@ __global__ void __launch_bounds__(512, 1)
             umma::mbar_arrive(v_full(vb));
             umma::mbar_arrive(empty(st));
         }
-    } else {
+    } else if (warp < 4) {
         // ======================= softmax (thread = head) =======================
         const int h = tid; // 0..127
+        const int d0 = warp * 32 + lane; // this thread's O^T lane: value dim d0 (+128) of the half
         const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
         const float kvs = *a.kv_scale;
-        const float fac = a.scale * kLog2e * a.q_scale[(int64_t)t * a.H + hg * kHeads + h] * kvs;
-        float m_ref = -INFINITY, l = 0.f;
-        // validity of the tile's 64 keys (the same for every head): lane j
-        // checks keys j and j + 32, a ballot gathers the mask
-        auto load_idx = [&](int tile, int off) {
-            const int p = tile * kKeys + off + lane;
-            return (tile < ntiles && p < a.topk) ? __ldg(row_idx + p) : -1;
+        float m_ref = -INFINITY, l = 0.f, fac = 0.f;
+        int kp = 0, jp = 0; // the current piece's first key tile and its tile index
+        Cur cu;
+        cur_load(cu, sg, 0);
+        // validity of a tile's 64 keys (the same for every head): lane j checks
+        // keys j and j + 32, a ballot gathers the mask; the indices are loaded
+        // four tiles ahead (cursor cf), since under the gathers' traffic a load
+        // can take longer than a tile
+        Cur cf;
+        cur_load(cf, sg, 0);
+        auto load_idx = [&](int off) {
+            if (cf.seg >= sg.n)
+                return -1;
+            const int p = cf.k * kKeys + off + lane;
+            return p < a.topk ? __ldg(a.indices + cf.t * (int64_t)a.topk + p) : -1;
         };
-        int xa0 = load_idx(0, 0), xb0 = load_idx(0, 32), xa1 = load_idx(1, 0), xb1 = load_idx(1, 32);
-        int xa2 = load_idx(2, 0), xb2 = load_idx(2, 32), xa3 = load_idx(3, 0), xb3 = load_idx(3, 32);
         auto ok = [&](int x) { return x >= 0 && (int64_t)x < a.num_slots; };
-        auto step = [&](int i, int &xa, int &xb) {
-            if (i >= ntiles)
+        int xa0 = load_idx(0), xb0 = load_idx(32);
+        if (cf.seg < sg.n)
+            cur_next(cf, sg, ntiles, G);
+        int xa1 = load_idx(0), xb1 = load_idx(32);
+        if (cf.seg < sg.n)
+            cur_next(cf, sg, ntiles, G);
+        int xa2 = load_idx(0), xb2 = load_idx(32);
+        if (cf.seg < sg.n)
+            cur_next(cf, sg, ntiles, G);
+        int xa3 = load_idx(0), xb3 = load_idx(32);
+        if (cf.seg < sg.n)
+            cur_next(cf, sg, ntiles, G);
+        __nv_bfloat16 *const out_b = static_cast<__nv_bfloat16 *>(a.out);
+        // output staging: [64 heads][256 dims] bf16 of this half in the P^T
+        // buffers (free while a piece finishes: its last PV is done, and the
+        // next piece's P^T comes from these threads), then written out with
+        // 16-byte stores, a head's 512 bytes contiguous
+        __nv_bfloat16 *const stage = reinterpret_cast<__nv_bfloat16 *>(smem + kOffPT);
+        static_assert(2 * kPT == 64 * kDvHalf * 2, "the staging block fills the P^T buffers");
+        auto flush_stage = [&](int64_t t, int hg, int c0) {
+            umma::named_bar(1, 128); // the block is staged
+            __nv_bfloat16 *orow = out_b + (t * a.H + hg * kHeads + c0) * kDv + half * kDvHalf;
+            const uint4 *src = reinterpret_cast<const uint4 *>(stage);
+#pragma unroll 4
+            for (int i = h; i < 64 * (kDvHalf / 8); i += 128)
+                *reinterpret_cast<uint4 *>(orow + (int64_t)(i >> 5) * kDv + (i & 31) * 8) = src[i];
+            umma::named_bar(1, 128); // the block may be restaged
+        };
+
+        // ---- the end of a piece: O^T / l -> out (a whole row), or a partial to
+        // the workspace and, for the second piece of a shared row, the merge ----
+        auto finish_piece = [&](int j) {
+            const int64_t t = cu.t;
+            const int hg = cu.hg;
+            const bool whole = kp == 0 && cu.k == ntiles - 1;
+            wait_bar(p_empty(j & 1), (uint32_t)((j >> 1) & 1)); // the piece's last PV (and every earlier one)
+            umma::fence_after_sync();
+            const float sk = a.sinks != nullptr ? a.sinks[hg * kHeads + h] * kLog2e : -INFINITY;
+            // the piece's output factor and lse (natural log; with the sink for a whole row)
+            float f = 0.f, lse_p = -INFINITY;
+            if (whole) {
+                // a sink logit (base-2 units sk) joins the denominator: l 2^m_ref + 2^sk,
+                // taken relative to M = max(m_ref, sk)
+                if (l > 0.f) {
+                    const float M = fmaxf(m_ref, sk);
+                    const float lt = l * exp2f(m_ref - M) + (sk == -INFINITY ? 0.f : exp2f(sk - M));
+                    f = kvs * exp2f(m_ref - M) / lt;
+                    lse_p = (M + log2f(lt)) * kLn2;
+                } else if (sk != -INFINITY) {
+                    lse_p = sk * kLn2; // no valid key: the sink alone
+                }
+                if (half == 0 && a.lse != nullptr)
+                    a.lse[t * a.H + hg * kHeads + h] = lse_p;
+            } else if (l > 0.f) {
+                f = 1.0f / l; // a partial stays in units of the cache's codes
+                lse_p = (m_ref + log2f(l)) * kLn2;
+            }
+            alpha_s[h] = f; // output factor per head
+            umma::named_bar(1, 128);
+            if (whole) {
+                // thread = value dims 128 mb + d0; columns = heads; each store
+                // instruction writes 32 consecutive dims of one head (direct
+                // stores measured faster than staging the block through
+                // shared memory)
+                __nv_bfloat16 *const obase = out_b + (t * a.H + hg * kHeads) * kDv + half * kDvHalf + d0;
+#pragma unroll 1
+                for (int mb = 0; mb < 2; ++mb) {
+#pragma unroll 1
+                    for (int c = 0; c < kHeads; c += 32) {
+                        uint32_t o[32];
+                        umma::ld16(tl + 128 * mb + c, reinterpret_cast<uint32_t(&)[16]>(o[0]));
+                        umma::ld16(tl + 128 * mb + c + 16, reinterpret_cast<uint32_t(&)[16]>(o[16]));
+                        umma::wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const float fe = alpha_s[c + e];
+                            obase[(int64_t)(c + e) * kDv + 128 * mb] =
+                                __float2bfloat16_rn(fe > 0.f ? __uint_as_float(o[e]) * fe : 0.f);
+                        }
+                    }
+                }
+                umma::fence_before_sync();
+                umma::mbar_arrive(o_free);
                 return;
-            const int b = i & 1;
-            const uint32_t m_lo = __ballot_sync(0xffffffffu, ok(xa));
-            const uint32_t m_hi = __ballot_sync(0xffffffffu, ok(xb));
-            xa = load_idx(i + kIdxAhead, 0);
-            xb = load_idx(i + kIdxAhead, 32);
-            wait_bar(s_full(b), (uint32_t)((i >> 1) & 1));
+            }
+            // a piece of a shared row: the end of the pair's first row (slot
+            // 2 pair) or the beginning of its last (slot 2 pair + 1). The row's
+            // flag word holds bit 1 once the end piece's partial is visible and
+            // bit 2 once the beginning piece's is.
+            const bool beginning = kp == 0;
+            const int64_t slot = 2 * pair + (beginning ? 1 : 0);
+            const int my_bit = beginning ? 2 : 1, other_bit = 3 - my_bit;
+            int *flag = a.wide_tickets + (t * G + hg) * 2 + half;
+            if (h == 0)
+                *last_s = (atomicOr(flag, 0) & other_bit) != 0; // the other piece has finished
+            umma::named_bar(1, 128);
+            if (!*last_s) {
+                // store this piece as [256 dims][128 heads] binary16 of this half and its 128 lse
+                uint16_t *po = a.wide_part + (slot * 2 + half) * (int64_t)(kDvHalf * kHeads);
+#pragma unroll 1
+                for (int mb = 0; mb < 2; ++mb) {
+                    uint4 *pd = reinterpret_cast<uint4 *>(po + (int64_t)(128 * mb + d0) * kHeads);
+#pragma unroll 1
+                    for (int c = 0; c < kHeads; c += 32) {
+                        uint32_t o[32];
+                        umma::ld16(tl + 128 * mb + c, reinterpret_cast<uint32_t(&)[16]>(o[0]));
+                        umma::ld16(tl + 128 * mb + c + 16, reinterpret_cast<uint32_t(&)[16]>(o[16]));
+                        umma::wait_ld();
+                        uint32_t w[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float f0 = alpha_s[c + 2 * e], f1 = alpha_s[c + 2 * e + 1];
+                            w[e] = pack_f16x2(f0 > 0.f ? __uint_as_float(o[2 * e]) * f0 : 0.f,
+                                              f1 > 0.f ? __uint_as_float(o[2 * e + 1]) * f1 : 0.f);
+                        }
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            __stcg(pd + c / 8 + q, make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
+                    }
+                }
+                __stcg(a.wide_part_lse + (slot * 2 + half) * kHeads + h, lse_p);
+                __threadfence();
+                umma::named_bar(1, 128);
+                if (h == 0)
+                    *last_s = (atomicOr(flag, my_bit) & other_bit) != 0;
+                umma::named_bar(1, 128);
+                if (!*last_s) {
+                    umma::fence_before_sync();
+                    umma::mbar_arrive(o_free);
+                    return;
+                }
+            }
+            if (h == 0)
+                *flag = 0; // both pieces are in: ready for the next call
+            __threadfence();
+            // ---- the merge: the row's beginning piece and its end piece, in that
+            // order; this CTA's own piece comes from tensor memory, rounded to
+            // binary16 exactly as it was stored, the other from the workspace ----
+            const int64_t other = beginning ? 2 * (pair + 1) : 2 * (pair - 1) + 1;
+            const float lo = __ldcg(a.wide_part_lse + (other * 2 + half) * kHeads + h) * kLog2e;
+            const float lm = lse_p * kLog2e;
+            const float lb = beginning ? lm : lo, le = beginning ? lo : lm;
+            const float mx = fmaxf(sk, fmaxf(lb, le));
+            const float eb = mx == -INFINITY ? 0.f : exp2f(lb - mx), ee = mx == -INFINITY ? 0.f : exp2f(le - mx);
+            const float tot = eb + ee + ((mx == -INFINITY || sk == -INFINITY) ? 0.f : exp2f(sk - mx)); // the sink: no output
+            if (half == 0 && a.lse != nullptr)
+                a.lse[t * a.H + hg * kHeads + h] = mx == -INFINITY ? -INFINITY : (mx + log2f(tot)) * kLn2;
+            wts_s[h] = tot > 0.f ? kvs * (eb / tot) : 0.f;
+            wts_s[kHeads + h] = tot > 0.f ? kvs * (ee / tot) : 0.f;
+            umma::named_bar(1, 128);
+            const uint4 *ps = reinterpret_cast<const uint4 *>(a.wide_part + (other * 2 + half) * (int64_t)(kDvHalf * kHeads));
+#pragma unroll 1
+            for (int c0 = 0; c0 < kHeads; c0 += 64) {
+                uint4 v[2][8]; // the other piece's 64 heads of this thread's two dims, loaded together
+#pragma unroll
+                for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        v[mb][u] = __ldcg(ps + (int64_t)(128 * mb + d0) * (kHeads / 8) + c0 / 8 + u);
+#pragma unroll
+                for (int mb = 0; mb < 2; ++mb) {
+#pragma unroll
+                    for (int cc = 0; cc < 64; cc += 16) {
+                        const int c = c0 + cc;
+                        uint32_t o[16];
+                        umma::ld16(tl + 128 * mb + c, o);
+                        umma::wait_ld();
+                        const uint32_t wv[8] = {v[mb][cc / 8].x,     v[mb][cc / 8].y,     v[mb][cc / 8].z,
+                                                v[mb][cc / 8].w,     v[mb][cc / 8 + 1].x, v[mb][cc / 8 + 1].y,
+                                                v[mb][cc / 8 + 1].z, v[mb][cc / 8 + 1].w};
+#pragma unroll
+                        for (int e = 0; e < 16; e += 2) {
+                            const float f0 = alpha_s[c + e], f1 = alpha_s[c + e + 1];
+                            const uint32_t own = pack_f16x2(f0 > 0.f ? __uint_as_float(o[e]) * f0 : 0.f,
+                                                            f1 > 0.f ? __uint_as_float(o[e + 1]) * f1 : 0.f);
+                            const float2 pm = __half22float2(*reinterpret_cast<const __half2 *>(&own));
+                            const float2 px = __half22float2(*reinterpret_cast<const __half2 *>(&wv[e / 2]));
+                            const float2 pb = beginning ? pm : px, pe = beginning ? px : pm;
+                            stage[(cc + e) * kDvHalf + 128 * mb + d0] =
+                                __float2bfloat16_rn(wts_s[c + e] * pb.x + wts_s[kHeads + c + e] * pe.x);
+                            stage[(cc + e + 1) * kDvHalf + 128 * mb + d0] =
+                                __float2bfloat16_rn(wts_s[c + e + 1] * pb.y + wts_s[kHeads + c + e + 1] * pe.y);
+                        }
+                    }
+                }
+                flush_stage(t, hg, c0);
+            }
+            umma::fence_before_sync();
+            umma::mbar_arrive(o_free);
+        };
+
+#pragma unroll 1
+        for (int j = 0; j < n; ++j) {
+            const int b = j & 1;
+            if (cu.begin) {
+                jp = j;
+                kp = cu.k;
+                m_ref = -INFINITY;
+                l = 0.f;
+                fac = a.scale * kLog2e * a.q_scale[cu.t * a.H + cu.hg * kHeads + h] * kvs;
+            }
+            const uint32_t m_lo = __ballot_sync(0xffffffffu, ok(xa0));
+            const uint32_t m_hi = __ballot_sync(0xffffffffu, ok(xb0));
+            xa0 = xa1;
+            xb0 = xb1;
+            xa1 = xa2;
+            xb1 = xb2;
+            xa2 = xa3;
+            xb2 = xb3;
+            xa3 = load_idx(0); // tile j + 4
+            xb3 = load_idx(32);
+            if (cf.seg < sg.n)
+                cur_next(cf, sg, ntiles, G);
+            wait_bar(s_full(b), (uint32_t)((j >> 1) & 1));
             umma::fence_after_sync();
             float sv[64];
 #pragma unroll
             for (int c = 0; c < 4; ++c)
                 umma::ld16(tl + kSCol + 64 * b + 16 * c, reinterpret_cast<uint32_t(&)[16]>(sv[16 * c]));
             umma::wait_ld();
-            float mt = -INFINITY;
+            // the tile max in four independent chains; a tile whose 64 keys are all
+            // valid (the common case) skips the masking
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if ((m_lo & m_hi) == 0xffffffffu) {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                const bool v = ((j < 32 ? m_lo >> j : m_hi >> (j - 32)) & 1u) != 0;
-                sv[j] = v ? sv[j] * fac : -INFINITY;
-                mt = fmaxf(mt, sv[j]);
+                for (int q = 0; q < 64; ++q) {
+                    sv[q] *= fac;
+                    mx[q & 3] = fmaxf(mx[q & 3], sv[q]);
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 64; ++q) {
+                    const bool v = ((q < 32 ? m_lo >> q : m_hi >> (q - 32)) & 1u) != 0;
+                    sv[q] = v ? sv[q] * fac : -INFINITY;
+                    mx[q & 3] = fmaxf(mx[q & 3], sv[q]);
+                }
             }
+            const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
             // move the reference max: every head's O^T column spans all four warps'
             // lanes, so the four softmax warps agree on it per tile
             const bool exceed = mt > m_ref + kRescaleThreshold;
@@ -481,9 +886,9 @@ __global__ void __launch_bounds__(512, 1)
                 l *= al;
                 alpha_s[h] = al;
                 umma::named_bar(1, 128);
-                if (i >= 1) {
-                    // O^T holds PV(0..i-1): let PV(i-1) finish, then scale each head column
-                    wait_bar(p_empty((i - 1) & 1), (uint32_t)(((i - 1) >> 1) & 1));
+                if (j > jp) {
+                    // O^T holds PV(jp..j-1): let PV(j-1) finish, then scale each head column
+                    wait_bar(p_empty((j - 1) & 1), (uint32_t)(((j - 1) >> 1) & 1));
                     umma::fence_after_sync();
 #pragma unroll 1
                     for (int c = 0; c < 2 * kHeads; c += 16) {
@@ -500,70 +905,32 @@ __global__ void __launch_bounds__(512, 1)
                 umma::named_bar(1, 128); // alpha_s is read by all before the next tile writes it
             }
             const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
-            uint32_t pw[32];
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const float p0 = ex2_approx(sv[2 * c] - mu), p1 = ex2_approx(sv[2 * c + 1] - mu);
-                l += p0 + p1;
-                pw[c] = pack_f16x2(p0, p1);
-            }
-            if (i >= 2) // PV(i-2) has read P^T(b)
-                wait_bar(p_empty(b), (uint32_t)(((i - 2) >> 1) & 1));
-            // this head's row of P^T: 64 keys x fp16 = one 128-byte swizzled row
+            if (j >= 2) // PV(j-2) has read P^T(b)
+                wait_bar(p_empty(b), (uint32_t)(((j - 2) >> 1) & 1));
+            // this head's row of P^T: 64 keys x fp16 = one 128-byte swizzled row,
+            // written 16 bytes (8 keys) at a time
             const uint32_t prow = pt_s + b * kPT + h * 128;
+            float ls[4] = {0.f, 0.f, 0.f, 0.f}; // the tile's sum in four independent chains
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow + ((c ^ (h & 7)) << 4)),
-                             "r"(pw[4 * c]), "r"(pw[4 * c + 1]), "r"(pw[4 * c + 2]), "r"(pw[4 * c + 3])
+            for (int c8 = 0; c8 < 8; ++c8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float p0 = ex2_approx(sv[8 * c8 + 2 * e] - mu), p1 = ex2_approx(sv[8 * c8 + 2 * e + 1] - mu);
+                    ls[e] += p0 + p1;
+                    w[e] = pack_f16x2(p0, p1);
+                }
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow + ((c8 ^ (h & 7)) << 4)), "r"(w[0]),
+                             "r"(w[1]), "r"(w[2]), "r"(w[3])
                              : "memory");
+            }
+            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             umma::fence_async_smem();
             umma::fence_before_sync();
             umma::mbar_arrive(p_full(b));
-        };
-        for (int i0 = 0; i0 < ntiles; i0 += kIdxAhead) {
-            step(i0, xa0, xb0);
-            step(i0 + 1, xa1, xb1);
-            step(i0 + 2, xa2, xb2);
-            step(i0 + 3, xa3, xb3);
-        }
-        // ---- epilogue: O^T / l -> out, lse ----
-        if (ntiles > 0) // the last PV (and every earlier one) is done
-            wait_bar(p_empty((ntiles - 1) & 1), (uint32_t)(((ntiles - 1) >> 1) & 1));
-        umma::fence_after_sync();
-        {
-            // output factor and lse per head; a sink logit (base-2 units sk) joins the
-            // denominator: l 2^m_ref + 2^sk, taken relative to M = max(m_ref, sk)
-            const float sk = a.sinks != nullptr ? a.sinks[hg * kHeads + h] * kLog2e : -INFINITY;
-            float f = 0.f, lse_h = -INFINITY;
-            if (l > 0.f) {
-                const float M = fmaxf(m_ref, sk);
-                const float lt = l * exp2f(m_ref - M) + (sk == -INFINITY ? 0.f : exp2f(sk - M));
-                f = kvs * exp2f(m_ref - M) / lt;
-                lse_h = (M + log2f(lt)) * kLn2;
-            } else if (sk != -INFINITY) {
-                lse_h = sk * kLn2; // no valid key: the sink alone
-            }
-            alpha_s[h] = f; // output factor per head
-            if (half == 0 && a.lse != nullptr)
-                a.lse[(int64_t)t * a.H + hg * kHeads + h] = lse_h;
-        }
-        umma::named_bar(1, 128);
-        // thread = value dim 128 mb + 32 warp + lane; columns = heads
-        __nv_bfloat16 *obase = static_cast<__nv_bfloat16 *>(a.out) + ((int64_t)t * a.H + hg * kHeads) * kDv +
-                               half * kDvHalf + warp * 32 + lane;
-#pragma unroll 1
-        for (int mb = 0; mb < 2; ++mb) {
-#pragma unroll 1
-            for (int c = 0; c < kHeads; c += 16) {
-                uint32_t o[16];
-                umma::ld16(tl + 128 * mb + c, o);
-                umma::wait_ld();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float f = alpha_s[c + e];
-                    obase[(int64_t)(c + e) * kDv + 128 * mb] = __float2bfloat16_rn(f > 0.f ? __uint_as_float(o[e]) * f : 0.f);
-                }
-            }
+            if (cu.left == 1 || cu.k == ntiles - 1)
+                finish_piece(j);
+            cur_next(cu, sg, ntiles, G);
         }
         umma::fence_before_sync();
     }
@@ -600,7 +967,7 @@ cudaError_t launch_fwd_wide(const FwdArgs &a, cudaStream_t stream)
             return e;
         attr_done.fetch_or(bit, std::memory_order_release);
     }
-    const int64_t blocks = (int64_t)a.T * (a.H / kHeads) * 2;
+    const int64_t blocks = (int64_t)a.wide_pairs * 2;
     if (blocks == 0)
         return cudaSuccess;
     // The cache as a 2-D tensor [rows x 576] bytes, read in boxes of 128 bytes

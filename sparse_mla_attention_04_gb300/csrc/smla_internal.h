@@ -20,7 +20,7 @@ struct FwdArgs {
     const int32_t *indices; // [T, topk]
     void *out;              // bf16 [T, H, D_v]
     float *lse;             // [T, H] or nullptr
-    float *part_o;          // [T, S, H, D_v]   (S > kClusterMaxSplits)
+    uint16_t *part_o16;     // [T, S, H, D_v] binary16 split partials (S > kClusterMaxSplits)
     float *part_lse;        // [T, S, H]        (S > kClusterMaxSplits)
     int *tickets;           // [T, H / 16]      (S > kClusterMaxSplits)
     uint8_t *q8;            // [T, H, 512] E4M3 codes of q's first 512 columns (128-head kernel)
@@ -36,6 +36,16 @@ struct FwdArgs {
     bool bf16_dots;         // E4M3 cache with bf16 q . dequantized K dots (warp-MMA kernel)
     bool q_fp8_in;          // q holds E4M3 codes [T, H, D_qk] with one per-tensor scale
     const float *q_scale_in; // that scale (device scalar), or nullptr
+    // 128-head kernel: pairs of CTAs the (row, key tile) sequence is cut into
+    // (rows = T * H / 128 gives one row per pair), and for rows a pair shares
+    // with its neighbour the partial outputs [2 * pairs][2 halves][256 dims]
+    // [128 heads] (binary16, in units of the cache's codes), their lse
+    // [2 * pairs][2][128], and per (row, half) merge flags [rows][2] (in the
+    // counter region)
+    int wide_pairs;
+    uint16_t *wide_part;
+    float *wide_part_lse;
+    int *wide_tickets;
 };
 
 // Key tile of the warp-MMA kernel (keys per pipeline stage).
@@ -45,7 +55,8 @@ constexpr int kUmma16TileKeys = 64;
 
 // Up to this many splits of a row's top-k list run as one thread-block
 // cluster and merge their partial results through distributed shared memory
-// (no workspace). More splits (very small T) merge through the workspace.
+// (no workspace; the automatic plan stays within it). More splits (very small
+// T, explicit split counts up to kMaxSplits) merge through the workspace.
 constexpr int kClusterMaxSplits = 8;
 constexpr int kMaxSplits = 128;
 
@@ -53,23 +64,26 @@ constexpr int kMaxSplits = 128;
 // counters of any call land in memory that is zero between calls: each call
 // returns the counters it used to zero, and partial results never overlap
 // the region, whatever the shapes of earlier calls.
-constexpr int kTicketSlots = 4096;
+constexpr int kTicketSlots = 16384;
 
-// Workspace layout (byte offsets, 256-byte aligned): merge counters and
-// split partials for S > kClusterMaxSplits, or, for the 128-head kernel, the
-// quantized q and its scales (after the counter region, which every layout
-// leaves zero).
+// Workspace layout (byte offsets, 256-byte aligned): a region of merge
+// counters that every call leaves zero, then, for S > kClusterMaxSplits, the
+// split partials in binary16 and their lse, or, for the 128-head kernel, the quantized q and
+// its scales (and the partials of rows its CTA pairs share).
 struct WorkspaceLayout {
-    size_t tickets, part_lse, part_o, q8, q8_rope, q_scale, total;
+    size_t tickets, part_lse, part_o16, q8, q8_rope, q_scale, wide_part_lse, wide_part, total;
 };
-WorkspaceLayout workspace_layout(int T, int H, int D_qk, int D_v, int S, bool wide);
+// wide_pairs: the 128-head kernel's pairs when they are fewer than its rows
+// (rows shared between pairs need partial slots), else 0
+WorkspaceLayout workspace_layout(int T, int H, int D_qk, int D_v, int S, bool wide, int wide_pairs = 0);
 
 // The plan of one forward call (see plan_forward in smla_api.cu).
 struct FwdPlan {
     int path;            // the kernel that serves the call
     int S;               // splits of each row's top-k list
     bool bf16_dots;      // E4M3 cache with bf16 dots
-    bool uses_tickets;   // the workspace's merge counters take part (S > kClusterMaxSplits)
+    bool uses_tickets;   // the workspace's merge counters take part (S > kClusterMaxSplits, or shared rows)
+    int wide_pairs;      // 128-head kernel: CTA pairs of the launch
     WorkspaceLayout layout;
 };
 // Plans a call whose arguments are valid; returns SMLA_OK or the status that
@@ -81,7 +95,6 @@ cudaError_t launch_fwd_mma(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_fwd_wide(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_fwd_umma16(const FwdArgs &a, cudaStream_t stream);
 cudaError_t launch_fwd_lean16(const FwdArgs &a, cudaStream_t stream);
-cudaError_t launch_fwd_wide2(const FwdArgs &a, cudaStream_t stream);
 // The 128-head kernels' q pass: per (row, head) E4M3 codes and scales of q
 // (or the pre-quantized codes rearranged) into the workspace.
 cudaError_t launch_quantize_q_wide(const FwdArgs &a, cudaStream_t stream);
@@ -91,7 +104,6 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 cudaError_t read_umma_error(int *out, bool reset);
 cudaError_t read_wide_error(int *out, bool reset);
 cudaError_t read_lean_error(int *out, bool reset);
-cudaError_t read_wide2_error(int *out, bool reset);
 
 // The fused producer step (RoPE + q concat + cache write), validated by the ABI layer.
 struct FusedProducerArgs {
@@ -121,8 +133,8 @@ cudaError_t read_producer_error(int *out, bool reset);
 // Measurement kernels: a pure indexed-row copy at the forward kernels' gather
 // pattern, and an L2 -> SM streaming read.
 cudaError_t launch_gather_probe(const void *pool, int64_t num_rows, int row_bytes, const int32_t *indices,
-                                int64_t n_indices, int ctas_per_sm, int stages, int hold_ns, uint32_t *checksum,
-                                int sm_count, cudaStream_t stream);
+                                int64_t n_indices, int ctas_per_sm, int stages, int hold_ns, int pair_mode,
+                                int issue_warps, uint32_t *checksum, int sm_count, cudaStream_t stream);
 cudaError_t launch_l2_read_probe(const void *buf, int64_t bytes, int reps, uint32_t *checksum, int blocks,
                                  cudaStream_t stream);
 cudaError_t read_probe_error(int *out, bool reset);

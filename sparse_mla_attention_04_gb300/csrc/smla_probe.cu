@@ -3,8 +3,8 @@
 // smla_gather_probe_kernel: a pure indexed-row copy. It moves the rows named
 // by an index list from a row pool into a shared-memory ring exactly as the
 // forward kernels do (a 2-D tensor map over the pool, boxes of 128 bytes x 1
-// row with the 128-byte swizzle, tile::gather4 copies issued from four
-// warps, 64 rows per tile, -1 passed as row -1 so the engine fills zeros and
+// row with the 128-byte swizzle, tile::gather4 copies issued by the lanes of
+// up to eight producer warps, 64 rows per tile, -1 passed as row -1 so the engine fills zeros and
 // reads nothing), and does nothing with them but fold the first word of each
 // row into a checksum. Its rate is the most a kernel that gathers the same
 // rows this way can reach; the consumer may hold each tile for a while, as
@@ -30,9 +30,9 @@ __device__ int g_probe_error = 0; // set when a bounded wait gives up
 namespace {
 
 constexpr int kRows = 64;            // rows per tile
-constexpr int kProducerWarps = 4;
+constexpr int kProducerWarps = 8;
 constexpr int kProducerThreads = 32 * kProducerWarps;
-constexpr int kThreads = kProducerThreads + 32; // + one consumer warp
+constexpr int kThreads = kProducerThreads + 64; // + a consumer warp and a relay warp
 constexpr int kMaxStages = 8;
 
 struct ProbeArgs {
@@ -43,6 +43,11 @@ struct ProbeArgs {
     int boxes;          // 128-byte boxes per row (1..8)
     int stages;
     int hold_ns;
+    int pair_mode;      // 0: single CTAs; CTA pairs in clusters, each gathering half of every tile and
+                        // delivering it to both: 1 by TMA multicast, 2 by a bulk copy into the peer;
+                        // 3: single CTAs launched in clusters of two
+    int issue_warps;    // 0: copy c issued by producer thread c; k (1..8): the copies spread evenly
+                        // over warps 0..k-1, ceil(copies / k) lanes each
 };
 
 __global__ void __launch_bounds__(kThreads) smla_gather_probe_kernel(const ProbeArgs a,
@@ -55,26 +60,36 @@ __global__ void __launch_bounds__(kThreads) smla_gather_probe_kernel(const Probe
     const uint32_t ring = sbase;
     const uint32_t bar0 = sbase + a.stages * tile_bytes;
     uint8_t *smem = smem_raw + (sbase - raw_base);
-    volatile int *go_s = reinterpret_cast<volatile int *>(smem + a.stages * tile_bytes + 16 * kMaxStages);
+    volatile int *go_s = reinterpret_cast<volatile int *>(smem + a.stages * tile_bytes + 24 * kMaxStages);
     int *abort_s = const_cast<int *>(go_s) + 2;
-    auto full = [&](int st) { return bar0 + 8 * st; };
+    auto full = [&](int st) { return bar0 + 8 * st; };                   // this CTA's gathers
     auto empty = [&](int st) { return bar0 + 8 * (kMaxStages + st); };
+    auto xfull = [&](int st) { return bar0 + 8 * (2 * kMaxStages + st); }; // the peer's half (pair_mode 2)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // pair_mode 3: independent CTAs, launched in clusters of two (a control)
+    const bool mc = a.pair_mode == 1 || a.pair_mode == 2, xc = a.pair_mode == 2;
+    const uint32_t rank = mc ? umma::cluster_rank() : 0u;
+    const int half_bytes = tile_bytes / 2;
+    // tiles are split over CTAs, or over CTA pairs in the multicast mode
+    const int64_t units = mc ? gridDim.x / 2 : gridDim.x, unit = mc ? blockIdx.x / 2 : blockIdx.x;
     const int64_t ntiles_all = (a.n_indices + kRows - 1) / kRows;
-    const int64_t j0 = ntiles_all * blockIdx.x / gridDim.x;
-    const int64_t j1 = ntiles_all * (blockIdx.x + 1) / gridDim.x;
+    const int64_t j0 = ntiles_all * unit / units;
+    const int64_t j1 = ntiles_all * (unit + 1) / units;
     const int ntiles = (int)(j1 - j0);
 
     if (tid == 0) {
         for (int st = 0; st < a.stages; ++st) {
             umma::mbar_init(full(st), 1);
-            umma::mbar_init(empty(st), 1);
+            umma::mbar_init(empty(st), mc ? 2 : 1); // a pair's stage is refilled once both consumers are done
+            umma::mbar_init(xfull(st), 1);
         }
         umma::mbar_init_fence();
         *abort_s = 0;
     }
     __syncthreads();
+    if (mc) // both CTAs' barriers are initialised before either sends to the other
+        umma::cluster_barrier();
 
     auto wait_bar = [&](uint32_t mbar, uint32_t parity) {
         if (*(volatile int *)abort_s)
@@ -86,10 +101,13 @@ __global__ void __launch_bounds__(kThreads) smla_gather_probe_kernel(const Probe
     };
 
     if (warp < kProducerWarps) {
-        // copy `tid`: key quad qd (rows 4qd..4qd+3 of the tile), box cb
-        const int copies = 16 * a.boxes;
-        const bool copier = tid < copies;
-        const int qd = tid / a.boxes, cb = tid % a.boxes;
+        // copy `tid`: key quad qd (rows 4qd..4qd+3 of the tile), box cb; in the
+        // multicast mode each CTA of the pair issues half of the 16 quads
+        const int copies = (mc ? 8 : 16) * a.boxes;
+        const int per_warp = a.issue_warps > 0 ? (copies + a.issue_warps - 1) / a.issue_warps : 32;
+        const int cid = a.issue_warps > 0 ? warp * per_warp + lane : tid;
+        const bool copier = (a.issue_warps == 0 || (warp < a.issue_warps && lane < per_warp)) && cid < copies;
+        const int qd = (mc ? 8 * (int)rank : 0) + cid / a.boxes, cb = cid % a.boxes;
         auto fetch = [&](int j, int (&r)[4]) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -113,8 +131,8 @@ __global__ void __launch_bounds__(kThreads) smla_gather_probe_kernel(const Probe
                 if (j >= a.stages)
                     wait_bar(empty(st), (uint32_t)((j / a.stages - 1) & 1));
                 const int go = !*(volatile int *)abort_s;
-                if (go)
-                    umma::mbar_arrive_expect_tx(full(st), (uint32_t)tile_bytes);
+                if (go) // the whole tile, or (pair_mode 2) this CTA's half
+                    umma::mbar_arrive_expect_tx(full(st), (uint32_t)(xc ? half_bytes : tile_bytes));
                 go_s[j & 1] = go;
             }
             umma::named_bar(1, kProducerThreads);
@@ -122,7 +140,10 @@ __global__ void __launch_bounds__(kThreads) smla_gather_probe_kernel(const Probe
                 stop = true;
                 return;
             }
-            if (copier)
+            if (copier && mc && !xc)
+                umma::tma_gather4_multicast(ring + st * tile_bytes + cb * (kRows * 128) + qd * 512, &map, 128 * cb,
+                                            row(r[0]), row(r[1]), row(r[2]), row(r[3]), full(st), (uint16_t)3);
+            else if (copier)
                 umma::tma_gather4(ring + st * tile_bytes + cb * (kRows * 128) + qd * 512, &map, 128 * cb,
                                   row(r[0]), row(r[1]), row(r[2]), row(r[3]), full(st));
             issued = j + 1;
@@ -138,6 +159,29 @@ __global__ void __launch_bounds__(kThreads) smla_gather_probe_kernel(const Probe
                 if (!umma::mbar_wait(full(j % a.stages), (uint32_t)((j / a.stages) & 1)))
                     atomicOr(&g_probe_error, 2);
         }
+    } else if (warp == kProducerWarps + 1) {
+        // relay (pair_mode 2): once this CTA's half of a tile has landed, copy it
+        // into the same place of the peer's ring (one bulk copy per 128-byte
+        // column block: 8 key quads x 512 B), counted on the peer's xfull; the
+        // peer's stage is free once both consumers released the tile before
+        if (xc && lane == 0) {
+            const uint32_t peer = rank ^ 1u;
+            for (int j = 0; j < ntiles; ++j) {
+                const int st = j % a.stages;
+                if (j >= a.stages)
+                    wait_bar(empty(st), (uint32_t)((j / a.stages - 1) & 1));
+                if (*(volatile int *)abort_s)
+                    break;
+                umma::mbar_arrive_expect_tx(xfull(st), (uint32_t)half_bytes); // the peer's half, into this CTA
+                wait_bar(full(st), (uint32_t)((j / a.stages) & 1));
+                if (*(volatile int *)abort_s)
+                    break;
+                for (int cb = 0; cb < a.boxes; ++cb) {
+                    const uint32_t off = ring + st * tile_bytes + cb * (kRows * 128) + rank * 8 * 512;
+                    umma::bulk_copy_s2peer(off, off, 8 * 512, xfull(st), peer);
+                }
+            }
+        }
     } else if (lane == 0) {
         // consumer: fold word 0 of every row (box 0; row r's first 16-byte chunk
         // sits at chunk r & 7 of its 128-byte swizzled line), hold, release
@@ -145,6 +189,8 @@ __global__ void __launch_bounds__(kThreads) smla_gather_probe_kernel(const Probe
         for (int j = 0; j < ntiles; ++j) {
             const int st = j % a.stages;
             wait_bar(full(st), (uint32_t)((j / a.stages) & 1));
+            if (xc)
+                wait_bar(xfull(st), (uint32_t)((j / a.stages) & 1));
             if (*(volatile int *)abort_s)
                 break;
             const uint32_t base = ring + st * tile_bytes;
@@ -154,11 +200,18 @@ __global__ void __launch_bounds__(kThreads) smla_gather_probe_kernel(const Probe
             if (a.hold_ns > 0)
                 while (umma::globaltimer() - t_land < (uint64_t)a.hold_ns) {
                 }
-            umma::mbar_arrive(empty(st));
+            if (mc) {
+                umma::mbar_arrive_cluster(empty(st), rank);
+                umma::mbar_arrive_cluster(empty(st), rank ^ 1u);
+            } else {
+                umma::mbar_arrive(empty(st));
+            }
         }
-        a.checksum[blockIdx.x] = x;
+        a.checksum[blockIdx.x] = rank == 0 ? x : 0u; // a pair's two CTAs see the same rows
     }
     __syncthreads();
+    if (mc) // the peer may still send to this CTA's ring and barriers
+        umma::cluster_barrier();
 }
 
 // Streams `n16` 16-byte words `reps` times; each block starts at its own
@@ -197,14 +250,18 @@ constexpr int kCtaReservedBytes = 1024;
 
 int gather_probe_smem(int boxes, int stages)
 {
-    return 1024 + stages * kRows * 128 * boxes + 16 * kMaxStages + 64;
+    return 1024 + stages * kRows * 128 * boxes + 24 * kMaxStages + 64;
 }
 
 cudaError_t launch_gather_probe(const void *pool, int64_t num_rows, int row_bytes, const int32_t *indices,
-                                int64_t n_indices, int ctas_per_sm, int stages, int hold_ns, uint32_t *checksum,
-                                int sm_count, cudaStream_t stream)
+                                int64_t n_indices, int ctas_per_sm, int stages, int hold_ns, int pair_mode,
+                                int issue_warps, uint32_t *checksum, int sm_count, cudaStream_t stream)
 {
+    if (pair_mode && ctas_per_sm != 1)
+        return cudaErrorInvalidValue;
     const int boxes = (row_bytes + 127) / 128;
+    if (issue_warps > 0 && ((pair_mode == 1 || pair_mode == 2 ? 8 : 16) * boxes + issue_warps - 1) / issue_warps > 32)
+        return cudaErrorInvalidValue;
     const int need = gather_probe_smem(boxes, stages);
     // pad each CTA so that no more than ctas_per_sm fit on an SM
     const int pad = kSmPerSmBytes / (ctas_per_sm + 1) - kCtaReservedBytes + 1;
@@ -246,9 +303,22 @@ cudaError_t launch_gather_probe(const void *pool, int64_t num_rows, int row_byte
     a.boxes = boxes;
     a.stages = stages;
     a.hold_ns = hold_ns;
-    const int grid = sm_count * ctas_per_sm;
-    smla_gather_probe_kernel<<<grid, kThreads, smem, stream>>>(a, map);
-    return cudaGetLastError();
+    a.pair_mode = pair_mode;
+    a.issue_warps = issue_warps;
+    const int grid = pair_mode ? (sm_count / 2) * 2 : sm_count * ctas_per_sm;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = pair_mode ? 2 : 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, smla_gather_probe_kernel, a, map);
 }
 
 cudaError_t launch_l2_read_probe(const void *buf, int64_t bytes, int reps, uint32_t *checksum, int blocks,

@@ -207,6 +207,27 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uin
                  : "memory");
 }
 
+// Prefetch of `bytes` (a multiple of 16, 16-byte aligned) of global memory
+// into L2, without waiting.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16; 16-byte aligned offsets) from this
+// CTA's shared memory at src to the same-numbered shared-memory offset dst of
+// cluster CTA `rank`, counted on that CTA's mbarrier at offset `mbar`.
+__device__ __forceinline__ void bulk_copy_s2peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t mbar,
+                                                 uint32_t rank)
+{
+    uint32_t rdst, rbar;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(rdst) : "r"(dst), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(rbar) : "r"(mbar), "r"(rank));
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(rdst),
+                 "r"(src), "r"(bytes), "r"(rbar)
+                 : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t mbar)
 {
     asm volatile("{\n.reg .b64 st;\nmbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(mbar) : "memory");
@@ -241,8 +262,10 @@ __device__ __forceinline__ uint64_t globaltimer()
     return t;
 }
 
-// Wait for phase `parity` of `mbar` to complete, for at most ~2 s. Returns
-// false on timeout (the caller records the error and stops waiting).
+// Wait for phase `parity` of `mbar` to complete, for at most 2^32 SM cycles
+// (about 2 s at 2 GHz). Returns false on timeout (the caller records the
+// error and stops waiting). The bound is kept on the SM's cycle counter,
+// which is read in a few cycles, so a phase that completes is seen at once.
 __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity)
 {
     uint32_t done = 0;
@@ -252,7 +275,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity)
                  : "memory");
     if (done)
         return true;
-    const uint64_t t0 = globaltimer();
+    const long long c0 = clock64();
     while (true) {
         asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
                      : "=r"(done)
@@ -260,7 +283,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity)
                      : "memory");
         if (done)
             return true;
-        if (globaltimer() - t0 > 2000000000ull)
+        if (clock64() - c0 > (1ll << 32))
             return false;
     }
 }

@@ -55,18 +55,17 @@ def test_split_plan(L):
 
 def test_workspace_size(L):
     from sparse_mla_attention_04_gb300 import binding as b
-    # up to 8 splits merge inside a thread-block cluster: no workspace
+    up = lambda x: (x + 255) // 256 * 256
+    tickets = 16384 * 4
+    # up to 8 splits merge inside a thread-block cluster: no workspace; more:
+    # counters, then binary16 partials and their lse
     for S in (1, 2, 4, 8):
         assert b.sparse_mla_fwd_workspace_size(64, 16, 512, 512, 2048, 0, S) == 0
-    up = lambda x: (x + 255) // 256 * 256
-    tickets = 4096 * 4
     for T, S in ((64, 16), (3, 9)):
         n = b.sparse_mla_fwd_workspace_size(T, 16, 512, 512, 2048, 0, S)
-        assert n == up(up(tickets + T * S * 16 * 4) + T * S * 16 * 512 * 4)
-    with pytest.raises(b.SmlaError):
-        b.sparse_mla_fwd_workspace_size(64, 12, 512, 512, 2048, 0, 16)
+        assert n == up(up(tickets + T * S * 16 * 4) + T * S * 16 * 512 * 2)
     with pytest.raises(b.SmlaError):                       # more (row, group) pairs than counters
-        b.sparse_mla_fwd_workspace_size(8192, 16, 512, 512, 2048, 0, 16)
+        b.sparse_mla_fwd_workspace_size(16385, 16, 512, 512, 2048, 0, 16)
 
 
 def _call(L, q=0x1000, kv=0x2000, kvd=0, kvs=None, idx=0x3000, T=2, H=16, Dqk=512, Dv=512,
@@ -100,7 +99,7 @@ def test_argument_checks_return_before_any_launch(L):
     assert _call(L, splits=16, ws=0x8000, wsb=100) == b.SMLA_ERR_WORKSPACE_TOO_SMALL
     need = b.sparse_mla_fwd_workspace_size(2, 16, 512, 512, 8, 0, 16)
     assert _call(L, splits=16, ws=0x8010, wsb=need) == b.SMLA_ERR_MISALIGNED
-    assert _call(L, T=5000, splits=16, ws=0x8000, wsb=1 << 40) == b.SMLA_ERR_UNSUPPORTED
+    assert _call(L, T=16385, splits=16, ws=0x8000, wsb=1 << 40) == b.SMLA_ERR_UNSUPPORTED
     assert _call(L, T=0) == b.SMLA_OK                                   # no-op
 
 
@@ -180,12 +179,17 @@ def test_probe_host_checks(L):
     from sparse_mla_attention_04_gb300 import binding as b
     P = 1 << 12   # fake, never dereferenced: every call below fails its host checks
     lib = b.lib()
-    assert lib.smla_gather_probe(None, 10, 1024, P, 64, 1, 1, 0, P, None) == b.SMLA_ERR_NULL_POINTER
-    assert lib.smla_gather_probe(P, 10, 1000, P, 64, 1, 1, 0, P, None) == b.SMLA_ERR_BAD_SHAPE   # not 16-byte rows
-    assert lib.smla_gather_probe(P, 10, 2048, P, 64, 1, 1, 0, P, None) == b.SMLA_ERR_BAD_SHAPE   # > 1 KB rows
-    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 5, 1, 0, P, None) == b.SMLA_ERR_BAD_SHAPE   # > 4 CTAs/SM
-    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 1, 9, 0, P, None) == b.SMLA_ERR_BAD_SHAPE   # > 8 stages
-    assert lib.smla_gather_probe(P + 8, 10, 1024, P, 64, 1, 1, 0, P, None) == b.SMLA_ERR_MISALIGNED
+    assert lib.smla_gather_probe(None, 10, 1024, P, 64, 1, 1, 0, 0, 0, P, None) == b.SMLA_ERR_NULL_POINTER
+    assert lib.smla_gather_probe(P, 10, 1000, P, 64, 1, 1, 0, 0, 0, P, None) == b.SMLA_ERR_BAD_SHAPE   # not 16-byte rows
+    assert lib.smla_gather_probe(P, 10, 2048, P, 64, 1, 1, 0, 0, 0, P, None) == b.SMLA_ERR_BAD_SHAPE   # > 1 KB rows
+    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 5, 1, 0, 0, 0, P, None) == b.SMLA_ERR_BAD_SHAPE   # > 4 CTAs/SM
+    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 1, 9, 0, 0, 0, P, None) == b.SMLA_ERR_BAD_SHAPE   # > 8 stages
+    assert lib.smla_gather_probe(P + 8, 10, 1024, P, 64, 1, 1, 0, 0, 0, P, None) == b.SMLA_ERR_MISALIGNED
+    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 2, 1, 0, 1, 0, P, None) == b.SMLA_ERR_UNSUPPORTED  # pairs: 1 CTA/SM
+    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 1, 1, 0, 4, 0, P, None) == b.SMLA_ERR_BAD_SHAPE
+    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 1, 1, 0, 0, 9, P, None) == b.SMLA_ERR_BAD_SHAPE  # > 8 warps
+    # 1 KB rows: 128 copies a tile, more than 32 lanes of each of 3 warps
+    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 1, 1, 0, 0, 3, P, None) == b.SMLA_ERR_BAD_SHAPE
     assert lib.smla_l2_read_probe(P, 1000, 1, P, 4, None) == b.SMLA_ERR_BAD_SHAPE
     assert lib.smla_l2_read_probe(None, 1024, 1, P, 4, None) == b.SMLA_ERR_NULL_POINTER
 

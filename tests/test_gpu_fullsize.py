@@ -81,4 +81,5 @@ def test_prefill_bf16_full():
 
 
 def test_wide_fp8_full():
-    run_full(inputs.wide(), [0, 127])
+    # rows 1, 2, 65 and 126 straddle two SM pairs of the stream-K split (76 pairs on 152 SMs)
+    run_full(inputs.wide(), [0, 1, 2, 65, 126, 127])

@@ -66,8 +66,10 @@ def test_prefill_small(kernel):
 
 @pytest.fixture(params=["auto", "basic"])
 def wide_kernel(request):
-    """The 128-head kernels: the cluster pair that gathers each key once
-    (auto), and the first one whose two CTAs per row each gather every key."""
+    """The 128-head kernel's two launch plans: the (row, key tile) sequence
+    spread evenly over one CTA pair per two SMs, rows cut between pairs
+    merging through the workspace (auto), and one CTA pair per row
+    (basic)."""
     yield request.param
     assert binding.smla_device_error() == 0
 
@@ -116,6 +118,35 @@ def test_wide_head_rescale_path(wide_kernel):
     assert "mirror" in res
 
 
+@pytest.mark.parametrize("T,H,topk", [(80, 128, 200), (90, 128, 130), (77, 128, 64), (41, 256, 300),
+                                    (160, 128, 2048)])
+def test_wide_head_rows_shared_between_pairs(T, H, topk, wide_kernel):
+    """More rows than SM pairs: the (row, key tile) sequence is cut into one
+    range per pair, so rows straddle two pairs and merge through the
+    workspace (with "basic" every pair keeps one whole row); with 256 heads
+    a row is one of two head groups of a query row."""
+    w = inputs.Workload("wide_shared", T, H, 576, 512, 3000, topk, True, 1 / math.sqrt(576), "uniform",
+                        seed=T + topk)
+    idx = inputs.make_indices(w)
+    idx[3, :] = -1                     # an empty row
+    idx[5, topk // 2:] = -1            # a short one
+    res, out, lse = parity.case(w, idx=idx, kernel=wide_kernel)
+    assert (out[3] == 0).all() and np.isneginf(lse[3]).all()
+
+
+@pytest.mark.parametrize("T", [3, 80])
+def test_wide_head_topk_zero(T, wide_kernel):
+    """No keys at all: every row is empty (out = 0, lse = -inf), also when
+    the rows outnumber the SM pairs."""
+    w = inputs.Workload("wide_topk0", T, 128, 576, 512, 3000, 1, True, 1 / math.sqrt(576), "uniform", seed=3)
+    q = inputs.make_q(w).to(DEV)
+    cache, kvs = binding.build_fp8_cache(inputs.make_kv_source(w).to(DEV))
+    idx = torch.empty((T, 0), dtype=torch.int32, device=DEV)
+    out, lse = parity.fwd(wide_kernel, q, cache, idx, w.scale, kv_scale=kvs, dot_precision="fp8")
+    torch.cuda.synchronize()
+    assert (out == 0).all() and torch.isneginf(lse).all()
+
+
 def test_wide_head_two_head_groups(wide_kernel):
     w = inputs.Workload("wide_h256", 2, 256, 576, 512, 3000, 300, True, 1 / math.sqrt(576), "uniform", seed=5)
     parity.case(w, kernel=wide_kernel)
@@ -132,7 +163,7 @@ def test_wide_head_then_many_splits_share_a_workspace():
     """The 128-head kernel's quantized q lives in the workspace after the
     merge counters: a 16-split call that follows on the same buffer still
     finds its counters at zero."""
-    ww = inputs.Workload("wide_ws", 2, 128, 576, 512, 3000, 300, True, 1 / math.sqrt(576), "uniform", seed=21)
+    ww = inputs.Workload("wide_ws", 81, 128, 576, 512, 3000, 200, True, 1 / math.sqrt(576), "uniform", seed=21)
     wd = inputs.decode(n_seqs=4, ctx=8192, topk=2048, name="decode_after_wide")
     need = max(binding.sparse_mla_fwd_workspace_size(ww.T, ww.H, ww.D_qk, ww.D_v, ww.topk, 1, 0),
                binding.sparse_mla_fwd_workspace_size(wd.T, wd.H, wd.D_qk, wd.D_v, wd.topk, 0, 16))

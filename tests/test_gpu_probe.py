@@ -40,6 +40,39 @@ def test_gather_probe_checksum(row_bytes, ctas_stages):
     assert binding.smla_device_error() == 0
 
 
+@pytest.mark.parametrize("row_bytes,issue_warps", [(576, 4), (576, 5), (576, 8), (1024, 4), (1024, 8), (128, 1),
+                                                   (512, 3)])
+def test_gather_probe_issue_warps(row_bytes, issue_warps):
+    """The copies spread evenly over 1-8 producer warps gather the same rows."""
+    rng = np.random.default_rng(row_bytes + issue_warps)
+    rows = 4000
+    pool = torch.from_numpy(rng.integers(0, 256, (rows, row_bytes), dtype=np.uint8)).to(DEV)
+    idx = rng.integers(0, rows, 64 * 250 + 19).astype(np.int32)
+    idx[::9] = -1
+    ck = binding.smla_gather_probe(pool, torch.from_numpy(idx).to(DEV), ctas_per_sm=1, stages=3,
+                                   issue_warps=issue_warps)
+    torch.cuda.synchronize()
+    got = int(np.bitwise_xor.reduce(ck.cpu().numpy().view(np.uint32)))
+    assert got == _expected(pool.cpu().numpy(), idx)
+    assert binding.smla_device_error() == 0
+
+
+@pytest.mark.parametrize("row_bytes", [576, 1024])
+@pytest.mark.parametrize("pair_mode", [1, 2, 3])
+def test_gather_probe_pairs(row_bytes, pair_mode):
+    rng = np.random.default_rng(row_bytes + 3)
+    rows = 4000
+    pool = torch.from_numpy(rng.integers(0, 256, (rows, row_bytes), dtype=np.uint8)).to(DEV)
+    idx = rng.integers(0, rows, 64 * 200 + 5).astype(np.int32)
+    idx[::7] = -1
+    ck = binding.smla_gather_probe(pool, torch.from_numpy(idx).to(DEV), ctas_per_sm=1, stages=2, pair_mode=pair_mode)
+    # (pair_mode 3 runs independent CTAs: every checksum counts)
+    torch.cuda.synchronize()
+    got = int(np.bitwise_xor.reduce(ck.cpu().numpy().view(np.uint32)))
+    assert got == _expected(pool.cpu().numpy(), idx)
+    assert binding.smla_device_error() == 0
+
+
 def test_gather_probe_empty_and_hold():
     pool = torch.zeros((64, 1024), dtype=torch.uint8, device=DEV)
     ck = binding.smla_gather_probe(pool, torch.empty(0, dtype=torch.int32, device=DEV), ctas_per_sm=1, stages=1)

@@ -69,8 +69,24 @@ def test_sinks_empty_rows_give_the_sink(kernel):
         assert np.isneginf(l[2][~fin]).all()
 
 
-def test_sinks_wide_128_heads():
-    w = inputs.wide(T=3, ctx=4096, topk=2048, name="wide_sinks")
+@pytest.mark.parametrize("T", [3, 80])
+def test_sinks_wide_topk_zero_gives_the_sink(T):
+    """128 heads, no keys: out = 0 and lse = the head's sink (or -inf)."""
+    w = inputs.wide(T=T, ctx=4096, topk=1, name="wide_sinks_topk0")
+    cache, kvs = binding.build_fp8_cache(inputs.make_kv_source(w).to(DEV))
+    sinks = _sinks(128, 5)
+    out, lse = binding.sparse_mla_fwd(inputs.make_q(w).to(DEV), cache, torch.empty((T, 0), dtype=torch.int32,
+                                      device=DEV), w.scale, kv_scale=kvs, dot_precision="fp8",
+                                      sinks=torch.from_numpy(sinks).to(DEV))
+    torch.cuda.synchronize()
+    assert (out == 0).all()
+    want = np.broadcast_to(sinks.astype(np.float32), (T, 128))
+    np.testing.assert_array_equal(lse.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("T,topk", [(3, 2048), (80, 200), (160, 2048)])
+def test_sinks_wide_128_heads(T, topk):
+    w = inputs.wide(T=T, ctx=4096, topk=topk, name="wide_sinks")
     q = inputs.make_q(w)
     src = inputs.make_kv_source(w)
     cache, kvs = binding.build_fp8_cache(src.to(DEV))

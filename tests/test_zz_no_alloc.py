@@ -144,7 +144,7 @@ def test_no_alloc_128_head_rows_beyond_the_array_are_refused():
 def test_no_alloc_rejects_oversized_workspace():
     """A call whose split partials would exceed the static array returns
     SMLA_ERR_WORKSPACE_TOO_SMALL and launches nothing."""
-    T, H, topk, S = 64, 16, 4096, 64          # partials alone: 64*64*16*512*4 B = 128 MiB
+    T, H, topk, S = 64, 16, 4096, 64          # partials alone: 64*64*16*512*2 B = 64 MiB
     need = binding.sparse_mla_fwd_workspace_size(T, H, 512, 512, topk, binding.SMLA_KV_BF16, S)
     assert need > SCRATCH
     q = torch.zeros((T, H, 512), dtype=torch.bfloat16, device=DEV)
