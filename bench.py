@@ -566,7 +566,7 @@ def run_ours(args):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": ("bf16 QK over e4m3 / fp16 PV" if args.bf16_dots else "fp8-e4m3 QK / fp16 PV") if w.kv_fp8
+            "dtype": ("bf16 q . e4m3 codes as fp16 QK / fp16 PV" if args.bf16_dots else "fp8-e4m3 QK / fp16 PV") if w.kv_fp8
                      else "bf16",
             "data": "synthetic (seeded N(0,1) bf16 q and KV, uniform distinct top-k over paged contexts)",
             "config": {
@@ -746,6 +746,7 @@ def time_oracle(w, q, kv_rows, remap, kvs_val, nthreads: int = 0):
 
 def cpu_baseline(w, src, s, budget_s: float = 10.0):
     import oracle
+    cores = oracle.max_threads()
     kvs_val = oracle_scale(src) if w.kv_fp8 else 1.0
     rows = list(range(w.T))
     q, kv_rows, remap, nbytes = oracle_inputs(w, src, s, rows, kvs_val)
@@ -762,7 +763,7 @@ def cpu_baseline(w, src, s, budget_s: float = 10.0):
         el1 += time_oracle(w, q1, kv1, remap1, kvs_val, nthreads=1)
         done1 += nbytes1
         reps1 += 1
-    return {"value": round(done / el / 1e9, 4), "unit": "GB/s", "cores": oracle.max_threads(),
+    return {"value": round(done / el / 1e9, 4), "unit": "GB/s", "cores": cores,
             "kind": "oracle",
             "sample": "%d pass(es) over all %d rows of one index set (%d heads, fp64 C + OpenMP), %.1f s"
                       % (reps, w.T, w.H, el),

@@ -420,11 +420,14 @@ static int64_t sparse_mla_core(const uint16_t *q, const double *qf, const void *
 {
     int64_t bad = 0;
     e4m3_init();
+    /* the thread count applies to this call alone (no process-wide setting) */
 #ifdef _OPENMP
-    if (nthreads > 0)
-        omp_set_num_threads(nthreads);
+    const int nt = nthreads > 0 ? nthreads : omp_get_max_threads();
+#else
+    const int nt = 1;
+    (void)nthreads;
 #endif
-#pragma omp parallel reduction(+ : bad)
+#pragma omp parallel reduction(+ : bad) num_threads(nt)
     {
         double *qv = (double *)malloc(sizeof(double) * (size_t)D_qk);
         double *s = (double *)malloc(sizeof(double) * (size_t)(topk > 0 ? topk : 1));

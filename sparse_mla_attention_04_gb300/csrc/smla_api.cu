@@ -56,19 +56,23 @@ enum class Path { Mma, Umma16, Wide, Lean16 };
 
 // 16 heads with D_qk = D_v = 512: an E4M3 cache with fp8 dots runs on the
 // lean tcgen05 16-head kernel (two CTAs per SM: its random 512-byte row
-// gathers complete faster with more CTAs per SM), a bf16 cache on the
-// tcgen05 16-head kernel that takes a whole SM per CTA (its 1 KB row gathers
-// reach the DRAM bound already); a multiple of 128 heads with D_qk = 576,
-// D_v = 512 and an E4M3 cache with fp8 dots: the tcgen05 128-head kernel (no
-// split of the top-k list); every other shape or precision: the warp-MMA
-// kernel. `kernel` (smla_kernel_choice) can ask for the warp-MMA kernel, or
-// for the first tcgen05 kernels (whole SM per CTA, nothing shared).
+// gathers complete faster with more CTAs per SM), a bf16 cache, or an E4M3
+// cache with bf16 dots, on the tcgen05 16-head kernel that takes a whole SM
+// per CTA (its 1 KB row gathers reach the DRAM bound already; with bf16 dots
+// it expands the gathered E4M3 rows to binary16 in shared memory); a
+// multiple of 128 heads with D_qk = 576, D_v = 512 and an E4M3 cache with
+// fp8 dots: the tcgen05 128-head kernel (no split of the top-k list); every
+// other shape or precision: the warp-MMA kernel. `kernel`
+// (smla_kernel_choice) can ask for the warp-MMA kernel, or for the first
+// tcgen05 kernels (whole SM per CTA, nothing shared).
 Path choose_path(int H, int D_qk, int D_v, bool kv_fp8, bool fp8_dots, int kernel)
 {
-    if (kernel == SMLA_KERNEL_WARP_MMA || (kv_fp8 && !fp8_dots))
+    if (kernel == SMLA_KERNEL_WARP_MMA)
         return Path::Mma;
     if (H == 16 && D_qk == 512 && D_v == 512)
-        return kv_fp8 && kernel != SMLA_KERNEL_TCGEN05_BASIC ? Path::Lean16 : Path::Umma16;
+        return kv_fp8 && fp8_dots && kernel != SMLA_KERNEL_TCGEN05_BASIC ? Path::Lean16 : Path::Umma16;
+    if (kv_fp8 && !fp8_dots)
+        return Path::Mma;
     if (H % 128 == 0 && D_qk == 576 && D_v == 512 && kv_fp8)
         return Path::Wide;
     return Path::Mma;

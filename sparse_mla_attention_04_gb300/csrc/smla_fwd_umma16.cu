@@ -96,7 +96,6 @@ constexpr int kProducerWarp0 = 5;
 constexpr int kProducerWarps = 4;
 constexpr int kProducerThreads = 32 * kProducerWarps;
 constexpr int kMmaWarp2 = kProducerWarp0 + kProducerWarps; // more MMA issuers: warps 9, 10 (and 11 for bf16)
-constexpr int kConverterWarp0 = kMmaWarp2 + 2;             // E4M3 only
 constexpr int kConverterThreads = 128;
 // tensor memory columns: O^T 0..63, S^T partial p of buffer b at kSCol + 32 p + 16 b
 constexpr int kSCol = 64;
@@ -109,26 +108,43 @@ constexpr float kRescaleThreshold = 8.0f; // log2 units a logit may exceed the r
 constexpr float kHeadroom = 8.0f;         // a moved reference sits this far above the tile max
 constexpr int kIdxAhead = 4;              // tiles of index look-ahead
 
-template <bool FP8>
+// The three variants: a bf16 cache; an E4M3 cache with fp8 dots; an E4M3
+// cache with bf16 dots (q . code * kv_scale with q unquantized), run as the
+// bf16 variant on binary16 operands that converter warps expand exactly from
+// the gathered E4M3 tile.
+enum Mode : int { kBf16 = 0, kFp8 = 1, kBf16Dots = 2 };
+
+template <int MODE>
 struct Cfg {
-    static constexpr int EB = FP8 ? 1 : 2;        // bytes per cache element
+    static constexpr bool FP8 = MODE == kFp8;
+    static constexpr bool BD = MODE == kBf16Dots;
+    static constexpr bool G8 = MODE != kBf16;     // the gathered cache rows are E4M3
+    static constexpr int EB = G8 ? 1 : 2;         // bytes per cache element
     static constexpr int ROW = kD * EB;           // bytes per cache row
     static constexpr int NCB = ROW / 128;         // 128-byte column blocks per row (8 | 4)
     static constexpr int BOXW = 128 / EB;         // elements per gather box
     static constexpr int BLK = kKeys * 128;       // one column block of a tile (8 KB)
     static constexpr int TILE = NCB * BLK;        // 64 keys (64 KB | 32 KB)
     static constexpr int COPIES = 16 * NCB;       // gather4 copies per tile (128 | 64)
-    static constexpr int STAGES = FP8 ? 5 : 3;
+    static constexpr int STAGES = FP8 ? 5 : (BD ? 2 : 3);
+    // bf16 dots: binary16 stages [64 keys x 512] in the layout of the bf16
+    // variant's tile, each written by the converters and read by QK and PV
+    static constexpr int FSTAGES = BD ? 2 : 0;
+    static constexpr int FTILE = 8 * BLK;         // 64 KB
+    static constexpr int OFF_FRING = STAGES * TILE;
     static constexpr int KSTEP = FP8 ? 32 : 16;   // reduction depth of one QK MMA
     static constexpr int QK_MMAS = kD / KSTEP;    // per tile (32 | 16)
     static constexpr int QK_ISSUERS = FP8 ? 1 : 2; // threads issuing QK (S partial sums)
     static constexpr int PV_ISSUERS = 2;           // threads issuing PV (halves of the 512 dims)
-    static constexpr int OFF_QSTG = STAGES * TILE; // E4M3: bf16 q staged for the quantizer (16 KB)
-    static constexpr int OFF_Q = OFF_QSTG + (FP8 ? kHeads * kD * 2 : 0); // q [16 x 512] in core matrices
-    static constexpr int QGRP = 8 * ROW;          // q: 8 heads x 512 elements
+    // E4M3 / bf16 dots: bf16 q staged for the quantizer (16 KB); with bf16 dots
+    // inside the second binary16 stage, which is first written after q is done
+    static constexpr int OFF_QSTG = BD ? OFF_FRING + FTILE : OFF_FRING;
+    static constexpr int OFF_Q = OFF_FRING + FSTAGES * FTILE + (FP8 ? kHeads * kD * 2 : 0); // q in core matrices
+    static constexpr int QROW = kD * (FP8 ? 1 : 2); // bytes of one head's q
+    static constexpr int QGRP = 8 * QROW;         // q: 8 heads x 512 elements
     static constexpr int OFF_P = OFF_Q + 2 * QGRP;// P^T [64 keys x 16 heads] 16-bit, 2 buffers x 2 KB
-    static constexpr int OFF_SQ = OFF_P + 2 * 2048; // [16] per-head q scales (E4M3)
-    static constexpr int OFF_FAC = OFF_SQ + 16 * 4; // [16] per-head logit factors (E4M3)
+    static constexpr int OFF_SQ = OFF_P + 2 * 2048; // [16] per-head q scales (E4M3, bf16 dots)
+    static constexpr int OFF_FAC = OFF_SQ + 16 * 4; // [16] per-head logit factors
     static constexpr int OFF_EX = OFF_FAC + 16 * 4; // [2][4] exceed flags
     static constexpr int OFF_GO = OFF_EX + 32;    // [2] producer issue decisions
     static constexpr int OFF_WMAX = OFF_GO + 8;
@@ -139,24 +155,30 @@ struct Cfg {
     static constexpr int OFF_MBAR = (OFF_MISC + 16 + 7) & ~7;
     // full[S], empty[S], s_full[2] (a commit per QK issuer), p_full[2], p_empty[2] (a
     // commit per PV issuer), q_full, drain (a commit per MMA issuer), v_full[3] (E4M3:
-    // V^T buffer written), v_free[3] (E4M3: a commit per PV issuer, V^T buffer read)
+    // V^T buffer written), v_free[3] (E4M3: a commit per PV issuer, V^T buffer read),
+    // f_full[2] (bf16 dots: binary16 stage written), f_free[2] (a commit per PV issuer)
     static constexpr int VBUFS = 3;
-    static constexpr int NBAR = 2 * STAGES + 8 + 2 * VBUFS;
+    static constexpr int NBAR = 2 * STAGES + 8 + 2 * VBUFS + 2 * 2;
     // tensor memory: O^T 0..63, S^T 64..127; E4M3: V^T buffers at 128 + 128 v
     static constexpr int TMEM_COLS = FP8 ? 512 : 128;
     static constexpr int VCOL = 128;
     static_assert(!FP8 || VCOL + VBUFS * 128 <= TMEM_COLS, "the V^T buffers fit in tensor memory");
     static constexpr int SMEM = OFF_MBAR + NBAR * 8;
     static constexpr int SMEM_ALLOC = SMEM + 1024; // the base is aligned up to 1 KB in the kernel
-    static constexpr int THREADS = 32 * (FP8 ? kConverterWarp0 + 4 : kMmaWarp2 + 3);
-    // E4M3: 15 warps share the register file, so at most 128 registers a thread
-    static constexpr int BOUND_THREADS = FP8 ? 512 : THREADS;
-    // stage "empty" arrivals: the PV commits (bf16), or the QK commits and every
-    // converter thread (E4M3: PV reads V^T from tensor memory, not the stage)
-    static constexpr int EMPTY_COUNT = FP8 ? QK_ISSUERS + kConverterThreads : PV_ISSUERS;
+    // MMA issuers in warps 4 and kMmaWarp2.. (bf16, bf16 dots: 2 QK + 2 PV; E4M3: 1 + 2)
+    static constexpr int MMA_WARPS2 = QK_ISSUERS + PV_ISSUERS - 1;
+    static constexpr int CONVERTER_WARP0 = kMmaWarp2 + MMA_WARPS2; // E4M3, bf16 dots
+    static constexpr int THREADS = 32 * (G8 ? CONVERTER_WARP0 + 4 : kMmaWarp2 + MMA_WARPS2);
+    // 15 or 16 warps share the register file, so at most 128 registers a thread
+    static constexpr int BOUND_THREADS = G8 ? 512 : THREADS;
+    // stage "empty" arrivals: the PV commits (bf16), the QK commits and every
+    // converter thread (E4M3: PV reads V^T from tensor memory, not the stage),
+    // every converter thread (bf16 dots: QK and PV read the binary16 stage)
+    static constexpr int EMPTY_COUNT = FP8 ? QK_ISSUERS + kConverterThreads : (BD ? kConverterThreads : PV_ISSUERS);
     static_assert(STAGES * TILE >= kHeads * kD * 4, "epilogue staging fits in the ring");
     static_assert(2 * QGRP >= 128 * kHeads * 4, "merge weights fit in the q area");
     static_assert(COPIES <= kProducerThreads, "one copy per producer thread at most");
+    static_assert(!BD || OFF_QSTG + kHeads * kD * 2 <= OFF_FRING + FSTAGES * FTILE, "q staging fits in a stage");
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
@@ -165,14 +187,18 @@ constexpr uint32_t kIdescQKbf16 = umma::idesc(64, 16, 1, 1, 0, 0);
 constexpr uint32_t kIdescQKe4m3 = umma::idesc(64, 16, 0, 0, 0, 0);
 // PV: A = V^T (MN-major), B = P^T (MN-major), M = 128 dims, N = 16; bf16 or fp16
 constexpr uint32_t kIdescPVbf16 = umma::idesc(128, 16, 1, 1, 1, 1);
+// bf16 dots: the same two contractions on binary16 operands
+constexpr uint32_t kIdescQKf16 = umma::idesc(64, 16, 0, 0, 0, 0);
+constexpr uint32_t kIdescPVf16 = umma::idesc(128, 16, 0, 0, 1, 1);
 // E4M3: A = V^T in tensor memory (binary16), B = P^T fp16 (MN-major)
 constexpr uint32_t kIdescPVf16ts = umma::idesc(128, 16, 0, 0, 0, 1);
 
-template <bool FP8>
-__global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
+template <int MODE>
+__global__ void __launch_bounds__(Cfg<MODE>::BOUND_THREADS, 1)
     sparse_mla_fwd_umma16_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap kv_map)
 {
-    using C = Cfg<FP8>;
+    using C = Cfg<MODE>;
+    constexpr bool FP8 = C::FP8, BD = C::BD, G8 = C::G8;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t sbase = (raw_base + 1023u) & ~1023u; // swizzle atoms need 1 KB alignment
@@ -200,6 +226,9 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
     const uint32_t drain = bar0 + 8 * (2 * S_ + 7);
     auto v_full = [&](int vb) { return bar0 + 8 * (2 * S_ + 8 + vb); };
     auto v_free = [&](int vb) { return bar0 + 8 * (2 * S_ + 8 + C::VBUFS + vb); };
+    auto f_full = [&](int fs) { return bar0 + 8 * (2 * S_ + 8 + 2 * C::VBUFS + fs); };
+    auto f_free = [&](int fs) { return bar0 + 8 * (2 * S_ + 8 + 2 * C::VBUFS + 2 + fs); };
+    const uint32_t fring = sbase + C::OFF_FRING;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int s = blockIdx.x % a.S;
@@ -224,6 +253,10 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
         for (int vb = 0; vb < C::VBUFS; ++vb) {
             umma::mbar_init(v_full(vb), kConverterThreads);
             umma::mbar_init(v_free(vb), C::PV_ISSUERS);
+        }
+        for (int fs = 0; fs < 2; ++fs) {
+            umma::mbar_init(f_full(fs), kConverterThreads);
+            umma::mbar_init(f_free(fs), C::PV_ISSUERS);
         }
         umma::mbar_init_fence();
         *abort_s = 0;
@@ -260,10 +293,10 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
         const int pt = tid - kProducerWarp0 * 32;
         const __nv_bfloat16 *__restrict__ qg =
             static_cast<const __nv_bfloat16 *>(a.q) + (int64_t)t * kHeads * kD;
-        // this thread's copy (bf16: all 128 threads; E4M3: lanes 0-15 of each
-        // warp): key quad qd (keys 4qd..4qd+3), column block cb
-        const int cid = FP8 ? (pt >> 5) * 16 + (pt & 15) : pt;
-        const bool copier = FP8 ? (pt & 31) < 16 : true;
+        // this thread's copy (bf16: all 128 threads; E4M3 rows: lanes 0-15 of
+        // each warp): key quad qd (keys 4qd..4qd+3), column block cb
+        const int cid = G8 ? (pt >> 5) * 16 + (pt & 15) : pt;
+        const bool copier = G8 ? (pt & 31) < 16 : true;
         const int qd = cid / C::NCB, cb = cid % C::NCB;
         // raw indices only: checking them here would wait for the loads
         auto fetch = [&](int tile, int (&r)[4]) {
@@ -286,12 +319,12 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
         // q [16 x 512] -> core matrices (8 heads x 16 B): LBO 128 (K), SBO = 8 heads;
         // published once the first tile's copies are in flight, so both latencies overlap
         auto issue_q = [&] {
-            if constexpr (!FP8) {
+            if constexpr (!G8) {
                 for (int e = pt; e < kHeads * 64; e += kProducerThreads) {
                     const int h = e >> 6, c = e & 63;
                     cp_async_16(q_s + (h >> 3) * C::QGRP + c * 128 + (h & 7) * 16, qg + h * kD + c * 8, 16);
                 }
-            } else if (a.q_fp8_in) {
+            } else if (FP8 && a.q_fp8_in) {
                 // pre-quantized q: each head's 512 codes straight into core matrices
                 // (a core-matrix row holds 16 codes)
                 const uint8_t *q8g = static_cast<const uint8_t *>(a.q) + (int64_t)t * kHeads * kD;
@@ -301,7 +334,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
                 }
             } else {
                 // bf16 q staged row-major: this thread's 64 elements of head pt/8,
-                // the ones it quantizes
+                // the ones it quantizes (E4M3) or rescales to binary16 (bf16 dots)
                 const int h = pt >> 3, e0 = h * kD + (pt & 7) * 64;
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
@@ -352,6 +385,54 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
                         w[v] = quant4_e4m3(f0.x, f0.y, f1.x, f1.y, sq);
                     }
                     const int c = (pt & 7) * 4 + cc; // 16-byte column of the head's row
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(q_s + (h >> 3) * C::QGRP + c * 128 +
+                                                                                 (h & 7) * 16),
+                                 "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                                 : "memory");
+                }
+            }
+            if constexpr (BD) {
+                // thread pt rescales the 64 elements of head pt/8 by 2^e, e chosen so
+                // that the head's amax lands in [2^14, 2^15): every bf16 value of q
+                // at least 2^-29 of the amax is exactly a binary16 normal (the
+                // smaller ones, worth less than 2^-29 of the largest term, round as
+                // binary16 subnormals), and 2^-e goes into the logits' factor
+                const int h = pt >> 3;
+                uint4 qraw[8];
+                const uint4 *src = reinterpret_cast<const uint4 *>(smem + C::OFF_QSTG + (h * kD + (pt & 7) * 64) * 2);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    qraw[u] = src[u];
+                float m = 0.f;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&qraw[u]);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __bfloat1622float2(b2[e]);
+                        m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+                    }
+                }
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) // the 8 threads of a head are adjacent lanes
+                    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                // the amax's binary exponent from its bits (q is finite); a zero head keeps 2^0
+                const int ex = m > 0.f ? (int)((__float_as_uint(m) >> 23) & 0xff) - 127 : 14;
+                const int e = max(-126, min(126, 14 - ex));
+                const float up = __uint_as_float((uint32_t)(127 + e) << 23), down = __uint_as_float((uint32_t)(127 - e) << 23);
+                if ((pt & 7) == 0)
+                    sq_s[h] = down;
+                // 64 binary16 values = 8 core-matrix rows of 16 B
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&qraw[u]);
+                    uint32_t w[4];
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const float2 f = __bfloat1622float2(b2[v]);
+                        w[v] = pack_f16x2(f.x * up, f.y * up);
+                    }
+                    const int c = (pt & 7) * 8 + u; // 16-byte column of the head's row
                     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(q_s + (h >> 3) * C::QGRP + c * 128 +
                                                                                  (h & 7) * 16),
                                  "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
@@ -419,8 +500,11 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
                 constexpr int kHalf = C::QK_MMAS / C::QK_ISSUERS;
                 const int ks0 = kHalf * role;
                 for (int i = 0; i < ntiles; ++i) {
-                    const int b = i & 1, st = i % S_;
-                    wait_bar(full(st), (uint32_t)((i / S_) & 1));
+                    const int b = i & 1, st = i % S_, fs = i & 1;
+                    if constexpr (BD) // the binary16 stage holds tile i
+                        wait_bar(f_full(fs), (uint32_t)((i >> 1) & 1));
+                    else
+                        wait_bar(full(st), (uint32_t)((i / S_) & 1));
                     if (i >= 2) // the softmax has read S buffer b for tile i-2
                         wait_bar(p_full(b), (uint32_t)(((i - 2) >> 1) & 1));
                     if (*(volatile int *)abort_s)
@@ -428,7 +512,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
                     umma::fence_after_sync();
                     // KV tile: K-major, 8-key atoms 1 KB apart; k-step ks reads column
                     // block ks/4, starting 32 B * (ks%4) into its 128-byte rows
-                    const uint64_t ad = umma::desc_sw128(ring + st * C::TILE, 16, 1024);
+                    const uint64_t ad = umma::desc_sw128(BD ? fring + fs * C::FTILE : ring + st * C::TILE, 16, 1024);
 #pragma unroll
                     for (int ks = ks0; ks < ks0 + kHalf; ++ks) {
                         const uint64_t ak = ad + (uint64_t)(((ks >> 2) * C::BLK + (ks & 3) * 32) >> 4);
@@ -436,7 +520,8 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
                         if constexpr (FP8)
                             umma::mma_f8(tmem + kSCol + 32 * role + 16 * b, ak, bk, kIdescQKe4m3, ks > ks0);
                         else
-                            umma::mma_f16(tmem + kSCol + 32 * role + 16 * b, ak, bk, kIdescQKbf16, ks > ks0);
+                            umma::mma_f16(tmem + kSCol + 32 * role + 16 * b, ak, bk, BD ? kIdescQKf16 : kIdescQKbf16,
+                                          ks > ks0);
                     }
                     umma::commit(s_full(b));
                     if constexpr (FP8)
@@ -464,20 +549,24 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
                                                  kIdescPVf16ts, (i > 0 || kk > 0) ? 1u : 0u);
                     } else {
                         // V^T: MN-major, 64-column atoms 8 KB apart (LBO), 8-key atoms 1 KB apart (SBO)
-                        const uint64_t ad = umma::desc_sw128(ring + st * C::TILE, C::BLK, 1024);
+                        const uint64_t ad =
+                            umma::desc_sw128(BD ? fring + (i & 1) * C::FTILE : ring + st * C::TILE, C::BLK, 1024);
                         for (int blk = blk0; blk < blk1; ++blk)
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
                                 umma::mma_f16(tmem + 16 * blk, ad + (uint64_t)((blk * 2 * C::BLK + kk * 2048) >> 4),
-                                              bd + (uint64_t)(kk * 32), kIdescPVbf16, (i > 0 || kk > 0) ? 1u : 0u);
+                                              bd + (uint64_t)(kk * 32), BD ? kIdescPVf16 : kIdescPVbf16,
+                                              (i > 0 || kk > 0) ? 1u : 0u);
                     }
                     // PV(i) follows the softmax's read of S(i), so QK(i) is complete too.
                     // p_empty(b) also tells the softmax (and the converters) that O^T holds
                     // PV(0..i): each issuer's commit covers all its earlier MMAs.
-                    if constexpr (!FP8)
-                        umma::commit(empty(st)); // this half of PV(i) no longer reads the stage
-                    else
+                    if constexpr (FP8)
                         umma::commit(v_free(vb));
+                    else if constexpr (BD)
+                        umma::commit(f_free(i & 1)); // this half of PV(i) no longer reads the binary16 stage
+                    else
+                        umma::commit(empty(st)); // this half of PV(i) no longer reads the stage
                     umma::commit(p_empty(b));
                 }
             }
@@ -488,9 +577,52 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
             }
         }
         __syncwarp();
-    } else if (warp >= kConverterWarp0) {
+    } else if (G8 && warp >= C::CONVERTER_WARP0) {
         // ======================= converters (E4M3) =======================
-        if constexpr (FP8) {
+        if constexpr (BD) {
+            // tile i (E4M3, 4 swizzled column blocks) -> binary16 stage i%2 (8
+            // swizzled column blocks, the bf16 variant's layout), once PV(i-2) has
+            // read that stage. Item w of 2048: key r = w % 64 (a warp's lanes take
+            // consecutive keys, so each 16-byte access spreads over all banks),
+            // E4M3 16-byte chunk c = w / 64 of the row, i.e. codes 16c..16c+15,
+            // which become binary16 chunks 2(c%4), 2(c%4)+1 of column block c/4*...
+            const int ct = tid - C::CONVERTER_WARP0 * 32;
+            wait_bar(q_full, 0); // the q staging (inside binary16 stage 1) has been read
+            for (int i = 0; i < ntiles; ++i) {
+                const int st = i % S_, fs = i & 1;
+                wait_bar(full(st), (uint32_t)((i / S_) & 1));
+                if (i >= 2) // PV(i-2) has read binary16 stage fs
+                    wait_bar(f_free(fs), (uint32_t)(((i >> 1) - 1) & 1));
+                const uint32_t src0 = ring + st * C::TILE, dst0 = fring + fs * C::FTILE;
+#pragma unroll 4
+                for (int w = ct; w < kKeys * 32; w += kConverterThreads) {
+                    const int r = w & (kKeys - 1), c = w >> 6; // c = 8 cb + c16
+                    const int cb = c >> 3, c16 = c & 7;
+                    uint4 v;
+                    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
+                                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                                 : "r"(src0 + cb * C::BLK + r * 128 + ((c16 ^ (r & 7)) << 4)));
+                    uint32_t h[8];
+                    e4m3x4_to_f16x4(v.x, h[0], h[1]);
+                    e4m3x4_to_f16x4(v.y, h[2], h[3]);
+                    e4m3x4_to_f16x4(v.z, h[4], h[5]);
+                    e4m3x4_to_f16x4(v.w, h[6], h[7]);
+                    // codes 128 cb + 16 c16 .. +15 = binary16 columns of block 2 cb + c16 / 4,
+                    // 16-byte chunks 2 (c16 % 4) and 2 (c16 % 4) + 1 of its row
+                    const int fb = 2 * cb + (c16 >> 2), f0 = 2 * (c16 & 3);
+                    const uint32_t drow = dst0 + fb * C::BLK + r * 128;
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(drow + ((f0 ^ (r & 7)) << 4)),
+                                 "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
+                                 : "memory");
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(drow + (((f0 + 1) ^ (r & 7)) << 4)),
+                                 "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
+                                 : "memory");
+                }
+                umma::fence_async_smem(); // the MMAs read what these threads wrote
+                umma::mbar_arrive(f_full(fs));
+                umma::mbar_arrive(empty(st)); // done reading the E4M3 stage
+            }
+        } else if constexpr (FP8) {
             // lane quad (g, ii): member ii loads 4 dims (4g..4g+3 of this warp's 32)
             // of key 4kq+ii; after the transpose it holds dim 4g+ii of keys 4kq..4kq+3
             const int q4 = warp & 3, g = lane >> 2, ii = lane & 3;
@@ -527,9 +659,10 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
         // ======================= softmax =======================
         const uint32_t tm_lane = (uint32_t)(warp * 32) << 16;
         const int key = warp * 16 + lane; // meaningful for lane < 16
-        // log2-domain logit factor: per head for E4M3 (in shared memory), one for bf16
+        // log2-domain logit factor: per head for an E4M3 cache (the q scale, or the
+        // power of two that brought q into binary16; in shared memory), one for bf16
         float ovs = 1.0f; // output factor besides 1/l
-        if constexpr (FP8) {
+        if constexpr (G8) {
             const float kvs = *a.kv_scale;
             ovs = kvs;
             wait_bar(q_full, 0); // the per-head q scales
@@ -537,7 +670,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
                 fac_s[tid] = a.scale * kLog2e * sq_s[tid] * kvs;
             umma::named_bar(1, kSoftmaxWarps * 32);
         }
-        auto fac = [&](int h) { return FP8 ? fac_s[h] : a.scale * kLog2e; };
+        auto fac = [&](int h) { return G8 ? fac_s[h] : a.scale * kLog2e; };
         float m_ref[16], l_part[16];
 #pragma unroll
         for (int h = 0; h < 16; ++h) {
@@ -631,7 +764,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
             if (i >= 2)
                 wait_bar(p_empty(b), (uint32_t)(((i - 2) >> 1) & 1)); // PV(i-2) is done with this P buffer
             if (lane < 16) {
-                auto pk = [&](float x, float y) { return FP8 ? pack_f16x2(x, y) : pack_bf16x2(x, y); };
+                auto pk = [&](float x, float y) { return G8 ? pack_f16x2(x, y) : pack_bf16x2(x, y); };
                 const uint32_t prow = p_s + b * 2048 + (key >> 3) * 256 + (key & 7) * 16;
                 asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow), "r"(pk(sv[0], sv[1])),
                              "r"(pk(sv[2], sv[3])), "r"(pk(sv[4], sv[5])), "r"(pk(sv[6], sv[7])));
@@ -702,11 +835,11 @@ __global__ void __launch_bounds__(Cfg<FP8>::BOUND_THREADS, 1)
 }
 
 
-template <bool FP8>
+template <int MODE>
 cudaError_t launch(const FwdArgs &a, cudaStream_t stream)
 {
-    using C = Cfg<FP8>;
-    auto kern = sparse_mla_fwd_umma16_kernel<FP8>;
+    using C = Cfg<MODE>;
+    auto kern = sparse_mla_fwd_umma16_kernel<MODE>;
     static std::atomic<uint64_t> attr_done{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -735,7 +868,7 @@ cudaError_t launch(const FwdArgs &a, cudaStream_t stream)
     cuuint64_t gstride[1] = {(cuuint64_t)C::ROW};
     cuuint32_t box[2] = {(cuuint32_t)C::BOXW, 1};
     cuuint32_t estride[2] = {1, 1};
-    if (encode(&kv_map, FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+    if (encode(&kv_map, C::G8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                const_cast<void *>(a.kv), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -783,7 +916,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 
 cudaError_t launch_fwd_umma16(const FwdArgs &a, cudaStream_t stream)
 {
-    return a.kv_fp8 ? launch<true>(a, stream) : launch<false>(a, stream);
+    if (!a.kv_fp8)
+        return launch<kBf16>(a, stream);
+    return a.bf16_dots ? launch<kBf16Dots>(a, stream) : launch<kFp8>(a, stream);
 }
 
 cudaError_t read_umma_error(int *out, bool reset)
