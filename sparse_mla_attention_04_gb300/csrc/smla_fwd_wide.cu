@@ -153,6 +153,10 @@ __global__ void __launch_bounds__(128) quantize_q_e4m3_kernel(const __nv_bfloat1
                                                              const uint8_t *__restrict__ codes_in,
                                                              const float *__restrict__ scale_in)
 {
+    // launched as a programmatic dependent of the previous kernel in the stream:
+    // its blocks may be resident early, but nothing is read or written before
+    // that kernel (which may produce q, or still read this workspace) completes
+    umma::grid_wait();
     const int64_t r = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (r >= rows)
@@ -946,10 +950,19 @@ cudaError_t launch_quantize_q_wide(const FwdArgs &a, cudaStream_t stream)
     const int64_t qrows = (int64_t)a.T * a.H;
     if (qrows == 0)
         return cudaSuccess;
-    quantize_q_e4m3_kernel<<<dim3((unsigned)((qrows + 3) / 4)), dim3(128), 0, stream>>>(
-        static_cast<const __nv_bfloat16 *>(a.q), qrows, a.H, a.q8, a.q8_rope, a.q_scale,
-        a.q_fp8_in ? static_cast<const uint8_t *>(a.q) : nullptr, a.q_scale_in);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((qrows + 3) / 4));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, quantize_q_e4m3_kernel, static_cast<const __nv_bfloat16 *>(a.q), qrows, a.H,
+                              a.q8, a.q8_rope, a.q_scale,
+                              a.q_fp8_in ? static_cast<const uint8_t *>(a.q) : nullptr, a.q_scale_in);
 }
 
 cudaError_t launch_fwd_wide(const FwdArgs &a, cudaStream_t stream)
