@@ -581,7 +581,8 @@ def run_ours(args):
             },
             "query_rows_per_s": round(job_rate(rows * K, world, ms_max), 1),
             "gpu_launches": K * (2 if (w.kind == "wide" and not args.bf16_dots) else 1),
-            "roofline": roofline(w, per_launch_bytes, valid_per_launch, ms / K * 1e-3, ncu_traffic(w.name)),
+            "roofline": roofline(w, per_launch_bytes, valid_per_launch, ms / K * 1e-3, ncu_traffic(w.name),
+                                 l2_gbs=l2_read_gbs(binding, dev, stream) if w.kind == "prefill" else None),
             "ms_isolated_launch": round(iso, 6),
             "clocks": clk,
             "e2e": e2e,

@@ -34,10 +34,14 @@
 // shared-memory traffic per 32 KB tile, more than the rest of the tile.
 //
 // Warp roles, handing tiles over through mbarriers:
-//   producers (warps 5-8): q into shared memory once (quantized for E4M3);
-//     then per tile one gather4 per thread into the stage ring, completing
-//     the stage's "full" barrier by transaction bytes. A stage is refilled
-//     once everything that reads it is done ("empty").
+//   producers (warps 5-8; 5-12 for a bf16 pool that fits in L2): q into
+//     shared memory once (quantized for E4M3); then per tile one gather4 per
+//     thread into the stage ring, completing the stage's "full" barrier by
+//     transaction bytes. A stage is refilled once everything that reads it is
+//     done ("empty"). A warp issues its lanes' copies one after another: from
+//     L2 eight warps of 16 copies gather faster than four of 32 (prefill over
+//     an 8 MiB pool: 2.43 against 2.92 ms), from DRAM slower (decode: 40.6
+//     against 34.6 us), so the launch picks by the pool's size.
 //   MMA issuers (one thread each in warps 4, 9, 10, and 11 for bf16): QK(i)
 //     as soon as tile i has landed (and the softmax is done with the S
 //     buffer), in two halves for bf16; PV(i) as soon as the softmax has
@@ -92,10 +96,7 @@ namespace {
 
 constexpr int kSoftmaxWarps = 4;
 constexpr int kMmaWarp = 4;       // QK, first half of the columns
-constexpr int kProducerWarp0 = 5;
-constexpr int kProducerWarps = 4;
-constexpr int kProducerThreads = 32 * kProducerWarps;
-constexpr int kMmaWarp2 = kProducerWarp0 + kProducerWarps; // more MMA issuers: warps 9, 10 (and 11 for bf16)
+constexpr int kProducerWarp0 = 5; // 4 producer warps (8 for a bf16 pool held in L2), then more MMA issuers
 constexpr int kConverterThreads = 128;
 // tensor memory columns: O^T 0..63, S^T partial p of buffer b at kSCol + 32 p + 16 b
 constexpr int kSCol = 64;
@@ -112,13 +113,16 @@ constexpr int kIdxAhead = 4;              // tiles of index look-ahead
 // cache with bf16 dots (q . code * kv_scale with q unquantized), run as the
 // bf16 variant on binary16 operands that converter warps expand exactly from
 // the gathered E4M3 tile.
-enum Mode : int { kBf16 = 0, kFp8 = 1, kBf16Dots = 2 };
+// A fourth: a bf16 cache whose pool fits in L2 (e.g. prefill over one
+// sequence's keys), where the gathers come from L2 and eight producer warps
+// issue them faster than four; from DRAM eight are slower than four.
+enum Mode : int { kBf16 = 0, kFp8 = 1, kBf16Dots = 2, kBf16L2 = 3 };
 
 template <int MODE>
 struct Cfg {
     static constexpr bool FP8 = MODE == kFp8;
     static constexpr bool BD = MODE == kBf16Dots;
-    static constexpr bool G8 = MODE != kBf16;     // the gathered cache rows are E4M3
+    static constexpr bool G8 = FP8 || BD;         // the gathered cache rows are E4M3
     static constexpr int EB = G8 ? 1 : 2;         // bytes per cache element
     static constexpr int ROW = kD * EB;           // bytes per cache row
     static constexpr int NCB = ROW / 128;         // 128-byte column blocks per row (8 | 4)
@@ -126,6 +130,10 @@ struct Cfg {
     static constexpr int BLK = kKeys * 128;       // one column block of a tile (8 KB)
     static constexpr int TILE = NCB * BLK;        // 64 keys (64 KB | 32 KB)
     static constexpr int COPIES = 16 * NCB;       // gather4 copies per tile (128 | 64)
+    static constexpr int PWARPS = MODE == kBf16L2 ? 8 : 4;      // producer warps
+    static constexpr int PTHREADS = 32 * PWARPS;
+    static constexpr int COPY_LANES = COPIES / PWARPS;          // copies a producer warp issues per tile
+    static constexpr int MMA_WARP2 = kProducerWarp0 + PWARPS;   // further MMA issuers from here
     static constexpr int STAGES = FP8 ? 5 : (BD ? 2 : 3);
     // bf16 dots: binary16 stages [64 keys x 512] in the layout of the bf16
     // variant's tile, each written by the converters and read by QK and PV
@@ -165,19 +173,20 @@ struct Cfg {
     static_assert(!FP8 || VCOL + VBUFS * 128 <= TMEM_COLS, "the V^T buffers fit in tensor memory");
     static constexpr int SMEM = OFF_MBAR + NBAR * 8;
     static constexpr int SMEM_ALLOC = SMEM + 1024; // the base is aligned up to 1 KB in the kernel
-    // MMA issuers in warps 4 and kMmaWarp2.. (bf16, bf16 dots: 2 QK + 2 PV; E4M3: 1 + 2)
+    // MMA issuers in warps 4 and MMA_WARP2.. (bf16, bf16 dots: 2 QK + 2 PV; E4M3: 1 + 2)
     static constexpr int MMA_WARPS2 = QK_ISSUERS + PV_ISSUERS - 1;
-    static constexpr int CONVERTER_WARP0 = kMmaWarp2 + MMA_WARPS2; // E4M3, bf16 dots
-    static constexpr int THREADS = 32 * (G8 ? CONVERTER_WARP0 + 4 : kMmaWarp2 + MMA_WARPS2);
+    static constexpr int CONVERTER_WARP0 = MMA_WARP2 + MMA_WARPS2; // E4M3, bf16 dots
+    static constexpr int THREADS = 32 * (G8 ? CONVERTER_WARP0 + 4 : MMA_WARP2 + MMA_WARPS2);
     // 15 or 16 warps share the register file, so at most 128 registers a thread
     static constexpr int BOUND_THREADS = G8 ? 512 : THREADS;
+    static_assert(THREADS <= 512 && COPY_LANES <= 32 && COPIES % PWARPS == 0, "the warp layout fits");
     // stage "empty" arrivals: the PV commits (bf16), the QK commits and every
     // converter thread (E4M3: PV reads V^T from tensor memory, not the stage),
     // every converter thread (bf16 dots: QK and PV read the binary16 stage)
     static constexpr int EMPTY_COUNT = FP8 ? QK_ISSUERS + kConverterThreads : (BD ? kConverterThreads : PV_ISSUERS);
     static_assert(STAGES * TILE >= kHeads * kD * 4, "epilogue staging fits in the ring");
     static_assert(2 * QGRP >= 128 * kHeads * 4, "merge weights fit in the q area");
-    static_assert(COPIES <= kProducerThreads, "one copy per producer thread at most");
+    static_assert(COPIES <= PTHREADS, "one copy per producer thread at most");
     static_assert(!BD || OFF_QSTG + kHeads * kD * 2 <= OFF_FRING + FSTAGES * FTILE, "q staging fits in a stage");
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
@@ -248,7 +257,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::BOUND_THREADS, 1)
             umma::mbar_init(p_full(b), kSoftmaxWarps * 32);
             umma::mbar_init(p_empty(b), C::PV_ISSUERS);
         }
-        umma::mbar_init(q_full, kProducerThreads);
+        umma::mbar_init(q_full, C::PTHREADS);
         umma::mbar_init(drain, C::QK_ISSUERS + C::PV_ISSUERS);
         for (int vb = 0; vb < C::VBUFS; ++vb) {
             umma::mbar_init(v_full(vb), kConverterThreads);
@@ -288,15 +297,16 @@ __global__ void __launch_bounds__(Cfg<MODE>::BOUND_THREADS, 1)
             atomicOr(&g_umma_error, 2);
     };
 
-    if (warp >= kProducerWarp0 && warp < kProducerWarp0 + kProducerWarps) {
+    if (warp >= kProducerWarp0 && warp < kProducerWarp0 + C::PWARPS) {
         // ======================= producers =======================
         const int pt = tid - kProducerWarp0 * 32;
         const __nv_bfloat16 *__restrict__ qg =
             static_cast<const __nv_bfloat16 *>(a.q) + (int64_t)t * kHeads * kD;
-        // this thread's copy (bf16: all 128 threads; E4M3 rows: lanes 0-15 of
-        // each warp): key quad qd (keys 4qd..4qd+3), column block cb
-        const int cid = G8 ? (pt >> 5) * 16 + (pt & 15) : pt;
-        const bool copier = G8 ? (pt & 31) < 16 : true;
+        // this thread's copy (the first COPY_LANES lanes of each producer warp:
+        // all 32 for bf16 rows from four warps, 16 otherwise): key quad qd (keys
+        // 4qd..4qd+3), column block cb
+        const int cid = (pt >> 5) * C::COPY_LANES + (pt & 31);
+        const bool copier = (pt & 31) < C::COPY_LANES;
         const int qd = cid / C::NCB, cb = cid % C::NCB;
         // raw indices only: checking them here would wait for the loads
         auto fetch = [&](int tile, int (&r)[4]) {
@@ -320,7 +330,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::BOUND_THREADS, 1)
         // published once the first tile's copies are in flight, so both latencies overlap
         auto issue_q = [&] {
             if constexpr (!G8) {
-                for (int e = pt; e < kHeads * 64; e += kProducerThreads) {
+                for (int e = pt; e < kHeads * 64; e += C::PTHREADS) {
                     const int h = e >> 6, c = e & 63;
                     cp_async_16(q_s + (h >> 3) * C::QGRP + c * 128 + (h & 7) * 16, qg + h * kD + c * 8, 16);
                 }
@@ -328,7 +338,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::BOUND_THREADS, 1)
                 // pre-quantized q: each head's 512 codes straight into core matrices
                 // (a core-matrix row holds 16 codes)
                 const uint8_t *q8g = static_cast<const uint8_t *>(a.q) + (int64_t)t * kHeads * kD;
-                for (int e = pt; e < kHeads * (kD / 16); e += kProducerThreads) {
+                for (int e = pt; e < kHeads * (kD / 16); e += C::PTHREADS) {
                     const int h = e / (kD / 16), c = e % (kD / 16);
                     cp_async_16(q_s + (h >> 3) * C::QGRP + c * 128 + (h & 7) * 16, q8g + h * kD + c * 16, 16);
                 }
@@ -461,7 +471,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::BOUND_THREADS, 1)
             }
             // all or none of a tile's copies are issued, so a stage's barrier
             // always completes once its copies are in flight
-            umma::named_bar(2, kProducerThreads);
+            umma::named_bar(2, C::PTHREADS);
             if (!go_s[j & 1]) {
                 stop = true;
                 return;
@@ -487,12 +497,12 @@ __global__ void __launch_bounds__(Cfg<MODE>::BOUND_THREADS, 1)
             for (int j = max(0, issued - S_); j < issued; ++j)
                 wait_issued(full(j % S_), (uint32_t)((j / S_) & 1));
         }
-    } else if (warp == kMmaWarp || (warp >= kMmaWarp2 && warp < kMmaWarp2 + C::QK_ISSUERS + C::PV_ISSUERS - 1)) {
+    } else if (warp == kMmaWarp || (warp >= C::MMA_WARP2 && warp < C::MMA_WARP2 + C::MMA_WARPS2)) {
         // ======================= MMA issuers =======================
         if (lane == 0) {
             // roles 0 .. QK_ISSUERS-1: parts of QK; the next PV_ISSUERS: PV over
             // halves of the value dims (M-blocks 2 v, 2 v + 1 for PV issuer v)
-            const int role = warp == kMmaWarp ? 0 : 1 + warp - kMmaWarp2;
+            const int role = warp == kMmaWarp ? 0 : 1 + warp - C::MMA_WARP2;
             const bool is_pv = role >= C::QK_ISSUERS;
             if (role < C::QK_ISSUERS) {
                 wait_bar(q_full, 0);
@@ -916,8 +926,21 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 
 cudaError_t launch_fwd_umma16(const FwdArgs &a, cudaStream_t stream)
 {
-    if (!a.kv_fp8)
-        return launch<kBf16>(a, stream);
+    if (!a.kv_fp8) {
+        // a pool that fits in a quarter of L2 is gathered from L2
+        static std::atomic<int> l2_bytes[64];
+        int dev = 0;
+        if (const cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess)
+            return e;
+        int l2 = l2_bytes[dev & 63].load(std::memory_order_relaxed);
+        if (l2 == 0) {
+            if (const cudaError_t e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev); e != cudaSuccess)
+                return e;
+            l2_bytes[dev & 63].store(l2, std::memory_order_relaxed);
+        }
+        const bool in_l2 = a.num_slots * (int64_t)(kD * 2) * 4 <= (int64_t)l2;
+        return in_l2 ? launch<kBf16L2>(a, stream) : launch<kBf16>(a, stream);
+    }
     return a.bf16_dots ? launch<kBf16Dots>(a, stream) : launch<kFp8>(a, stream);
 }
 
