@@ -166,13 +166,10 @@ smla_status plan_forward(int T, int H, int D_qk, int D_v, int topk, int kv_dtype
         if (num_splits == 0 && kernel != SMLA_KERNEL_TCGEN05_BASIC && topk > 0 && rows * 2 <= kTicketSlots) {
             if (const cudaError_t e = current_sm_count(&sms); e != cudaSuccess)
                 return cuda_status(e);
-            // spread only when one pair per row would leave many pairs idle in
-            // its last wave: the pieces of shared rows cost about as much as
-            // a sixth of a wave (128 rows on 76 pairs, 84% of the slots busy:
-            // 107 us per row pair against 109 us spread)
+            // (128 rows on 76 pairs: 104 us spread against 107 us with one
+            // pair per row and its second wave 68% full)
             const int64_t P = sms / 2;
-            const int64_t waves = P > 0 ? (rows + P - 1) / P : 0;
-            if (P > 0 && rows > P && rows * 5 < waves * P * 4 && rows * ntiles / P + ntiles < (int64_t(1) << 30)) {
+            if (P > 0 && rows > P && rows * ntiles / P + ntiles < (int64_t(1) << 30)) {
                 pairs = (int)P;
                 shared_rows = rows % pairs != 0;
             }
@@ -202,7 +199,7 @@ WorkspaceLayout workspace_layout(int T, int H, int D_qk, int D_v, int S, bool wi
         w.q_scale = up(w.q8_rope + (size_t)T * H * (D_qk - 512));
         w.total = up(w.q_scale + (size_t)T * H * sizeof(float));
         if (wide_pairs > 0) {
-            // two partial slots per pair and value half: [256 dims][128 heads] binary16 and 128 lse
+            // two partial slots per pair and value half: 256 dims x 128 heads binary16 and 128 lse
             w.wide_part_lse = w.total;
             w.wide_part = up(w.wide_part_lse + (size_t)wide_pairs * 2 * 2 * 128 * sizeof(float));
             w.total = up(w.wide_part + (size_t)wide_pairs * 2 * 2 * 128 * 256 * sizeof(uint16_t));

@@ -735,11 +735,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *last_s = (atomicOr(flag, 0) & other_bit) != 0; // the other piece has finished
             umma::named_bar(1, 128);
             if (!*last_s) {
-                // store this piece as [256 dims][128 heads] binary16 of this half and its 128 lse
-                uint16_t *po = a.wide_part + (slot * 2 + half) * (int64_t)(kDvHalf * kHeads);
+                // store this piece (binary16 of this half) as 16-byte granules of 8
+                // heads, [head group][256 dims][8 heads], so that a warp's lanes
+                // (consecutive dims) store, and the merge later loads, contiguous
+                // 512 bytes; and its 128 lse
+                uint4 *po = reinterpret_cast<uint4 *>(a.wide_part + (slot * 2 + half) * (int64_t)(kDvHalf * kHeads));
 #pragma unroll 1
                 for (int mb = 0; mb < 2; ++mb) {
-                    uint4 *pd = reinterpret_cast<uint4 *>(po + (int64_t)(128 * mb + d0) * kHeads);
+                    uint4 *pd = po + 128 * mb + d0;
 #pragma unroll 1
                     for (int c = 0; c < kHeads; c += 32) {
                         uint32_t o[32];
@@ -755,7 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
-                            __stcg(pd + c / 8 + q, make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
+                            __stcg(pd + (c / 8 + q) * kDvHalf, make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
                     }
                 }
                 __stcg(a.wide_part_lse + (slot * 2 + half) * kHeads + h, lse_p);
@@ -796,7 +799,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int mb = 0; mb < 2; ++mb)
 #pragma unroll
                     for (int u = 0; u < 8; ++u)
-                        v[mb][u] = __ldcg(ps + (int64_t)(128 * mb + d0) * (kHeads / 8) + c0 / 8 + u);
+                        v[mb][u] = __ldcg(ps + (c0 / 8 + u) * kDvHalf + 128 * mb + d0);
 #pragma unroll
                 for (int mb = 0; mb < 2; ++mb) {
 #pragma unroll

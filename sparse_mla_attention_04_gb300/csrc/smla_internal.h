@@ -38,8 +38,8 @@ struct FwdArgs {
     const float *q_scale_in; // that scale (device scalar), or nullptr
     // 128-head kernel: pairs of CTAs the (row, key tile) sequence is cut into
     // (rows = T * H / 128 gives one row per pair), and for rows a pair shares
-    // with its neighbour the partial outputs [2 * pairs][2 halves][256 dims]
-    // [128 heads] (binary16, in units of the cache's codes), their lse
+    // with its neighbour the partial outputs [2 * pairs][2 halves][16 head
+    // groups][256 dims][8 heads] (binary16, in units of the cache's codes), their lse
     // [2 * pairs][2][128], and per (row, half) merge flags [rows][2] (in the
     // counter region)
     int wide_pairs;
