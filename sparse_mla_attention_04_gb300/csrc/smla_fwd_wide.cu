@@ -708,8 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
                     for (int c = 0; c < kHeads; c += 32) {
                         uint32_t o[32];
-                        umma::ld16(tl + 128 * mb + c, reinterpret_cast<uint32_t(&)[16]>(o[0]));
-                        umma::ld16(tl + 128 * mb + c + 16, reinterpret_cast<uint32_t(&)[16]>(o[16]));
+                        umma::ld32(tl + 128 * mb + c, o);
                         umma::wait_ld();
 #pragma unroll
                         for (int e = 0; e < 32; ++e) {
@@ -746,8 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
                     for (int c = 0; c < kHeads; c += 32) {
                         uint32_t o[32];
-                        umma::ld16(tl + 128 * mb + c, reinterpret_cast<uint32_t(&)[16]>(o[0]));
-                        umma::ld16(tl + 128 * mb + c + 16, reinterpret_cast<uint32_t(&)[16]>(o[16]));
+                        umma::ld32(tl + 128 * mb + c, o);
                         umma::wait_ld();
                         uint32_t w[16];
 #pragma unroll
@@ -857,9 +855,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             wait_bar(s_full(b), (uint32_t)((j >> 1) & 1));
             umma::fence_after_sync();
             float sv[64];
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                umma::ld16(tl + kSCol + 64 * b + 16 * c, reinterpret_cast<uint32_t(&)[16]>(sv[16 * c]));
+            umma::ld32(tl + kSCol + 64 * b, reinterpret_cast<uint32_t(&)[32]>(sv[0]));
+            umma::ld32(tl + kSCol + 64 * b + 32, reinterpret_cast<uint32_t(&)[32]>(sv[32]));
             umma::wait_ld();
             // the tile max in four independent chains; a tile whose 64 keys are all
             // valid (the common case) skips the masking
