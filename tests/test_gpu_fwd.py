@@ -306,6 +306,28 @@ def test_lse_optional_and_t_zero():
     assert e.shape == (0, 16, 512)
 
 
+@pytest.mark.parametrize("splits", [1, 2, 9])
+def test_pool_in_l2_and_in_dram_give_the_same_bits(splits):
+    """A bf16 pool that fits in a quarter of L2 is gathered by eight producer
+    warps, a larger one by four; the arithmetic is the same, so the same rows
+    in a 4 MB pool and in that pool padded to 64 MB give identical bits."""
+    w = inputs.Workload("pool_modes", 6, 16, 512, 512, 4096, 1500, False, 1 / math.sqrt(512), "uniform", seed=21)
+    q = inputs.make_q(w).to(DEV)
+    small = inputs.make_kv_source(w).to(DEV)
+    big = torch.zeros((65536, 512), dtype=torch.bfloat16, device=DEV)
+    big[:4096] = small
+    big[4096:] = float("nan")  # never referenced
+    idx = inputs.make_indices(w)
+    idx[1, 700:] = -1
+    ti = torch.from_numpy(idx).to(DEV)
+    o1, l1 = binding.sparse_mla_fwd(q, small, ti, w.scale, num_splits=splits)
+    o2, l2 = binding.sparse_mla_fwd(q, big, ti, w.scale, num_splits=splits)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert torch.isfinite(o1.float()).all()
+    assert binding.smla_device_error() == 0
+
+
 def test_topk_zero_gives_empty_rows(kernel):
     w = inputs.tiny()
     q = inputs.make_q(w).to(DEV)

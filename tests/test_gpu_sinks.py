@@ -121,6 +121,34 @@ def test_sinks_prequantized_q():
             TOL_FP8_MIRROR, "pre-quantized q, sinks")
 
 
+@pytest.mark.parametrize("kernel", ["auto", "mma"])
+@pytest.mark.parametrize("splits", [1, 4, 10])
+def test_sinks_bf16_dots_over_e4m3(kernel, splits):
+    """bf16 dots over an E4M3 cache with sinks (the tcgen05 16-head kernel's
+    bf16-dots mode, and the warp-MMA kernel), against the oracle with q
+    unquantized and the same codes; an empty row gives the sink."""
+    w = inputs.decode(n_seqs=4, ctx=8192, topk=2048, fp8=True, name="decode_fp8_bf16dots_sinks")
+    q = inputs.make_q(w)
+    src = inputs.make_kv_source(w)
+    cache, kvs = binding.build_fp8_cache(src.to(DEV))
+    ocache, oscale = parity.oracle_cache(src, True)
+    idx = inputs.make_indices(w)
+    idx[2, :] = -1
+    sinks = _sinks(16, 6)
+    out, lse = binding.sparse_mla_fwd(q.to(DEV), cache, torch.from_numpy(idx).to(DEV), w.scale, kv_scale=kvs,
+                                      dot_precision="bf16", num_splits=splits,
+                                      sinks=torch.from_numpy(sinks).to(DEV), kernel=kernel)
+    torch.cuda.synchronize()
+    ro, rl, _ = oracle.sparse_mla(q, ocache, idx, w.scale, kv_fp8=True, kv_scale=oscale, sinks=sinks)
+    o = out.float().cpu().numpy().astype(np.float64)
+    l = lse.cpu().numpy().astype(np.float64)
+    compare(o, l, ro, rl, TOL_BF16, "bf16 dots over E4M3, sinks")
+    assert (o[2] == 0).all()
+    fin = np.isfinite(sinks)
+    np.testing.assert_allclose(l[2][fin], sinks[fin].astype(np.float64), rtol=0, atol=1e-6)
+    assert binding.smla_device_error() == 0
+
+
 def test_no_sinks_through_ex_is_the_plain_forward():
     """sinks = -inf for every head equals the forward without sinks, bit for bit."""
     w = inputs.decode(n_seqs=4, ctx=8192, topk=2048, name="decode_bf16_nosink")
