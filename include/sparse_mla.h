@@ -293,8 +293,11 @@ SMLA_API smla_status sparse_mla_fwd_q8(const void *q8, const float *q_scale, con
  *     binary16 partial results);
  *   - the 128-head E4M3 kernel with fp8 dots (H a multiple of 128, D_qk = 576,
  *     one split), at any split plan: its quantized q, T * H * 580 bytes after
- *     a 64 KB counter region. T * H must stay below about 14,300: 128 rows of
- *     128 heads (9.5 MB) do not fit and are rejected.
+ *     a 64 KB counter region. When its automatic plan spreads the rows over
+ *     CTA pairs (more rows than pairs) it also keeps partials of shared rows;
+ *     if those do not fit, this entry point runs the call with one CTA pair
+ *     per row, which needs the quantized q only. T * H must stay below about
+ *     14,300: 128 rows of 128 heads (9.5 MB) do not fit and are rejected.
  * Calls with bf16 dots or a bf16 cache and at most 8 splits use no workspace
  * and never touch the array. Nothing is allocated or freed. Each call looks
  * the array's device address up (cudaGetSymbolAddress) with its device

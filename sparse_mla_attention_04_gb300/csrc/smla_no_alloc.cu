@@ -59,16 +59,27 @@ extern "C" SMLA_API smla_status sparse_mla_fwd_no_alloc(const void *q, const voi
     p.num_splits = num_splits;
     p.stream = stream;
     p.kernel = SMLA_KERNEL_AUTO;
-    const size_t need = sparse_mla_fwd_ex_workspace_size(&p);
+    size_t need = sparse_mla_fwd_ex_workspace_size(&p);
     if (need == (size_t)-1 || need == 0) // invalid (the full checks report why), or no workspace needed
         return sparse_mla_fwd_ex(&p);
-    if (need > kScratchBytes)
-        return SMLA_ERR_WORKSPACE_TOO_SMALL;
     smla::FwdPlan plan;
     if (const smla_status st = smla::plan_forward(T, H, D_qk, D_v, topk, kv_dtype, dot_precision, num_splits,
                                                   SMLA_KERNEL_AUTO, &plan);
         st != SMLA_OK)
         return st;
+    if (need > kScratchBytes && plan.wide_pairs > 0 && num_splits == 0) {
+        // the 128-head kernel's automatic plan spreads rows over CTA pairs and
+        // keeps partials of the rows they share; one pair per row needs only
+        // the quantized q, so run that plan when it fits
+        p.kernel = SMLA_KERNEL_TCGEN05_BASIC;
+        need = sparse_mla_fwd_ex_workspace_size(&p);
+        if (const smla_status st = smla::plan_forward(T, H, D_qk, D_v, topk, kv_dtype, dot_precision, num_splits,
+                                                      p.kernel, &plan);
+            st != SMLA_OK)
+            return st;
+    }
+    if (need > kScratchBytes)
+        return SMLA_ERR_WORKSPACE_TOO_SMALL;
     void *ws = nullptr;
     if (cudaGetSymbolAddress(&ws, g_no_alloc_scratch) != cudaSuccess)
         return SMLA_ERR_CUDA;

@@ -10,7 +10,8 @@ match the fp64 oracle within the tolerances the other parity tests use:
   - bf16 cache, more than 8 splits (the array holds counters and partials);
   - E4M3 cache, fp8 dots, 16 heads, 16 splits (the same, E4M3 path);
   - E4M3 cache, fp8 dots, 128 heads, D_qk = 576 (the array holds the
-    quantized q of the 128-head kernel at its single split);
+    quantized q of the 128-head kernel at its single split; with more rows
+    than CTA pairs the call runs one pair per row, whose q fits);
   - calls that need no workspace, including 128 heads with bf16 dots and
     calls that follow ones that used the array with another shape;
 and that a call needing more than the array (the 128-row, 128-head fp8 call)
@@ -99,6 +100,35 @@ def test_no_alloc_128_heads_fp8_dots():
     assert 0 < need <= SCRATCH
     for seed in (45, 46):
         _case(w, "fp8", 0, seed)
+
+
+def test_no_alloc_128_heads_more_rows_than_pairs():
+    """80 rows x 128 heads with fp8 dots: the automatic plan spreads the rows
+    over CTA pairs and would keep partials of shared rows (more than the
+    array holds); the entry point then runs one CTA pair per row, whose
+    quantized q (5.9 MB) fits. Bit-identical to the forward asked for that
+    plan, and within tolerance of the oracle."""
+    w = inputs.Workload("noalloc_wide80", 80, 128, 576, 512, 4000, 256, True, 1 / math.sqrt(576), "uniform", seed=48)
+    assert _need(w, "fp8", 0) > SCRATCH
+    assert 0 < binding.sparse_mla_fwd_ex_workspace_size(w.T, w.H, w.D_qk, w.D_v, w.topk, 1, dot_precision="fp8",
+                                                         num_splits=0, kernel="basic") <= SCRATCH
+    q = inputs.make_q(w)
+    src = inputs.make_kv_source(w)
+    idx = inputs.make_indices(w)
+    cache, kvs = parity.gpu_cache(src.to(DEV), True)
+    qd, idd = q.to(DEV), torch.from_numpy(idx).to(DEV)
+    for _ in range(2):  # two calls in a row through the static array
+        st, o_new, l_new = _call_no_alloc(qd, cache, kvs, idd, w.scale, "fp8", 0)
+        assert st == binding.SMLA_OK, binding.status_string(st)
+        o_ref, l_ref = binding.sparse_mla_fwd(qd, cache, idd, w.scale, kv_scale=kvs, dot_precision="fp8",
+                                              kernel="basic")
+        torch.cuda.synchronize()
+        assert torch.equal(o_new, o_ref) and torch.equal(l_new, l_ref)
+    ocache, oscale = parity.oracle_cache(src, True)
+    ro, rl, _ = oracle.sparse_mla(q, ocache, idx, w.scale, kv_fp8=True, kv_scale=oscale, q_mode=1)
+    compare(o_new.float().cpu().numpy().astype(np.float64), l_new.cpu().numpy().astype(np.float64), ro, rl,
+            TOL_FP8_MIRROR, "no_alloc, 128 heads, one pair per row")
+    assert binding.smla_device_error() == 0
 
 
 def test_no_alloc_calls_without_workspace_after_ones_with():
