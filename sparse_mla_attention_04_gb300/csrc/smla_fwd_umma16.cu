@@ -34,24 +34,22 @@
 // shared-memory traffic per 32 KB tile, more than the rest of the tile.
 //
 // Warp roles, handing tiles over through mbarriers:
-//   producers (warps 5-8; 5-12 for a bf16 pool that fits in L2): q into
-//     shared memory once (quantized for E4M3); then per tile one gather4 per
-//     thread into the stage ring, completing the stage's "full" barrier by
-//     transaction bytes. A stage is refilled once everything that reads it is
-//     done ("empty"). A warp issues its lanes' copies one after another: from
-//     L2 eight warps of 16 copies gather faster than four of 32 (prefill over
-//     an 8 MiB pool: 2.43 against 2.92 ms), from DRAM slower (decode: 40.6
-//     against 34.6 us), so the launch picks by the pool's size. A pool that
-//     fits in L2 is copied without the TMA altogether: each of the eight
-//     warps' threads issues 16-byte cp.async copies (16 a tile, 512
-//     contiguous bytes of a row per warp instruction) straight into the same
-//     128-byte swizzled layout, and the stage's barrier counts every producer
-//     thread once its copies have landed (prefill: 2.24 against 2.44 ms for
-//     the eight-warp gathers); the MMA issuers fence the generic proxy's
-//     writes before their MMAs read the stage. In that mode the CTA first
+//   producers (warps 5-12 for a bf16 cache, 5-8 for E4M3): q into shared
+//     memory once (quantized for E4M3); then the rows of each tile. bf16
+//     rows are copied by 16-byte cp.async: each of the 256 producer threads
+//     issues 16 per tile (a warp instruction reads 512 contiguous bytes of a
+//     row) straight into the 128-byte swizzled layout, and the stage's
+//     "full" barrier counts every producer thread once its copies have
+//     landed; the MMA issuers fence the generic proxy's writes before their
+//     MMAs read the stage. E4M3 rows come by TMA gather4, one per thread,
+//     completing "full" by transaction bytes. A stage is refilled once
+//     everything that reads it is done ("empty"). The TMA gathers of bf16
+//     rows were slower both from DRAM (decode 34.6 against 32.6 us) and from
+//     L2 (prefill 2.44 against 2.24 ms): a warp issues its lanes' gather
+//     copies one after another. For a pool that fits in L2 the CTA first
 //     finds its split's last valid index and runs only the tiles up to it
 //     (a row shorter than top-k is padded at its end: prefill 2.01 ms).
-//   MMA issuers (one thread each in warps 4, 9, 10, and 11 for bf16): QK(i)
+//   MMA issuers (one thread each in warps 4, 13, 14 and 15 for bf16): QK(i)
 //     as soon as tile i has landed (and the softmax is done with the S
 //     buffer), in two halves for bf16; PV(i) as soon as the softmax has
 //     written P(i), two threads each taking half of the value dims. A single
@@ -125,7 +123,8 @@ constexpr int kIdxAhead = 4;              // tiles of index look-ahead
 // A fourth: a bf16 cache whose pool fits in L2 (e.g. prefill over one
 // sequence's keys), where the gathers come from L2 and eight producer warps
 // issue them faster than four; from DRAM eight are slower than four.
-enum Mode : int { kBf16 = 0, kFp8 = 1, kBf16Dots = 2, kBf16L2 = 3, kBf16Async = 4 };
+// bf16 cache rows are copied by cp.async (kBf16Async); E4M3 rows by TMA gathers
+enum Mode : int { kFp8 = 1, kBf16Dots = 2, kBf16Async = 4 };
 
 template <int MODE>
 struct Cfg {
@@ -139,9 +138,9 @@ struct Cfg {
     static constexpr int BLK = kKeys * 128;       // one column block of a tile (8 KB)
     static constexpr int TILE = NCB * BLK;        // 64 keys (64 KB | 32 KB)
     static constexpr int COPIES = 16 * NCB;       // gather4 copies per tile (128 | 64)
-    // bf16 rows copied by 16-byte cp.async instead of TMA gathers (a pool in L2)
+    // bf16 rows are copied by 16-byte cp.async from eight producer warps
     static constexpr bool ASYNC = MODE == kBf16Async;
-    static constexpr int PWARPS = (MODE == kBf16L2 || ASYNC) ? 8 : 4; // producer warps
+    static constexpr int PWARPS = ASYNC ? 8 : 4; // producer warps
     static constexpr int PTHREADS = 32 * PWARPS;
     static constexpr int COPY_LANES = COPIES / PWARPS;          // copies a producer warp issues per tile
     static constexpr int MMA_WARP2 = kProducerWarp0 + PWARPS;   // further MMA issuers from here
@@ -296,7 +295,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::BOUND_THREADS, 1)
     // own prologue on free SMs meanwhile
     umma::grid_launch_dependents();
     umma::grid_wait();
-    if constexpr (C::ASYNC) {
+    if (C::ASYNC && a.trim_tail) {
         // tiles after the split's last valid index hold only masked keys (a row
         // shorter than top-k is padded at its end): find that index (one load
         // per thread and round from L2) and run only the tiles up to it
@@ -992,7 +991,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 cudaError_t launch_fwd_umma16(const FwdArgs &a, cudaStream_t stream)
 {
     if (!a.kv_fp8) {
-        // a pool that fits in a quarter of L2 is gathered from L2
+        // bf16 rows by cp.async; a pool that fits in a quarter of L2 also skips
+        // the padded tail of short rows
         static std::atomic<int> l2_bytes[64];
         int dev = 0;
         if (const cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess)
@@ -1004,7 +1004,9 @@ cudaError_t launch_fwd_umma16(const FwdArgs &a, cudaStream_t stream)
             l2_bytes[dev & 63].store(l2, std::memory_order_relaxed);
         }
         const bool in_l2 = a.num_slots * (int64_t)(kD * 2) * 4 <= (int64_t)l2;
-        return in_l2 ? launch<kBf16Async>(a, stream) : launch<kBf16>(a, stream);
+        FwdArgs b = a;
+        b.trim_tail = in_l2; // one more round of loads pays off only from L2
+        return launch<kBf16Async>(b, stream);
     }
     return a.bf16_dots ? launch<kBf16Dots>(a, stream) : launch<kFp8>(a, stream);
 }

@@ -46,6 +46,9 @@ struct FwdArgs {
     uint16_t *wide_part;
     float *wide_part_lse;
     int *wide_tickets;
+    // 16-head kernel, cp.async copies: first find the split's last valid index
+    // and skip the tiles after it (set by its launcher for pools in L2)
+    bool trim_tail;
 };
 
 // Key tile of the warp-MMA kernel (keys per pipeline stage).
