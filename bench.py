@@ -380,12 +380,13 @@ def time_isolated(call, stream, flush, n=9):
 
 
 def ceiling_configs(row_bytes: int):
-    """(CTAs per SM, stages, pair mode, issue warps) of the gather-ceiling
-    sweep: for each CTA count the most 64-row tiles that fit (as the probe pads
-    its CTAs), with a tile's copies issued as the first forward kernels did
-    (0) and spread evenly over more warps (a warp issues its lanes' copies one
-    after another); and CTA pairs that share each tile (1: cluster multicast,
-    2: bulk copy into the peer)."""
+    """(CTAs per SM, stages, pair mode, issue warps, copy mode) of the
+    gather-ceiling sweep: for each CTA count the most 64-row tiles that fit (as
+    the probe pads its CTAs), filled by TMA gather4 copies (copy mode 0) issued
+    as the first forward kernels did (issue warps 0) and spread evenly over
+    more warps (a warp issues its lanes' copies one after another), or by
+    16-byte cp.async copies from eight warps (copy mode 1); and CTA pairs that
+    share each tile (1: cluster multicast, 2: bulk copy into the peer)."""
     boxes = (row_bytes + 127) // 128
     tile = 64 * 128 * boxes
     copies = 16 * boxes
@@ -393,35 +394,39 @@ def ceiling_configs(row_bytes: int):
     for k in (1, 2, 3, 4):
         st = min(8, (233472 // k - 1024 - 1024 - 256) // tile)
         if st >= 1:
-            out.append((k, st, 0, 0))
-            out.append((k, st, 0, max(-(-copies // 32), max(2, 8 // k))))
+            out.append((k, st, 0, 0, 0))
+            out.append((k, st, 0, max(-(-copies // 32), max(2, 8 // k)), 0))
+            out.append((k, st, 0, 0, 1))
     for pm in (1, 2):
-        out.append((1, min(8, (233472 - 1024 - 1024 - 256) // tile), pm, 0))
+        out.append((1, min(8, (233472 - 1024 - 1024 - 256) // tile), pm, 0, 0))
     return out
 
 
 def gather_ceiling(binding, cache, sets, stream, reps: int = 4):
     """The pure indexed-row copy probe on this workload's own pool and index
-    sets, for 1-4 CTAs per SM: rows/s and GB/s of the valid rows."""
+    sets, for 1-4 CTAs per SM and both copy methods: rows/s and GB/s of the
+    valid rows."""
     row_bytes = cache.shape[1] * cache.element_size()
     valid = sum(int((s["idx_np"] != -1).sum()) for s in sets)
     sms = torch.cuda.get_device_properties(cache.device).multi_processor_count
     res = []
-    for k, st, pm, iw in ceiling_configs(row_bytes):
+    for k, st, pm, iw, cm in ceiling_configs(row_bytes):
         ck = torch.zeros(sms * k, dtype=torch.int32, device=cache.device)
 
-        def probe(i, k=k, st=st, pm=pm, iw=iw, ck=ck):
+        def probe(i, k=k, st=st, pm=pm, iw=iw, cm=cm, ck=ck):
             binding.smla_gather_probe(cache, sets[i % len(sets)]["idx"], ctas_per_sm=k, stages=st, pair_mode=pm,
-                                      issue_warps=iw, checksum=ck, stream=stream)
+                                      issue_warps=iw, copy_mode=cm, checksum=ck, stream=stream)
         g = graph_of(probe, len(sets), 3, stream)
         ms = time_steps(g, probe, len(sets), reps * len(sets), stream)
         sec = ms * 1e-3 / reps
         res.append({"ctas_per_sm": k, "stages": st, "pair_mode": pm, "issue_warps": iw,
+                    "copy": "cp.async" if cm else "tma_gather4",
                     "rows_per_s": round(valid / sec, 1), "gbs": round(valid * row_bytes / sec / 1e9, 1)})
     best = max((r for r in res if not r["pair_mode"]), key=lambda r: r["gbs"])
     return {"row_bytes": row_bytes, "best_gbs": best["gbs"], "best_rows_per_s": best["rows_per_s"],
-            "best": [best["ctas_per_sm"], best["stages"], best["issue_warps"]], "sweep": res,
-            "kernel": "smla_gather_probe (TMA tile::gather4 into a shared-memory ring, 64-row tiles, no arithmetic)"}
+            "best": [best["ctas_per_sm"], best["stages"], best["issue_warps"], best["copy"]], "sweep": res,
+            "kernel": "smla_gather_probe (TMA tile::gather4 or 16-byte cp.async into a shared-memory ring, "
+                      "64-row tiles, no arithmetic)"}
 
 
 def l2_read_gbs(binding, dev, stream, mb: int = 32, reps: int = 16):

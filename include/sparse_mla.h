@@ -414,7 +414,9 @@ SMLA_API smla_status smla_fused_qk_rope_cache(const void *ql_nope, int64_t ql_st
  * of 64 rows, split evenly over ctas_per_sm CTAs on each SM; each CTA copies
  * its tiles' rows [idx, 0:row_bytes) of the pool [num_rows, row_bytes]
  * (row_bytes a multiple of 16, at most 1024) into a ring of `stages` tiles in
- * shared memory by TMA tile::gather4 (128-byte boxes, 128-byte swizzle); -1
+ * shared memory (128-byte column blocks, 128-byte swizzle): copy_mode 0 by TMA
+ * tile::gather4 (128-byte boxes), copy_mode 1 by 16-byte cp.async copies from
+ * eight warps (pair_mode and issue_warps 0, else SMLA_ERR_UNSUPPORTED). -1
  * and out-of-range entries are zero-filled without a read. A consumer folds
  * the first 4 bytes of each row into checksum[cta] (XOR, written; device
  * uint32 [sm_count * ctas_per_sm]) and holds each tile hold_ns nanoseconds
@@ -441,7 +443,7 @@ SMLA_API smla_status smla_fused_qk_rope_cache(const void *ql_nope, int64_t ql_st
  */
 SMLA_API smla_status smla_gather_probe(const void *pool, int64_t num_rows, int row_bytes,
                                        const int32_t *indices, int64_t n_indices, int ctas_per_sm,
-                                       int stages, int hold_ns, int pair_mode, int issue_warps,
+                                       int stages, int hold_ns, int pair_mode, int issue_warps, int copy_mode,
                                        uint32_t *checksum, smla_stream_t stream);
 SMLA_API smla_status smla_l2_read_probe(const void *buf, int64_t bytes, int reps, uint32_t *checksum,
                                         int blocks, smla_stream_t stream);

@@ -57,7 +57,7 @@ SIGNATURES = {
     "sparse_mla_fwd_ex": ([_c.c_void_p], _c.c_int),
     "sparse_mla_fwd_ex_workspace_size": ([_c.c_void_p], _c.c_size_t),
     "smla_gather_probe": ([_c.c_void_p, _c.c_int64, _c.c_int, _c.c_void_p, _c.c_int64, _c.c_int, _c.c_int,
-                           _c.c_int, _c.c_int, _c.c_int, _c.c_void_p, _c.c_void_p], _c.c_int),
+                           _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_void_p, _c.c_void_p], _c.c_int),
     "smla_l2_read_probe": ([_c.c_void_p, _c.c_int64, _c.c_int, _c.c_void_p, _c.c_int, _c.c_void_p], _c.c_int),
     "smla_compute_fp8_scale": ([_c.c_void_p, _c.c_int64, _c.c_void_p, _c.c_void_p], _c.c_int),
     "smla_fp8_cache_write": ([_c.c_void_p, _c.c_void_p, _c.c_int64, _c.c_int, _c.c_void_p,
@@ -319,15 +319,16 @@ def sparse_mla_fwd_q8(q8: torch.Tensor, q_scale: torch.Tensor, kv_cache: torch.T
 
 
 def smla_gather_probe(pool: torch.Tensor, indices: torch.Tensor, *, ctas_per_sm: int = 1, stages: int = 1,
-                      hold_ns: int = 0, pair_mode: int = 0, issue_warps: int = 0,
+                      hold_ns: int = 0, pair_mode: int = 0, issue_warps: int = 0, copy_mode: int = 0,
                       checksum: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """The pure indexed-row copy probe: rows `indices` (int32, any shape,
     taken flat) of `pool` [num_rows, row_bytes] (any 1- or 2-byte dtype)
-    gathered by TMA into shared memory and folded into per-CTA checksums
-    (uint32 device tensor [sm_count * ctas_per_sm], returned); pair_mode 1 / 2:
-    CTA pairs sharing each tile by cluster multicast / by a bulk copy into the
-    peer; issue_warps > 0: a tile's copies spread evenly over that many
-    producer warps."""
+    gathered into shared memory (copy_mode 0: TMA gather4, 1: 16-byte cp.async)
+    and folded into per-CTA checksums (uint32 device tensor
+    [sm_count * ctas_per_sm], returned); pair_mode 1 / 2: CTA pairs sharing
+    each tile by cluster multicast / by a bulk copy into the peer;
+    issue_warps > 0: a tile's copies spread evenly over that many producer
+    warps."""
     if pool.dim() != 2 or not pool.is_contiguous() or not pool.is_cuda:
         raise ValueError("pool must be a contiguous CUDA tensor [num_rows, row]")
     _need(indices.reshape(-1), "indices", torch.int32, 1)
@@ -337,7 +338,7 @@ def smla_gather_probe(pool: torch.Tensor, indices: torch.Tensor, *, ctas_per_sm:
         checksum = torch.zeros(sms * ctas_per_sm, dtype=torch.int32, device=pool.device)
     _check(lib().smla_gather_probe(_ptr(pool), pool.shape[0], row_bytes, _ptr(indices), indices.numel(),
                                    int(ctas_per_sm), int(stages), int(hold_ns), int(pair_mode), int(issue_warps),
-                                   _ptr(checksum),
+                                   int(copy_mode), _ptr(checksum),
                                    _stream(stream)),
            "smla_gather_probe")
     return checksum

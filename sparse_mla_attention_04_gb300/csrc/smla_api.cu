@@ -561,18 +561,18 @@ SMLA_API smla_status smla_fp8_cache_write(const void *src, const int64_t *slot_m
 
 SMLA_API smla_status smla_gather_probe(const void *pool, int64_t num_rows, int row_bytes, const int32_t *indices,
                                        int64_t n_indices, int ctas_per_sm, int stages, int hold_ns, int pair_mode,
-                                       int issue_warps, uint32_t *checksum, smla_stream_t stream)
+                                       int issue_warps, int copy_mode, uint32_t *checksum, smla_stream_t stream)
 {
     if (pool == nullptr || checksum == nullptr || (indices == nullptr && n_indices > 0))
         return SMLA_ERR_NULL_POINTER;
     if (num_rows < 0 || n_indices < 0 || row_bytes < 16 || row_bytes > 1024 || row_bytes % 16 != 0 ||
         ctas_per_sm < 1 || ctas_per_sm > 4 || stages < 1 || stages > 8 || hold_ns < 0 ||
-        pair_mode < 0 || pair_mode > 3 || issue_warps < 0 || issue_warps > 8)
+        pair_mode < 0 || pair_mode > 3 || issue_warps < 0 || issue_warps > 8 || copy_mode < 0 || copy_mode > 1)
         return SMLA_ERR_BAD_SHAPE;
     const int copies = (pair_mode == 1 || pair_mode == 2 ? 8 : 16) * ((row_bytes + 127) / 128);
     if (issue_warps > 0 && (copies + issue_warps - 1) / issue_warps > 32)
         return SMLA_ERR_BAD_SHAPE;
-    if (pair_mode && ctas_per_sm != 1)
+    if ((pair_mode && ctas_per_sm != 1) || (copy_mode == 1 && (pair_mode != 0 || issue_warps != 0)))
         return SMLA_ERR_UNSUPPORTED;
     if (!aligned(pool, 16) || !aligned(indices, 4) || !aligned(checksum, 4))
         return SMLA_ERR_MISALIGNED;
@@ -580,7 +580,7 @@ SMLA_API smla_status smla_gather_probe(const void *pool, int64_t num_rows, int r
     if (const cudaError_t e = current_sm_count(&sms); e != cudaSuccess)
         return cuda_status(e);
     const cudaError_t e = smla::launch_gather_probe(pool, num_rows, row_bytes, indices, n_indices, ctas_per_sm,
-                                                    stages, hold_ns, pair_mode, issue_warps, checksum, sms,
+                                                    stages, hold_ns, pair_mode, issue_warps, copy_mode, checksum, sms,
                                                     reinterpret_cast<cudaStream_t>(stream));
     if (e == cudaErrorInvalidValue)
         return SMLA_ERR_UNSUPPORTED; // the stages do not fit ctas_per_sm CTAs on an SM

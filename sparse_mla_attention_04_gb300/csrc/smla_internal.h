@@ -137,7 +137,8 @@ cudaError_t read_producer_error(int *out, bool reset);
 // pattern, and an L2 -> SM streaming read.
 cudaError_t launch_gather_probe(const void *pool, int64_t num_rows, int row_bytes, const int32_t *indices,
                                 int64_t n_indices, int ctas_per_sm, int stages, int hold_ns, int pair_mode,
-                                int issue_warps, uint32_t *checksum, int sm_count, cudaStream_t stream);
+                                int issue_warps, int copy_mode, uint32_t *checksum, int sm_count,
+                                cudaStream_t stream);
 cudaError_t launch_l2_read_probe(const void *buf, int64_t bytes, int reps, uint32_t *checksum, int blocks,
                                  cudaStream_t stream);
 cudaError_t read_probe_error(int *out, bool reset);

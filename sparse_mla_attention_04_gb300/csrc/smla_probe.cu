@@ -2,11 +2,14 @@
 //
 // smla_gather_probe_kernel: a pure indexed-row copy. It moves the rows named
 // by an index list from a row pool into a shared-memory ring exactly as the
-// forward kernels do (a 2-D tensor map over the pool, boxes of 128 bytes x 1
-// row with the 128-byte swizzle, tile::gather4 copies issued by the lanes of
-// up to eight producer warps, 64 rows per tile, -1 passed as row -1 so the engine fills zeros and
-// reads nothing), and does nothing with them but fold the first word of each
-// row into a checksum. Its rate is the most a kernel that gathers the same
+// forward kernels do, and does nothing with them but fold the first word of
+// each row into a checksum. Two copy methods fill the same ring layout (64
+// rows per tile, 128-byte column blocks of 128-byte-swizzled rows): TMA
+// tile::gather4 copies through a 2-D tensor map over the pool (boxes of 128
+// bytes x 1 row, issued by the lanes of up to eight producer warps; -1 passed
+// as row -1 so the engine fills zeros and reads nothing), or 16-byte cp.async
+// copies from eight warps, a warp per 8 rows, that zero-fill a masked row
+// without reading it. Its rate is the most a kernel that gathers the same
 // rows this way can reach; the consumer may hold each tile for a while, as
 // a stand-in for the arithmetic a real kernel does on it.
 //
@@ -36,6 +39,7 @@ constexpr int kThreads = kProducerThreads + 64; // + a consumer warp and a relay
 constexpr int kMaxStages = 8;
 
 struct ProbeArgs {
+    const uint8_t *pool; // read by the cp.async copies (the TMA copies go through the tensor map)
     const int32_t *indices;
     int64_t n_indices;
     int64_t num_rows;
@@ -48,6 +52,8 @@ struct ProbeArgs {
                         // 3: single CTAs launched in clusters of two
     int issue_warps;    // 0: copy c issued by producer thread c; k (1..8): the copies spread evenly
                         // over warps 0..k-1, ceil(copies / k) lanes each
+    int row_bytes;
+    int copy_mode;      // 0: TMA tile::gather4; 1: 16-byte cp.async (pair_mode 0, issue_warps 0)
 };
 
 __global__ void __launch_bounds__(kThreads) smla_gather_probe_kernel(const ProbeArgs a,
@@ -69,6 +75,7 @@ __global__ void __launch_bounds__(kThreads) smla_gather_probe_kernel(const Probe
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // pair_mode 3: independent CTAs, launched in clusters of two (a control)
     const bool mc = a.pair_mode == 1 || a.pair_mode == 2, xc = a.pair_mode == 2;
+    const bool async = a.copy_mode == 1;
     const uint32_t rank = mc ? umma::cluster_rank() : 0u;
     const int half_bytes = tile_bytes / 2;
     // tiles are split over CTAs, or over CTA pairs in the multicast mode
@@ -80,7 +87,8 @@ __global__ void __launch_bounds__(kThreads) smla_gather_probe_kernel(const Probe
 
     if (tid == 0) {
         for (int st = 0; st < a.stages; ++st) {
-            umma::mbar_init(full(st), 1);
+            // cp.async: every producer thread arrives once its own copies of the tile land
+            umma::mbar_init(full(st), async ? kProducerThreads : 1);
             umma::mbar_init(empty(st), mc ? 2 : 1); // a pair's stage is refilled once both consumers are done
             umma::mbar_init(xfull(st), 1);
         }
@@ -109,6 +117,11 @@ __global__ void __launch_bounds__(kThreads) smla_gather_probe_kernel(const Probe
         const bool copier = (a.issue_warps == 0 || (warp < a.issue_warps && lane < per_warp)) && cid < copies;
         const int qd = (mc ? 8 * (int)rank : 0) + cid / a.boxes, cb = cid % a.boxes;
         auto fetch = [&](int j, int (&r)[4]) {
+            if (async) { // lane k < 8 holds row 8 warp + k of the tile
+                const int64_t p = (j0 + j) * kRows + 8 * warp + lane;
+                r[0] = (lane < 8 && j < ntiles && p < a.n_indices) ? __ldg(a.indices + p) : -1;
+                return;
+            }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int64_t p = (j0 + j) * kRows + 4 * qd + u;
@@ -131,7 +144,7 @@ __global__ void __launch_bounds__(kThreads) smla_gather_probe_kernel(const Probe
                 if (j >= a.stages)
                     wait_bar(empty(st), (uint32_t)((j / a.stages - 1) & 1));
                 const int go = !*(volatile int *)abort_s;
-                if (go) // the whole tile, or (pair_mode 2) this CTA's half
+                if (go && !async) // the whole tile, or (pair_mode 2) this CTA's half
                     umma::mbar_arrive_expect_tx(full(st), (uint32_t)(xc ? half_bytes : tile_bytes));
                 go_s[j & 1] = go;
             }
@@ -140,7 +153,19 @@ __global__ void __launch_bounds__(kThreads) smla_gather_probe_kernel(const Probe
                 stop = true;
                 return;
             }
-            if (copier && mc && !xc)
+            if (async) {
+                // row `key`: chunk c (16 bytes) to column block c / 8, swizzled chunk (c % 8) ^ (key % 8)
+                const uint32_t dst = ring + st * tile_bytes;
+                for (int k = 0; k < 8; ++k) {
+                    const int x = row(__shfl_sync(0xffffffffu, r[0], k));
+                    const int key = 8 * warp + k;
+                    const uint8_t *src = a.pool + (int64_t)(x < 0 ? 0 : x) * a.row_bytes;
+                    for (int c = lane; c < a.row_bytes / 16; c += 32)
+                        cp_async_16(dst + (c >> 3) * (kRows * 128) + key * 128 + (((c & 7) ^ (key & 7)) << 4),
+                                    src + c * 16, x < 0 ? 0u : 16u);
+                }
+                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(full(st)) : "memory");
+            } else if (copier && mc && !xc)
                 umma::tma_gather4_multicast(ring + st * tile_bytes + cb * (kRows * 128) + qd * 512, &map, 128 * cb,
                                             row(r[0]), row(r[1]), row(r[2]), row(r[3]), full(st), (uint16_t)3);
             else if (copier)
@@ -154,6 +179,8 @@ __global__ void __launch_bounds__(kThreads) smla_gather_probe_kernel(const Probe
             step(j + 1, r1);
         }
         // every copy issued has landed before the CTA finishes (also after an abort)
+        if (async)
+            asm volatile("cp.async.wait_all;\n" ::: "memory");
         if (tid == 0) {
             for (int j = max(0, issued - a.stages); j < issued; ++j)
                 if (!umma::mbar_wait(full(j % a.stages), (uint32_t)((j / a.stages) & 1)))
@@ -255,9 +282,11 @@ int gather_probe_smem(int boxes, int stages)
 
 cudaError_t launch_gather_probe(const void *pool, int64_t num_rows, int row_bytes, const int32_t *indices,
                                 int64_t n_indices, int ctas_per_sm, int stages, int hold_ns, int pair_mode,
-                                int issue_warps, uint32_t *checksum, int sm_count, cudaStream_t stream)
+                                int issue_warps, int copy_mode, uint32_t *checksum, int sm_count,
+                                cudaStream_t stream)
 {
-    if (pair_mode && ctas_per_sm != 1)
+    if ((pair_mode && ctas_per_sm != 1) || copy_mode < 0 || copy_mode > 1 ||
+        (copy_mode == 1 && (pair_mode != 0 || issue_warps != 0)))
         return cudaErrorInvalidValue;
     const int boxes = (row_bytes + 127) / 128;
     if (issue_warps > 0 && ((pair_mode == 1 || pair_mode == 2 ? 8 : 16) * boxes + issue_warps - 1) / issue_warps > 32)
@@ -296,6 +325,7 @@ cudaError_t launch_gather_probe(const void *pool, int64_t num_rows, int row_byte
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     ProbeArgs a;
+    a.pool = static_cast<const uint8_t *>(pool);
     a.indices = indices;
     a.n_indices = n_indices;
     a.num_rows = num_rows;
@@ -305,6 +335,8 @@ cudaError_t launch_gather_probe(const void *pool, int64_t num_rows, int row_byte
     a.hold_ns = hold_ns;
     a.pair_mode = pair_mode;
     a.issue_warps = issue_warps;
+    a.row_bytes = row_bytes;
+    a.copy_mode = copy_mode;
     const int grid = pair_mode ? (sm_count / 2) * 2 : sm_count * ctas_per_sm;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);

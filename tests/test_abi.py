@@ -179,17 +179,21 @@ def test_probe_host_checks(L):
     from sparse_mla_attention_04_gb300 import binding as b
     P = 1 << 12   # fake, never dereferenced: every call below fails its host checks
     lib = b.lib()
-    assert lib.smla_gather_probe(None, 10, 1024, P, 64, 1, 1, 0, 0, 0, P, None) == b.SMLA_ERR_NULL_POINTER
-    assert lib.smla_gather_probe(P, 10, 1000, P, 64, 1, 1, 0, 0, 0, P, None) == b.SMLA_ERR_BAD_SHAPE   # not 16-byte rows
-    assert lib.smla_gather_probe(P, 10, 2048, P, 64, 1, 1, 0, 0, 0, P, None) == b.SMLA_ERR_BAD_SHAPE   # > 1 KB rows
-    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 5, 1, 0, 0, 0, P, None) == b.SMLA_ERR_BAD_SHAPE   # > 4 CTAs/SM
-    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 1, 9, 0, 0, 0, P, None) == b.SMLA_ERR_BAD_SHAPE   # > 8 stages
-    assert lib.smla_gather_probe(P + 8, 10, 1024, P, 64, 1, 1, 0, 0, 0, P, None) == b.SMLA_ERR_MISALIGNED
-    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 2, 1, 0, 1, 0, P, None) == b.SMLA_ERR_UNSUPPORTED  # pairs: 1 CTA/SM
-    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 1, 1, 0, 4, 0, P, None) == b.SMLA_ERR_BAD_SHAPE
-    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 1, 1, 0, 0, 9, P, None) == b.SMLA_ERR_BAD_SHAPE  # > 8 warps
+    assert lib.smla_gather_probe(None, 10, 1024, P, 64, 1, 1, 0, 0, 0, 0, P, None) == b.SMLA_ERR_NULL_POINTER
+    assert lib.smla_gather_probe(P, 10, 1000, P, 64, 1, 1, 0, 0, 0, 0, P, None) == b.SMLA_ERR_BAD_SHAPE   # not 16-byte rows
+    assert lib.smla_gather_probe(P, 10, 2048, P, 64, 1, 1, 0, 0, 0, 0, P, None) == b.SMLA_ERR_BAD_SHAPE   # > 1 KB rows
+    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 5, 1, 0, 0, 0, 0, P, None) == b.SMLA_ERR_BAD_SHAPE   # > 4 CTAs/SM
+    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 1, 9, 0, 0, 0, 0, P, None) == b.SMLA_ERR_BAD_SHAPE   # > 8 stages
+    assert lib.smla_gather_probe(P + 8, 10, 1024, P, 64, 1, 1, 0, 0, 0, 0, P, None) == b.SMLA_ERR_MISALIGNED
+    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 2, 1, 0, 1, 0, 0, P, None) == b.SMLA_ERR_UNSUPPORTED  # pairs: 1 CTA/SM
+    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 1, 1, 0, 4, 0, 0, P, None) == b.SMLA_ERR_BAD_SHAPE
+    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 1, 1, 0, 0, 9, 0, P, None) == b.SMLA_ERR_BAD_SHAPE  # > 8 warps
     # 1 KB rows: 128 copies a tile, more than 32 lanes of each of 3 warps
-    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 1, 1, 0, 0, 3, P, None) == b.SMLA_ERR_BAD_SHAPE
+    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 1, 1, 0, 0, 3, 0, P, None) == b.SMLA_ERR_BAD_SHAPE
+    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 1, 1, 0, 0, 0, 2, P, None) == b.SMLA_ERR_BAD_SHAPE  # copy mode
+    # cp.async copies: single CTAs, every producer warp
+    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 1, 1, 0, 1, 0, 1, P, None) == b.SMLA_ERR_UNSUPPORTED
+    assert lib.smla_gather_probe(P, 10, 1024, P, 64, 1, 1, 0, 0, 4, 1, P, None) == b.SMLA_ERR_UNSUPPORTED
     assert lib.smla_l2_read_probe(P, 1000, 1, P, 4, None) == b.SMLA_ERR_BAD_SHAPE
     assert lib.smla_l2_read_probe(None, 1024, 1, P, 4, None) == b.SMLA_ERR_NULL_POINTER
 

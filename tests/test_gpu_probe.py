@@ -2,8 +2,8 @@
 
 The gather probe copies the rows an index list names; the XOR of its per-CTA
 checksums must equal the XOR of the first 4 bytes of every named row (a -1 or
-out-of-range entry contributes zero: the engine fills the row with zeros),
-whatever the row width, CTAs per SM and ring depth. The L2 read probe must be
+out-of-range entry contributes zero: the copy fills the row with zeros),
+whatever the row width, CTAs per SM, ring depth and copy method. The L2 read probe must be
 deterministic."""
 import numpy as np
 import pytest
@@ -34,6 +34,26 @@ def test_gather_probe_checksum(row_bytes, ctas_stages):
     idx[5] = rows                # out of range: masked
     idx[9] = -7
     ck = binding.smla_gather_probe(pool, torch.from_numpy(idx).to(DEV), ctas_per_sm=k, stages=st)
+    torch.cuda.synchronize()
+    got = int(np.bitwise_xor.reduce(ck.cpu().numpy().view(np.uint32)))
+    assert got == _expected(pool.cpu().numpy(), idx)
+    assert binding.smla_device_error() == 0
+
+
+@pytest.mark.parametrize("row_bytes", [1024, 576, 512, 128, 16])
+@pytest.mark.parametrize("ctas_stages", [(1, 3), (2, 1), (4, 1)])
+def test_gather_probe_cp_async(row_bytes, ctas_stages):
+    """16-byte cp.async copies fill the same swizzled ring as the TMA copies:
+    row r's first chunk lands where the consumer reads it."""
+    k, st = ctas_stages
+    rng = np.random.default_rng(row_bytes + 5 * k + 1)
+    rows = 3000
+    pool = torch.from_numpy(rng.integers(0, 256, (rows, row_bytes), dtype=np.uint8)).to(DEV)
+    idx = rng.integers(0, rows, 64 * 280 + 45).astype(np.int32)
+    idx[::13] = -1
+    idx[3] = rows
+    idx[4] = -9
+    ck = binding.smla_gather_probe(pool, torch.from_numpy(idx).to(DEV), ctas_per_sm=k, stages=st, copy_mode=1)
     torch.cuda.synchronize()
     got = int(np.bitwise_xor.reduce(ck.cpu().numpy().view(np.uint32)))
     assert got == _expected(pool.cpu().numpy(), idx)
