@@ -50,6 +50,18 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr)
     return v;
 }
 
+// Four 8 x 8 matrices of 16-bit elements, transposed on the way: lane l gives
+// the address of row l % 8 of matrix l / 8 (16 contiguous bytes); lane l gets
+// in d[m] element l / 4 of rows 2 (l % 4) (low half) and 2 (l % 4) + 1 (high
+// half) of matrix m.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&d)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
 // D += A(16x16, row) * B(16x8, col), bf16 inputs, fp32 accumulators.
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
 {

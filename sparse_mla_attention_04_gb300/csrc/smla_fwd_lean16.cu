@@ -29,7 +29,9 @@
 //     quantized per (row, head) straight from global memory (s_q =
 //     amax/448, q8 = RNE_satfinite(q / s_q)), or the pre-quantized codes;
 //     then per tile each half of the values, E4M3 -> binary16 (exact), as
-//     V^T into tensor memory (4x4 byte transposes within lane quads).
+//     V^T into tensor memory (transposing ldmatrix of 8 keys x 16 bytes, a
+//     byte permute, 16x256b stores; the lane and K orders this gives are
+//     kVLaneDim and kPRow below).
 // Splits of a row merge as in the 16-head kernel (a cluster of up to 8 CTAs
 // through distributed shared memory, or the workspace ticket merge).
 //
@@ -104,6 +106,21 @@ static_assert(2 * kQGrp >= 128 * kHeads * 4, "merge weights fit in the q area");
 constexpr int kTmemCols = 256;
 constexpr int kSCol = 64;
 constexpr int kVCol = 128;
+
+// V^T layout in tensor memory (as the converters write it): lane 32w + l of a
+// 128-dim block holds dim 32w + kVLaneDim(l); within a 16-key group the K
+// order of the PV contraction is keys 0,1,8,9, 2,3,10,11, 4,5,12,13, 6,7,14,15,
+// so key k's P^T row is kPRow(k)
+__device__ __forceinline__ int kVLaneDim(int l)
+{
+    const int r = l & 15;
+    return (l & 16) + (r < 8 ? 2 * r : 2 * r - 15);
+}
+__device__ __forceinline__ int kPRow(int key)
+{
+    const int s = key & 15;
+    return (key & ~15) + 4 * ((s >> 1) & 3) + 2 * (s >> 3) + (s & 1);
+}
 
 constexpr uint32_t kIdescQK = umma::idesc(64, 16, 0, 0, 0, 0);        // E4M3 x E4M3, K-major
 constexpr uint32_t kIdescPV = umma::idesc(128, 16, 0, 0, 0, 1);       // fp16: A in TMEM, B = P^T MN-major
@@ -369,13 +386,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             umma::fence_async_smem();
             umma::mbar_arrive(q_full);
         }
-        // values: lane quad (g, ii), member ii loads 4 dims (4g..4g+3 of this
-        // warp's 32) of key 4kq+ii; after the transpose it holds dim 4g+ii of
-        // keys 4kq..4kq+3
-        const int q4 = warp & 3, g = lane >> 2, ii = lane & 3;
-        const uint32_t selA = ii < 2 ? 0x5410u : 0x3276u; // keep / take 16-bit halves (xor 2)
-        const uint32_t selB = ii & 1 ? 0x3715u : 0x6240u; // interleave bytes (xor 1)
-        const uint32_t tlane = (uint32_t)(32 * q4) << 16;
+        // values: this warp's 32 dims of each 128-dim block are two 16-dim
+        // chunks (16 bytes of every key row). A transposing ldmatrix of 8 keys x
+        // 16 bytes hands lane (c, j) = (lane / 4, lane % 4) dims 2c, 2c+1 of keys
+        // 2j, 2j+1; one byte permute pairs the two keys of each dim, and the
+        // 16x256b store puts dim 2c at TMEM lane c and dim 2c+1 at lane c + 8 of
+        // the chunk's 16 lanes (kVLaneDim; the softmax reads O^T back that way),
+        // keys 16G + 2j, +1 at column 8G + 2j and keys 16G + 8 + 2j, +1 at column
+        // 8G + 2j + 1 (kPRow orders P^T's rows the same way)
+        const int q4 = warp & 3;
         for (int i = 0; i < ntiles; ++i) {
             const int st = i % kStages;
             wait_bar(full(st), (uint32_t)((i / kStages) & 1));
@@ -387,17 +406,26 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll 1
                 for (int m = 0; m < 2; ++m) {
                     const int mb = 2 * h + m;
-                    uint32_t col[32];
 #pragma unroll
-                    for (int kq = 0; kq < 16; ++kq) {
-                        const int key = 4 * kq + ii;
-                        const uint32_t w = lds32(src0 + mb * kBlk + key * 128 +
-                                                 (((2 * q4 + (g >> 2)) ^ (key & 7)) << 4) + (g & 3) * 4);
-                        const uint32_t x = __byte_perm(w, __shfl_xor_sync(0xffffffffu, w, 2), selA);
-                        const uint32_t y = __byte_perm(x, __shfl_xor_sync(0xffffffffu, x, 1), selB);
-                        e4m3x4_to_f16x4(y, col[2 * kq], col[2 * kq + 1]);
+                    for (int u = 0; u < 2; ++u) {
+                        const int cl = 2 * q4 + u; // the chunk's 16-byte slot in its line, before the swizzle
+                        uint32_t col[16];
+#pragma unroll
+                        for (int g2 = 0; g2 < 2; ++g2) {
+                            // matrix mm = lane / 8: keys 32 g2 + 8 mm .. +7, i.e. key group
+                            // G = 2 g2 + mm / 2, its first (mm even) or second 8 keys
+                            const int key = 32 * g2 + 8 * (lane >> 3) + (lane & 7);
+                            uint32_t d[4];
+                            ldsm_x4_trans(src0 + mb * kBlk + key * 128 + ((cl ^ (lane & 7)) << 4), d);
+#pragma unroll
+                            for (int mm = 0; mm < 4; ++mm) {
+                                const int G = 2 * g2 + (mm >> 1), ab = mm & 1;
+                                // bytes (key 2j: dim 2c, 2c+1), (key 2j+1: dim 2c, 2c+1) -> per dim
+                                e4m3x4_to_f16x4(__byte_perm(d[mm], 0u, 0x3120u), col[4 * G + ab], col[4 * G + 2 + ab]);
+                            }
+                        }
+                        umma::st16x256b_x4(tmem + ((uint32_t)(32 * q4 + 16 * u) << 16) + kVCol + 64 * h + 32 * m, col);
                     }
-                    umma::st32(tmem + tlane + kVCol + 64 * h + 32 * m, col);
                 }
                 umma::wait_st();
                 umma::fence_before_sync();
@@ -498,7 +526,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (i >= 2)
                 wait_bar(p_empty(b), (uint32_t)(((i - 2) >> 1) & 1)); // PV(i-2) is done with this P buffer
             if (lane < 16) {
-                const uint32_t prow = p_s + b * 2048 + (key >> 3) * 256 + (key & 7) * 16;
+                const int pk = kPRow(key);
+                const uint32_t prow = p_s + b * 2048 + (pk >> 3) * 256 + (pk & 7) * 16;
                 asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow), "r"(pack_f16x2(sv[0], sv[1])),
                              "r"(pack_f16x2(sv[2], sv[3])), "r"(pack_f16x2(sv[4], sv[5])), "r"(pack_f16x2(sv[6], sv[7])));
                 asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow + 128), "r"(pack_f16x2(sv[8], sv[9])),
@@ -551,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             umma::wait_ld();
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-                const int d = (2 * half + u) * 128 + warp * 32 + lane;
+                const int d = (2 * half + u) * 128 + warp * 32 + kVLaneDim(lane);
 #pragma unroll
                 for (int h = 0; h < 16; ++h) {
                     const float iv = alpha_s[h];

@@ -160,6 +160,18 @@ __device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&r)[32])
                  : "memory");
 }
 
+// 16 lanes x 4 repetitions of 8 consecutive 32-bit columns (warp-wide; the
+// lane base is 32 * (warp % 4) or 16 more). Thread T's registers 4i..4i+3 go
+// to repetition i as (lane T/4, column 2(T%4)), (lane T/4, column 2(T%4)+1),
+// (lane T/4+8, column 2(T%4)), (lane T/4+8, column 2(T%4)+1).
+__device__ __forceinline__ void st16x256b_x4(uint32_t taddr, const uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+                 "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+                 : "memory");
+}
+
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
