@@ -379,6 +379,50 @@ def time_isolated(call, stream, flush, n=9):
     return statistics.median(times)
 
 
+
+def concurrent_steps(binding, w, cache, kvs, sets, dev, stream, args, sinks=None, lanes=2, reps=20):
+    """Device milliseconds per step with `lanes` independent steps in flight
+    (as a server runs independent batches): step i runs on lane i % lanes,
+    each lane its own stream with its own output and workspace buffers; the
+    lanes fork from and join back into the timing stream inside one CUDA
+    graph. Returns (ms per step, steps timed)."""
+    R = len(sets)
+    ls = [torch.cuda.Stream(device=dev) for _ in range(lanes)]
+    calls = [forward_setup(binding, w, cache, kvs, sets, dev, s_, args, sinks)[0] for s_ in ls]
+    G = R * lanes * max(1, 40 // (R * lanes))
+
+    def seq():
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        for s_ in ls:
+            s_.wait_event(fork)
+        for i in range(G):
+            calls[i % lanes](i)
+        for s_ in ls:
+            join = torch.cuda.Event()
+            join.record(s_)
+            stream.wait_event(join)
+
+    with torch.cuda.stream(stream):
+        seq()
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        seq()
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        b.record(stream)
+    b.synchronize()
+    del graph
+    return a.elapsed_time(b) / (reps * G), reps * G
+
+
 def ceiling_configs(row_bytes: int):
     """(CTAs per SM, stages, pair mode, issue warps, copy mode) of the
     gather-ceiling sweep: for each CTA count the most 64-row tiles that fit (as
@@ -468,6 +512,7 @@ def measure_config(binding, name, args, dev, stream, flush, l2_gbs):
     flop = 2.0 * w.H * (w.D_qk + w.D_v) * nvalid / K
     ceil = gather_ceiling(binding, cache, sets, stream)
     gbs = nbytes / K / sec / 1e9
+    ms2, _ = concurrent_steps(binding, w, cache, kvs, sets, dev, stream, args, reps=10)
     entry = {
         "config": {"workload": w.name, "T": w.T, "H": w.H, "D_qk": w.D_qk, "D_v": w.D_v, "topk": w.topk,
                    "num_slots": w.num_slots, "kv_dtype": "e4m3" if w.kv_fp8 else "bf16", "dot_precision": dot,
@@ -481,6 +526,8 @@ def measure_config(binding, name, args, dev, stream, flush, l2_gbs):
         "gather_ceiling": ceil,
         "frac_of_gather_ceiling": round(gbs / ceil["best_gbs"], 4),
         "gpu_launches_per_call": 2 if (w.kind == "wide" and not args.bf16_dots) else 1,
+        "two_streams": {"ms_per_call": round(ms2, 6), "gathered_gbs": round(nbytes / K / (ms2 * 1e-3) / 1e9, 2),
+                        "note": "two independent calls in flight (two streams), per-call device time of the job"},
     }
     if w.kind == "prefill":
         entry["l2_bound"] = {"l2_read_gbs": round(l2_gbs, 1), "bound_ms": round(nbytes / K / (l2_gbs * 1e9) * 1e3, 4),
@@ -541,6 +588,13 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(w, cache, kvs, sets, dot, 0, dev, stream, K, world, q8=args.q8)
+    ms2, k2 = concurrent_steps(binding, w, cache, kvs, sets, dev, stream, args, sinks)
+    ms2 = max_over_ranks(ms2, world, dev)
+    gbs2 = job_rate(per_launch_bytes, world, ms2) / 1e9
+    two = {"ms_per_step": round(ms2, 6), "value": round(gbs2, 2), "unit": "GB/s", "steps": k2,
+           "frac_of_hbm_peak": round(gbs2 / measured_peaks()[0], 4), "peak_source": measured_peaks()[1],
+           "note": "the same steps with two independent steps in flight (two streams, as a server runs "
+                   "independent batches); value above is one step at a time"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -591,6 +645,7 @@ def run_ours(args):
             "ms_isolated_launch": round(iso, 6),
             "clocks": clk,
             "e2e": e2e,
+            "two_streams": two,
             "cpu_baseline": cpu,
         }
         if ceil is not None:
@@ -614,19 +669,19 @@ def quantize_q_per_tensor(binding, q):
     return q8.view(T, H, D), qs
 
 
-def run_e2e(w, cache, kvs, sets, dot, splits, dev, stream, K, world, q8=False):
+def run_e2e(w, cache, kvs, sets, dot, splits, dev, stream, K, world, q8=False, slots=4):
     """Same metric through the public API with host buffers: every step copies
     that step's q and indices from pinned host memory and reads out and lse
     back into pinned host memory, inside the timed region.
 
-    The steps are pipelined as a serving loop would run them: two sets of
-    device buffers, host->device copies on one stream, device->host reads on
-    another, the calls on the compute stream, ordered by events. Step i's
-    inputs arrive while step i-1 computes and step i-1's results leave while
-    step i computes."""
+    The steps are pipelined as a serving loop would run them: `slots` sets of
+    device buffers, each with its own stream on which a step's host->device
+    copies, its call and its device->host reads run in order; step i uses slot
+    i % slots, so the slots' steps (their copies and calls) overlap one another
+    and stream order alone keeps a slot's buffers from being reused early."""
     from sparse_mla_attention_04_gb300 import binding
     R = len(sets)
-    NB = 2
+    NB = slots
     qkey = "q8" if q8 else "q"
     hq = [s[qkey].cpu().pin_memory() for s in sets]
     hi = [s["idx"].cpu().pin_memory() for s in sets]
@@ -637,52 +692,37 @@ def run_e2e(w, cache, kvs, sets, dot, splits, dev, stream, K, world, q8=False):
     out = [torch.empty((w.T, w.H, w.D_v), dtype=torch.bfloat16, device=dev) for _ in range(NB)]
     lse = [torch.empty((w.T, w.H), dtype=torch.float32, device=dev) for _ in range(NB)]
     need = binding.sparse_mla_fwd_workspace_size(w.T, w.H, w.D_qk, w.D_v, w.topk, int(w.kv_fp8), splits)
-    ws = torch.zeros(max(need, 1), dtype=torch.uint8, device=dev)
-    s_in = torch.cuda.Stream(device=dev)
-    s_out = torch.cuda.Stream(device=dev)
-    ev_in = [torch.cuda.Event() for _ in range(NB)]   # inputs of the slot's step have landed
-    ev_k = [torch.cuda.Event() for _ in range(NB)]    # the slot's call is done (its inputs are free)
-    ev_out = [torch.cuda.Event() for _ in range(NB)]  # the slot's results have been read back
+    ws = [torch.zeros(max(need, 1), dtype=torch.uint8, device=dev) for _ in range(NB)]
+    ss = [torch.cuda.Stream(device=dev) for _ in range(NB)]
 
-    def step(i, first):
-        # `first`: the slot's previous step is outside this sequence (nothing to wait for)
+    def step(i):
         k = i % NB
-        if not first:
-            s_in.wait_event(ev_k[k])
-        with torch.cuda.stream(s_in):
+        with torch.cuda.stream(ss[k]):
             dq[k].copy_(hq[i % R], non_blocking=True)
             di[k].copy_(hi[i % R], non_blocking=True)
-        ev_in[k].record(s_in)
-        stream.wait_event(ev_in[k])
-        if not first:
-            stream.wait_event(ev_out[k])
-        if q8:
-            binding.sparse_mla_fwd_q8(dq[k], sets[i % R]["qs"], cache, di[k], w.scale, kv_scale=kvs, D_v=w.D_v,
-                                      out=out[k], lse=lse[k], workspace=ws, num_splits=splits, stream=stream)
-        else:
-            binding.sparse_mla_fwd(dq[k], cache, di[k], w.scale, kv_scale=kvs, dot_precision=dot, D_v=w.D_v,
-                                   out=out[k], lse=lse[k], workspace=ws, num_splits=splits, stream=stream)
-        ev_k[k].record(stream)
-        s_out.wait_event(ev_k[k])
-        with torch.cuda.stream(s_out):
+            if q8:
+                binding.sparse_mla_fwd_q8(dq[k], sets[i % R]["qs"], cache, di[k], w.scale, kv_scale=kvs, D_v=w.D_v,
+                                          out=out[k], lse=lse[k], workspace=ws[k], num_splits=splits, stream=ss[k])
+            else:
+                binding.sparse_mla_fwd(dq[k], cache, di[k], w.scale, kv_scale=kvs, dot_precision=dot, D_v=w.D_v,
+                                       out=out[k], lse=lse[k], workspace=ws[k], num_splits=splits, stream=ss[k])
             ho[k].copy_(out[k], non_blocking=True)
             hl[k].copy_(lse[k], non_blocking=True)
-        ev_out[k].record(s_out)
 
     def sequence(n):
-        # fork the copy streams off the compute stream, run n pipelined steps, join them back
+        # fork the slot streams off the timing stream, run n steps, join them back
         fork = torch.cuda.Event()
         fork.record(stream)
-        s_in.wait_event(fork)
-        s_out.wait_event(fork)
+        for s_ in ss:
+            s_.wait_event(fork)
         for i in range(n):
-            step(i, i < NB)
-        for sj in (s_in, s_out):
+            step(i)
+        for s_ in ss:
             join = torch.cuda.Event()
-            join.record(sj)
+            join.record(s_)
             stream.wait_event(join)
 
-    # the host issues ~10 CUDA operations per step, more than a call's device
+    # the host issues ~6 CUDA operations per step, more than a call's device
     # time: the pipelined sequence is captured once as a CUDA graph and replayed
     G = R * NB * max(1, 40 // (R * NB))
     sequence(G)
@@ -703,14 +743,33 @@ def run_e2e(w, cache, kvs, sets, dot, splits, dev, stream, K, world, q8=False):
         b.record(stream)
     b.synchronize()
     ms = max_over_ranks(a.elapsed_time(b), world, dev)
+    # the results each slot read back last (step G - NB + k of the sequence)
+    # against the same call on device-resident inputs, bit for bit
+    verified = True
+    for k in range(NB):
+        i = G - NB + k
+        ref_o = torch.empty_like(out[k])
+        ref_l = torch.empty_like(lse[k])
+        if q8:
+            binding.sparse_mla_fwd_q8(sets[i % R][qkey], sets[i % R]["qs"], cache, sets[i % R]["idx"], w.scale,
+                                      kv_scale=kvs, D_v=w.D_v, out=ref_o, lse=ref_l, workspace=ws[k],
+                                      num_splits=splits, stream=stream)
+        else:
+            binding.sparse_mla_fwd(sets[i % R][qkey], cache, sets[i % R]["idx"], w.scale, kv_scale=kvs,
+                                   dot_precision=dot, D_v=w.D_v, out=ref_o, lse=ref_l, workspace=ws[k],
+                                   num_splits=splits, stream=stream)
+        stream.synchronize()
+        verified &= bool(torch.equal(ho[k], ref_o.cpu()) and torch.equal(hl[k], ref_l.cpu()))
     reps, rem = divmod(steps, R)
     nbytes = reps * sum(s["bytes"] for s in sets) + sum(s["bytes"] for s in sets[:rem])
     h2d = sets[0][qkey].numel() * sets[0][qkey].element_size() + sets[0]["idx"].numel() * 4
     d2h = out[0].numel() * 2 + lse[0].numel() * 4
     return {"value": round(job_rate(nbytes, world, ms) / 1e9, 2), "unit": "GB/s", "steps": steps,
             "ms_per_step": round(ms / steps, 6), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "pipelining": "2 buffer sets; copies in and out on their own streams overlap the neighbouring "
-                          "steps' calls; sequences of %d steps replayed from a CUDA graph" % G}
+            "results_match_device_call": verified,
+            "pipelining": "%d buffer slots, each with its own stream running a step's copies in, call and "
+                          "copies out in order; the slots' steps overlap one another; sequences of %d steps "
+                          "replayed from a CUDA graph" % (NB, G)}
 
 
 # ----------------------------------------------------------------------------
