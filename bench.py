@@ -292,9 +292,10 @@ def build_workload(name: str, seed: int, rotations: int, device, rank: int, ctx:
 # our arm
 # ----------------------------------------------------------------------------
 
-def forward_setup(binding, w, cache, kvs, sets, dev, stream, args, sinks=None):
+def forward_setup(binding, w, cache, kvs, sets, dev, stream, args, sinks=None, num_splits=0):
     """Buffers, split plan and the call of one workload (call(i) runs the
-    forward on input set i % R on `stream`)."""
+    forward on input set i % R on `stream`; num_splits 0 = the library's
+    automatic plan)."""
     R = len(sets)
     dot = "fp8" if w.kv_fp8 else "auto"
     if args.bf16_dots:
@@ -313,7 +314,7 @@ def forward_setup(binding, w, cache, kvs, sets, dev, stream, args, sinks=None):
     # the library's automatic plan (0); the split count it takes is reported
     planned = binding.smla_plan_num_splits(T, H, w.D_qk, w.topk, int(w.kv_fp8),
                                            torch.cuda.get_device_properties(dev).multi_processor_count)
-    splits = 0
+    splits = num_splits
     need = binding.sparse_mla_fwd_workspace_size(T, H, w.D_qk, w.D_v, w.topk, int(w.kv_fp8), splits)
     ws = torch.zeros(max(need, 1), dtype=torch.uint8, device=dev)
 
@@ -380,15 +381,27 @@ def time_isolated(call, stream, flush, n=9):
 
 
 
-def concurrent_steps(binding, w, cache, kvs, sets, dev, stream, args, sinks=None, lanes=2, reps=20):
+def shared_gpu_splits(binding, w, dev):
+    """The split count for calls that share the GPU with another call in
+    flight: the library's plan for half the SMs (the automatic plan for the
+    128-head path, whose explicit splits change its kernel)."""
+    if w.kind == "wide":
+        return 0
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    return binding.smla_plan_num_splits(w.T, w.H, w.D_qk, w.topk, int(w.kv_fp8), max(1, sms // 2))
+
+
+def concurrent_steps(binding, w, cache, kvs, sets, dev, stream, args, sinks=None, lanes=3, reps=20):
     """Device milliseconds per step with `lanes` independent steps in flight
     (as a server runs independent batches): step i runs on lane i % lanes,
-    each lane its own stream with its own output and workspace buffers; the
-    lanes fork from and join back into the timing stream inside one CUDA
-    graph. Returns (ms per step, steps timed)."""
+    each lane its own stream with its own output and workspace buffers, each
+    call planned for a shared GPU (shared_gpu_splits); the lanes fork from
+    and join back into the timing stream inside one CUDA graph. Returns (ms
+    per step, steps timed, splits)."""
     R = len(sets)
+    S = shared_gpu_splits(binding, w, dev)
     ls = [torch.cuda.Stream(device=dev) for _ in range(lanes)]
-    calls = [forward_setup(binding, w, cache, kvs, sets, dev, s_, args, sinks)[0] for s_ in ls]
+    calls = [forward_setup(binding, w, cache, kvs, sets, dev, s_, args, sinks, num_splits=S)[0] for s_ in ls]
     G = R * lanes * max(1, 40 // (R * lanes))
 
     def seq():
@@ -420,7 +433,7 @@ def concurrent_steps(binding, w, cache, kvs, sets, dev, stream, args, sinks=None
         b.record(stream)
     b.synchronize()
     del graph
-    return a.elapsed_time(b) / (reps * G), reps * G
+    return a.elapsed_time(b) / (reps * G), reps * G, S
 
 
 def ceiling_configs(row_bytes: int):
@@ -512,7 +525,7 @@ def measure_config(binding, name, args, dev, stream, flush, l2_gbs):
     flop = 2.0 * w.H * (w.D_qk + w.D_v) * nvalid / K
     ceil = gather_ceiling(binding, cache, sets, stream)
     gbs = nbytes / K / sec / 1e9
-    ms2, _ = concurrent_steps(binding, w, cache, kvs, sets, dev, stream, args, reps=10)
+    ms2, _, s2 = concurrent_steps(binding, w, cache, kvs, sets, dev, stream, args, reps=10)
     entry = {
         "config": {"workload": w.name, "T": w.T, "H": w.H, "D_qk": w.D_qk, "D_v": w.D_v, "topk": w.topk,
                    "num_slots": w.num_slots, "kv_dtype": "e4m3" if w.kv_fp8 else "bf16", "dot_precision": dot,
@@ -526,8 +539,9 @@ def measure_config(binding, name, args, dev, stream, flush, l2_gbs):
         "gather_ceiling": ceil,
         "frac_of_gather_ceiling": round(gbs / ceil["best_gbs"], 4),
         "gpu_launches_per_call": 2 if (w.kind == "wide" and not args.bf16_dots) else 1,
-        "two_streams": {"ms_per_call": round(ms2, 6), "gathered_gbs": round(nbytes / K / (ms2 * 1e-3) / 1e9, 2),
-                        "note": "two independent calls in flight (two streams), per-call device time of the job"},
+        "concurrent": {"streams": 3, "splits": s2, "ms_per_call": round(ms2, 6),
+                       "gathered_gbs": round(nbytes / K / (ms2 * 1e-3) / 1e9, 2),
+                       "note": "three independent calls in flight (three streams), per-call device time of the job"},
     }
     if w.kind == "prefill":
         entry["l2_bound"] = {"l2_read_gbs": round(l2_gbs, 1), "bound_ms": round(nbytes / K / (l2_gbs * 1e9) * 1e3, 4),
@@ -587,14 +601,15 @@ def run_ours(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(w, cache, kvs, sets, dot, 0, dev, stream, K, world, q8=args.q8)
-    ms2, k2 = concurrent_steps(binding, w, cache, kvs, sets, dev, stream, args, sinks)
+        e2e = run_e2e(w, cache, kvs, sets, dot, shared_gpu_splits(binding, w, dev), dev, stream, K, world, q8=args.q8)
+    ms2, k2, s2 = concurrent_steps(binding, w, cache, kvs, sets, dev, stream, args, sinks)
     ms2 = max_over_ranks(ms2, world, dev)
     gbs2 = job_rate(per_launch_bytes, world, ms2) / 1e9
-    two = {"ms_per_step": round(ms2, 6), "value": round(gbs2, 2), "unit": "GB/s", "steps": k2,
+    two = {"streams": 3, "splits": s2, "ms_per_step": round(ms2, 6), "value": round(gbs2, 2), "unit": "GB/s",
+           "steps": k2,
            "frac_of_hbm_peak": round(gbs2 / measured_peaks()[0], 4), "peak_source": measured_peaks()[1],
-           "note": "the same steps with two independent steps in flight (two streams, as a server runs "
-                   "independent batches); value above is one step at a time"}
+           "note": "the same steps with three independent steps in flight (three streams, as a server runs "
+                   "independent batches; each call planned for half the SMs); value above is one step at a time"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -645,7 +660,7 @@ def run_ours(args):
             "ms_isolated_launch": round(iso, 6),
             "clocks": clk,
             "e2e": e2e,
-            "two_streams": two,
+            "concurrent": two,
             "cpu_baseline": cpu,
         }
         if ceil is not None:
@@ -766,10 +781,11 @@ def run_e2e(w, cache, kvs, sets, dot, splits, dev, stream, K, world, q8=False, s
     d2h = out[0].numel() * 2 + lse[0].numel() * 4
     return {"value": round(job_rate(nbytes, world, ms) / 1e9, 2), "unit": "GB/s", "steps": steps,
             "ms_per_step": round(ms / steps, 6), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "results_match_device_call": verified,
+            "results_match_device_call": verified, "splits": splits,
             "pipelining": "%d buffer slots, each with its own stream running a step's copies in, call and "
-                          "copies out in order; the slots' steps overlap one another; sequences of %d steps "
-                          "replayed from a CUDA graph" % (NB, G)}
+                          "copies out in order; the slots' steps overlap one another, each call planned for "
+                          "half the SMs (splits 0 = the automatic plan); sequences of %d steps replayed from a "
+                          "CUDA graph" % (NB, G)}
 
 
 # ----------------------------------------------------------------------------
