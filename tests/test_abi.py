@@ -51,6 +51,9 @@ def test_split_plan(L):
     assert b.smla_plan_num_splits(128, 128, 576, 2048, 1, 152) == 1
     assert b.smla_plan_num_splits(1, 16, 512, 100000, 0, 152) == 8    # automatic plans stay in one cluster
     assert b.smla_plan_num_splits(4, 15, 512, 128, 0, 152) == 0       # invalid H
+    # a call that shares the GPU with another, planned for half the SMs
+    assert b.smla_plan_num_splits(64, 16, 512, 2048, 0, 76) == 1
+    assert b.smla_plan_num_splits(64, 16, 512, 2048, 1, 76) == 2
 
 
 def test_workspace_size(L):

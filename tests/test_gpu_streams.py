@@ -31,6 +31,8 @@ def _inputs(T, H, D_qk, topk, slots, seed):
     (16, 512, False, 0, 2),     # cluster merge of the automatic plan
     (16, 512, False, 12, 3),    # workspace merge (tickets in the workspace)
     (16, 512, True, 0, 2),      # lean E4M3 kernel, fp8 dots
+    (16, 512, False, 1, 3),     # one split per row (the plan for a shared GPU), no merge
+    (16, 512, True, 2, 3),      # lean E4M3 kernel, two splits (the plan for a shared GPU)
     (128, 576, True, 0, 2),     # q pre-pass + 128-head kernel
 ])
 def test_concurrent_calls_match_serial(H, D_qk, fp8, num_splits, lanes):
