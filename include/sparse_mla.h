@@ -106,7 +106,10 @@ SMLA_API const char *smla_last_error_string(void);
 /* Number of splits of the top-k list ("split-K", [P3] jin-amd A/B: decode-sized
  * calls need it) that sparse_mla_fwd uses when num_splits == 0, for a device
  * with `sm_count` SMs. Host-only arithmetic; returns >= 1, or 0 for invalid
- * arguments. */
+ * arguments. A caller that runs independent calls concurrently (each on its
+ * own stream with its own buffers) can pass the SMs one call will get, e.g.
+ * half the device's with two or more in flight, and give the result as the
+ * calls' num_splits. */
 SMLA_API int smla_plan_num_splits(int T, int H, int D_qk, int topk, int kv_dtype,
                                   int sm_count);
 
