@@ -1,5 +1,6 @@
 """Host-side helpers of bench.py: the kernel-source hash that ties the
-committed DRAM-traffic counters to the code they were taken on."""
+committed DRAM-traffic counters to the code they were taken on, and the
+gather-ceiling sweep's probe configurations."""
 import os
 import sys
 
@@ -27,3 +28,20 @@ def test_traffic_is_tied_to_the_current_sources():
     assert len(h) == 16 and int(h, 16) >= 0
     assert bench.kernel_source_hash() == h          # deterministic
     assert bench.ncu_traffic("no such workload") is None
+
+
+def test_ceiling_sweep_fits_and_covers_both_copy_methods():
+    """Every probe configuration of the gather-ceiling sweep fits its CTAs on
+    one SM (as the probe pads them), and both copy methods are swept for each
+    CTA count; the pair modes copy by TMA only."""
+    import bench
+    for row_bytes in (1024, 576, 512, 128):
+        tile = 64 * 128 * ((row_bytes + 127) // 128)
+        cfgs = bench.ceiling_configs(row_bytes)
+        for k, st, pm, iw, cm in cfgs:
+            assert 1 <= st <= 8 and 1 <= k <= 4
+            assert k * (1024 + st * tile + 24 * 8 + 64 + 1024) <= 233472
+            assert cm in (0, 1) and not (cm and (pm or iw))
+        for k in {c[0] for c in cfgs if not c[2]}:
+            assert {c[4] for c in cfgs if c[0] == k and not c[2]} == {0, 1}
+        assert {c[2] for c in cfgs} == {0, 1, 2}
