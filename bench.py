@@ -684,7 +684,7 @@ def quantize_q_per_tensor(binding, q):
     return q8.view(T, H, D), qs
 
 
-def run_e2e(w, cache, kvs, sets, dot, splits, dev, stream, K, world, q8=False, slots=4):
+def run_e2e(w, cache, kvs, sets, dot, splits, dev, stream, K, world, q8=False, slots=8):
     """Same metric through the public API with host buffers: every step copies
     that step's q and indices from pinned host memory and reads out and lse
     back into pinned host memory, inside the timed region.
