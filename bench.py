@@ -381,13 +381,12 @@ def time_isolated(call, stream, flush, n=9):
 
 
 
-def shared_gpu_splits(binding, w, dev):
-    """The split count for calls that share the GPU with another call in
-    flight: the library's plan for half the SMs (the automatic plan for the
-    128-head path, whose explicit splits change its kernel)."""
+def shared_gpu_splits(binding, w, sms):
+    """The split count for calls that share a GPU of `sms` SMs with another
+    call in flight: the library's plan for half the SMs (0, the automatic
+    plan, for the 128-head path, whose explicit splits change its kernel)."""
     if w.kind == "wide":
         return 0
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     return binding.smla_plan_num_splits(w.T, w.H, w.D_qk, w.topk, int(w.kv_fp8), max(1, sms // 2))
 
 
@@ -399,7 +398,7 @@ def concurrent_steps(binding, w, cache, kvs, sets, dev, stream, args, sinks=None
     and join back into the timing stream inside one CUDA graph. Returns (ms
     per step, steps timed, splits)."""
     R = len(sets)
-    S = shared_gpu_splits(binding, w, dev)
+    S = shared_gpu_splits(binding, w, torch.cuda.get_device_properties(dev).multi_processor_count)
     ls = [torch.cuda.Stream(device=dev) for _ in range(lanes)]
     calls = [forward_setup(binding, w, cache, kvs, sets, dev, s_, args, sinks, num_splits=S)[0] for s_ in ls]
     G = R * lanes * max(1, 40 // (R * lanes))
@@ -601,7 +600,9 @@ def run_ours(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(w, cache, kvs, sets, dot, shared_gpu_splits(binding, w, dev), dev, stream, K, world, q8=args.q8)
+        e2e = run_e2e(w, cache, kvs, sets, dot,
+                      shared_gpu_splits(binding, w, torch.cuda.get_device_properties(dev).multi_processor_count),
+                      dev, stream, K, world, q8=args.q8)
     ms2, k2, s2 = concurrent_steps(binding, w, cache, kvs, sets, dev, stream, args, sinks)
     ms2 = max_over_ranks(ms2, world, dev)
     gbs2 = job_rate(per_launch_bytes, world, ms2) / 1e9

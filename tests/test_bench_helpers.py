@@ -45,3 +45,15 @@ def test_ceiling_sweep_fits_and_covers_both_copy_methods():
         for k in {c[0] for c in cfgs if not c[2]}:
             assert {c[4] for c in cfgs if c[0] == k and not c[2]} == {0, 1}
         assert {c[2] for c in cfgs} == {0, 1, 2}
+
+
+def test_shared_gpu_split_plan():
+    """Calls that share the GPU are planned for half its SMs: one split per row
+    for decode bf16, two for decode fp8 (two lean CTAs per SM), none for
+    prefill; the 128-head path keeps its automatic plan (0)."""
+    from sparse_mla_attention_04_gb300 import binding, build, inputs
+    build.build()   # the library's host-only plan (nvcc cross-compiles; no GPU needed)
+    want = {"decode_bf16": 1, "decode_fp8": 2, "prefill_bf16": 1, "wide_fp8": 0}
+    for name, S in want.items():
+        w = inputs.CONFIGS[name](seed=0)
+        assert bench.shared_gpu_splits(binding, w, 152) == S, name
