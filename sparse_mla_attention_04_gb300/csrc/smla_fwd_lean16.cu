@@ -6,7 +6,8 @@
 // gathers complete is limited per CTA: random 512-byte rows arrive about
 // twice as fast with two or three CTAs per SM as with one (measured with the
 // gather probe). So each CTA here stays within half an SM: at most 113 KB of
-// shared memory, 256 columns of tensor memory and 384 threads.
+// shared memory, 256 columns of tensor memory and 448 threads (72 registers
+// each; the softmax keeps its per-head reference max in shared memory to fit).
 //
 // One CTA = (query row t, split s of its top-k list). As in the 16-head
 // kernel the contraction runs transposed, keys on the MMA's M axis:
@@ -20,12 +21,17 @@
 // Warp roles, handing tiles over through mbarriers (every wait bounded):
 //   softmax (warps 0-3, one key per thread of lanes 0-15): as in the 16-head
 //     kernel (lazy reference max, rescale of O^T in tensor memory only when
-//     a logit passes the reference by more than 2^8), writes P^T (fp16).
+//     a logit passes the reference by more than 2^8), writes P^T (fp16). The
+//     reference max per head, the same in every softmax thread, lives in
+//     shared memory (two buffers: the new one is written while the old one
+//     is read).
 //   QK issuer (warp 4), PV issuer (warp 5): one thread each.
-//   producers (warps 6-7): one gather4 copy per thread per tile (16 key quads
-//     x 4 column blocks of 128 codes) into a 3-stage ring; -1 and
-//     out-of-range indices go to the TMA as row -1 (zero fill, no read).
-//   converters (warps 8-11, one per quarter of the TMEM lanes): first q,
+//   producers (warps 6-9): one gather4 copy per thread of lanes 0-15 per tile
+//     (16 key quads x 4 column blocks of 128 codes; a warp issues its lanes'
+//     copies one after another, so four warps issue a tile in half the time
+//     of two) into a 3-stage ring; -1 and out-of-range indices go to the TMA
+//     as row -1 (zero fill, no read).
+//   converters (warps 10-13, one per quarter of the TMEM lanes): first q,
 //     quantized per (row, head) straight from global memory (s_q =
 //     amax/448, q8 = RNE_satfinite(q / s_q)), or the pre-quantized codes;
 //     then per tile each half of the values, E4M3 -> binary16 (exact), as
@@ -62,10 +68,10 @@ constexpr int kSoftmaxWarps = 4;
 constexpr int kQkWarp = 4;
 constexpr int kPvWarp = 5;
 constexpr int kProducerWarp0 = 6;
-constexpr int kProducerThreads = 64;
-constexpr int kConverterWarp0 = 8;
+constexpr int kProducerThreads = 128;
+constexpr int kConverterWarp0 = 10;
 constexpr int kConverterThreads = 128;
-constexpr int kThreads = 12 * 32;
+constexpr int kThreads = 14 * 32;
 constexpr int kKeys = kUmma16TileKeys; // keys per tile (M of QK)
 constexpr int kHeads = 16;
 constexpr int kD = 512;
@@ -93,7 +99,8 @@ constexpr int kOffLred = kOffWmax + 4 * 16 * 4;
 constexpr int kOffLse = kOffLred + 4 * 16 * 4;
 constexpr int kOffAlpha = kOffLse + 16 * 4;
 constexpr int kOffMisc = kOffAlpha + 16 * 4;      // flag, tmem address, abort
-constexpr int kOffMbar = (kOffMisc + 16 + 7) & ~7;
+constexpr int kOffMref = kOffMisc + 16;            // [2][16] reference max per head (double-buffered)
+constexpr int kOffMbar = (kOffMref + 128 + 7) & ~7;
 // full[3], empty[3], s_full[2], p_full[2], p_empty[2], q_full, drain, v_full[2], v_free[2]
 constexpr int kNBar = 2 * kStages + 6 + 2 + 4;
 constexpr int kSmem = kOffMbar + kNBar * 8;
@@ -207,13 +214,15 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (warp >= kProducerWarp0 && warp < kConverterWarp0) {
         // ======================= producers =======================
-        const int pt = tid - kProducerWarp0 * 32; // copy: key quad pt / 4, column block pt % 4
-        const int qd = pt / kNcb, cb = pt % kNcb;
+        const int pt = tid - kProducerWarp0 * 32;
+        const bool copier = (pt & 31) < 16; // copy cid: key quad cid / 4, column block cid % 4
+        const int cid = (pt >> 5) * 16 + (pt & 15);
+        const int qd = cid / kNcb, cb = cid % kNcb;
         auto fetch = [&](int tile, int (&r)[4]) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int p = kb + tile * kKeys + 4 * qd + u;
-                r[u] = (tile < ntiles && p < ke) ? __ldg(row_idx + p) : -1;
+                r[u] = (copier && tile < ntiles && p < ke) ? __ldg(row_idx + p) : -1;
             }
         };
         auto row = [&](int x) { return (x >= 0 && (int64_t)x < a.num_slots) ? x : -1; };
@@ -246,8 +255,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                 stop = true;
                 return;
             }
-            umma::tma_gather4(ring + st * kTile + cb * kBlk + qd * 512, &kv_map, 128 * cb, row(r[0]), row(r[1]),
-                              row(r[2]), row(r[3]), full(st));
+            if (copier)
+                umma::tma_gather4(ring + st * kTile + cb * kBlk + qd * 512, &kv_map, 128 * cb, row(r[0]), row(r[1]),
+                                  row(r[2]), row(r[3]), full(st));
             issued = j + 1;
             fetch(j + kIdxAhead, r);
         };
@@ -439,15 +449,17 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int key = warp * 16 + lane; // meaningful for lane < 16
         const float kvs = *a.kv_scale;
         wait_bar(q_full, 0); // the per-head q scales
-        if (tid < 16)
+        float *mref_s = reinterpret_cast<float *>(smem + kOffMref);
+        int mcur = 0;
+        if (tid < 16) {
             fac_s[tid] = a.scale * kLog2e * sq_s[tid] * kvs;
-        umma::named_bar(1, kSoftmaxWarps * 32);
-        float m_ref[16], l_part[16];
-#pragma unroll
-        for (int h = 0; h < 16; ++h) {
-            m_ref[h] = -INFINITY;
-            l_part[h] = 0.f;
+            mref_s[tid] = -INFINITY;
         }
+        umma::named_bar(1, kSoftmaxWarps * 32);
+        float l_part[16];
+#pragma unroll
+        for (int h = 0; h < 16; ++h)
+            l_part[h] = 0.f;
         auto load_idx = [&](int tile) {
             const int p = kb + tile * kKeys + key;
             return (lane < 16 && tile < ntiles && p < ke) ? __ldg(row_idx + p) : -1;
@@ -468,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int h = 0; h < 16; ++h) {
                 sv[h] = kvalid ? sv[h] * fac_s[h] : -INFINITY;
-                exceed |= sv[h] > m_ref[h] + kRescaleThreshold;
+                exceed |= sv[h] > mref_s[mcur * 16 + h] + kRescaleThreshold;
             }
             exceed = __any_sync(0xffffffffu, exceed);
             if (lane == 0)
@@ -489,14 +501,17 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                 for (int h = 0; h < 16; ++h) {
                     const float tmx = fmaxf(fmaxf(wmax_s[h], wmax_s[16 + h]), fmaxf(wmax_s[32 + h], wmax_s[48 + h]));
-                    const float mn = fmaxf(m_ref[h], tmx + kHeadroom);
-                    const float al = (m_ref[h] == -INFINITY) ? 0.f : exp2f(m_ref[h] - mn);
-                    m_ref[h] = mn;
+                    const float mo = mref_s[mcur * 16 + h];
+                    const float mn = fmaxf(mo, tmx + kHeadroom);
+                    const float al = (mo == -INFINITY) ? 0.f : exp2f(mo - mn);
                     l_part[h] *= al;
-                    if (tid == 0)
+                    if (tid == 0) {
                         alpha_s[h] = al;
+                        mref_s[(mcur ^ 1) * 16 + h] = mn;
+                    }
                 }
                 umma::named_bar(1, kSoftmaxWarps * 32);
+                mcur ^= 1;
                 if (i >= 1) {
                     // O^T holds PV(0..i-1): let PV(i-1) finish (its P buffer's barrier; this
                     // thread already waited there for PV(i-3), so the phase cannot alias),
@@ -519,7 +534,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
 #pragma unroll
             for (int h = 0; h < 16; ++h) {
-                const float mu = (m_ref[h] == -INFINITY) ? 0.f : m_ref[h];
+                const float mr = mref_s[mcur * 16 + h];
+                const float mu = (mr == -INFINITY) ? 0.f : mr;
                 sv[h] = ex2_approx(sv[h] - mu);
                 l_part[h] += sv[h];
             }
@@ -561,10 +577,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         umma::named_bar(1, kSoftmaxWarps * 32);
         if (tid < 16) { // thread h finishes head h
-            float mh = m_ref[0];
-#pragma unroll
-            for (int h = 1; h < 16; ++h)
-                mh = tid == h ? m_ref[h] : mh;
+            const float mh = mref_s[mcur * 16 + tid];
             const float l = lred_s[tid] + lred_s[16 + tid] + lred_s[32 + tid] + lred_s[48 + tid];
             lse_s[tid] = l > 0.f ? (mh + log2f(l)) * kLn2 : -INFINITY;
             alpha_s[tid] = l > 0.f ? kvs / l : 0.f; // reused: output factor per head
