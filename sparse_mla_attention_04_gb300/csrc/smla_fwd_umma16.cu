@@ -170,7 +170,8 @@ struct Cfg {
     static constexpr int OFF_LSE = OFF_LRED + 4 * 16 * 4;
     static constexpr int OFF_ALPHA = OFF_LSE + 16 * 4;
     static constexpr int OFF_MISC = OFF_ALPHA + 16 * 4; // flag, tmem address, abort
-    static constexpr int OFF_MBAR = (OFF_MISC + 16 + 7) & ~7;
+    static constexpr int OFF_MREF = OFF_MISC + 16;  // [2][16] reference max per head (double-buffered)
+    static constexpr int OFF_MBAR = (OFF_MREF + 128 + 7) & ~7;
     // full[S], empty[S], s_full[2] (a commit per QK issuer), p_full[2], p_empty[2] (a
     // commit per PV issuer), q_full, drain (a commit per MMA issuer), v_full[3] (E4M3:
     // V^T buffer written), v_free[3] (E4M3: a commit per PV issuer, V^T buffer read),
@@ -745,12 +746,15 @@ __global__ void __launch_bounds__(Cfg<MODE>::BOUND_THREADS, 1)
             umma::named_bar(1, kSoftmaxWarps * 32);
         }
         auto fac = [&](int h) { return G8 ? fac_s[h] : a.scale * kLog2e; };
-        float m_ref[16], l_part[16];
+        float *mref_s = reinterpret_cast<float *>(smem + C::OFF_MREF);
+        int mcur = 0;
+        if (tid < 16)
+            mref_s[tid] = -INFINITY;
+        umma::named_bar(1, kSoftmaxWarps * 32);
+        float l_part[16];
 #pragma unroll
-        for (int h = 0; h < 16; ++h) {
-            m_ref[h] = -INFINITY;
+        for (int h = 0; h < 16; ++h)
             l_part[h] = 0.f;
-        }
         auto load_idx = [&](int tile) {
             const int p = kb + tile * kKeys + key;
             return (lane < 16 && tile < ntiles && p < ke) ? __ldg(row_idx + p) : -1;
@@ -781,7 +785,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::BOUND_THREADS, 1)
 #pragma unroll
             for (int h = 0; h < 16; ++h) {
                 sv[h] = kvalid ? sv[h] * fac(h) : -INFINITY;
-                exceed |= sv[h] > m_ref[h] + kRescaleThreshold;
+                exceed |= sv[h] > mref_s[mcur * 16 + h] + kRescaleThreshold;
             }
             exceed = __any_sync(0xffffffffu, exceed);
             if (lane == 0)
@@ -802,14 +806,17 @@ __global__ void __launch_bounds__(Cfg<MODE>::BOUND_THREADS, 1)
 #pragma unroll
                 for (int h = 0; h < 16; ++h) {
                     const float tmx = fmaxf(fmaxf(wmax_s[h], wmax_s[16 + h]), fmaxf(wmax_s[32 + h], wmax_s[48 + h]));
-                    const float mn = fmaxf(m_ref[h], tmx + kHeadroom);
-                    const float al = (m_ref[h] == -INFINITY) ? 0.f : exp2f(m_ref[h] - mn);
-                    m_ref[h] = mn;
+                    const float mo = mref_s[mcur * 16 + h];
+                    const float mn = fmaxf(mo, tmx + kHeadroom);
+                    const float al = (mo == -INFINITY) ? 0.f : exp2f(mo - mn);
                     l_part[h] *= al;
-                    if (tid == 0)
+                    if (tid == 0) {
                         alpha_s[h] = al;
+                        mref_s[(mcur ^ 1) * 16 + h] = mn;
+                    }
                 }
                 umma::named_bar(1, kSoftmaxWarps * 32);
+                mcur ^= 1;
                 if (i >= 1) {
                     // O^T holds PV(0..i-1): let PV(i-1) finish (its P buffer's barrier; this
                     // thread already waited there for PV(i-3), so the phase cannot alias),
@@ -831,7 +838,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::BOUND_THREADS, 1)
             }
 #pragma unroll
             for (int h = 0; h < 16; ++h) {
-                const float mu = (m_ref[h] == -INFINITY) ? 0.f : m_ref[h];
+                const float mr = mref_s[mcur * 16 + h];
+                const float mu = (mr == -INFINITY) ? 0.f : mr;
                 sv[h] = ex2_approx(sv[h] - mu);
                 l_part[h] += sv[h];
             }
@@ -872,10 +880,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::BOUND_THREADS, 1)
         }
         umma::named_bar(1, kSoftmaxWarps * 32);
         if (tid < 16) { // thread h finishes head h (all heads at once)
-            float mh = m_ref[0];
-#pragma unroll
-            for (int h = 1; h < 16; ++h)
-                mh = tid == h ? m_ref[h] : mh;
+            const float mh = mref_s[mcur * 16 + tid];
             const float l = lred_s[tid] + lred_s[16 + tid] + lred_s[32 + tid] + lred_s[48 + tid];
             lse_s[tid] = l > 0.f ? (mh + log2f(l)) * kLn2 : -INFINITY;
             alpha_s[tid] = l > 0.f ? ovs / l : 0.f; // reused: output factor per head
