@@ -71,7 +71,9 @@
 //     than 2^8, and the reference then moves to 2^8 above the tile max (p
 //     stays <= 1; O/l does not depend on the reference), so the common tile
 //     needs no cross-thread reduction beyond one flag exchange; writes one
-//     row of P^T.
+//     row of P^T. The reference max per head, the same in every softmax
+//     thread, lives in shared memory (two buffers: thread 0 writes the new
+//     one while the others read the old), not in 16 registers a thread.
 // Every barrier completes once per use of the resource it guards, so no
 // waiter can fall two phases behind; every wait gives up after about 2 s
 // (the call then records an error, stops issuing, waits with a bound for the
